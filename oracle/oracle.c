@@ -1,0 +1,246 @@
+/*
+ * oracle.c -- plain, slow, double-precision CPU oracle for the Qwen3-style
+ * RMSNorm forward and backward, its fused residual-add variant and (through
+ * the same definition) its split-row forward.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark load this library. The CUDA library shares no
+ * code, header, helper, table or constant with it, and neither side includes
+ * or calls the other.
+ *
+ * Sources, cited below by tag:
+ *   [P1] "训推加速 Qwen3 实战：从“调包”到手写 Triton Kernel（含 backward）"
+ *        (iqiancheng.github.io, posts/triton-kernel-fusion-practice)
+ *   [P2] the article on hand-writing 21 Triton kernels for decoding a 0.8B
+ *        Qwen model on one consumer GPU (trdm.cn, news/483216; the extracted
+ *        page carries no title)
+ *
+ * Every function writes its definition out with plain loops in double
+ * precision: no blocking, no fusion, no reordering beyond what the definition
+ * states, so that it can be checked against the pages by eye. Inputs are read
+ * in their stored format (fp32, bf16 bit patterns or fp64) and decoded here,
+ * exactly, to double. Results stay in double and are never rounded, except the
+ * residual sum h, which the method stores in the input dtype.
+ *
+ * Parity status: every function below is pinned by the CPU tests (closed
+ * forms, invariants, central finite differences, a library rounding routine);
+ * none is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+#define ORACLE_F64 2
+
+/* ---------------------------------------------------------------- formats */
+
+/* bfloat16 is the upper 16 bits of an IEEE binary32; widening is exact. */
+double oracle_bf16_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Round a double to the nearest bfloat16, ties to even, in one step (no
+ * intermediate rounding to binary32, which could round twice).
+ * bfloat16 keeps 8 significant bits, normal exponents -126..127, subnormals
+ * down to 2^-133.
+ */
+uint16_t oracle_bf16_from_double(double v)
+{
+    if (isnan(v))
+        return (uint16_t)(signbit(v) ? 0xFFC0u : 0x7FC0u);
+    if (v == 0.0)
+        return (uint16_t)(signbit(v) ? 0x8000u : 0x0000u);
+    int e;
+    (void)frexp(v, &e);            /* |v| in [2^(e-1), 2^e) */
+    int q = e - 8;                 /* spacing of 8-bit significands there */
+    if (q < -133)
+        q = -133;                  /* subnormal spacing */
+    double scaled = ldexp(v, -q);  /* exact: a power-of-two scaling */
+    double n = nearbyint(scaled);  /* default mode: nearest, ties to even */
+    double r = ldexp(n, q);
+    const double bf16_max = ldexp(255.0, 120); /* (2 - 2^-7) * 2^127 */
+    if (fabs(r) > bf16_max)
+        return (uint16_t)(v < 0 ? 0xFF80u : 0x7F80u);
+    float f = (float)r;            /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+static double dec(const void *p, int dtype, int64_t i)
+{
+    switch (dtype) {
+    case ORACLE_F32:
+        return (double)((const float *)p)[i];
+    case ORACLE_BF16:
+        return oracle_bf16_to_double(((const uint16_t *)p)[i]);
+    default:
+        return ((const double *)p)[i];
+    }
+}
+
+/* Store v in the given format, rounding to nearest-even; returns the stored
+ * value read back as a double. */
+static double store_rounded(void *p, int dtype, int64_t i, double v)
+{
+    switch (dtype) {
+    case ORACLE_F32: {
+        float f = (float)v; /* C conversion in the default rounding mode */
+        ((float *)p)[i] = f;
+        return (double)f;
+    }
+    case ORACLE_BF16: {
+        uint16_t b = oracle_bf16_from_double(v);
+        ((uint16_t *)p)[i] = b;
+        return oracle_bf16_to_double(b);
+    }
+    default:
+        ((double *)p)[i] = v;
+        return v;
+    }
+}
+
+/* ---------------------------------------------------------------- forward */
+
+/*
+ * [P1 §4.1]: per row i of x (M rows of H features) and a per-feature weight w,
+ *   r_i   = 1 / sqrt( (1/H) * sum_j x_ij^2 + eps )
+ *   y_ij  = w_j * x_ij * r_i
+ * [P1 §4.2] divides the sum of squares by the true feature count H and adds
+ * eps inside the square root. [P2 §3.2] computes the same sum of squares in
+ * pieces and merges them; the merged value is this same sum, so the split-row
+ * forward has this definition too.
+ * y (M*H) and rstd (M) are outputs; either may be NULL.
+ */
+void oracle_rmsnorm_fwd(int64_t M, int64_t H, const void *x, const void *w,
+                        int dtype, double eps, double *y, double *rstd)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        double ss = 0.0;
+        for (int64_t j = 0; j < H; ++j) {
+            double xv = dec(x, dtype, i * H + j);
+            ss += xv * xv;
+        }
+        double ms = ss / (double)H;
+        double r = 1.0 / sqrt(ms + eps);
+        if (rstd)
+            rstd[i] = r;
+        if (y)
+            for (int64_t j = 0; j < H; ++j)
+                y[i * H + j] = dec(w, dtype, j) * dec(x, dtype, i * H + j) * r;
+    }
+}
+
+/* --------------------------------------------------------------- backward */
+
+/*
+ * [P1 §5.3]: with wdy_j = w_j * dy_j and c = (1/H) * sum_j wdy_j * x_j,
+ *   dx_ij = r_i * ( w_j * dy_ij - x_ij * r_i^2 * c_i )
+ *   dw_j  = sum_i dy_ij * x_ij * r_i          (a sum over all rows)
+ * with r_i recomputed from x as in the forward ([P1 §5.4] recomputes it).
+ *
+ * Optional error-scale outputs (sums of absolute values of the terms that
+ * make up each result; used by the tests' tolerances):
+ *   tdx_ij = |r_i w_j dy_ij| + |x_ij| r_i^3 (1/H) sum_k |w_k dy_ik x_ik|
+ *   tdw_j  = sum_i |dy_ij x_ij r_i|
+ * dx, dw, tdx, tdw may each be NULL. dw and tdw have H entries and are
+ * overwritten (not accumulated into).
+ */
+void oracle_rmsnorm_bwd(int64_t M, int64_t H, const void *dy, const void *x,
+                        const void *w, int dtype, double eps, double *dx,
+                        double *dw, double *tdx, double *tdw)
+{
+    if (dw)
+        for (int64_t j = 0; j < H; ++j)
+            dw[j] = 0.0;
+    if (tdw)
+        for (int64_t j = 0; j < H; ++j)
+            tdw[j] = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        double ss = 0.0;
+        for (int64_t j = 0; j < H; ++j) {
+            double xv = dec(x, dtype, i * H + j);
+            ss += xv * xv;
+        }
+        double r = 1.0 / sqrt(ss / (double)H + eps);
+
+        double csum = 0.0, cabs = 0.0;
+        for (int64_t j = 0; j < H; ++j) {
+            double wdy = dec(w, dtype, j) * dec(dy, dtype, i * H + j);
+            double xv = dec(x, dtype, i * H + j);
+            csum += wdy * xv;
+            cabs += fabs(wdy * xv);
+        }
+        double c = csum / (double)H;
+
+        for (int64_t j = 0; j < H; ++j) {
+            double xv = dec(x, dtype, i * H + j);
+            double dyv = dec(dy, dtype, i * H + j);
+            double wdy = dec(w, dtype, j) * dyv;
+            if (dx)
+                dx[i * H + j] = r * (wdy - xv * r * r * c);
+            if (tdx)
+                tdx[i * H + j] =
+                    fabs(r * wdy) + fabs(xv) * r * r * r * (cabs / (double)H);
+            if (dw)
+                dw[j] += dyv * xv * r;
+            if (tdw)
+                tdw[j] += fabs(dyv * xv * r);
+        }
+    }
+}
+
+/* -------------------------------------------------------- residual variant */
+
+/*
+ * Residual add fused with the norm ([P1 §1] names "residual + next RMSNorm"
+ * as the cross-block fusion a compiler misses; [P2 §2.1] lists residual_add
+ * followed by rms_norm and plans their fused kernel):
+ *   h_ij = round_to_dtype(x_ij + r_ij)       written out (the new residual)
+ *   y, rstd = the forward above applied to the stored h
+ * The sum of two bf16 (or two fp32) values is formed in double and rounded
+ * once to the stored format. h has the input dtype; y and rstd are doubles.
+ */
+void oracle_residual_fwd(int64_t M, int64_t H, const void *x, const void *res,
+                         const void *w, int dtype, double eps, void *h,
+                         double *y, double *rstd)
+{
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < H; ++j) {
+            double s = dec(x, dtype, i * H + j) + dec(res, dtype, i * H + j);
+            (void)store_rounded(h, dtype, i * H + j, s);
+        }
+    oracle_rmsnorm_fwd(M, H, h, w, dtype, eps, y, rstd);
+}
+
+/*
+ * Backward of the residual variant. h = x + r feeds the norm and also flows
+ * on as the residual stream, whose gradient dh_out arrives from the next
+ * block (NULL means zero). Since dh/dx = dh/dr = identity, the gradient of
+ * both x and r is
+ *   dx_ij = (backward of the norm at h)_ij + dh_out_ij
+ * and dw is the norm's dw at h ([P1 §5.3] applied to h).
+ */
+void oracle_residual_bwd(int64_t M, int64_t H, const void *dy,
+                         const void *dh_out, const void *h, const void *w,
+                         int dtype, double eps, double *dx, double *dw,
+                         double *tdx, double *tdw)
+{
+    oracle_rmsnorm_bwd(M, H, dy, h, w, dtype, eps, dx, dw, tdx, tdw);
+    if (dh_out)
+        for (int64_t i = 0; i < M; ++i)
+            for (int64_t j = 0; j < H; ++j) {
+                double g = dec(dh_out, dtype, i * H + j);
+                if (dx)
+                    dx[i * H + j] += g;
+                if (tdx)
+                    tdx[i * H + j] += fabs(g);
+            }
+}

@@ -1,0 +1,126 @@
+"""Seeded synthetic inputs for the RMSNorm workloads.
+
+The only module shared by the CUDA path's tests/benchmark and the oracle's
+checks. It draws random numbers and nothing else: no normalisation, no
+reduction, none of the method's arithmetic.
+
+Shapes and distributions are those of the Qwen3 workloads the RMSNorm pages
+work on ("训推加速 Qwen3 实战：从“调包”到手写 Triton Kernel（含 backward）" §4.4
+and §6.2: bf16 activations of batch 4-8 x 4096 tokens x hidden 4096; the
+decode article on a 0.8B Qwen model, trdm.cn news/483216 §1: hidden 896, one
+token at a time). Every tensor is drawn on the CPU from its own
+``torch.Generator`` seed, in float32, scaled, then rounded once to the
+storage dtype. Outlier entries ("0.1 % of entries x50 / x100") are exactly
+``round(0.001 * numel)`` positions drawn without replacement by numpy's
+PCG64 generator, scaled in float32 before the rounding.
+"""
+from dataclasses import dataclass, replace
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    H: int
+    dtype: torch.dtype
+    eps: float = 1e-6
+    seed: int = 0
+    dy_std: float = 1.0
+    outlier_frac: float = 0.0      # fraction of x (and r) entries scaled
+    outlier_scale: float = 1.0
+    residual: bool = False         # also draw r (residual) and dh_out
+    backward: bool = True          # the workload runs the backward too
+    note: str = ""
+
+    def with_rows(self, M: int) -> "Workload":
+        return replace(self, M=int(M), name=f"{self.name}[M={M}]")
+
+    @property
+    def elem_bytes(self) -> int:
+        return torch.empty(0, dtype=self.dtype).element_size()
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("tiny-fp32", 64, 896, torch.float32, seed=0, dy_std=1.0,
+                 note="tiny reference case: x, dy ~ N(0,1), w ~ 1+0.1N(0,1)"),
+        Workload("decode-m1", 1, 896, torch.bfloat16, seed=1, outlier_frac=1e-3,
+                 outlier_scale=50.0, backward=False,
+                 note="decode split-row, one token"),
+        Workload("decode-m8", 8, 896, torch.bfloat16, seed=1, outlier_frac=1e-3,
+                 outlier_scale=50.0, backward=False,
+                 note="decode split-row, 8 tokens"),
+        Workload("decode-m64", 64, 896, torch.bfloat16, seed=1,
+                 outlier_frac=1e-3, outlier_scale=50.0, backward=False,
+                 note="decode split-row, 64 tokens"),
+        Workload("qwen3-8b-train", 32768, 4096, torch.bfloat16, seed=2,
+                 dy_std=1e-2,
+                 note="Qwen3-8B training shape, batch 8 x seq 4096, hidden 4096"),
+        Workload("qwen3-qknorm", 524288, 128, torch.bfloat16, seed=3,
+                 dy_std=1e-2,
+                 note="Qwen3 QK-norm: 4 x 4096 tokens x 32 heads, head_dim 128, "
+                      "one shared weight"),
+        Workload("residual-14b", 16384, 5120, torch.bfloat16, seed=4,
+                 dy_std=1e-2, outlier_frac=1e-3, outlier_scale=100.0,
+                 residual=True,
+                 note="fused residual-add + RMSNorm at Qwen3-14B width"),
+    ]
+}
+
+
+def _normal(shape, seed, std=1.0, mean=0.0):
+    g = torch.Generator().manual_seed(int(seed))
+    t = torch.randn(shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    if mean != 0.0:
+        t.add_(mean)
+    return t
+
+
+def _outliers(t, seed, frac, scale):
+    """Scale exactly round(frac * numel) distinct entries of t (in place)."""
+    n = t.numel()
+    k = int(round(frac * n))
+    if k == 0:
+        return t
+    idx = np.random.default_rng(int(seed)).choice(n, size=k, replace=False)
+    flat = t.view(-1)
+    flat[torch.from_numpy(idx.astype(np.int64))] *= scale
+    return t
+
+
+def make_inputs(w: Workload) -> dict:
+    """CPU tensors for workload ``w``: x, w (weight), dy, and with
+    ``w.residual`` also r and dh (the incoming gradient of the residual
+    stream). Same seed, same values, on every machine with the same torch
+    random generator."""
+    base = 1000 * w.seed
+    shape = (w.M, w.H)
+    x = _normal(shape, base + 1)
+    if w.outlier_frac:
+        _outliers(x, base + 11, w.outlier_frac, w.outlier_scale)
+    out = {"x": x}
+    out["w"] = _normal((w.H,), base + 2, std=0.1, mean=1.0)
+    out["dy"] = _normal(shape, base + 3, std=w.dy_std)
+    if w.residual:
+        r = _normal(shape, base + 4)
+        if w.outlier_frac:
+            _outliers(r, base + 14, w.outlier_frac, w.outlier_scale)
+        out["r"] = r
+        out["dh"] = _normal(shape, base + 5, std=w.dy_std)
+    return {k: v.to(w.dtype).contiguous() for k, v in out.items()}
+
+
+def random_rows(M: int, k: int, seed: int = 0):
+    """k distinct row indices in [0, M) including the first and last rows
+    (for sampled parity checks at full size)."""
+    k = min(k, M)
+    rng = np.random.default_rng(seed)
+    pick = set([0, M - 1])
+    if M > 2:
+        pick.update(rng.choice(M, size=max(0, k - 2), replace=False).tolist())
+    return sorted(pick)[:max(k, min(2, M))]

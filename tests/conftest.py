@@ -1,0 +1,13 @@
+"""Shared pytest setup: the repository root on sys.path and the ``gpu``
+marker (tests that need a CUDA device; the CPU tier runs with -m "not gpu")."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line(
+        "markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")

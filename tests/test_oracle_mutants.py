@@ -1,0 +1,96 @@
+"""CPU tier: the pins have teeth. Each case copies oracle/oracle.c, plants one
+plausible mistake (a dropped term, a wrong sign, divisor or index, a
+different rounding rule), builds the copy with gcc in a temporary directory
+and requires at least one pin of tests/oracle_pins.py to fail on it.
+
+Mistakes are planted only in throw-away copies on the CPU; the oracle itself
+is never modified.
+"""
+import os
+import shutil
+
+import pytest
+
+import oracle
+from oracle import build as obuild
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, original text, mutated text); the original must occur exactly once.
+MUTANTS = [
+    ("fwd_divisor_H_plus_1", "double ms = ss / (double)H;",
+     "double ms = ss / (double)(H + 1);"),
+    ("fwd_eps_dropped", "double r = 1.0 / sqrt(ms + eps);",
+     "double r = 1.0 / sqrt(ms);"),
+    ("fwd_eps_outside_sqrt", "double r = 1.0 / sqrt(ms + eps);",
+     "double r = 1.0 / (sqrt(ms) + eps);"),
+    ("fwd_no_sqrt", "double r = 1.0 / sqrt(ms + eps);",
+     "double r = 1.0 / (ms + eps);"),
+    ("fwd_weight_reversed",
+     "y[i * H + j] = dec(w, dtype, j) * dec(x, dtype, i * H + j) * r;",
+     "y[i * H + j] = dec(w, dtype, H - 1 - j) * dec(x, dtype, i * H + j) * r;"),
+    ("fwd_store_transposed",
+     "y[i * H + j] = dec(w, dtype, j)", "y[j * M + i] = dec(w, dtype, j)"),
+    ("fwd_weight_dropped",
+     "y[i * H + j] = dec(w, dtype, j) * dec(x, dtype, i * H + j) * r;",
+     "y[i * H + j] = dec(x, dtype, i * H + j) * r;"),
+    ("bwd_eps_dropped", "double r = 1.0 / sqrt(ss / (double)H + eps);",
+     "double r = 1.0 / sqrt(ss / (double)H);"),
+    ("bwd_divisor_wrong", "double r = 1.0 / sqrt(ss / (double)H + eps);",
+     "double r = 1.0 / sqrt(ss / (double)(H + 1) + eps);"),
+    ("bwd_dx_sign", "r * (wdy - xv * r * r * c)", "r * (wdy + xv * r * r * c)"),
+    ("bwd_dx_term_dropped", "r * (wdy - xv * r * r * c)", "r * (wdy)"),
+    ("bwd_dx_r_power", "r * (wdy - xv * r * r * c)", "r * (wdy - xv * r * c)"),
+    ("bwd_dx_outer_r_dropped", "dx[i * H + j] = r * (wdy - xv * r * r * c);",
+     "dx[i * H + j] = (wdy - xv * r * r * c);"),
+    ("bwd_c_not_mean", "double c = csum / (double)H;", "double c = csum;"),
+    ("bwd_c_without_w", "double wdy = dec(w, dtype, j) * dec(dy, dtype, i * H + j);",
+     "double wdy = dec(dy, dtype, i * H + j);"),
+    ("bwd_dx_without_w", "double wdy = dec(w, dtype, j) * dyv;",
+     "double wdy = dyv;"),
+    ("bwd_dw_no_r", "dw[j] += dyv * xv * r;", "dw[j] += dyv * xv;"),
+    ("bwd_dw_with_w", "dw[j] += dyv * xv * r;", "dw[j] += wdy * xv * r;"),
+    ("bwd_dw_last_row_only", "dw[j] += dyv * xv * r;", "dw[j] = dyv * xv * r;"),
+    ("bwd_tdx_power", "fabs(xv) * r * r * r * (cabs / (double)H)",
+     "fabs(xv) * r * (cabs / (double)H)"),
+    ("bwd_tdw_signed", "tdw[j] += fabs(dyv * xv * r);", "tdw[j] += dyv * xv * r;"),
+    ("bf16_ties_away", "double n = nearbyint(scaled);", "double n = round(scaled);"),
+    ("bf16_truncate", "double n = nearbyint(scaled);", "double n = trunc(scaled);"),
+    ("bf16_double_rounding", "(void)frexp(v, &e);",
+     "v = (double)(float)v;\n    (void)frexp(v, &e);"),
+    ("bf16_no_subnormal_clamp", "if (q < -133)\n        q = -133;", ""),
+    ("bf16_decode_shift", "((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
+    ("resid_subtract",
+     "double s = dec(x, dtype, i * H + j) + dec(res, dtype, i * H + j);",
+     "double s = dec(x, dtype, i * H + j) - dec(res, dtype, i * H + j);"),
+    ("resid_unrounded_norm_input",
+     "oracle_rmsnorm_fwd(M, H, h, w, dtype, eps, y, rstd);",
+     "oracle_rmsnorm_fwd(M, H, x, w, dtype, eps, y, rstd);"),
+    ("resid_dh_dropped", "dx[i * H + j] += g;", "dx[i * H + j] += 0.0 * g;"),
+    ("resid_dh_sign", "dx[i * H + j] += g;", "dx[i * H + j] -= g;"),
+]
+
+
+@pytest.fixture(scope="module")
+def workdir(tmp_path_factory):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    return tmp_path_factory.mktemp("mutants")
+
+
+def test_mutant_table_is_unique():
+    src = open(SRC).read()
+    for name, old, _ in MUTANTS:
+        assert src.count(old) == 1, f"{name}: anchor occurs {src.count(old)}x"
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(workdir, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"{name}: anchor not unique in oracle.c"
+    msrc = workdir / f"{name}.c"
+    msrc.write_text(src.replace(old, new))
+    lib = obuild.build(force=True, src=str(msrc), out=str(workdir / f"{name}.so"))
+    bad = oracle_pins.failing_pins(oracle.Oracle(lib))
+    assert bad, f"planted mistake {name!r} passed every pin"
