@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Benchmark: Qwen3-style RMSNorm forward + backward on GB300.
+
+One step = one pass of the hot path over one batch: rmsnorm_fwd then
+rmsnorm_bwd (dx plus the two-stage dw) on the Qwen3-8B training shape
+(M = 8 x 4096 = 32768 rows, H = 4096, bf16, fp32 rstd and dw), the shape the
+throughput metric is quoted on. Other workloads (--workload) are for
+investigation; their correctness is covered by the tests.
+
+Prints ONE JSON line (rank 0). value = algorithmic HBM bytes of all ranks'
+steps / max-over-ranks time, in GB/s; rows/s and the roofline fraction ride
+along. Inputs stay resident in HBM during the timed region and exceed L2
+(each x or dy tensor is 268 MB; three buffer sets rotate). The e2e leg goes
+through the same C ABI with pinned host buffers and the host<->device copies
+inside its timed region. The cpu_baseline leg times the fp64 CPU oracle on a
+bounded sample of rows on this host.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rmsnorm_fwd_bwd_02_gb300 import workloads as W  # noqa: E402
+
+METRIC = "RMSNorm fwd/bwd achieved HBM GB/s and % of GB300 roofline; rows/s"
+DEFAULT_WORKLOAD = "qwen3-8b-train"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- bytes
+def step_bytes(wl):
+    """Algorithmic (minimal) HBM bytes of one step, split by call: every
+    input read once, every output written once; the saved rstd read by the
+    backward and the dw workspace are not counted (rstd can be recomputed
+    from x; the workspace is overhead)."""
+    es = wl.elem_bytes
+    MH, H, M = wl.M * wl.H, wl.H, wl.M
+    if wl.residual:
+        fwd = 4 * MH * es + H * es + 4 * M          # x, r in; h, y out; rstd
+        bwd = 4 * MH * es + H * es + 4 * H          # dy, h, dh in; dx out; dw
+    else:
+        fwd = 2 * MH * es + H * es + 4 * M          # x in; y out; rstd
+        bwd = 3 * MH * es + H * es + 4 * H          # dy, x in; dx out; dw
+    if not wl.backward:
+        bwd = 0
+    return fwd, bwd
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def buffer_sets(wl):
+    """Rotating buffer sets: three for workloads whose row tensors exceed L2
+    (each step then streams from HBM); enough to cycle through more than
+    twice the L2 size otherwise (decode-sized workloads stay launch-bound)."""
+    x_bytes = wl.M * wl.H * wl.elem_bytes
+    if x_bytes >= L2_BYTES:
+        return 3
+    return int(min(64, max(3, -(-2 * L2_BYTES // max(x_bytes, 1)))))
+
+
+def base_config(wl):
+    return {"workload": wl.name, "M": wl.M, "H": wl.H, "eps": wl.eps,
+            "dtype": str(wl.dtype).replace("torch.", ""),
+            "step": "fwd+bwd" if wl.backward else "fwd"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, in a background
+    process, so the ones inside the timed region can be reported."""
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return None
+        mine = [r for t, r in self.rows if len(r) >= 10 and
+                (self.uuid is None or r[1] == self.uuid)]
+        inside = [r for t, r in self.rows if t0 - 0.05 <= t <= t1 + 0.15 and len(r) >= 10
+                  and (self.uuid is None or r[1] == self.uuid)]
+        use = inside or mine[-3:]
+        if not use:
+            return None
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in use if num(r[2]) is not None]
+        mx = [num(r[3]) for r in use if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i in range(4)
+                          if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "samples_inside_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------- oracle leg
+def time_oracle(wl, inp, rows, reps=1):
+    """Seconds for the fp64 CPU oracle to run the workload's forward and
+    backward on `rows` rows (single thread, the oracle as it stands)."""
+    import oracle
+    orc = oracle.get()
+    sub = {k: (v[:rows].contiguous() if v.dim() == 2 else v) for k, v in inp.items()}
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        if wl.residual:
+            h, _, _ = orc.residual_fwd(sub["x"], sub["r"], sub["w"], wl.eps)
+            if wl.backward:
+                orc.residual_bwd(sub["dy"], sub["dh"], h, sub["w"], wl.eps)
+        else:
+            orc.fwd(sub["x"], sub["w"], wl.eps)
+            if wl.backward:
+                orc.bwd(sub["dy"], sub["x"], sub["w"], wl.eps)
+    return (time.perf_counter() - t0) / reps
+
+
+def cpu_baseline(wl, inp, budget_s=12.0):
+    """The oracle on a bounded sample of the workload's rows, scaled to GB/s
+    of the same algorithmic bytes per row."""
+    probe = min(wl.M, 64)
+    t = time_oracle(wl, inp, probe)
+    rows = int(max(1, min(wl.M, budget_s / max(t / probe, 1e-9))))
+    secs = time_oracle(wl, inp, rows)
+    fwd_b, bwd_b = step_bytes(wl.with_rows(rows))
+    return {"value": round((fwd_b + bwd_b) / secs / 1e9, 4), "unit": "GB/s",
+            "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {wl.M} rows of {wl.name} (H={wl.H}), fwd+bwd, "
+                      f"single-threaded fp64 oracle, {secs:.2f} s",
+            "rows_per_s": round(rows / secs, 2)}
+
+
+def run_reference(args, wl):
+    """The oracle arm: the same metric on bounded CPU samples per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inp = W.make_inputs(wl.with_rows(min(wl.M, 4096)))
+    probe = 16
+    t_row = time_oracle(wl, inp, probe) / probe
+    per_step = int(max(1, min(4096, 90.0 / max(args.steps + args.warmup, 1) / t_row)))
+    for _ in range(args.warmup):
+        time_oracle(wl, inp, per_step)
+    times = [time_oracle(wl, inp, per_step) for _ in range(args.steps)]
+    total = sum(times)
+    fwd_b, bwd_b = step_bytes(wl.with_rows(per_step))
+    value = (fwd_b + bwd_b) * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4),
+        "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": base_config(wl),
+        "rows_per_s": round(per_step * args.steps / total, 2),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"{per_step} rows of {wl.name} per step "
+                                   f"(fwd+bwd), single-threaded fp64 oracle"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU leg
+class Calls:
+    """Device buffers for one step and the two C-ABI calls of the step."""
+
+    def __init__(self, rn, wl, src, dev, ws):
+        self.rn, self.wl = rn, wl
+        e = lambda: torch.empty(wl.M, wl.H, device=dev, dtype=wl.dtype)  # noqa: E731
+        self.x = src["x"].to(dev)
+        self.dy = src["dy"].to(dev) if wl.backward else None
+        self.r = src["r"].to(dev) if wl.residual else None
+        self.dh = src["dh"].to(dev) if wl.residual else None
+        self.y, self.h = e(), (e() if wl.residual else None)
+        self.dx = e() if wl.backward else None
+        self.rstd = torch.empty(wl.M, device=dev)
+        self.dw = torch.empty(wl.H, device=dev)
+        self.ws = ws
+
+    def fwd(self, w):
+        rn, wl = self.rn, self.wl
+        if wl.residual:
+            rn.rmsnorm_residual_fwd(self.x, self.r, w, h=self.h, y=self.y,
+                                    rstd=self.rstd, eps=wl.eps)
+        else:
+            rn.rmsnorm_fwd(self.x, w, y=self.y, rstd=self.rstd, eps=wl.eps)
+
+    def bwd(self, w):
+        rn, wl = self.rn, self.wl
+        if not wl.backward:
+            return
+        if wl.residual:
+            rn.rmsnorm_residual_bwd(self.dy, self.dh, self.h, w, self.rstd,
+                                    dx=self.dx, dw=self.dw, workspace=self.ws,
+                                    eps=wl.eps)
+        else:
+            rn.rmsnorm_bwd(self.dy, self.x, w, self.rstd, dx=self.dx, dw=self.dw,
+                           workspace=self.ws, eps=wl.eps)
+
+
+def gpu_uuid():
+    try:
+        u = torch.cuda.get_device_properties(torch.cuda.current_device()).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+def run_ours(args, wl):
+    from rmsnorm_fwd_bwd_02_gb300 import rmsnorm as rn
+    rn.lib()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    src = W.make_inputs(wl)
+    w = src["w"].to(dev)
+    ws = torch.empty(max(16, rn.bwd_workspace_bytes(wl.M, wl.H, wl.dtype)),
+                     device=dev, dtype=torch.uint8)
+    x_bytes = wl.M * wl.H * wl.elem_bytes
+    n_sets = buffer_sets(wl)
+    sets = [Calls(rn, wl, src, dev, ws) for _ in range(n_sets)]
+    fwd_b, bwd_b = step_bytes(wl)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up: W steps
+    for i in range(args.warmup):
+        c = sets[i % n_sets]
+        c.fwd(w)
+        c.bwd(w)
+    barrier()
+
+    sampler = ClockSampler(gpu_uuid()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+          for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        c = sets[i % n_sets]
+        ev[i][0].record(stream)
+        c.fwd(w)
+        ev[i][1].record(stream)
+        c.bwd(w)
+        ev[i][2].record(stream)
+    end.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    clocks = None
+    if sampler:
+        time.sleep(0.2)
+        sampler.stop()
+        clocks = sampler.summary(t_wall0, t_wall1)
+
+    total_ms = start.elapsed_time(end)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev] if wl.backward else [0.0]
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+
+    # ---- e2e: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(rn, wl, src, dev, ws, args, dist)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = read_peaks()
+    value = (fwd_b + bwd_b) * world / (ms_step * 1e-3) / 1e9
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_avg = statistics.mean(bwd_ms)
+    dom_is_bwd = wl.backward and bwd_b >= fwd_b
+    dom_bytes, dom_ms = (bwd_b, bwd_avg) if dom_is_bwd else (fwd_b, fwd_avg)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = load_traffic(wl, "bwd" if dom_is_bwd else "fwd")
+
+    def roof(b, ms, kernel):
+        a = b / (ms * 1e-3) / 1e9
+        return {"kernel": kernel, "bound": "hbm", "achieved": round(a, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(a / peak, 4),
+                "peak_kind": peak_kind, "bytes_per_launch": b,
+                "avg_ms": round(ms, 5),
+                "frac_of_nominal_8TBs": round(a / NOMINAL_HBM_GBS, 4)}
+
+    fwd_kernel = "rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd"
+    bwd_kernel = ("rmsnorm_residual_bwd" if wl.residual else "rmsnorm_bwd") + \
+        " (rms_bwd_rows + dw_reduce)"
+    roofline = roof(dom_bytes, dom_ms, bwd_kernel if dom_is_bwd else fwd_kernel)
+    roofline["achieved"] = round(achieved, 1)
+    roofline["traffic"] = traffic
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if wl.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": dict(base_config(wl), **{
+            "l2": (f"inputs larger than L2: {n_sets} rotating buffer sets, "
+                   f"{x_bytes / 1e6:.0f} MB per row tensor"
+                   if x_bytes >= L2_BYTES else
+                   f"{n_sets} rotating buffer sets of {x_bytes / 1e6:.3f} MB per "
+                   f"row tensor (L2-resident; launch-bound)"),
+            "parallelism": "replicas" if world > 1 else "single"}),
+        "rows_per_s": round(wl.M * world / (ms_step * 1e-3), 1),
+        "pct_of_measured_hbm": round(100 * value / world / peak, 2),
+        "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "step_bytes": {"fwd": fwd_b, "bwd": bwd_b},
+        "roofline": roofline,
+        "roofline_fwd": roof(fwd_b, fwd_avg, fwd_kernel),
+        "gpu_launches": args.steps * (1 + (2 if wl.backward else 0)),
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": None,
+    }
+    if wl.backward:
+        line["roofline_bwd"] = roof(bwd_b, bwd_avg, bwd_kernel)
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, src)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(rn, wl, src, dev, ws, args, dist):
+    """Same metric through the C ABI with pinned host inputs and outputs:
+    each step copies its inputs host->device, runs fwd + bwd, and copies
+    every result back (y, rstd, dx, dw and h)."""
+    pin = {k: v.pin_memory() for k, v in src.items()}
+    c = Calls(rn, wl, src, dev, ws)
+    outs = {"y": c.y, "rstd": c.rstd}
+    if wl.backward:
+        outs.update(dx=c.dx, dw=c.dw)
+    if wl.residual:
+        outs["h"] = c.h
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                for k, v in outs.items()}
+    ins = {"x": c.x, "w": None}
+    if wl.backward:
+        ins["dy"] = c.dy
+    if wl.residual:
+        ins.update(r=c.r, dh=c.dh)
+    w = torch.empty_like(src["w"], device=dev)
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in ins)
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for k in ins:
+            (w if k == "w" else ins[k]).copy_(pin[k], non_blocking=True)
+        c.fwd(w)
+        c.bwd(w)
+        for k, v in outs.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    steps = max(1, min(args.steps, 200))
+    for _ in range(max(1, min(args.warmup, 5))):
+        step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    world = dist.get_world_size() if dist is not None else 1
+    fwd_b, bwd_b = step_bytes(wl)
+    return {"value": round((fwd_b + bwd_b) * world / (ms * 1e-3) / 1e9, 1),
+            "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "rows_per_s": round(wl.M * world / (ms * 1e-3), 1)}
+
+
+def load_traffic(wl, which):
+    """DRAM bytes per launch of the dominant call from the committed ncu
+    summary, when one exists for this workload and the current kernels."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        v = d.get(wl.name, {}).get(which)
+        return None if v is None else int(v)
+    except (OSError, ValueError):
+        return None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,170 @@
+/*
+ * rmsnorm.h -- C ABI of librmsnorm.so: Qwen3-style RMSNorm forward and
+ * backward, the fused residual-add variant and the split-row forward for
+ * decode-sized batches, as hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * Sources, cited by tag:
+ *   [P1] "训推加速 Qwen3 实战：从“调包”到手写 Triton Kernel（含 backward）"
+ *        (iqiancheng.github.io, posts/triton-kernel-fusion-practice)
+ *   [P2] the article on hand-writing 21 Triton kernels for decoding a 0.8B
+ *        Qwen model (trdm.cn, news/483216; the extracted page has no title)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are dense, row-major [M, H] (M rows of H features), owned by the
+ *    caller, in device memory (or memory the device can address). The
+ *    weight w has H entries. x, r, w, y, h, dy, dh_out and dx share one
+ *    dtype (RMSNORM_F32 or RMSNORM_BF16); rstd, dw and the workspace are
+ *    always fp32.
+ *  - Every pointer must be aligned to its element size. Rows whose start is
+ *    16-byte aligned (aligned base pointer and H * element size a multiple of
+ *    16) take the 128-bit vectorised kernels; anything else takes a scalar
+ *    kernel with the same results up to fp32 summation order.
+ *  - 1 <= H <= RMSNORM_MAX_H, 0 <= M. eps is a finite float >= 0 (a plain
+ *    float, never a tensor: [P1 §5.6] gotcha table).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream). They allocate nothing, never synchronise and never copy
+ *    to or from the host, so they can be recorded in a CUDA graph ([P2 §4.1,
+ *    §4.3]: no allocation and no synchronisation inside the captured region).
+ *  - Arguments are checked on the host before anything is launched; on error
+ *    nothing is launched and no output is touched. A failed launch returns
+ *    RMSNORM_ERR_CUDA (rmsnorm_last_cuda_error() gives the cudaError_t).
+ *  - Results are deterministic: the same inputs on the same GPU model give the
+ *    same bits on every run. No atomics are used ([P1 §5.4], [P1 §7.3]: a
+ *    fixed reduction order instead of atomic adds; [P2 §3.3]).
+ *  - Output buffers may coincide exactly with the input named in each entry
+ *    point's comment (in-place use); any other overlap is rejected with
+ *    RMSNORM_ERR_ALIAS.
+ */
+#ifndef RMSNORM_GB300_H
+#define RMSNORM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of the row tensors and the weight. */
+typedef enum { RMSNORM_F32 = 0, RMSNORM_BF16 = 1 } rmsnorm_dtype;
+
+/* Return codes. */
+typedef enum {
+    RMSNORM_OK = 0,
+    RMSNORM_ERR_NULLPTR = -1,     /* a required pointer is NULL */
+    RMSNORM_ERR_BAD_SHAPE = -2,   /* M < 0, H < 1, or M * H overflows */
+    RMSNORM_ERR_BAD_DTYPE = -3,   /* dtype is not an rmsnorm_dtype */
+    RMSNORM_ERR_BAD_EPS = -4,     /* eps is negative, NaN or infinite */
+    RMSNORM_ERR_MISALIGNED = -5,  /* a pointer is not aligned to its element
+                                     size (16 bytes for the workspace) */
+    RMSNORM_ERR_WORKSPACE = -6,   /* workspace NULL or smaller than
+                                     rmsnorm_bwd_workspace_bytes() */
+    RMSNORM_ERR_UNSUPPORTED = -7, /* H > RMSNORM_MAX_H */
+    RMSNORM_ERR_CUDA = -8,        /* a CUDA runtime call failed */
+    RMSNORM_ERR_ALIAS = -9        /* buffers overlap in a way not allowed */
+} rmsnorm_status;
+
+/* Largest feature count the kernels hold in registers ([P1 §7.1] puts the
+ * whole-row-per-block limit near 16K features). */
+#define RMSNORM_MAX_H 16384
+
+/*
+ * Forward ([P1 §4.1, §4.2]): for each row i,
+ *   rstd_i = 1 / sqrt( (1/H) sum_j x_ij^2 + eps )
+ *   y_ij   = round( x_ij * rstd_i * w_j )
+ * summed and scaled in fp32, rounded once to the dtype (round-to-nearest-
+ * even for bf16).
+ *   x    [M,H] in, w [H] in, y [M,H] out (y may equal x: in place)
+ *   rstd [M] fp32 out, or NULL when not wanted (the backward can recompute it)
+ * M <= 64 rows take the split-row kernel ([P2 §3.2]): each row is spread over
+ * a cluster of 2-8 CTAs whose fp32 partial sums of squares are combined in
+ * rank order through distributed shared memory; larger M takes the row-wise
+ * kernels (each row held in registers by a group of lanes).
+ * M == 0 launches nothing.
+ */
+int rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd,
+                int64_t M, int64_t H, float eps, int dtype, void *stream);
+
+/*
+ * Backward ([P1 §5.3, §5.4]): with r_i = rstd_i and
+ *   c_i   = (1/H) sum_j w_j dy_ij x_ij,
+ *   dx_ij = round( r_i * (w_j dy_ij - x_ij r_i^2 c_i) )
+ *   dw_j  = sum_i dy_ij x_ij r_i          (fp32, over all M rows)
+ *   dy [M,H], x [M,H], w [H] in; dx [M,H] out (dx may equal dy: in place)
+ *   rstd [M] fp32 in as saved by the forward, or NULL to recompute it from x
+ *   dw [H] fp32 out (overwritten; all zeros when M == 0)
+ *   workspace: caller-owned device scratch of at least
+ *     rmsnorm_bwd_workspace_bytes(M, H, dtype) bytes, 16-byte aligned. It
+ *     holds one fp32 partial dw row per CTA; a second kernel sums them in a
+ *     fixed order. Its contents on entry do not matter; it must not be used
+ *     by another call that overlaps on the GPU.
+ */
+int rmsnorm_bwd(const void *dy, const void *x, const void *w,
+                const float *rstd, void *dx, float *dw, void *workspace,
+                size_t workspace_bytes, int64_t M, int64_t H, float eps,
+                int dtype, void *stream);
+
+/*
+ * Residual add fused with the forward ([P1 §1]: "residual + next RMSNorm"
+ * across a block boundary; [P2 §2.1]: residual_add then rms_norm, with a
+ * fused kernel planned):
+ *   h_ij = round(x_ij + r_ij)   (fp32 add, one rounding to the dtype)
+ *   then the forward above on the stored h: y, rstd.
+ *   x, r [M,H] in; w [H] in; h [M,H] out (h may equal x or r: in place);
+ *   y [M,H] out (must not overlap anything); rstd [M] out or NULL.
+ * Same kernel choice as rmsnorm_fwd (split-row for M <= 64).
+ */
+int rmsnorm_residual_fwd(const void *x, const void *r, const void *w, void *h,
+                         void *y, float *rstd, int64_t M, int64_t H, float eps,
+                         int dtype, void *stream);
+
+/*
+ * Backward of the residual variant: the norm's backward at h, plus the
+ * gradient dh_out that reaches h from the residual stream's other consumer
+ * (NULL means zero). Because dh/dx = dh/dr = identity, the one output dx is
+ * the gradient of both x and r:
+ *   dx_ij = round( r_i (w_j dy_ij - h_ij r_i^2 c_i) + dh_out_ij )
+ *   dw_j  = sum_i dy_ij h_ij r_i
+ *   dy, h [M,H] in; dh_out [M,H] in or NULL; w [H] in; rstd [M] in or NULL;
+ *   dx [M,H] out (dx may equal dy or dh_out); dw [H] out; workspace as for
+ *   rmsnorm_bwd.
+ */
+int rmsnorm_residual_bwd(const void *dy, const void *dh_out, const void *h,
+                         const void *w, const float *rstd, void *dx, float *dw,
+                         void *workspace, size_t workspace_bytes, int64_t M,
+                         int64_t H, float eps, int dtype, void *stream);
+
+/*
+ * Bytes of workspace rmsnorm_bwd / rmsnorm_residual_bwd need for (M, H,
+ * dtype) on the current CUDA device (one fp32 row of H per CTA of the
+ * backward grid; the grid is sized from the device's SM count). Returns 0 on
+ * invalid arguments or when no device is available.
+ */
+size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype);
+
+/* A static, human-readable name for a status code. */
+const char *rmsnorm_status_string(int status);
+
+/* The cudaError_t of the last failed CUDA call made by this library on the
+ * calling thread (0 if none). */
+int rmsnorm_last_cuda_error(void);
+
+/*
+ * Test hook: force the forward kernel family for later calls in this
+ * process. 0 = automatic (default), 1 = row-wise vectorised, 2 = split-row,
+ * 3 = row-wise scalar (also used by the backward). Forcing a vectorised
+ * family on rows that are not 16-byte aligned still takes the scalar one.
+ * Not thread-safe against concurrent calls; intended for tests only.
+ */
+void rmsnorm_set_path_override(int path);
+
+/* Which kernel family the last forward/backward call on this thread used:
+ * 1 row-wise vectorised, 2 split-row, 3 row-wise scalar, 0 none. */
+int rmsnorm_last_path(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_GB300_H */

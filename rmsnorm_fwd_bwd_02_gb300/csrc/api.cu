@@ -1,0 +1,432 @@
+// api.cu -- the C ABI declared in include/rmsnorm.h: host-side argument
+// checks, kernel choice, grid sizing and launches. No allocation, no
+// synchronisation, no host copies; everything is enqueued on the caller's
+// stream.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "rmsnorm.h"
+#include "params.h"
+#include "reduce.cuh"
+#include "registry.h"
+
+using namespace rmsk;
+
+namespace {
+
+constexpr int kPathAuto = 0, kPathRows = 1, kPathSplit = 2, kPathScalar = 3;
+constexpr int kSplitMaxRows = 64;      // decode-sized batches ([P2 §3.2])
+constexpr int kReduceCols = 32, kReduceRows = 16;
+
+thread_local int t_last_cuda_error = 0;
+thread_local int t_last_path = 0;
+std::atomic<int> g_path_override{kPathAuto};
+
+int cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = (int)e;
+    return RMSNORM_ERR_CUDA;
+}
+
+size_t elem_size(int dtype) { return dtype == RMSNORM_BF16 ? 2 : 4; }
+
+bool aligned(const void *p, size_t a) { return p == nullptr || (uintptr_t)p % a == 0; }
+
+struct Buf {
+    const void *p;
+    size_t n;
+};
+
+bool overlap(Buf a, Buf b)
+{
+    if (!a.p || !b.p || !a.n || !b.n)
+        return false;
+    const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
+    return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+// Allowed: the same buffer exactly, or no overlap at all.
+bool same_or_disjoint(Buf a, Buf b)
+{
+    return (a.p == b.p && a.n == b.n) || !overlap(a, b);
+}
+
+int check_common(int64_t M, int64_t H, float eps, int dtype)
+{
+    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16)
+        return RMSNORM_ERR_BAD_DTYPE;
+    if (M < 0 || H < 1)
+        return RMSNORM_ERR_BAD_SHAPE;
+    if (H > RMSNORM_MAX_H)
+        return RMSNORM_ERR_UNSUPPORTED;
+    if (M > INT64_MAX / 8 / H)
+        return RMSNORM_ERR_BAD_SHAPE;
+    if (!(eps >= 0.f) || !std::isfinite(eps))
+        return RMSNORM_ERR_BAD_EPS;
+    return RMSNORM_OK;
+}
+
+// ------------------------------------------------------- device properties
+int current_device(int *dev)
+{
+    cudaError_t e = cudaGetDevice(dev);
+    return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e);
+}
+
+int sm_count(int dev, int *sms)
+{
+    cudaError_t e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e);
+}
+
+// Resident CTAs per SM for a kernel, cached per (kernel, device).
+int blocks_per_sm(const void *fn, int threads, int dev, int *out)
+{
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> cache;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find({fn, dev});
+        if (it != cache.end()) {
+            *out = it->second;
+            return RMSNORM_OK;
+        }
+    }
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    if (n < 1)
+        return cuda_fail(cudaErrorInvalidConfiguration);
+    std::lock_guard<std::mutex> g(mu);
+    cache[{fn, dev}] = n;
+    *out = n;
+    return RMSNORM_OK;
+}
+
+// Persistent grid: no more CTAs than tiles, no more than fit at once.
+int rows_grid(const RowKernels &k, const void *fn, int64_t M, int64_t *grid)
+{
+    int dev, sms, bps, st;
+    if ((st = current_device(&dev)) || (st = sm_count(dev, &sms)) ||
+        (st = blocks_per_sm(fn, k.threads(), dev, &bps)))
+        return st;
+    const int64_t tiles = (M + k.tile_rows() - 1) / k.tile_rows();
+    const int64_t cap = (int64_t)bps * sms;
+    *grid = tiles < cap ? tiles : cap;
+    return RMSNORM_OK;
+}
+
+// -------------------------------------------------------- kernel choice
+const RowKernels &pick_rows(int dtype, int64_t H, bool vec)
+{
+    if (dtype == RMSNORM_BF16) {
+        if (!vec)
+            return H <= b_s32.max_cols() ? b_s32 : b_s1024;
+        if (H == 128) return b_h128;
+        if (H == 896) return b_h896;
+        if (H == 4096) return b_h4096;
+        if (H == 5120) return b_h5120;
+        if (H <= b_g32.max_cols()) return b_g32;
+        if (H <= b_g128.max_cols()) return b_g128;
+        return b_g512;
+    }
+    if (!vec)
+        return H <= f_s32.max_cols() ? f_s32 : f_s1024;
+    if (H == 896) return f_h896;
+    if (H <= f_g32.max_cols()) return f_g32;
+    if (H <= f_g128.max_cols()) return f_g128;
+    return f_g512;
+}
+
+const SplitKernels &pick_split(int dtype, bool vec)
+{
+    if (dtype == RMSNORM_BF16)
+        return vec ? split_bf16_v : split_bf16_s;
+    return vec ? split_f32_v : split_f32_s;
+}
+
+cudaError_t launch(const void *fn, dim3 grid, dim3 block, cudaStream_t s, void *arg,
+                   bool pdl, unsigned cluster_x)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    unsigned n = 0;
+    if (pdl) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_x) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = cluster_x;
+        attrs[n].val.clusterDim.y = 1;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    void *args[1] = {arg};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// ------------------------------------------------------------- forward
+int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, float *rstd,
+             int64_t M, int64_t H, float eps, int dtype, cudaStream_t stream)
+{
+    const bool res = r != nullptr;
+    const size_t es = elem_size(dtype);
+    const bool vec16 = (H * (int64_t)es) % 16 == 0 && aligned(x, 16) && aligned(w, 16) &&
+                       aligned(y, 16) && aligned(r, 16) && aligned(h, 16);
+    const int ov = g_path_override.load(std::memory_order_relaxed);
+    const bool vec = vec16 && ov != kPathScalar;
+    const bool split = M <= 65535 && (ov == kPathSplit || (ov == kPathAuto && M <= kSplitMaxRows));
+
+    if (split) {
+        const SplitKernels &k = pick_split(dtype, vec);
+        const int E = vec ? k.E : 1;
+        const int NV = (int)(H / E);
+        int K = (NV + 31) / 32;
+        K = K < 2 ? 2 : (K > 8 ? 8 : K);
+        const int SV = (NV + K - 1) / K;
+        int NT = (SV + 31) / 32 * 32;
+        NT = NT > 256 ? 256 : NT;
+        const int V = (SV + NT - 1) / NT;   // <= 8 for H <= RMSNORM_MAX_H
+        const void *fn = V == 1 ? (res ? k.v1_res : k.v1) : (res ? k.v8_res : k.v8);
+        SplitParams p = {x, r, w, y, h, rstd, (int)H, NV, SV, eps};
+        cudaError_t e = launch(fn, dim3(K, (unsigned)M), dim3(NT), stream, &p, false, K);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+        t_last_path = kPathSplit;
+        return RMSNORM_OK;
+    }
+
+    const RowKernels &k = pick_rows(dtype, H, vec);
+    const void *fn = res ? k.fwd_res : k.fwd;
+    int64_t grid;
+    int st = rows_grid(k, fn, M, &grid);
+    if (st)
+        return st;
+    FwdParams p = {x, r, w, y, h, rstd, M, (int)H, eps};
+    cudaError_t e = launch(fn, dim3((unsigned)grid), dim3(k.threads()), stream, &p, false, 0);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    t_last_path = vec ? kPathRows : kPathScalar;
+    return RMSNORM_OK;
+}
+
+// ------------------------------------------------------------ backward
+// Grid (and so partial-row count) of the backward kernel for these args.
+int bwd_plan(int dtype, int64_t M, int64_t H, bool vec, bool dh, const RowKernels **kk,
+             const void **fn, int64_t *grid)
+{
+    const RowKernels &k = pick_rows(dtype, H, vec);
+    *kk = &k;
+    *fn = dh ? k.bwd_dh : k.bwd;
+    if (M == 0) {
+        *grid = 0;
+        return RMSNORM_OK;
+    }
+    return rows_grid(k, *fn, M, grid);
+}
+
+int bwd_impl(const void *dy, const void *dh, const void *x, const void *w, const float *rstd,
+             void *dx, float *dw, void *ws, size_t ws_bytes, int64_t M, int64_t H, float eps,
+             int dtype, cudaStream_t stream)
+{
+    int st = check_common(M, H, eps, dtype);
+    if (st)
+        return st;
+    if (dw == nullptr)
+        return RMSNORM_ERR_NULLPTR;
+    if (M > 0 && (!dy || !x || !w || !dx))
+        return RMSNORM_ERR_NULLPTR;
+    const size_t es = elem_size(dtype);
+    if (!aligned(dy, es) || !aligned(x, es) || !aligned(w, es) || !aligned(dx, es) ||
+        !aligned(dh, es) || !aligned(rstd, 4) || !aligned(dw, 4) || !aligned(ws, 16))
+        return RMSNORM_ERR_MISALIGNED;
+
+    const bool vec16 = (H * (int64_t)es) % 16 == 0 && aligned(dy, 16) && aligned(x, 16) &&
+                       aligned(w, 16) && aligned(dx, 16) && aligned(dh, 16);
+    const bool vec = vec16 && g_path_override.load(std::memory_order_relaxed) != kPathScalar;
+    const RowKernels *k;
+    const void *fn;
+    int64_t grid;
+    if ((st = bwd_plan(dtype, M, H, vec, dh != nullptr, &k, &fn, &grid)))
+        return st;
+    const size_t need = (size_t)grid * (size_t)H * sizeof(float);
+    if (need > 0 && (ws == nullptr || ws_bytes < need))
+        return RMSNORM_ERR_WORKSPACE;
+
+    const size_t rows = (size_t)M * (size_t)H * es;
+    const Buf bdy{dy, rows}, bdh{dh, rows}, bx{x, rows}, bw{w, (size_t)H * es},
+        br{rstd, (size_t)M * 4}, bdx{dx, rows}, bdw{dw, (size_t)H * 4}, bws{ws, need};
+    if (!same_or_disjoint(bdx, bdy) || !same_or_disjoint(bdx, bdh) || overlap(bdx, bx) ||
+        overlap(bdx, bw) || overlap(bdx, br) || overlap(bdx, bdw) || overlap(bdx, bws))
+        return RMSNORM_ERR_ALIAS;
+    for (Buf b : {bdy, bdh, bx, bw, br, bws})
+        if (overlap(bdw, b))
+            return RMSNORM_ERR_ALIAS;
+    for (Buf b : {bdy, bdh, bx, bw, br})
+        if (overlap(bws, b))
+            return RMSNORM_ERR_ALIAS;
+
+    if (M > 0) {
+        BwdParams p = {dy, x, w, rstd, dh, dx, static_cast<float *>(ws), M, (int)H, eps};
+        cudaError_t e = launch(fn, dim3((unsigned)grid), dim3(k->threads()), stream, &p, false, 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+    }
+    const float *part = static_cast<const float *>(ws);
+    int P = (int)grid, Hi = (int)H;
+    struct {
+        const float *part;
+        int P, H;
+        float *dw;
+    } a = {part, P, Hi, dw};
+    void *args[4] = {&a.part, &a.P, &a.H, &a.dw};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((H + kReduceCols - 1) / kReduceCols));
+    cfg.blockDim = dim3(kReduceCols * kReduceRows);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelExC(
+        &cfg, (const void *)&dw_reduce<kReduceCols, kReduceRows>, args);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    t_last_path = M == 0 ? 0 : (vec ? kPathRows : kPathScalar);
+    return RMSNORM_OK;
+}
+
+} // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+int rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd, int64_t M, int64_t H,
+                float eps, int dtype, void *stream)
+{
+    int st = check_common(M, H, eps, dtype);
+    if (st)
+        return st;
+    if (M == 0)
+        return RMSNORM_OK;
+    if (!x || !w || !y)
+        return RMSNORM_ERR_NULLPTR;
+    const size_t es = elem_size(dtype);
+    if (!aligned(x, es) || !aligned(w, es) || !aligned(y, es) || !aligned(rstd, 4))
+        return RMSNORM_ERR_MISALIGNED;
+    const size_t rows = (size_t)M * (size_t)H * es;
+    const Buf bx{x, rows}, bw{w, (size_t)H * es}, by{y, rows}, br{rstd, (size_t)M * 4};
+    if (!same_or_disjoint(by, bx) || overlap(by, bw) || overlap(br, bx) || overlap(br, bw) ||
+        overlap(br, by))
+        return RMSNORM_ERR_ALIAS;
+    return fwd_impl(x, nullptr, w, y, nullptr, rstd, M, H, eps, dtype,
+                    static_cast<cudaStream_t>(stream));
+}
+
+int rmsnorm_residual_fwd(const void *x, const void *r, const void *w, void *h, void *y,
+                         float *rstd, int64_t M, int64_t H, float eps, int dtype, void *stream)
+{
+    int st = check_common(M, H, eps, dtype);
+    if (st)
+        return st;
+    if (M == 0)
+        return RMSNORM_OK;
+    if (!x || !r || !w || !h || !y)
+        return RMSNORM_ERR_NULLPTR;
+    const size_t es = elem_size(dtype);
+    if (!aligned(x, es) || !aligned(r, es) || !aligned(w, es) || !aligned(h, es) ||
+        !aligned(y, es) || !aligned(rstd, 4))
+        return RMSNORM_ERR_MISALIGNED;
+    const size_t rows = (size_t)M * (size_t)H * es;
+    const Buf bx{x, rows}, br{r, rows}, bw{w, (size_t)H * es}, bh{h, rows}, by{y, rows},
+        bs{rstd, (size_t)M * 4};
+    if (!same_or_disjoint(bh, bx) || !same_or_disjoint(bh, br) || overlap(bh, bw) ||
+        overlap(bh, bs))
+        return RMSNORM_ERR_ALIAS;
+    for (Buf b : {bx, br, bw, bh, bs})
+        if (overlap(by, b))
+            return RMSNORM_ERR_ALIAS;
+    for (Buf b : {bx, br, bw})
+        if (overlap(bs, b))
+            return RMSNORM_ERR_ALIAS;
+    return fwd_impl(x, r, w, y, h, rstd, M, H, eps, dtype, static_cast<cudaStream_t>(stream));
+}
+
+int rmsnorm_bwd(const void *dy, const void *x, const void *w, const float *rstd, void *dx,
+                float *dw, void *workspace, size_t workspace_bytes, int64_t M, int64_t H,
+                float eps, int dtype, void *stream)
+{
+    return bwd_impl(dy, nullptr, x, w, rstd, dx, dw, workspace, workspace_bytes, M, H, eps,
+                    dtype, static_cast<cudaStream_t>(stream));
+}
+
+int rmsnorm_residual_bwd(const void *dy, const void *dh_out, const void *h, const void *w,
+                         const float *rstd, void *dx, float *dw, void *workspace,
+                         size_t workspace_bytes, int64_t M, int64_t H, float eps, int dtype,
+                         void *stream)
+{
+    return bwd_impl(dy, dh_out, h, w, rstd, dx, dw, workspace, workspace_bytes, M, H, eps,
+                    dtype, static_cast<cudaStream_t>(stream));
+}
+
+size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype)
+{
+    if (check_common(M, H, 0.f, dtype) != RMSNORM_OK)
+        return 0;
+    size_t most = 0;
+    for (int vec = 0; vec < 2; ++vec)
+        for (int dh = 0; dh < 2; ++dh) {
+            const RowKernels *k;
+            const void *fn;
+            int64_t grid;
+            if (bwd_plan(dtype, M, H, vec != 0, dh != 0, &k, &fn, &grid) != RMSNORM_OK)
+                return 0;
+            const size_t need = (size_t)grid * (size_t)H * sizeof(float);
+            most = need > most ? need : most;
+        }
+    return most;
+}
+
+const char *rmsnorm_status_string(int status)
+{
+    switch (status) {
+    case RMSNORM_OK: return "ok";
+    case RMSNORM_ERR_NULLPTR: return "a required pointer is NULL";
+    case RMSNORM_ERR_BAD_SHAPE: return "bad shape (M < 0, H < 1 or M*H too large)";
+    case RMSNORM_ERR_BAD_DTYPE: return "dtype is not RMSNORM_F32 or RMSNORM_BF16";
+    case RMSNORM_ERR_BAD_EPS: return "eps must be finite and >= 0";
+    case RMSNORM_ERR_MISALIGNED: return "pointer not aligned to its element size (workspace: 16 bytes)";
+    case RMSNORM_ERR_WORKSPACE: return "workspace missing or smaller than rmsnorm_bwd_workspace_bytes()";
+    case RMSNORM_ERR_UNSUPPORTED: return "H exceeds RMSNORM_MAX_H";
+    case RMSNORM_ERR_CUDA: return "a CUDA runtime call failed (see rmsnorm_last_cuda_error)";
+    case RMSNORM_ERR_ALIAS: return "output buffers overlap inputs or each other in a way not allowed";
+    default: return "unknown status";
+    }
+}
+
+int rmsnorm_last_cuda_error(void) { return t_last_cuda_error; }
+
+void rmsnorm_set_path_override(int path)
+{
+    g_path_override.store(path >= kPathAuto && path <= kPathScalar ? path : kPathAuto);
+}
+
+int rmsnorm_last_path(void) { return t_last_path; }
+
+} // extern "C"

@@ -1,0 +1,220 @@
+// common.cuh -- device helpers shared by the RMSNorm kernels: element packs
+// moved with one memory instruction, streaming loads/stores, bf16 <-> fp32,
+// lane-group reductions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsk {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------- memory ops
+// Row data is touched once per kernel: loads skip L1 allocation so the
+// weight (reused by every row) stays resident there. All are volatile asm so
+// the compiler keeps their program order (a thread always reads an element
+// before it overwrites it, which makes the documented in-place uses safe).
+
+__device__ __forceinline__ uint4 ld_row_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_row_b32(const void *p)
+{
+    uint32_t v;
+    asm volatile("ld.global.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t ld_row_b16(const void *p)
+{
+    uint16_t v;
+    asm volatile("ld.global.L1::no_allocate.b16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_row_v4(void *p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :
+                 : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_row_b32(void *p, uint32_t v)
+{
+    asm volatile("st.global.b32 [%0], %1;" : : "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_row_b16(void *p, uint16_t v)
+{
+    asm volatile("st.global.b16 [%0], %1;" : : "l"(p), "h"(v) : "memory");
+}
+
+// ------------------------------------------------------------ bf16 <-> fp32
+// bf16 is the upper half of an fp32 word, so widening is a shift.
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Two fp32 -> packed bf16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__device__ __forceinline__ uint16_t pack_bf16(float v)
+{
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t *>(&b);
+}
+
+// ----------------------------------------------------------------- packs
+// Pack<T, E>: E consecutive elements of T moved by one memory instruction
+// (E * sizeof(T) == 16 for the vectorised kernels, E == 1 for the scalar
+// ones). idx counts packs from `base`.
+template <typename T, int E> struct Pack;
+
+template <> struct Pack<bf16, 8> {
+    uint4 u;
+    static constexpr int E = 8;
+    __device__ __forceinline__ static Pack zero() { Pack p; p.u = make_uint4(0, 0, 0, 0); return p; }
+    __device__ __forceinline__ static Pack load(const void *base, int64_t idx)
+    {
+        Pack p; p.u = ld_row_v4(static_cast<const uint4 *>(base) + idx); return p;
+    }
+    __device__ __forceinline__ static Pack load_cached(const void *base, int64_t idx)
+    {
+        Pack p; p.u = __ldg(static_cast<const uint4 *>(base) + idx); return p;
+    }
+    __device__ __forceinline__ void store(void *base, int64_t idx) const
+    {
+        st_row_v4(static_cast<uint4 *>(base) + idx, u);
+    }
+    __device__ __forceinline__ void to_float(float (&f)[8]) const
+    {
+        f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+        f[4] = bf16lo(u.z); f[5] = bf16hi(u.z); f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+    }
+    __device__ __forceinline__ static Pack from_float(const float (&f)[8])
+    {
+        Pack p;
+        p.u.x = pack_bf16x2(f[0], f[1]); p.u.y = pack_bf16x2(f[2], f[3]);
+        p.u.z = pack_bf16x2(f[4], f[5]); p.u.w = pack_bf16x2(f[6], f[7]);
+        return p;
+    }
+};
+
+template <> struct Pack<bf16, 1> {
+    uint16_t u;
+    static constexpr int E = 1;
+    __device__ __forceinline__ static Pack zero() { Pack p; p.u = 0; return p; }
+    __device__ __forceinline__ static Pack load(const void *base, int64_t idx)
+    {
+        Pack p; p.u = ld_row_b16(static_cast<const uint16_t *>(base) + idx); return p;
+    }
+    __device__ __forceinline__ static Pack load_cached(const void *base, int64_t idx)
+    {
+        Pack p; p.u = __ldg(static_cast<const unsigned short *>(base) + idx); return p;
+    }
+    __device__ __forceinline__ void store(void *base, int64_t idx) const
+    {
+        st_row_b16(static_cast<uint16_t *>(base) + idx, u);
+    }
+    __device__ __forceinline__ void to_float(float (&f)[1]) const { f[0] = bf16lo(u); }
+    __device__ __forceinline__ static Pack from_float(const float (&f)[1])
+    {
+        Pack p; p.u = pack_bf16(f[0]); return p;
+    }
+};
+
+template <> struct Pack<float, 4> {
+    uint4 u;
+    static constexpr int E = 4;
+    __device__ __forceinline__ static Pack zero() { Pack p; p.u = make_uint4(0, 0, 0, 0); return p; }
+    __device__ __forceinline__ static Pack load(const void *base, int64_t idx)
+    {
+        Pack p; p.u = ld_row_v4(static_cast<const uint4 *>(base) + idx); return p;
+    }
+    __device__ __forceinline__ static Pack load_cached(const void *base, int64_t idx)
+    {
+        Pack p; p.u = __ldg(static_cast<const uint4 *>(base) + idx); return p;
+    }
+    __device__ __forceinline__ void store(void *base, int64_t idx) const
+    {
+        st_row_v4(static_cast<uint4 *>(base) + idx, u);
+    }
+    __device__ __forceinline__ void to_float(float (&f)[4]) const
+    {
+        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    }
+    __device__ __forceinline__ static Pack from_float(const float (&f)[4])
+    {
+        Pack p;
+        p.u = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                         __float_as_uint(f[2]), __float_as_uint(f[3]));
+        return p;
+    }
+};
+
+template <> struct Pack<float, 1> {
+    uint32_t u;
+    static constexpr int E = 1;
+    __device__ __forceinline__ static Pack zero() { Pack p; p.u = 0; return p; }
+    __device__ __forceinline__ static Pack load(const void *base, int64_t idx)
+    {
+        Pack p; p.u = ld_row_b32(static_cast<const uint32_t *>(base) + idx); return p;
+    }
+    __device__ __forceinline__ static Pack load_cached(const void *base, int64_t idx)
+    {
+        Pack p; p.u = __ldg(static_cast<const unsigned int *>(base) + idx); return p;
+    }
+    __device__ __forceinline__ void store(void *base, int64_t idx) const
+    {
+        st_row_b32(static_cast<uint32_t *>(base) + idx, u);
+    }
+    __device__ __forceinline__ void to_float(float (&f)[1]) const { f[0] = __uint_as_float(u); }
+    __device__ __forceinline__ static Pack from_float(const float (&f)[1])
+    {
+        Pack p; p.u = __float_as_uint(f[0]); return p;
+    }
+};
+
+// ------------------------------------------------------------ reductions
+// Butterfly sum over groups of N adjacent lanes (N a power of two <= 32).
+// Every lane of a group ends with bit-identical sums: each step adds the
+// same two values in either order, and fp32 addition is commutative.
+template <int N>
+__device__ __forceinline__ float group_allreduce(float v)
+{
+#pragma unroll
+    for (int o = N / 2; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------- launch ordering
+// Programmatic dependent launch: a kernel launched with the
+// programmatic-serialization attribute may start while the previous kernel
+// on the stream finishes; griddep_wait() blocks until that kernel has
+// completed and its memory is visible. griddep_launch_dependents() lets the
+// next such kernel be scheduled early. Both are no-ops without the attribute.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
+} // namespace rmsk

@@ -1,0 +1,50 @@
+// params.h -- kernel argument blocks, passed by value; shared by the
+// kernels and the host code that launches them.
+#pragma once
+
+#include <stdint.h>
+
+namespace rmsk {
+
+// Row-wise forward (rows.cuh).
+struct FwdParams {
+    const void *x;   // [M,H]
+    const void *r;   // [M,H] residual input (residual variant), else unused
+    const void *w;   // [H]
+    void *y;         // [M,H]
+    void *h;         // [M,H] residual sum out (residual variant), else unused
+    float *rstd;     // [M] or nullptr
+    int64_t M;
+    int H;
+    float eps;
+};
+
+// Row-wise backward (rows.cuh).
+struct BwdParams {
+    const void *dy;     // [M,H]
+    const void *x;      // [M,H] (h for the residual variant)
+    const void *w;      // [H]
+    const float *rstd;  // [M] or nullptr (recompute)
+    const void *dh;     // [M,H] incoming residual-stream gradient, or unused
+    void *dx;           // [M,H]
+    float *part;        // [gridDim.x, H] fp32 partial dw rows
+    int64_t M;
+    int H;
+    float eps;
+};
+
+// Split-row forward (split.cuh).
+struct SplitParams {
+    const void *x;   // [M,H]
+    const void *r;   // [M,H] residual input (residual variant), else unused
+    const void *w;   // [H]
+    void *y;         // [M,H]
+    void *h;         // [M,H] residual sum out (residual variant), else unused
+    float *rstd;     // [M] or nullptr
+    int H;           // features per row
+    int NV;          // packs per row
+    int SV;          // packs per CTA (the last ranks may hold fewer or none)
+    float eps;
+};
+
+} // namespace rmsk

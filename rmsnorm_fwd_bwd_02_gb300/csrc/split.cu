@@ -1,0 +1,11 @@
+// Split-row (cluster) forward kernels, both element types, vectorised and
+// scalar.
+#include "registry.h"
+#include "split.cuh"
+
+namespace rmsk {
+RMSK_SPLIT(split_bf16_v, bf16, 8)
+RMSK_SPLIT(split_bf16_s, bf16, 1)
+RMSK_SPLIT(split_f32_v, float, 4)
+RMSK_SPLIT(split_f32_s, float, 1)
+} // namespace rmsk

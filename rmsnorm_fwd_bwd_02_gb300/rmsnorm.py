@@ -1,0 +1,194 @@
+"""Thin ctypes binding over librmsnorm.so (C ABI in include/rmsnorm.h).
+
+Same entry-point names as the C ABI. Argument marshalling only: tensors are
+checked (CUDA, contiguous, dtype, shape), outputs that the caller did not
+pass are allocated with torch, and raw device pointers plus the current torch
+CUDA stream are handed to the library. Every arithmetic step runs in the
+CUDA kernels. If the library has not been built this module raises at load
+time; there is no fallback.
+"""
+import ctypes
+import os
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "librmsnorm.so")
+
+RMSNORM_F32, RMSNORM_BF16 = 0, 1
+DTYPES = {torch.float32: RMSNORM_F32, torch.bfloat16: RMSNORM_BF16}
+MAX_H = 16384
+PATH_AUTO, PATH_ROWS, PATH_SPLIT, PATH_SCALAR = 0, 1, 2, 3
+
+# Entry points of include/rmsnorm.h with their ctypes signatures.
+_i64, _vp, _sz, _int, _f = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
+                            ctypes.c_int, ctypes.c_float)
+SIGNATURES = {
+    "rmsnorm_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _f, _int, _vp]),
+    "rmsnorm_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64,
+                           _f, _int, _vp]),
+    "rmsnorm_residual_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                    _f, _int, _vp]),
+    "rmsnorm_residual_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _sz, _i64, _i64, _f, _int, _vp]),
+    "rmsnorm_bwd_workspace_bytes": (_sz, [_i64, _i64, _int]),
+    "rmsnorm_status_string": (ctypes.c_char_p, [_int]),
+    "rmsnorm_last_cuda_error": (_int, []),
+    "rmsnorm_set_path_override": (None, [_int]),
+    "rmsnorm_last_path": (_int, []),
+}
+
+
+class RmsNormError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = lib().rmsnorm_status_string(status).decode()
+        if status == -8:
+            msg += f" (cudaError {lib().rmsnorm_last_cuda_error()})"
+        super().__init__(f"{where}: status {status}: {msg}")
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(there is no CPU fallback)")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(status, where):
+    if status != 0:
+        raise RmsNormError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _rows(name, t, H, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.shape[-1] != H:
+        raise ValueError(f"{name} last dim must be {H}")
+    return t.numel() // H if H else 0
+
+
+def _dtype_code(t):
+    if t.dtype not in DTYPES:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return DTYPES[t.dtype]
+
+
+def set_path_override(path: int):
+    lib().rmsnorm_set_path_override(int(path))
+
+
+def last_path() -> int:
+    return lib().rmsnorm_last_path()
+
+
+def bwd_workspace_bytes(M: int, H: int, dtype: torch.dtype) -> int:
+    return lib().rmsnorm_bwd_workspace_bytes(int(M), int(H), DTYPES[dtype])
+
+
+def rmsnorm_fwd(x, w, y=None, rstd=None, eps=1e-6, want_rstd=True, stream=None):
+    """y = RMSNorm(x) * w over the last dim; returns (y, rstd or None)."""
+    H = w.numel()
+    M = _rows("x", x, H)
+    _rows("w", w.view(-1), H, x.dtype)
+    if y is None:
+        y = torch.empty_like(x)
+    _rows("y", y, H, x.dtype)
+    if rstd is None and want_rstd:
+        rstd = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32)
+    if rstd is not None and rstd.dtype != torch.float32:
+        raise ValueError("rstd must be float32")
+    _check(lib().rmsnorm_fwd(_ptr(x), _ptr(w), _ptr(y), _ptr(rstd), M, H,
+                             float(eps), _dtype_code(x), _stream(stream)),
+           "rmsnorm_fwd")
+    return y, rstd
+
+
+def rmsnorm_bwd(dy, x, w, rstd=None, dx=None, dw=None, workspace=None,
+                eps=1e-6, stream=None):
+    """(dx, dw) of the RMSNorm; rstd=None recomputes it from x."""
+    H = w.numel()
+    M = _rows("x", x, H)
+    _rows("dy", dy, H, x.dtype)
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        dw = torch.empty(H, device=x.device, dtype=torch.float32)
+    need = bwd_workspace_bytes(M, H, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=x.device, dtype=torch.uint8)
+    _check(lib().rmsnorm_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx),
+                             _ptr(dw), _ptr(workspace), workspace.numel()
+                             * workspace.element_size(), M, H, float(eps),
+                             _dtype_code(x), _stream(stream)), "rmsnorm_bwd")
+    return dx, dw
+
+
+def rmsnorm_residual_fwd(x, r, w, h=None, y=None, rstd=None, eps=1e-6,
+                         want_rstd=True, stream=None):
+    """h = x + r (rounded to the dtype), y = RMSNorm(h) * w; returns
+    (h, y, rstd or None)."""
+    H = w.numel()
+    M = _rows("x", x, H)
+    _rows("r", r, H, x.dtype)
+    if h is None:
+        h = torch.empty_like(x)
+    if y is None:
+        y = torch.empty_like(x)
+    if rstd is None and want_rstd:
+        rstd = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32)
+    _check(lib().rmsnorm_residual_fwd(_ptr(x), _ptr(r), _ptr(w), _ptr(h),
+                                      _ptr(y), _ptr(rstd), M, H, float(eps),
+                                      _dtype_code(x), _stream(stream)),
+           "rmsnorm_residual_fwd")
+    return h, y, rstd
+
+
+def rmsnorm_residual_bwd(dy, dh_out, h, w, rstd=None, dx=None, dw=None,
+                         workspace=None, eps=1e-6, stream=None):
+    """(dx, dw): dx is the gradient of both the input and the residual."""
+    H = w.numel()
+    M = _rows("h", h, H)
+    _rows("dy", dy, H, h.dtype)
+    if dh_out is not None:
+        _rows("dh_out", dh_out, H, h.dtype)
+    if dx is None:
+        dx = torch.empty_like(h)
+    if dw is None:
+        dw = torch.empty(H, device=h.device, dtype=torch.float32)
+    need = bwd_workspace_bytes(M, H, h.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=h.device, dtype=torch.uint8)
+    _check(lib().rmsnorm_residual_bwd(
+        _ptr(dy), _ptr(dh_out), _ptr(h), _ptr(w), _ptr(rstd), _ptr(dx),
+        _ptr(dw), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        M, H, float(eps), _dtype_code(h), _stream(stream)),
+        "rmsnorm_residual_bwd")
+    return dx, dw

@@ -1,0 +1,162 @@
+"""CPU tier: the C-ABI library loads, exports every entry point that
+include/rmsnorm.h declares, and rejects bad arguments on the host before any
+CUDA call (no GPU needed; no compute is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from rmsnorm_fwd_bwd_02_gb300 import rmsnorm as rn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
+
+OK, NULLPTR, BAD_SHAPE, BAD_DTYPE, BAD_EPS, MISALIGNED, WORKSPACE, \
+    UNSUPPORTED, CUDA, ALIAS = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+F32, BF16 = 0, 1
+NAN = float("nan")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(rn.LIB_PATH):
+        from rmsnorm_fwd_bwd_02_gb300 import build
+        build.build()
+    return rn.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rmsnorm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_four_entry_points():
+    names = declared_functions()
+    for n in ("rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_residual_fwd",
+              "rmsnorm_residual_bwd"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in rmsnorm.h but not exported"
+        assert n in rn.SIGNATURES, f"{n} has no ctypes signature in the binding"
+
+
+def test_status_strings(lib):
+    for code in (OK, NULLPTR, BAD_SHAPE, BAD_DTYPE, BAD_EPS, MISALIGNED,
+                 WORKSPACE, UNSUPPORTED, CUDA, ALIAS):
+        s = lib.rmsnorm_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.rmsnorm_status_string(12345).decode() == "unknown status"
+
+
+# Fake device addresses: the checks below all fail on the host, before the
+# library touches CUDA, so nothing is dereferenced.
+A = 0x7f0000000000
+B = 0x7f0100000000
+C = 0x7f0200000000
+D = 0x7f0300000000
+
+
+def fwd(lib, x=A, w=B, y=C, rstd=D, M=4, H=8, eps=1e-6, dtype=BF16):
+    return lib.rmsnorm_fwd(x, w, y, rstd, M, H, eps, dtype, None)
+
+
+def test_fwd_argument_checks(lib):
+    assert fwd(lib, dtype=7) == BAD_DTYPE
+    assert fwd(lib, M=-1) == BAD_SHAPE
+    assert fwd(lib, H=0) == BAD_SHAPE
+    assert fwd(lib, H=16385) == UNSUPPORTED
+    assert fwd(lib, M=2 ** 62) == BAD_SHAPE
+    for e in (NAN, -1e-6, float("inf")):
+        assert fwd(lib, eps=e) == BAD_EPS
+    assert fwd(lib, x=None) == NULLPTR
+    assert fwd(lib, w=None) == NULLPTR
+    assert fwd(lib, y=None) == NULLPTR
+    assert fwd(lib, x=A + 1) == MISALIGNED           # bf16 needs 2-byte
+    assert fwd(lib, x=A + 2, dtype=F32) == MISALIGNED
+    assert fwd(lib, rstd=D + 2) == MISALIGNED
+    # y overlapping x partially (not the same buffer) is rejected ...
+    assert fwd(lib, y=A + 2) == ALIAS
+    # ... rstd inside y too
+    assert fwd(lib, rstd=C + 4) == ALIAS
+    # nothing to do for M == 0, even with NULL pointers
+    assert fwd(lib, x=None, w=None, y=None, rstd=None, M=0) == OK
+
+
+def test_residual_fwd_argument_checks(lib):
+    f = lib.rmsnorm_residual_fwd
+    E = 0x7f0400000000
+    F = 0x7f0500000000
+    assert f(A, B, C, D, E, F, 4, 8, 1e-6, BF16 + 5, None) == BAD_DTYPE
+    assert f(A, None, C, D, E, F, 4, 8, 1e-6, BF16, None) == NULLPTR
+    # y may not alias anything, h may not partially overlap x
+    assert f(A, B, C, D, A, F, 4, 8, 1e-6, BF16, None) == ALIAS
+    assert f(A, B, C, A + 2, E, F, 4, 8, 1e-6, BF16, None) == ALIAS
+    assert f(A, B, C, D, E, F + 1, 4, 8, 1e-6, BF16, None) == MISALIGNED
+
+
+def test_bwd_argument_checks(lib):
+    f = lib.rmsnorm_bwd
+    E = 0x7f0400000000
+    W = 0x7f0500000000
+    # dy x w rstd dx dw ws
+    assert f(A, B, C, D, E, None, W, 1 << 20, 4, 8, 1e-6, BF16, None) == NULLPTR
+    assert f(None, B, C, D, E, 0x7f0600000000, W, 1 << 20, 4, 8, 1e-6, BF16,
+             None) == NULLPTR
+    assert f(A, B, C, D, E, 0x7f0600000000, W + 8, 1 << 20, 4, 8, 1e-6, BF16,
+             None) == MISALIGNED    # workspace must be 16-byte aligned
+    assert f(A, B, C, D, E, 0x7f0600000002, W, 1 << 20, 4, 8, 1e-6, BF16,
+             None) == MISALIGNED    # dw is fp32
+    assert f(A, B, C, D, E, 0x7f0600000000, W, 1 << 20, 4, 8, -1.0, BF16,
+             None) == BAD_EPS
+    assert f(A, B, C, D, E, 0x7f0600000000, W, 1 << 20, -4, 8, 1e-6, BF16,
+             None) == BAD_SHAPE
+
+
+def test_workspace_query_without_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    assert lib.rmsnorm_bwd_workspace_bytes(1024, 4096, BF16) == 0
+    assert lib.rmsnorm_bwd_workspace_bytes(-1, 4096, BF16) == 0
+
+
+def test_path_override_roundtrip(lib):
+    lib.rmsnorm_set_path_override(2)
+    lib.rmsnorm_set_path_override(99)     # out of range: back to automatic
+    lib.rmsnorm_set_path_override(0)
+    assert lib.rmsnorm_last_path() in (0, 1, 2, 3)
+    assert lib.rmsnorm_last_cuda_error() >= 0
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(2, 8, dtype=torch.bfloat16)
+    w = torch.ones(8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        rn.rmsnorm_fwd(x, w)
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The CUDA path never imports, links, loads or calls the oracle."""
+    pkg = os.path.join(ROOT, "rmsnorm_fwd_bwd_02_gb300")
+    pat = re.compile(r"\b(import|from)\s+oracle\b|liboracle|oracle_\w+\s*\(|"
+                     r"oracle\.c\b|oracle/")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn), encoding="utf-8").read()
+                m = pat.search(text)
+                assert m is None, f"{fn} refers to the oracle: {m.group(0)!r}"
+
+
+def test_ctypes_loads_standalone():
+    # a fresh handle to the same file loads too (no hidden state needed)
+    l2 = ctypes.CDLL(rn.LIB_PATH)
+    assert hasattr(l2, "rmsnorm_fwd")
