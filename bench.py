@@ -486,12 +486,17 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--rows", type=int, default=0,
+                    help="run the workload with this many rows (profiling a "
+                         "smaller case); the default is the workload's own M")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     wl = W.WORKLOADS[args.workload]
+    if args.rows:
+        wl = wl.with_rows(args.rows)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)
