@@ -62,7 +62,10 @@ typedef enum {
                                      rmsnorm_bwd_workspace_bytes() */
     RMSNORM_ERR_UNSUPPORTED = -7, /* H > RMSNORM_MAX_H */
     RMSNORM_ERR_CUDA = -8,        /* a CUDA runtime call failed */
-    RMSNORM_ERR_ALIAS = -9        /* buffers overlap in a way not allowed */
+    RMSNORM_ERR_ALIAS = -9,       /* buffers overlap in a way not allowed */
+    RMSNORM_ERR_SCRATCH_LIMIT = -10 /* rmsnorm_bwd_static_scratch: the problem
+                                       needs more scratch than the library's
+                                       built-in RMSNORM_STATIC_SCRATCH_BYTES */
 } rmsnorm_status;
 
 /* Largest feature count the kernels hold in registers ([P1 §7.1] puts the
@@ -162,6 +165,37 @@ void rmsnorm_set_path_override(int path);
 /* Which kernel family the last forward/backward call on this thread used:
  * 1 row-wise vectorised, 2 split-row, 3 row-wise scalar, 0 none. */
 int rmsnorm_last_path(void);
+
+/*
+ * Backward that allocates nothing and needs no workspace from the caller.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc at all: plug-ins hosted by a runtime that owns
+ * every byte of device memory and forbids its guests to allocate, and
+ * latency-critical loops that cannot tolerate the device-wide
+ * synchronisation cudaMalloc and cudaFree may imply.
+ *
+ * Same arguments, results and errors as rmsnorm_bwd without `workspace` and
+ * `workspace_bytes`: the per-CTA partial dw rows go to a scratch array of
+ * RMSNORM_STATIC_SCRATCH_BYTES that the library itself holds in device
+ * memory (a file-scope __device__ array). Every GPU that loads the library
+ * keeps that array until the process exits.
+ *  - Size limit: a call whose rmsnorm_bwd_workspace_bytes(M, H, dtype)
+ *    exceeds RMSNORM_STATIC_SCRATCH_BYTES is rejected with
+ *    RMSNORM_ERR_SCRATCH_LIMIT before anything is launched (for H <= 16384
+ *    on a 152-SM GB300 the need is at most about 10 MiB).
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress) with that device current; make that
+ *    first call before any stream capture.
+ *  - Sharing: all calls, on every stream and thread, share the one array.
+ *    Calls whose executions overlap on the GPU race on it and give wrong dw;
+ *    serialise them (one stream, or events). Nothing in it needs clearing
+ *    between calls: each call writes every partial row it later reads.
+ */
+#define RMSNORM_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+int rmsnorm_bwd_static_scratch(const void *dy, const void *x, const void *w,
+                               const float *rstd, void *dx, float *dw,
+                               int64_t M, int64_t H, float eps, int dtype,
+                               void *stream);
 
 #ifdef __cplusplus
 }

@@ -416,6 +416,8 @@ const char *rmsnorm_status_string(int status)
     case RMSNORM_ERR_UNSUPPORTED: return "H exceeds RMSNORM_MAX_H";
     case RMSNORM_ERR_CUDA: return "a CUDA runtime call failed (see rmsnorm_last_cuda_error)";
     case RMSNORM_ERR_ALIAS: return "output buffers overlap inputs or each other in a way not allowed";
+    case RMSNORM_ERR_SCRATCH_LIMIT:
+        return "problem needs more scratch than RMSNORM_STATIC_SCRATCH_BYTES (use rmsnorm_bwd with a workspace)";
     default: return "unknown status";
     }
 }
@@ -430,3 +432,57 @@ void rmsnorm_set_path_override(int path)
 int rmsnorm_last_path(void) { return t_last_path; }
 
 } // extern "C"
+
+// ============================================ backward with built-in scratch
+// For callers that cannot allocate device memory (see rmsnorm.h): the dw
+// partial rows live in this file-scope device array instead of a
+// caller-provided workspace. Host code must not use the array's name as a
+// pointer (on the host it is only a stand-in); the device address comes
+// from cudaGetSymbolAddress, looked up once per device on first use.
+namespace {
+
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) unsigned char g_static_scratch[RMSNORM_STATIC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device.
+int static_scratch_address(void **out)
+{
+    int dev, st;
+    if ((st = current_device(&dev)))
+        return st;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cuda_fail(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> g(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return RMSNORM_OK;
+}
+
+} // namespace
+
+extern "C" int rmsnorm_bwd_static_scratch(const void *dy, const void *x, const void *w,
+                                          const float *rstd, void *dx, float *dw, int64_t M,
+                                          int64_t H, float eps, int dtype, void *stream)
+{
+    int st = check_common(M, H, eps, dtype);
+    if (st)
+        return st;
+    // The bound covers every kernel variant this call could take. (Without a
+    // device the query gives 0 and the address lookup below reports it.)
+    if (rmsnorm_bwd_workspace_bytes(M, H, dtype) > RMSNORM_STATIC_SCRATCH_BYTES)
+        return RMSNORM_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    if ((st = static_scratch_address(&scratch)))
+        return st;
+    return bwd_impl(dy, nullptr, x, w, rstd, dx, dw, scratch, RMSNORM_STATIC_SCRATCH_BYTES, M,
+                    H, eps, dtype, static_cast<cudaStream_t>(stream));
+}

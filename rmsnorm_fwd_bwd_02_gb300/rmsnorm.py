@@ -36,6 +36,8 @@ SIGNATURES = {
     "rmsnorm_last_cuda_error": (_int, []),
     "rmsnorm_set_path_override": (None, [_int]),
     "rmsnorm_last_path": (_int, []),
+    "rmsnorm_bwd_static_scratch": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                          _i64, _f, _int, _vp]),
 }
 
 
@@ -191,4 +193,28 @@ def rmsnorm_residual_bwd(dy, dh_out, h, w, rstd=None, dx=None, dw=None,
         _ptr(dw), _ptr(workspace), workspace.numel() * workspace.element_size(),
         M, H, float(eps), _dtype_code(h), _stream(stream)),
         "rmsnorm_residual_bwd")
+    return dx, dw
+
+
+STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def rmsnorm_bwd_static_scratch(dy, x, w, rstd=None, dx=None, dw=None, eps=1e-6,
+                               stream=None):
+    """(dx, dw) like rmsnorm_bwd, but the library keeps the dw partial rows
+    in its own fixed device array instead of a workspace, so the call itself
+    allocates nothing (outputs the caller does not pass are still allocated
+    here by torch). For callers that cannot allocate device memory; calls
+    that overlap on the GPU share that array and race (see rmsnorm.h)."""
+    H = w.numel()
+    M = _rows("x", x, H)
+    _rows("dy", dy, H, x.dtype)
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        dw = torch.empty(H, device=x.device, dtype=torch.float32)
+    _check(lib().rmsnorm_bwd_static_scratch(
+        _ptr(dy), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw), M, H,
+        float(eps), _dtype_code(x), _stream(stream)),
+        "rmsnorm_bwd_static_scratch")
     return dx, dw
