@@ -70,15 +70,24 @@ def read_peaks():
 
 
 L2_BYTES = 129 * 2 ** 20
+EVERY = 8        # per-call CUDA events on one step in EVERY (see run_ours)
+
+
+def streams_from_hbm(wl):
+    """True when one step's row tensors exceed the L2 cache, so each step
+    streams from HBM."""
+    fwd_b, bwd_b = step_bytes(wl)
+    return fwd_b + bwd_b > L2_BYTES
 
 
 def buffer_sets(wl):
-    """Rotating buffer sets: three for workloads whose row tensors exceed L2
-    (each step then streams from HBM); enough to cycle through more than
-    twice the L2 size otherwise (decode-sized workloads stay launch-bound)."""
-    x_bytes = wl.M * wl.H * wl.elem_bytes
-    if x_bytes >= L2_BYTES:
+    """Rotating buffer sets: three when a step's tensors exceed L2 (each step
+    then streams from HBM; three sets keep any leftovers of the previous
+    step out of reach), else enough to cycle through twice the L2 size
+    (decode-sized steps stay launch-bound)."""
+    if streams_from_hbm(wl):
         return 3
+    x_bytes = wl.M * wl.H * wl.elem_bytes
     return int(min(64, max(3, -(-2 * L2_BYTES // max(x_bytes, 1)))))
 
 
@@ -86,6 +95,25 @@ def base_config(wl):
     return {"workload": wl.name, "M": wl.M, "H": wl.H, "eps": wl.eps,
             "dtype": str(wl.dtype).replace("torch.", ""),
             "step": "fwd+bwd" if wl.backward else "fwd"}
+
+
+def reduce_max(value, dist):
+    """Max of a float over all ranks (replicas time independently; the job
+    takes as long as its slowest rank). NCCL reduces on the GPU, gloo on the
+    CPU."""
+    if dist is None:
+        return float(value)
+    on_gpu = dist.get_backend() == "nccl"
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=torch.device("cuda", torch.cuda.current_device())
+                     if on_gpu else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step, world, ms_per_step):
+    """GB/s of all ranks' steps over the max-over-ranks step time."""
+    return bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------- clocks
@@ -186,7 +214,8 @@ def cpu_baseline(wl, inp, budget_s=12.0):
     fwd_b, bwd_b = step_bytes(wl.with_rows(rows))
     return {"value": round((fwd_b + bwd_b) / secs / 1e9, 4), "unit": "GB/s",
             "cores": 1, "kind": "oracle",
-            "sample": f"{rows} of {wl.M} rows of {wl.name} (H={wl.H}), fwd+bwd, "
+            "sample": f"{rows} of {wl.M} rows of {wl.name} (H={wl.H}), "
+                      f"{'fwd+bwd' if wl.backward else 'fwd'}, "
                       f"single-threaded fp64 oracle, {secs:.2f} s",
             "rows_per_s": round(rows / secs, 2)}
 
@@ -197,9 +226,10 @@ def run_reference(args, wl):
     if rank != 0:
         return 0
     inp = W.make_inputs(wl.with_rows(min(wl.M, 4096)))
-    probe = 16
+    probe = min(16, inp["x"].shape[0])
     t_row = time_oracle(wl, inp, probe) / probe
-    per_step = int(max(1, min(4096, 90.0 / max(args.steps + args.warmup, 1) / t_row)))
+    per_step = int(max(1, min(inp["x"].shape[0],
+                              90.0 / max(args.steps + args.warmup, 1) / t_row)))
     for _ in range(args.warmup):
         time_oracle(wl, inp, per_step)
     times = [time_oracle(wl, inp, per_step) for _ in range(args.steps)]
@@ -217,7 +247,8 @@ def run_reference(args, wl):
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                          "kind": "oracle",
                          "sample": f"{per_step} rows of {wl.name} per step "
-                                   f"(fwd+bwd), single-threaded fp64 oracle"},
+                                   f"({'fwd+bwd' if wl.backward else 'fwd'}), "
+                                   f"single-threaded fp64 oracle"},
         "e2e": {"value": round(value, 4), "unit": "GB/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -227,9 +258,11 @@ def run_reference(args, wl):
 
 # ---------------------------------------------------------------- GPU leg
 class Calls:
-    """Device buffers for one step and the two C-ABI calls of the step."""
+    """Device buffers for one step and the C-ABI calls of the step. The
+    ctypes arguments are marshalled once (bind), so a timed step costs the
+    host two or three foreign calls and nothing else."""
 
-    def __init__(self, rn, wl, src, dev, ws):
+    def __init__(self, rn, wl, src, dev, ws, w):
         self.rn, self.wl = rn, wl
         e = lambda: torch.empty(wl.M, wl.H, device=dev, dtype=wl.dtype)  # noqa: E731
         self.x = src["x"].to(dev)
@@ -241,26 +274,45 @@ class Calls:
         self.rstd = torch.empty(wl.M, device=dev)
         self.dw = torch.empty(wl.H, device=dev)
         self.ws = ws
+        self.w = w
+        self.bind(torch.cuda.current_stream())
 
-    def fwd(self, w):
-        rn, wl = self.rn, self.wl
+    def bind(self, stream):
+        """Marshal the C-ABI arguments for launches on `stream`."""
+        lib, wl = self.rn.lib(), self.wl
+        P = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        code = self.rn.DTYPES[wl.dtype]
+        s = stream.cuda_stream
+        ws_bytes = self.ws.numel()
         if wl.residual:
-            rn.rmsnorm_residual_fwd(self.x, self.r, w, h=self.h, y=self.y,
-                                    rstd=self.rstd, eps=wl.eps)
+            self._f = (lib.rmsnorm_residual_fwd,
+                       (P(self.x), P(self.r), P(self.w), P(self.h), P(self.y),
+                        P(self.rstd), wl.M, wl.H, wl.eps, code, s))
+            self._b = (lib.rmsnorm_residual_bwd,
+                       (P(self.dy), P(self.dh), P(self.h), P(self.w), P(self.rstd),
+                        P(self.dx), P(self.dw), P(self.ws), ws_bytes, wl.M, wl.H,
+                        wl.eps, code, s))
         else:
-            rn.rmsnorm_fwd(self.x, w, y=self.y, rstd=self.rstd, eps=wl.eps)
-
-    def bwd(self, w):
-        rn, wl = self.rn, self.wl
+            self._f = (lib.rmsnorm_fwd,
+                       (P(self.x), P(self.w), P(self.y), P(self.rstd), wl.M, wl.H,
+                        wl.eps, code, s))
+            self._b = (lib.rmsnorm_bwd,
+                       (P(self.dy), P(self.x), P(self.w), P(self.rstd), P(self.dx),
+                        P(self.dw), P(self.ws), ws_bytes, wl.M, wl.H, wl.eps, code, s))
         if not wl.backward:
-            return
-        if wl.residual:
-            rn.rmsnorm_residual_bwd(self.dy, self.dh, self.h, w, self.rstd,
-                                    dx=self.dx, dw=self.dw, workspace=self.ws,
-                                    eps=wl.eps)
-        else:
-            rn.rmsnorm_bwd(self.dy, self.x, w, self.rstd, dx=self.dx, dw=self.dw,
-                           workspace=self.ws, eps=wl.eps)
+            self._b = None
+
+    def _call(self, fa):
+        st = fa[0](*fa[1])
+        if st != 0:
+            raise self.rn.RmsNormError(st, fa[0].__name__)
+
+    def fwd(self):
+        self._call(self._f)
+
+    def bwd(self):
+        if self._b is not None:
+            self._call(self._b)
 
 
 def gpu_uuid():
@@ -292,7 +344,7 @@ def run_ours(args, wl):
                      device=dev, dtype=torch.uint8)
     x_bytes = wl.M * wl.H * wl.elem_bytes
     n_sets = buffer_sets(wl)
-    sets = [Calls(rn, wl, src, dev, ws) for _ in range(n_sets)]
+    sets = [Calls(rn, wl, src, dev, ws, w) for _ in range(n_sets)]
     fwd_b, bwd_b = step_bytes(wl)
 
     def barrier():
@@ -300,11 +352,42 @@ def run_ours(args, wl):
             dist.barrier()
         torch.cuda.synchronize()
 
+    # Decode-sized steps are a few microseconds of GPU work, less than the
+    # host needs to issue them one by one; they are timed the way a decoder
+    # runs them, replayed from a CUDA graph of consecutive calls.
+    use_graph = fwd_b + bwd_b < 16 * 2 ** 20
+    graphs = []
+    if use_graph:
+        gstream = torch.cuda.Stream()
+        gstream.wait_stream(torch.cuda.current_stream())
+        for c in sets:
+            c.bind(gstream)
+        with torch.cuda.stream(gstream):
+            for i in range(n_sets):          # warm the library's caches
+                sets[i].fwd()
+                sets[i].bwd()
+        torch.cuda.synchronize()
+        per = min(args.steps, 64)
+        for n in sorted({per, args.steps % per} - {0}, reverse=True):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=gstream):
+                for i in range(n):
+                    sets[i % n_sets].fwd()
+                    sets[i % n_sets].bwd()
+            graphs.append((n, gr))
+        for c in sets:
+            c.bind(torch.cuda.current_stream())
+
     # warm-up: W steps
+    path_f = path_b = 0
     for i in range(args.warmup):
         c = sets[i % n_sets]
-        c.fwd(w)
-        c.bwd(w)
+        c.fwd()
+        path_f = rn.last_path()
+        c.bwd()
+        path_b = rn.last_path()
+    for n, gr in graphs:
+        gr.replay()
     barrier()
 
     sampler = ClockSampler(gpu_uuid()) if rank == 0 else None
@@ -312,19 +395,36 @@ def run_ours(args, wl):
         sampler.start()
         time.sleep(0.3)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
-          for _ in range(args.steps)]
+          for _ in range((args.steps + EVERY - 1) // EVERY)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier()
     t_wall0 = time.time()
     start.record(stream)
-    for i in range(args.steps):
-        c = sets[i % n_sets]
-        ev[i][0].record(stream)
-        c.fwd(w)
-        ev[i][1].record(stream)
-        c.bwd(w)
-        ev[i][2].record(stream)
+    if use_graph:
+        big_n, big = graphs[0]
+        for _ in range(args.steps // big_n):
+            big.replay()
+        for n, gr in graphs[1:]:
+            gr.replay()
+    else:
+        # Per-call events on every EVERY-th step only: an event between two
+        # launches stops the second from starting while the first drains
+        # (programmatic dependent launch), so instrumented steps run a little
+        # slower; the per-call averages come from them (conservative) and the
+        # other steps run as a caller would run them.
+        for i in range(args.steps):
+            c = sets[i % n_sets]
+            if i % EVERY == 0:
+                e = ev[i // EVERY]
+                e[0].record(stream)
+                c.fwd()
+                e[1].record(stream)
+                c.bwd()
+                e[2].record(stream)
+            else:
+                c.fwd()
+                c.bwd()
     end.record(stream)
     barrier()
     t_wall1 = time.time()
@@ -334,13 +434,14 @@ def run_ours(args, wl):
         sampler.stop()
         clocks = sampler.summary(t_wall0, t_wall1)
 
-    total_ms = start.elapsed_time(end)
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev] if wl.backward else [0.0]
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = reduce_max(start.elapsed_time(end), dist)
+    if use_graph:      # per-call times: the step time split by the byte shares
+        step = total_ms / args.steps
+        fwd_ms = [step * fwd_b / (fwd_b + bwd_b)]
+        bwd_ms = [step * bwd_b / (fwd_b + bwd_b)] if wl.backward else [0.0]
+    else:
+        fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        bwd_ms = [e[1].elapsed_time(e[2]) for e in ev] if wl.backward else [0.0]
     ms_step = total_ms / args.steps
 
     # ---- e2e: host buffers, copies inside the timed region
@@ -354,7 +455,7 @@ def run_ours(args, wl):
         return 0
 
     peak, peak_kind = read_peaks()
-    value = (fwd_b + bwd_b) * world / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(fwd_b + bwd_b, world, ms_step)
     fwd_avg = statistics.mean(fwd_ms)
     bwd_avg = statistics.mean(bwd_ms)
     dom_is_bwd = wl.backward and bwd_b >= fwd_b
@@ -370,9 +471,11 @@ def run_ours(args, wl):
                 "avg_ms": round(ms, 5),
                 "frac_of_nominal_8TBs": round(a / NOMINAL_HBM_GBS, 4)}
 
-    fwd_kernel = "rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd"
+    fam = {1: "rows", 2: "split", 3: "rows, scalar", 4: "stream"}
+    fwd_kernel = ("rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd") + \
+        f" (rms_fwd_{fam.get(path_f, 'rows').split(',')[0]})"
     bwd_kernel = ("rmsnorm_residual_bwd" if wl.residual else "rmsnorm_bwd") + \
-        " (rms_bwd_rows + dw_reduce)"
+        f" (rms_bwd_{fam.get(path_b, 'rows').split(',')[0]} + dw_reduce)"
     roofline = roof(dom_bytes, dom_ms, bwd_kernel if dom_is_bwd else fwd_kernel)
     roofline["achieved"] = round(achieved, 1)
     roofline["traffic"] = traffic
@@ -385,7 +488,7 @@ def run_ours(args, wl):
         "config": dict(base_config(wl), **{
             "l2": (f"inputs larger than L2: {n_sets} rotating buffer sets, "
                    f"{x_bytes / 1e6:.0f} MB per row tensor"
-                   if x_bytes >= L2_BYTES else
+                   if streams_from_hbm(wl) else
                    f"{n_sets} rotating buffer sets of {x_bytes / 1e6:.3f} MB per "
                    f"row tensor (L2-resident; launch-bound)"),
             "parallelism": "replicas" if world > 1 else "single"}),
@@ -396,6 +499,10 @@ def run_ours(args, wl):
         "roofline": roofline,
         "roofline_fwd": roof(fwd_b, fwd_avg, fwd_kernel),
         "gpu_launches": args.steps * (1 + (2 if wl.backward else 0)),
+        "timing": ("CUDA-graph replay of consecutive calls (decode-sized step)"
+                   if use_graph else
+                   f"value from events around all {args.steps} steps; per-call "
+                   f"times from events on every {EVERY}th step, launching stream"),
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": None,
@@ -415,7 +522,8 @@ def run_e2e(rn, wl, src, dev, ws, args, dist):
     each step copies its inputs host->device, runs fwd + bwd, and copies
     every result back (y, rstd, dx, dw and h)."""
     pin = {k: v.pin_memory() for k, v in src.items()}
-    c = Calls(rn, wl, src, dev, ws)
+    w = torch.empty_like(src["w"], device=dev)
+    c = Calls(rn, wl, src, dev, ws, w)
     outs = {"y": c.y, "rstd": c.rstd}
     if wl.backward:
         outs.update(dx=c.dx, dw=c.dw)
@@ -423,21 +531,20 @@ def run_e2e(rn, wl, src, dev, ws, args, dist):
         outs["h"] = c.h
     host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
                 for k, v in outs.items()}
-    ins = {"x": c.x, "w": None}
+    ins = {"x": c.x, "w": w}
     if wl.backward:
         ins["dy"] = c.dy
     if wl.residual:
         ins.update(r=c.r, dh=c.dh)
-    w = torch.empty_like(src["w"], device=dev)
     h2d = sum(pin[k].numel() * pin[k].element_size() for k in ins)
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
     stream = torch.cuda.current_stream()
 
     def step():
         for k in ins:
-            (w if k == "w" else ins[k]).copy_(pin[k], non_blocking=True)
-        c.fwd(w)
-        c.bwd(w)
+            ins[k].copy_(pin[k], non_blocking=True)
+        c.fwd()
+        c.bwd()
         for k, v in outs.items():
             host_out[k].copy_(v, non_blocking=True)
 
@@ -453,14 +560,10 @@ def run_e2e(rn, wl, src, dev, ws, args, dist):
         step()
     e.record(stream)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item())
+    ms = reduce_max(s.elapsed_time(e) / steps, dist)
     world = dist.get_world_size() if dist is not None else 1
     fwd_b, bwd_b = step_bytes(wl)
-    return {"value": round((fwd_b + bwd_b) * world / (ms * 1e-3) / 1e9, 1),
+    return {"value": round(whole_job_gbs(fwd_b + bwd_b, world, ms), 1),
             "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms, 4), "steps": steps,
             "rows_per_s": round(wl.M * world / (ms * 1e-3), 1)}

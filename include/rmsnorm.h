@@ -154,17 +154,29 @@ const char *rmsnorm_status_string(int status);
 int rmsnorm_last_cuda_error(void);
 
 /*
- * Test hook: force the forward kernel family for later calls in this
- * process. 0 = automatic (default), 1 = row-wise vectorised, 2 = split-row,
- * 3 = row-wise scalar (also used by the backward). Forcing a vectorised
- * family on rows that are not 16-byte aligned still takes the scalar one.
- * Not thread-safe against concurrent calls; intended for tests only.
+ * Test hook: force the kernel family for later calls in this process.
+ * 0 = automatic (default), 1 = row-wise vectorised, 2 = split-row (forward
+ * only; the backward then takes row-wise), 3 = row-wise scalar, 4 = streamed
+ * (rows staged through shared memory by bulk asynchronous copies; bf16 with
+ * H = 4096 or 5120 only, row-wise elsewhere). Forcing a vectorised family on
+ * rows that are not 16-byte aligned still takes the scalar one. Not
+ * thread-safe against concurrent calls; intended for tests only.
  */
 void rmsnorm_set_path_override(int path);
 
 /* Which kernel family the last forward/backward call on this thread used:
- * 1 row-wise vectorised, 2 split-row, 3 row-wise scalar, 0 none. */
+ * 1 row-wise vectorised, 2 split-row, 3 row-wise scalar, 4 streamed, 0 none. */
 int rmsnorm_last_path(void);
+
+/*
+ * Diagnostic (synchronous, not for the hot path): the number of waits in the
+ * streamed kernels on the current device that ran out of time (a bulk copy
+ * that never completed; the affected rows are then left unwritten and the
+ * results must not be used). *count receives the value; reset != 0 also sets
+ * it back to zero. Every wait is bounded at about one second, so a failed
+ * copy ends the kernel instead of hanging the GPU.
+ */
+int rmsnorm_wait_timeouts(unsigned int *count, int reset);
 
 /*
  * Backward that allocates nothing and needs no workspace from the caller.

@@ -20,7 +20,7 @@ using namespace rmsk;
 
 namespace {
 
-constexpr int kPathAuto = 0, kPathRows = 1, kPathSplit = 2, kPathScalar = 3;
+constexpr int kPathAuto = 0, kPathRows = 1, kPathSplit = 2, kPathScalar = 3, kPathStream = 4;
 constexpr int kSplitMaxRows = 64;      // decode-sized batches ([P2 §3.2])
 constexpr int kReduceCols = 32, kReduceRows = 16;
 
@@ -85,8 +85,9 @@ int sm_count(int dev, int *sms)
     return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e);
 }
 
-// Resident CTAs per SM for a kernel, cached per (kernel, device).
-int blocks_per_sm(const void *fn, int threads, int dev, int *out)
+// Resident CTAs per SM for a kernel, cached per (kernel, device). Kernels
+// with dynamic shared memory above the default limit are opted in first.
+int blocks_per_sm(const void *fn, int threads, int dev, int *out, int smem = 0)
 {
     static std::mutex mu;
     static std::map<std::pair<const void *, int>, int> cache;
@@ -99,7 +100,11 @@ int blocks_per_sm(const void *fn, int threads, int dev, int *out)
         }
     }
     int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0);
+    cudaError_t e = cudaSuccess;
+    if (smem > 48 * 1024)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
     if (e != cudaSuccess)
         return cuda_fail(e);
     if (n < 1)
@@ -111,7 +116,7 @@ int blocks_per_sm(const void *fn, int threads, int dev, int *out)
 }
 
 // Persistent grid: no more CTAs than tiles, no more than fit at once.
-int rows_grid(const RowKernels &k, const void *fn, int64_t M, int64_t *grid)
+int rows_grid(const RowShape &k, const void *fn, int64_t M, int64_t *grid)
 {
     int dev, sms, bps, st;
     if ((st = current_device(&dev)) || (st = sm_count(dev, &sms)) ||
@@ -121,6 +126,62 @@ int rows_grid(const RowKernels &k, const void *fn, int64_t M, int64_t *grid)
     const int64_t cap = (int64_t)bps * sms;
     *grid = tiles < cap ? tiles : cap;
     return RMSNORM_OK;
+}
+
+// Streamed kernels: one group of NG rows in flight per CTA iteration.
+int stream_grid(const StreamShape &k, const void *fn, int smem, int64_t M, int64_t *grid,
+                int *dev_out)
+{
+    int dev, sms, bps, st;
+    if ((st = current_device(&dev)) || (st = sm_count(dev, &sms)) ||
+        (st = blocks_per_sm(fn, k.threads(), dev, &bps, smem)))
+        return st;
+    const int64_t tiles = (M + k.NG - 1) / k.NG;
+    const int64_t cap = (int64_t)bps * sms;
+    *grid = tiles < cap ? tiles : cap;
+    *dev_out = dev;
+    return RMSNORM_OK;
+}
+
+// Shapes with a streamed layout, and whether the automatic choice takes it
+// (set from measurements on GB300: the faster kernel family per direction).
+// At M = 32768 x 4096 the backward takes 116.6 us streamed against 132.9 us
+// row-wise, the forward 85.5 us against 82.2 us; at 16384 x 5120 with the
+// residual the backward takes 95.9 us against 128.3 us, the forward 106.6 us
+// against 101.5 us.
+struct StreamPolicy {
+    const StreamKernels *k;
+    bool auto_fwd, auto_bwd;
+};
+
+const StreamPolicy *pick_stream(int dtype, int64_t H, bool vec)
+{
+    static const StreamPolicy h4096 = {&s_h4096, false, true};
+    static const StreamPolicy h5120 = {&s_h5120, false, true};
+    if (dtype != RMSNORM_BF16 || !vec)
+        return nullptr;
+    if (H == 4096)
+        return &h4096;
+    if (H == 5120)
+        return &h5120;
+    return nullptr;
+}
+
+cudaError_t launch2(const void *fn, dim3 grid, dim3 block, int smem, cudaStream_t s, void *a0,
+                    void *a1)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    void *args[2] = {a0, a1};
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 // -------------------------------------------------------- kernel choice
@@ -204,21 +265,43 @@ int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, floa
         const int V = (SV + NT - 1) / NT;   // <= 8 for H <= RMSNORM_MAX_H
         const void *fn = V == 1 ? (res ? k.v1_res : k.v1) : (res ? k.v8_res : k.v8);
         SplitParams p = {x, r, w, y, h, rstd, (int)H, NV, SV, eps};
-        cudaError_t e = launch(fn, dim3(K, (unsigned)M), dim3(NT), stream, &p, false, K);
+        cudaError_t e = launch(fn, dim3(K, (unsigned)M), dim3(NT), stream, &p, true, K);
         if (e != cudaSuccess)
             return cuda_fail(e);
         t_last_path = kPathSplit;
         return RMSNORM_OK;
     }
 
+    const StreamPolicy *sp = pick_stream(dtype, H, vec);
+    if (sp && (ov == kPathStream || (ov == kPathAuto && sp->auto_fwd))) {
+        const StreamKernels &k = *sp->k;
+        const void *fn = k.fwd[res ? 1 : 0];
+        const int smem = k.fwd_smem[res ? 1 : 0];
+        int64_t grid;
+        int dev;
+        int st = stream_grid(k.f, fn, smem, M, &grid, &dev);
+        if (st)
+            return st;
+        unsigned int *tmo = stream_timeout_counter(dev);
+        if (tmo == nullptr)
+            return cuda_fail(cudaErrorInvalidSymbol);
+        FwdParams p = {x, r, w, y, h, rstd, M, (int)H, eps};
+        cudaError_t e = launch2(fn, dim3((unsigned)grid), dim3(k.f.threads()), smem, stream, &p,
+                                &tmo);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+        t_last_path = kPathStream;
+        return RMSNORM_OK;
+    }
+
     const RowKernels &k = pick_rows(dtype, H, vec);
-    const void *fn = res ? k.fwd_res : k.fwd;
+    const void *fn = k.fwd[res ? 1 : 0];
     int64_t grid;
-    int st = rows_grid(k, fn, M, &grid);
+    int st = rows_grid(k.f, fn, M, &grid);
     if (st)
         return st;
     FwdParams p = {x, r, w, y, h, rstd, M, (int)H, eps};
-    cudaError_t e = launch(fn, dim3((unsigned)grid), dim3(k.threads()), stream, &p, false, 0);
+    cudaError_t e = launch(fn, dim3((unsigned)grid), dim3(k.f.threads()), stream, &p, true, 0);
     if (e != cudaSuccess)
         return cuda_fail(e);
     t_last_path = vec ? kPathRows : kPathScalar;
@@ -226,18 +309,50 @@ int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, floa
 }
 
 // ------------------------------------------------------------ backward
-// Grid (and so partial-row count) of the backward kernel for these args.
-int bwd_plan(int dtype, int64_t M, int64_t H, bool vec, bool dh, const RowKernels **kk,
-             const void **fn, int64_t *grid)
+struct BwdPlan {
+    const void *fn;
+    int threads;
+    int smem;
+    int64_t grid;     // CTAs, and so partial dw rows
+    bool stream;
+    bool vec;
+    unsigned int *timeouts;
+};
+
+// Kernel, grid (and so partial-row count) of the backward for these args.
+int bwd_plan(int dtype, int64_t M, int64_t H, bool vec, bool dh, bool have_rstd, int ov,
+             BwdPlan *pl)
 {
+    const StreamPolicy *sp = pick_stream(dtype, H, vec);
+    pl->vec = vec;
+    pl->timeouts = nullptr;
+    if (sp && (ov == kPathStream || (ov == kPathAuto && sp->auto_bwd))) {
+        const StreamKernels &k = *sp->k;
+        pl->fn = k.bwd[dh ? 1 : 0][have_rstd ? 1 : 0];
+        pl->threads = k.b.threads();
+        pl->smem = k.bwd_smem[dh ? 1 : 0][have_rstd ? 1 : 0];
+        pl->stream = true;
+        if (M == 0) {
+            pl->grid = 0;
+            return RMSNORM_OK;
+        }
+        int dev;
+        int st = stream_grid(k.b, pl->fn, pl->smem, M, &pl->grid, &dev);
+        if (st)
+            return st;
+        pl->timeouts = stream_timeout_counter(dev);
+        return pl->timeouts ? RMSNORM_OK : cuda_fail(cudaErrorInvalidSymbol);
+    }
     const RowKernels &k = pick_rows(dtype, H, vec);
-    *kk = &k;
-    *fn = dh ? k.bwd_dh : k.bwd;
+    pl->fn = k.bwd[dh ? 1 : 0][have_rstd ? 1 : 0];
+    pl->threads = k.b.threads();
+    pl->smem = 0;
+    pl->stream = false;
     if (M == 0) {
-        *grid = 0;
+        pl->grid = 0;
         return RMSNORM_OK;
     }
-    return rows_grid(k, *fn, M, grid);
+    return rows_grid(k.b, pl->fn, M, &pl->grid);
 }
 
 int bwd_impl(const void *dy, const void *dh, const void *x, const void *w, const float *rstd,
@@ -258,13 +373,12 @@ int bwd_impl(const void *dy, const void *dh, const void *x, const void *w, const
 
     const bool vec16 = (H * (int64_t)es) % 16 == 0 && aligned(dy, 16) && aligned(x, 16) &&
                        aligned(w, 16) && aligned(dx, 16) && aligned(dh, 16);
-    const bool vec = vec16 && g_path_override.load(std::memory_order_relaxed) != kPathScalar;
-    const RowKernels *k;
-    const void *fn;
-    int64_t grid;
-    if ((st = bwd_plan(dtype, M, H, vec, dh != nullptr, &k, &fn, &grid)))
+    const int ov = g_path_override.load(std::memory_order_relaxed);
+    const bool vec = vec16 && ov != kPathScalar;
+    BwdPlan pl;
+    if ((st = bwd_plan(dtype, M, H, vec, dh != nullptr, rstd != nullptr, ov, &pl)))
         return st;
-    const size_t need = (size_t)grid * (size_t)H * sizeof(float);
+    const size_t need = (size_t)pl.grid * (size_t)H * sizeof(float);
     if (need > 0 && (ws == nullptr || ws_bytes < need))
         return RMSNORM_ERR_WORKSPACE;
 
@@ -283,12 +397,16 @@ int bwd_impl(const void *dy, const void *dh, const void *x, const void *w, const
 
     if (M > 0) {
         BwdParams p = {dy, x, w, rstd, dh, dx, static_cast<float *>(ws), M, (int)H, eps};
-        cudaError_t e = launch(fn, dim3((unsigned)grid), dim3(k->threads()), stream, &p, false, 0);
+        cudaError_t e =
+            pl.stream ? launch2(pl.fn, dim3((unsigned)pl.grid), dim3(pl.threads), pl.smem, stream,
+                                &p, &pl.timeouts)
+                      : launch(pl.fn, dim3((unsigned)pl.grid), dim3(pl.threads), stream, &p,
+                               true, 0);
         if (e != cudaSuccess)
             return cuda_fail(e);
     }
     const float *part = static_cast<const float *>(ws);
-    int P = (int)grid, Hi = (int)H;
+    int P = (int)pl.grid, Hi = (int)H;
     struct {
         const float *part;
         int P, H;
@@ -308,7 +426,7 @@ int bwd_impl(const void *dy, const void *dh, const void *x, const void *w, const
         &cfg, (const void *)&dw_reduce<kReduceCols, kReduceRows>, args);
     if (e != cudaSuccess)
         return cuda_fail(e);
-    t_last_path = M == 0 ? 0 : (vec ? kPathRows : kPathScalar);
+    t_last_path = M == 0 ? 0 : (pl.stream ? kPathStream : (vec ? kPathRows : kPathScalar));
     return RMSNORM_OK;
 }
 
@@ -390,16 +508,16 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype)
     if (check_common(M, H, 0.f, dtype) != RMSNORM_OK)
         return 0;
     size_t most = 0;
-    for (int vec = 0; vec < 2; ++vec)
-        for (int dh = 0; dh < 2; ++dh) {
-            const RowKernels *k;
-            const void *fn;
-            int64_t grid;
-            if (bwd_plan(dtype, M, H, vec != 0, dh != 0, &k, &fn, &grid) != RMSNORM_OK)
-                return 0;
-            const size_t need = (size_t)grid * (size_t)H * sizeof(float);
-            most = need > most ? need : most;
-        }
+    for (int ov : {kPathAuto, kPathRows, kPathStream})
+        for (int vec = 0; vec < 2; ++vec)
+            for (int dh = 0; dh < 2; ++dh)
+                for (int hr = 0; hr < 2; ++hr) {
+                    BwdPlan pl;
+                    if (bwd_plan(dtype, M, H, vec != 0, dh != 0, hr != 0, ov, &pl) != RMSNORM_OK)
+                        return 0;
+                    const size_t need = (size_t)pl.grid * (size_t)H * sizeof(float);
+                    most = need > most ? need : most;
+                }
     return most;
 }
 
@@ -426,7 +544,23 @@ int rmsnorm_last_cuda_error(void) { return t_last_cuda_error; }
 
 void rmsnorm_set_path_override(int path)
 {
-    g_path_override.store(path >= kPathAuto && path <= kPathScalar ? path : kPathAuto);
+    g_path_override.store(path >= kPathAuto && path <= kPathStream ? path : kPathAuto);
+}
+
+int rmsnorm_wait_timeouts(unsigned int *count, int reset)
+{
+    if (count == nullptr)
+        return RMSNORM_ERR_NULLPTR;
+    int dev, st;
+    if ((st = current_device(&dev)))
+        return st;
+    unsigned int *p = stream_timeout_counter(dev);
+    if (p == nullptr)
+        return cuda_fail(cudaErrorInvalidSymbol);
+    cudaError_t e = cudaMemcpy(count, p, sizeof(unsigned int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && reset)
+        e = cudaMemset(p, 0, sizeof(unsigned int));
+    return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e);
 }
 
 int rmsnorm_last_path(void) { return t_last_path; }

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace rmsk {
 
 typedef __nv_bfloat16 bf16;
@@ -76,6 +78,46 @@ __device__ __forceinline__ uint16_t pack_bf16(float v)
     return *reinterpret_cast<uint16_t *>(&b);
 }
 
+// ------------------------------------------------------- packed fp32 math
+// The sm_100 family issues two fp32 operations per FFMA2 / FMUL2 / FADD2
+// instruction; pairs of a pack's elements are computed together. Packs of
+// one element use plain fp32. The overloads keep the kernels generic.
+__device__ __forceinline__ float2 vfma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float vfma(float a, float b, float c) { return fmaf(a, b, c); }
+__device__ __forceinline__ float2 vmul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float vmul(float a, float b) { return a * b; }
+__device__ __forceinline__ float2 vadd(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float vadd(float a, float b) { return a + b; }
+__device__ __forceinline__ float hsum(float2 a) { return a.x + a.y; }
+__device__ __forceinline__ float hsum(float a) { return a; }
+template <typename F> __device__ __forceinline__ F splat(float s);
+template <> __device__ __forceinline__ float2 splat<float2>(float s) { return make_float2(s, s); }
+template <> __device__ __forceinline__ float splat<float>(float s) { return s; }
+
+// The E elements of one pack widened to fp32: N lanes of F (float2 pairs
+// when E is even, one float otherwise).
+template <int E>
+struct Vals {
+    using F = typename std::conditional<E % 2 == 0, float2, float>::type;
+    static constexpr int N = E % 2 == 0 ? E / 2 : 1;
+    F v[N];
+    __device__ __forceinline__ static Vals zero()
+    {
+        Vals r;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            r.v[i] = splat<F>(0.f);
+        return r;
+    }
+    __device__ __forceinline__ float get(int e) const
+    {
+        if constexpr (E % 2 == 0)
+            return (e & 1) ? v[e >> 1].y : v[e >> 1].x;
+        else
+            return v[0];
+    }
+};
+
 // ----------------------------------------------------------------- packs
 // Pack<T, E>: E consecutive elements of T moved by one memory instruction
 // (E * sizeof(T) == 16 for the vectorised kernels, E == 1 for the scalar
@@ -110,6 +152,20 @@ template <> struct Pack<bf16, 8> {
         p.u.z = pack_bf16x2(f[4], f[5]); p.u.w = pack_bf16x2(f[6], f[7]);
         return p;
     }
+    __device__ __forceinline__ void widen(Vals<8> &f) const
+    {
+        f.v[0] = make_float2(bf16lo(u.x), bf16hi(u.x));
+        f.v[1] = make_float2(bf16lo(u.y), bf16hi(u.y));
+        f.v[2] = make_float2(bf16lo(u.z), bf16hi(u.z));
+        f.v[3] = make_float2(bf16lo(u.w), bf16hi(u.w));
+    }
+    __device__ __forceinline__ static Pack narrow(const Vals<8> &f)
+    {
+        Pack p;
+        p.u.x = pack_bf16x2(f.v[0].x, f.v[0].y); p.u.y = pack_bf16x2(f.v[1].x, f.v[1].y);
+        p.u.z = pack_bf16x2(f.v[2].x, f.v[2].y); p.u.w = pack_bf16x2(f.v[3].x, f.v[3].y);
+        return p;
+    }
 };
 
 template <> struct Pack<bf16, 1> {
@@ -132,6 +188,11 @@ template <> struct Pack<bf16, 1> {
     __device__ __forceinline__ static Pack from_float(const float (&f)[1])
     {
         Pack p; p.u = pack_bf16(f[0]); return p;
+    }
+    __device__ __forceinline__ void widen(Vals<1> &f) const { f.v[0] = bf16lo(u); }
+    __device__ __forceinline__ static Pack narrow(const Vals<1> &f)
+    {
+        Pack p; p.u = pack_bf16(f.v[0]); return p;
     }
 };
 
@@ -163,6 +224,18 @@ template <> struct Pack<float, 4> {
                          __float_as_uint(f[2]), __float_as_uint(f[3]));
         return p;
     }
+    __device__ __forceinline__ void widen(Vals<4> &f) const
+    {
+        f.v[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+        f.v[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+    }
+    __device__ __forceinline__ static Pack narrow(const Vals<4> &f)
+    {
+        Pack p;
+        p.u = make_uint4(__float_as_uint(f.v[0].x), __float_as_uint(f.v[0].y),
+                         __float_as_uint(f.v[1].x), __float_as_uint(f.v[1].y));
+        return p;
+    }
 };
 
 template <> struct Pack<float, 1> {
@@ -185,6 +258,11 @@ template <> struct Pack<float, 1> {
     __device__ __forceinline__ static Pack from_float(const float (&f)[1])
     {
         Pack p; p.u = __float_as_uint(f[0]); return p;
+    }
+    __device__ __forceinline__ void widen(Vals<1> &f) const { f.v[0] = __uint_as_float(u); }
+    __device__ __forceinline__ static Pack narrow(const Vals<1> &f)
+    {
+        Pack p; p.u = __float_as_uint(f.v[0]); return p;
     }
 };
 

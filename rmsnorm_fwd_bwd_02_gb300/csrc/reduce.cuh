@@ -20,6 +20,7 @@ dw_reduce(const float *__restrict__ part, int P, int H, float *__restrict__ dw)
     // Launched with programmatic serialization after the backward kernel:
     // wait until its partial rows are complete and visible.
     griddep_wait();
+    griddep_launch_dependents();
     const int tx = threadIdx.x % CW;
     const int ty = threadIdx.x / CW;
     const int col = blockIdx.x * CW + tx;

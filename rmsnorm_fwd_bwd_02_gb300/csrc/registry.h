@@ -1,23 +1,49 @@
 // registry.h -- the instantiated kernel configurations the C ABI dispatches
-// to. Each RowKernels entry is one row layout (see rows.cuh) with its four
-// kernels; each SplitKernels entry is one element type of the split-row
-// forward (see split.cuh).
+// to. A RowKernels entry pairs a forward layout and a backward layout (see
+// rows.cuh; the best shapes differ) with their kernels; a SplitKernels
+// entry is one element type of the split-row forward (see split.cuh).
 #pragma once
 
 namespace rmsk {
 
-struct RowKernels {
-    const char *name;
-    int E;       // elements per pack (8 bf16 / 4 fp32 vectorised, 1 scalar)
+struct RowShape {
     int L;       // lanes per row group
     int V;       // packs per lane
     int G;       // rows per group per iteration
     int S;       // row groups per CTA
     bool exact;  // H == L * V * E (no column masking)
-    const void *fwd, *fwd_res, *bwd, *bwd_dh;
     int threads() const { return L * S; }
     int tile_rows() const { return S * G; }
-    long long max_cols() const { return (long long)L * V * E; }
+};
+
+struct RowKernels {
+    const char *name;
+    int E;               // elements per pack (8 bf16 / 4 fp32 vectorised, 1 scalar)
+    RowShape f, b;       // forward and backward layouts
+    const void *fwd[2];      // [residual]
+    const void *bwd[2][2];   // [dh_out given][rstd given]
+    long long max_cols() const
+    {
+        const long long cf = (long long)f.L * f.V * E, cb = (long long)b.L * b.V * E;
+        return cf < cb ? cf : cb;
+    }
+};
+
+// A streamed (bulk-copy fed) layout: NG groups of GW warps per CTA, each
+// thread V packs of a row, NS stages per group (stream.cuh). bf16 only.
+struct StreamShape {
+    int GW, V, NG, NS;
+    int threads() const { return NG * GW * 32; }
+};
+
+struct StreamKernels {
+    const char *name;
+    int H;
+    StreamShape f, b;
+    const void *fwd[2];        // [residual]
+    int fwd_smem[2];
+    const void *bwd[2][2];     // [dh_out given][rstd given]
+    int bwd_smem[2][2];
 };
 
 struct SplitKernels {
@@ -27,7 +53,7 @@ struct SplitKernels {
 };
 
 // bf16, 16-byte packs. Named for the feature count they are shaped for
-// (hNNN, exact) or the largest pack count per row they cover (gNNN lanes x 4).
+// (hNNN, exact) or the lanes of their masked layouts (gNNN).
 extern const RowKernels b_h128, b_h896, b_h4096, b_h5120, b_g32, b_g128, b_g512;
 // bf16, one element per access (rows not 16-byte aligned, odd H)
 extern const RowKernels b_s32, b_s1024;
@@ -38,15 +64,39 @@ extern const RowKernels f_s32, f_s1024;
 
 extern const SplitKernels split_bf16_v, split_bf16_s, split_f32_v, split_f32_s;
 
+extern const StreamKernels s_h4096, s_h5120;
+// Device address of the counter of streamed-kernel waits that ran out.
+unsigned int *stream_timeout_counter(int dev);
+
 } // namespace rmsk
 
-#define RMSK_ROWS(NAME, T, E, L, V, G, S, MINB, EXACT)                             \
-    const RowKernels NAME = {                                                     \
-        #NAME, E, L, V, G, S, EXACT,                                              \
-        (const void *)&rms_fwd_rows<T, E, L, V, G, S, MINB, EXACT, false>,        \
-        (const void *)&rms_fwd_rows<T, E, L, V, G, S, MINB, EXACT, true>,         \
-        (const void *)&rms_bwd_rows<T, E, L, V, G, S, MINB, EXACT, false>,        \
-        (const void *)&rms_bwd_rows<T, E, L, V, G, S, MINB, EXACT, true>};
+// RMSK_ROWS(name, type, E, forward L V G S MINB exact, backward L V G S MINB exact)
+#define RMSK_ROWS(NAME, T, E, FL, FV, FG, FS, FMB, FEX, BL, BV, BG, BS, BMB, BEX)      \
+    const RowKernels NAME = {                                                        \
+        #NAME, E, {FL, FV, FG, FS, FEX}, {BL, BV, BG, BS, BEX},                      \
+        {(const void *)&rms_fwd_rows<T, E, FL, FV, FG, FS, FMB, FEX, false>,         \
+         (const void *)&rms_fwd_rows<T, E, FL, FV, FG, FS, FMB, FEX, true>},         \
+        {{(const void *)&rms_bwd_rows<T, E, BL, BV, BG, BS, BMB, BEX, false, false>, \
+          (const void *)&rms_bwd_rows<T, E, BL, BV, BG, BS, BMB, BEX, false, true>}, \
+         {(const void *)&rms_bwd_rows<T, E, BL, BV, BG, BS, BMB, BEX, true, false>,  \
+          (const void *)&rms_bwd_rows<T, E, BL, BV, BG, BS, BMB, BEX, true, true>}}};
+
+#define RMSK_STREAM(NAME, H, FGW, FV, FNG, FNS, BGW, BV, BNG, BNS)                       \
+    static_assert(32 * FGW * FV * 8 == H && 32 * BGW * BV * 8 == H, "stream layout");    \
+    const StreamKernels NAME = {                                                         \
+        #NAME, H, {FGW, FV, FNG, FNS}, {BGW, BV, BNG, BNS},                              \
+        {(const void *)&rms_fwd_stream<FGW, FV, FNG, FNS, false>,                        \
+         (const void *)&rms_fwd_stream<FGW, FV, FNG, FNS, true>},                        \
+        {StreamSmem<FGW, FV, FNG, FNS, 1, 1>::kBytes,                                    \
+         StreamSmem<FGW, FV, FNG, FNS, 2, 1>::kBytes},                                   \
+        {{(const void *)&rms_bwd_stream<BGW, BV, BNG, BNS, false, false>,                \
+          (const void *)&rms_bwd_stream<BGW, BV, BNG, BNS, false, true>},                \
+         {(const void *)&rms_bwd_stream<BGW, BV, BNG, BNS, true, false>,                 \
+          (const void *)&rms_bwd_stream<BGW, BV, BNG, BNS, true, true>}},                \
+        {{StreamSmem<BGW, BV, BNG, BNS, 2, 2>::kBytes,                                   \
+          StreamSmem<BGW, BV, BNG, BNS, 2, 1>::kBytes},                                  \
+         {StreamSmem<BGW, BV, BNG, BNS, 3, 2>::kBytes,                                   \
+          StreamSmem<BGW, BV, BNG, BNS, 3, 1>::kBytes}}};
 
 #define RMSK_SPLIT(NAME, T, E)                                                    \
     const SplitKernels NAME = {                                                   \

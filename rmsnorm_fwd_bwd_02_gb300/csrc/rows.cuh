@@ -14,6 +14,7 @@
 // loop; every thread of a CTA runs the same number of iterations, rows past
 // M are masked, so barriers and shuffles are always uniform.
 //
+// Arithmetic is fp32, two elements per FFMA2/FMUL2 instruction (Vals).
 // Reductions: fp32 partials per lane, then a butterfly over the group's
 // lanes (every lane ends with the same bits); groups wider than a warp add
 // the per-warp sums from shared memory in warp order. The order is fixed, so
@@ -24,10 +25,21 @@
 // order and writes one partial row to the workspace. A second kernel
 // (reduce.cuh) sums those rows in a fixed order ([P1 §5.4]: two passes, no
 // atomics), with P = number of CTAs rows instead of M.
+//
+// Launch order. Every kernel is launched with programmatic stream
+// serialization: it waits (griddep_wait) before its first global memory
+// access until the previous kernel on the stream has completed, and lets the
+// next kernel be scheduled once its own main loop is done.
 #pragma once
 
 #include "common.cuh"
 #include "params.h"
+
+// Tuning knob (measured on GB300): largest number of fp32 registers a lane
+// spends on holding its weights widened.
+#ifndef RMSK_WIDE_W_FLOATS
+#define RMSK_WIDE_W_FLOATS 16
+#endif
 
 namespace rmsk {
 
@@ -39,6 +51,9 @@ struct RowLayout {
     static constexpr int kCols = L * V * E;
     // Column owners left after folding groups that share a warp.
     static constexpr int kColGroups = L < 32 ? kThreads / 32 : S;
+    // Weight held widened to fp32 when that costs at most RMSK_WIDE_W_FLOATS
+    // registers, else in its storage format (widened at each use).
+    static constexpr bool kWideW = V * E <= RMSK_WIDE_W_FLOATS && E > 1;
     static_assert(kThreads % 32 == 0, "a CTA is whole warps");
     static_assert(L <= 32 ? (32 % L == 0) : (L % 32 == 0 && S == 1),
                   "a group is a power of two <= 32 lanes, or whole warps "
@@ -77,12 +92,63 @@ __device__ __forceinline__ void row_allreduce(float (&v)[NR], float *red)
     }
 }
 
+// The weight of a lane's V packs: widened once, or kept packed, or (scalar
+// kernels) re-read from L1 at each use.
+template <typename T, int E, int L, int V, bool EXACT, bool WIDE>
+struct LaneWeight {
+    using P = Pack<T, E>;
+    using X = Vals<E>;
+    static constexpr bool kHold = E > 1;
+    X wide[WIDE ? V : 1];
+    P packed[(!WIDE && kHold) ? V : 1];
+    const void *w;
+    int lane, NV;
+
+    __device__ __forceinline__ void init(const void *w_, int lane_, int NV_)
+    {
+        w = w_;
+        lane = lane_;
+        NV = NV_;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int vi = lane + k * L;
+            const bool ok = EXACT || vi < NV;
+            if constexpr (WIDE) {
+                if (ok)
+                    P::load_cached(w, vi).widen(wide[k]);
+                else
+                    wide[k] = X::zero();
+            } else if constexpr (kHold) {
+                packed[k] = ok ? P::load_cached(w, vi) : P::zero();
+            }
+        }
+    }
+    __device__ __forceinline__ X get(int k) const
+    {
+        X r;
+        if constexpr (WIDE) {
+            r = wide[k];
+        } else if constexpr (kHold) {
+            packed[k].widen(r);
+        } else {
+            const int vi = lane + k * L;
+            if (EXACT || vi < NV)
+                P::load_cached(w, vi).widen(r);
+            else
+                r = X::zero();
+        }
+        return r;
+    }
+};
+
 // ------------------------------------------------------------------ forward
 template <typename T, int E, int L, int V, int G, int S, int MINB, bool EXACT, bool RES>
 __global__ void __launch_bounds__(L * S, MINB)
 rms_fwd_rows(const FwdParams p)
 {
     using P = Pack<T, E>;
+    using X = Vals<E>;
+    using F = typename X::F;
     using Lay = RowLayout<E, L, V, G, S>;
     constexpr int NW = Lay::kRowWarps;
     // Two buffers: a warp can only reuse one after the barrier of the next
@@ -94,13 +160,9 @@ rms_fwd_rows(const FwdParams p)
     const int NV = p.H / E;                 // packs per row
     const float fH = (float)p.H;
 
-    // The weight stays in registers in its storage format.
-    P wp[V];
-#pragma unroll
-    for (int k = 0; k < V; ++k) {
-        const int vi = lane + k * L;
-        wp[k] = (EXACT || vi < NV) ? P::load_cached(p.w, vi) : P::zero();
-    }
+    griddep_wait();
+    LaneWeight<T, E, L, V, EXACT, Lay::kWideW> wt;
+    wt.init(p.w, lane, NV);
 
     const int64_t ntiles = (p.M + Lay::kTileRows - 1) / Lay::kTileRows;
     int buf = 0;
@@ -137,13 +199,13 @@ rms_fwd_rows(const FwdParams p)
 #pragma unroll
                 for (int k = 0; k < V; ++k) {
                     const int vi = lane + k * L;
-                    float a[E], b[E];
-                    xv[g][k].to_float(a);
-                    rv[g][k].to_float(b);
+                    X a, b;
+                    xv[g][k].widen(a);
+                    rv[g][k].widen(b);
 #pragma unroll
-                    for (int e = 0; e < E; ++e)
-                        a[e] += b[e];
-                    xv[g][k] = P::from_float(a);
+                    for (int i = 0; i < X::N; ++i)
+                        a.v[i] = vadd(a.v[i], b.v[i]);
+                    xv[g][k] = P::narrow(a);
                     if (row < p.M && (EXACT || vi < NV))
                         xv[g][k].store(p.h, row * NV + vi);
                 }
@@ -153,15 +215,16 @@ rms_fwd_rows(const FwdParams p)
         float ss[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            ss[g] = 0.f;
+            F acc = splat<F>(0.f);
 #pragma unroll
             for (int k = 0; k < V; ++k) {
-                float f[E];
-                xv[g][k].to_float(f);
+                X a;
+                xv[g][k].widen(a);
 #pragma unroll
-                for (int e = 0; e < E; ++e)
-                    ss[g] = fmaf(f[e], f[e], ss[g]);
+                for (int i = 0; i < X::N; ++i)
+                    acc = vfma(a.v[i], a.v[i], acc);
             }
+            ss[g] = hsum(acc);
         }
         row_allreduce<L, G>(ss, red[buf]);
         buf ^= 1;
@@ -174,89 +237,72 @@ rms_fwd_rows(const FwdParams p)
             const float r = rsqrtf(ss[g] / fH + p.eps);
             if (p.rstd != nullptr && lane == 0)
                 p.rstd[row] = r;
+            const F r2 = splat<F>(r);
 #pragma unroll
             for (int k = 0; k < V; ++k) {
                 const int vi = lane + k * L;
                 if (!(EXACT || vi < NV))
                     continue;
-                float f[E], fw[E];
-                xv[g][k].to_float(f);
-                wp[k].to_float(fw);
+                X a;
+                xv[g][k].widen(a);
+                const X w = wt.get(k);
 #pragma unroll
-                for (int e = 0; e < E; ++e)
-                    f[e] = f[e] * r * fw[e];
-                P::from_float(f).store(p.y, row * NV + vi);
+                for (int i = 0; i < X::N; ++i)
+                    a.v[i] = vmul(vmul(a.v[i], r2), w.v[i]);
+                P::narrow(a).store(p.y, row * NV + vi);
             }
         }
     }
+    griddep_launch_dependents();
 }
 
 // ----------------------------------------------------------------- backward
 // Store E fp32 values at dst (16-byte aligned when E is a multiple of 4).
 template <int E>
-__device__ __forceinline__ void store_f32(float *dst, const float (&v)[E])
+__device__ __forceinline__ void store_vals(float *dst, const Vals<E> &v)
 {
     if constexpr (E % 4 == 0) {
 #pragma unroll
         for (int e = 0; e < E; e += 4)
-            *reinterpret_cast<float4 *>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            *reinterpret_cast<float4 *>(dst + e) =
+                make_float4(v.get(e), v.get(e + 1), v.get(e + 2), v.get(e + 3));
     } else {
 #pragma unroll
         for (int e = 0; e < E; ++e)
-            dst[e] = v[e];
+            dst[e] = v.get(e);
     }
 }
 
-template <typename T, int E, int L, int V, int G, int S, int MINB, bool EXACT, bool DH>
+// LOADR: rstd is given (read it) instead of recomputed from x.
+template <typename T, int E, int L, int V, int G, int S, int MINB, bool EXACT, bool DH,
+          bool LOADR>
 __global__ void __launch_bounds__(L * S, MINB)
 rms_bwd_rows(const BwdParams p)
 {
     using P = Pack<T, E>;
+    using X = Vals<E>;
+    using F = typename X::F;
     using Lay = RowLayout<E, L, V, G, S>;
     constexpr int NW = Lay::kRowWarps;
-    // The weight stays in registers in its storage format; the scalar
-    // kernels re-read it from L1 instead.
-    constexpr bool kWReg = E > 1;
+    constexpr int NR = LOADR ? G : 2 * G;      // values reduced per row group
     constexpr int kComb = Lay::kColGroups > 1 ? Lay::kColGroups * Lay::kCols : 1;
-    static_assert(kComb * 4 + 2 * NW * 2 * G * 4 <= 48 * 1024, "static shared memory");
-    __shared__ float red[2][NW * 2 * G];
+    static_assert(kComb * 4 + 2 * NW * NR * 4 <= 48 * 1024, "static shared memory");
+    __shared__ float red[2][NW * NR];
     __shared__ __align__(16) float comb[kComb];
 
     const int lane = threadIdx.x % L;
     const int grp = threadIdx.x / L;
     const int NV = p.H / E;
     const float fH = (float)p.H;
-    const bool have_rstd = p.rstd != nullptr;
 
-    P wp[kWReg ? V : 1];
-    if constexpr (kWReg) {
-#pragma unroll
-        for (int k = 0; k < V; ++k) {
-            const int vi = lane + k * L;
-            wp[k] = (EXACT || vi < NV) ? P::load_cached(p.w, vi) : P::zero();
-        }
-    }
-    auto weight = [&](int k, float (&f)[E]) {
-        if constexpr (kWReg) {
-            wp[k].to_float(f);
-        } else {
-            const int vi = lane + k * L;
-            if (EXACT || vi < NV) {
-                P::load_cached(p.w, vi).to_float(f);
-            } else {
-#pragma unroll
-                for (int e = 0; e < E; ++e)
-                    f[e] = 0.f;
-            }
-        }
-    };
+    griddep_wait();
+    LaneWeight<T, E, L, V, EXACT, Lay::kWideW> wt;
+    wt.init(p.w, lane, NV);
 
-    float acc[V][E];
+    X acc[V];
 #pragma unroll
     for (int k = 0; k < V; ++k)
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-            acc[k][e] = 0.f;
+        acc[k] = X::zero();
 
     const int64_t ntiles = (p.M + Lay::kTileRows - 1) / Lay::kTileRows;
     int buf = 0;
@@ -268,7 +314,8 @@ rms_bwd_rows(const BwdParams p)
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const int64_t row = row0 + g;
-            rs[g] = (have_rstd && row < p.M) ? p.rstd[row] : 0.f;
+            if constexpr (LOADR)
+                rs[g] = row < p.M ? p.rstd[row] : 0.f;
 #pragma unroll
             for (int k = 0; k < V; ++k) {
                 const int vi = lane + k * L;
@@ -278,27 +325,29 @@ rms_bwd_rows(const BwdParams p)
             }
         }
 
-        // [0, G): sum_j w_j dy_j x_j      [G, 2G): sum_j x_j^2
-        float sums[2 * G];
+        // [0, G): sum_j w_j dy_j x_j      [G, 2G): sum_j x_j^2 (recompute)
+        float sums[NR];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            float cs = 0.f, ss = 0.f;
+            F cs = splat<F>(0.f), ss = splat<F>(0.f);
 #pragma unroll
             for (int k = 0; k < V; ++k) {
-                float fx[E], fdy[E], fw[E];
-                xv[g][k].to_float(fx);
-                dyv[g][k].to_float(fdy);
-                weight(k, fw);
+                X a, b;
+                xv[g][k].widen(a);
+                dyv[g][k].widen(b);
+                const X w = wt.get(k);
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    cs = fmaf(fw[e] * fdy[e], fx[e], cs);
-                    ss = fmaf(fx[e], fx[e], ss);
+                for (int i = 0; i < X::N; ++i) {
+                    cs = vfma(vmul(w.v[i], b.v[i]), a.v[i], cs);
+                    if constexpr (!LOADR)
+                        ss = vfma(a.v[i], a.v[i], ss);
                 }
             }
-            sums[g] = cs;
-            sums[G + g] = ss;
+            sums[g] = hsum(cs);
+            if constexpr (!LOADR)
+                sums[G + g] = hsum(ss);
         }
-        row_allreduce<L, 2 * G>(sums, red[buf]);
+        row_allreduce<L, NR>(sums, red[buf]);
         buf ^= 1;
 
 #pragma unroll
@@ -306,31 +355,37 @@ rms_bwd_rows(const BwdParams p)
             const int64_t row = row0 + g;
             if (row >= p.M)
                 continue;
-            const float r = have_rstd ? rs[g] : rsqrtf(sums[G + g] / fH + p.eps);
+            float r;
+            if constexpr (LOADR)
+                r = rs[g];
+            else
+                r = rsqrtf(sums[G + g] / fH + p.eps);
             const float c = sums[g] / fH;
-            const float coef = r * r * c;
+            // dx = r (w dy - x r^2 c) = r (w dy) - x (r^3 c)
+            const F r2 = splat<F>(r);
+            const F negm = splat<F>(-(r * r * r * c));
 #pragma unroll
             for (int k = 0; k < V; ++k) {
                 const int vi = lane + k * L;
                 if (!(EXACT || vi < NV))
                     continue;
-                float fx[E], fdy[E], fw[E], o[E];
-                xv[g][k].to_float(fx);
-                dyv[g][k].to_float(fdy);
-                weight(k, fw);
+                X a, b, o;
+                xv[g][k].widen(a);
+                dyv[g][k].widen(b);
+                const X w = wt.get(k);
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    o[e] = r * (fw[e] * fdy[e] - fx[e] * coef);
-                    acc[k][e] = fmaf(fdy[e] * fx[e], r, acc[k][e]);
+                for (int i = 0; i < X::N; ++i) {
+                    o.v[i] = vfma(a.v[i], negm, vmul(r2, vmul(w.v[i], b.v[i])));
+                    acc[k].v[i] = vfma(vmul(b.v[i], a.v[i]), r2, acc[k].v[i]);
                 }
                 if constexpr (DH) {
-                    float fdh[E];
-                    P::load(p.dh, row * NV + vi).to_float(fdh);
+                    X d;
+                    P::load(p.dh, row * NV + vi).widen(d);
 #pragma unroll
-                    for (int e = 0; e < E; ++e)
-                        o[e] += fdh[e];
+                    for (int i = 0; i < X::N; ++i)
+                        o.v[i] = vadd(o.v[i], d.v[i]);
                 }
-                P::from_float(o).store(p.dx, row * NV + vi);
+                P::narrow(o).store(p.dx, row * NV + vi);
             }
         }
     }
@@ -345,7 +400,7 @@ rms_bwd_rows(const BwdParams p)
         for (int k = 0; k < V; ++k) {
             const int vi = lane + k * L;
             if (EXACT || vi < NV)
-                store_f32<E>(part + (int64_t)vi * E, acc[k]);
+                store_vals<E>(part + (int64_t)vi * E, acc[k]);
         }
     } else {
         if constexpr (L < 32) {
@@ -353,10 +408,16 @@ rms_bwd_rows(const BwdParams p)
 #pragma unroll
             for (int k = 0; k < V; ++k)
 #pragma unroll
-                for (int e = 0; e < E; ++e)
+                for (int i = 0; i < X::N; ++i)
 #pragma unroll
-                    for (int o = L; o < 32; o <<= 1)
-                        acc[k][e] += __shfl_xor_sync(0xFFFFFFFFu, acc[k][e], o);
+                    for (int o = L; o < 32; o <<= 1) {
+                        if constexpr (E % 2 == 0) {
+                            acc[k].v[i].x += __shfl_xor_sync(0xFFFFFFFFu, acc[k].v[i].x, o);
+                            acc[k].v[i].y += __shfl_xor_sync(0xFFFFFFFFu, acc[k].v[i].y, o);
+                        } else {
+                            acc[k].v[i] += __shfl_xor_sync(0xFFFFFFFFu, acc[k].v[i], o);
+                        }
+                    }
         }
         const int cg = L < 32 ? (int)(threadIdx.x / 32) : grp;
         if (L >= 32 || (threadIdx.x & 31) < L) {
@@ -364,7 +425,7 @@ rms_bwd_rows(const BwdParams p)
             for (int k = 0; k < V; ++k) {
                 const int vi = lane + k * L;
                 if (EXACT || vi < NV)
-                    store_f32<E>(comb + cg * Lay::kCols + vi * E, acc[k]);
+                    store_vals<E>(comb + cg * Lay::kCols + vi * E, acc[k]);
             }
         }
         __syncthreads();

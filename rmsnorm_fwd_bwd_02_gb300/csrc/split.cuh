@@ -71,6 +71,7 @@ rms_fwd_split(const SplitParams p)
     const int v0 = (int)rank * p.SV;
     const int v1 = min(v0 + p.SV, p.NV);
 
+    griddep_wait();
     P xv[V];
 #pragma unroll
     for (int k = 0; k < V; ++k) {
@@ -125,6 +126,7 @@ rms_fwd_split(const SplitParams p)
     for (uint32_t q = 0; q < K; ++q)
         total += ld_cluster_f32(&cta_sum, q);
     cluster_arrive_release();   // this CTA is done reading the others
+    griddep_launch_dependents();
 
     const float rs = rsqrtf(total / (float)p.H + p.eps);
     if (rank == 0 && tid == 0 && p.rstd != nullptr)

@@ -1,0 +1,38 @@
+// Streamed (bulk-copy fed) row kernels for the shaped bf16 feature counts,
+// and the device counter of bounded waits that ran out.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "registry.h"
+#include "stream.cuh"
+
+namespace rmsk {
+
+namespace {
+__device__ unsigned int g_stream_timeouts;
+std::mutex g_mu;
+unsigned int *g_addr[64] = {};
+} // namespace
+
+unsigned int *stream_timeout_counter(int dev)
+{
+    if (dev < 0 || dev >= 64)
+        return nullptr;
+    std::lock_guard<std::mutex> g(g_mu);
+    if (g_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_stream_timeouts) != cudaSuccess)
+            return nullptr;
+        g_addr[dev] = static_cast<unsigned int *>(p);
+    }
+    return g_addr[dev];
+}
+
+// Stage counts are upper bounds: variants that stage more tensors per row get
+// as many stages as fit in shared memory (StreamSmem).
+//           name     H     |-- forward: GW V NG NS --| |-- backward: GW V NG NS --|
+RMSK_STREAM(s_h4096, 4096,   4, 4, 4, 4,               8, 2, 2, 6)
+RMSK_STREAM(s_h5120, 5120,   4, 5, 3, 3,              10, 2, 2, 3)
+
+} // namespace rmsk

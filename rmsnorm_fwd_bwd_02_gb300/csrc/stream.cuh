@@ -1,0 +1,467 @@
+// stream.cuh -- row kernels fed by bulk asynchronous copies (the TMA engine)
+// for the feature counts with a shaped layout (H = 32 * GW * V * E).
+//
+// Same arithmetic as rows.cuh ([P1] "训推加速 Qwen3 实战：从“调包”到手写 Triton
+// Kernel（含 backward）" §4.1-4.2 forward, §5.3-5.4 backward); what differs is
+// how rows reach the SM. A CTA holds NG groups of GW warps. Each group owns
+// a ring of NS shared-memory stages, one row per stage (x, plus r or dy and
+// dh where the variant reads them). One elected thread of the group issues
+// one cp.async.bulk per tensor and row, completing on the stage's mbarrier,
+// NS rows ahead of the group's compute, so the bytes in flight per SM are set
+// by shared memory (NG * NS stages) rather than by registers. The group
+// reads a stage into registers (conflict-free 16-byte shared loads), reduces
+// over its warps with one named barrier per row, and that barrier also
+// releases the stage for the next copy. Outputs are stored from registers.
+//
+// Every wait on an mbarrier is bounded in time (%globaltimer). A wait that
+// runs out means a copy never landed: the group records it in a device
+// counter, waits (again bounded) for its other copies in flight, skips its
+// remaining rows and still joins the CTA-wide barriers, so the kernel ends.
+#pragma once
+
+#include "common.cuh"
+#include "params.h"
+
+namespace rmsk {
+
+constexpr unsigned long long kStageWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with this parity to complete; false if it has not
+// within kStageWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kStageWaitLimitNs)
+            return false;
+    return true;
+}
+
+// Order this thread's earlier generic-proxy accesses to shared memory before
+// later async-proxy (bulk copy) writes to it.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk copy global -> shared of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), completing `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                 "[%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// Named barrier over `count` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool bar_red_or(int id, int count, bool pred)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                 "setp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.or.pred q, %2, %3, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)pred), "r"(id), "r"(count)
+                 : "memory");
+    return r != 0;
+}
+
+template <int E>
+__device__ __forceinline__ Pack<bf16, 8> as_pack(uint4 u)
+{
+    Pack<bf16, 8> p;
+    p.u = u;
+    return p;
+}
+
+// Shared-memory layout of one CTA. The stage ring of each group holds NS
+// stages, or as many as fit in kBudget bytes for all groups (at least one).
+template <int GW, int V, int NG, int NS, int NTEN, int NR>
+struct StreamSmem {
+    static constexpr int kRowBytes = 32 * GW * V * 16;        // one tensor row
+    static constexpr int kStageBytes = NTEN * kRowBytes;
+    static constexpr int kBudget = 210 * 1024;
+    static constexpr int kFit = kBudget / (NG * kStageBytes);
+    static constexpr int kNS = NS * NG * kStageBytes <= kBudget ? NS : (kFit > 0 ? kFit : 1);
+    static constexpr int kStagesBytes = NG * kNS * kStageBytes;
+    static constexpr int kBarOff = kStagesBytes;                 // NG*kNS mbarriers
+    static constexpr int kRedOff = kBarOff + NG * kNS * 8;       // [NG][2][GW][NR]
+    static constexpr int kBytes = kRedOff + NG * 2 * GW * NR * 4;
+    static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
+    static_assert(kNS >= 2, "a stage is refilled one iteration after use: two at least");
+};
+
+// Both kernels read a stage twice (sums, then outputs) instead of holding the
+// row in registers across the group barrier. A stage is refilled one
+// iteration after it was consumed: the barrier of iteration k proves every
+// thread of the group has finished iteration k-1, whose stage then takes the
+// row NS-1 ahead. NS stages therefore keep NS-1 rows in flight per group.
+
+// ------------------------------------------------------------------ forward
+// The bf16 shaped rows only (E = 8).
+template <int GW, int V, int NG, int NS, bool RES>
+__global__ void __launch_bounds__(NG * GW * 32, 1)
+rms_fwd_stream(const FwdParams p, unsigned int *timeouts)
+{
+    using P = Pack<bf16, 8>;
+    using X = Vals<8>;
+    using F = float2;
+    constexpr int GT = GW * 32;
+    constexpr int NV = GT * V;             // packs per row
+    constexpr int NTEN = RES ? 2 : 1;
+    using SM = StreamSmem<GW, V, NG, NS, NTEN, 1>;
+    constexpr int NSE = SM::kNS;           // stages per group
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int g = threadIdx.x / GT;
+    const int t = threadIdx.x % GT;
+    const int wg = t / 32;
+    const uint32_t stage0 = smem_addr(smem) + g * NSE * SM::kStageBytes;
+    const uint32_t bar0 = smem_addr(smem) + SM::kBarOff + g * NSE * 8;
+    float *red = reinterpret_cast<float *>(smem + SM::kRedOff) + g * 2 * GW;   // [2][GW]
+
+    if (t == 0)
+        for (int s = 0; s < NSE; ++s)
+            mbar_init(bar0 + 8 * s, 1);
+    mbar_init_fence();
+    __syncthreads();
+    griddep_wait();
+
+    P wp[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+        wp[j] = P::load_cached(p.w, t + j * GT);
+
+    const int64_t gg = (int64_t)blockIdx.x * NG + g;
+    const int64_t TG = (int64_t)gridDim.x * NG;
+    const int64_t nk = gg < p.M ? (p.M - 1 - gg) / TG + 1 : 0;
+    const float fH = (float)p.H;
+
+    auto issue = [&](int64_t k) {
+        const int64_t row = gg + k * TG;
+        const int s = (int)(k % NSE);
+        const uint32_t st = stage0 + s * SM::kStageBytes;
+        const uint32_t bar = bar0 + 8 * s;
+        mbar_expect_tx(bar, SM::kStageBytes);
+        bulk_g2s(st, static_cast<const uint4 *>(p.x) + row * NV, SM::kRowBytes, bar);
+        if constexpr (RES)
+            bulk_g2s(st + SM::kRowBytes, static_cast<const uint4 *>(p.r) + row * NV,
+                     SM::kRowBytes, bar);
+    };
+    // x (+ r) of pack j of the current stage, widened; with the residual,
+    // rounded to bf16 first (h as stored).
+    auto row_pack = [&](uint32_t st, int j, X &a) {
+        if constexpr (RES) {
+            X b;
+            as_pack<8>(lds128(st + (t + j * GT) * 16)).widen(a);
+            as_pack<8>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+#pragma unroll
+            for (int i = 0; i < X::N; ++i)
+                a.v[i] = vadd(a.v[i], b.v[i]);
+            P::narrow(a).widen(a);
+        } else {
+            as_pack<8>(lds128(st + (t + j * GT) * 16)).widen(a);
+        }
+    };
+    if (t == 0) {
+        fence_proxy_async_smem();
+        for (int64_t k = 0; k < NSE && k < nk; ++k)
+            issue(k);
+    }
+
+    int64_t k = 0;
+    bool failed = false;
+    for (; k < nk; ++k) {
+        const int64_t row = gg + k * TG;
+        const uint32_t st = stage0 + (int)(k % NSE) * SM::kStageBytes;
+        const bool ok = mbar_wait_bounded(bar0 + 8 * (int)(k % NSE), (uint32_t)((k / NSE) & 1));
+
+        F acc = splat<F>(0.f);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            X a;
+            row_pack(st, j, a);
+#pragma unroll
+            for (int i = 0; i < X::N; ++i)
+                acc = vfma(a.v[i], a.v[i], acc);
+        }
+        float ss = group_allreduce<32>(hsum(acc));
+        float *rb = red + (k & 1) * GW;   // double buffer
+        if ((t & 31) == 0)
+            rb[wg] = ss;
+        // Every thread of the group has posted its sums and finished the
+        // previous iteration (whose stage is refilled below).
+        if (bar_red_or(1 + g, GT, !ok)) {
+            failed = true;
+            break;
+        }
+        if (t == 0 && k >= 1 && k - 1 + NSE < nk) {
+            fence_proxy_async_smem();
+            issue(k - 1 + NSE);
+        }
+        ss = 0.f;
+#pragma unroll
+        for (int q = 0; q < GW; ++q)
+            ss += rb[q];
+        const float r = rsqrtf(ss / fH + p.eps);
+        if (p.rstd != nullptr && t == 0)
+            p.rstd[row] = r;
+        const F r2 = splat<F>(r);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            X a, wv;
+            row_pack(st, j, a);
+            if constexpr (RES)
+                P::narrow(a).store(p.h, row * NV + t + j * GT);
+            wp[j].widen(wv);
+#pragma unroll
+            for (int i = 0; i < X::N; ++i)
+                a.v[i] = vmul(vmul(a.v[i], r2), wv.v[i]);
+            P::narrow(a).store(p.y, row * NV + t + j * GT);
+        }
+    }
+    if (failed && t == 0) {
+        atomicAdd(timeouts, 1u);
+        // drain this group's copies still in flight (bounded):
+        // rows k .. k+NSE-2 were issued and not consumed
+        for (int64_t q = k; q < k + NSE - 1 && q < nk; ++q)
+            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1));
+    }
+    griddep_launch_dependents();
+}
+
+// ----------------------------------------------------------------- backward
+template <int GW, int V, int NG, int NS, bool DH, bool LOADR>
+__global__ void __launch_bounds__(NG * GW * 32, 1)
+rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
+{
+    using P = Pack<bf16, 8>;
+    using X = Vals<8>;
+    using F = float2;
+    constexpr int GT = GW * 32;
+    constexpr int NV = GT * V;
+    constexpr int NTEN = DH ? 3 : 2;      // x, dy, [dh]
+    constexpr int NR = LOADR ? 1 : 2;
+    using SM = StreamSmem<GW, V, NG, NS, NTEN, NR>;
+    constexpr int NSE = SM::kNS;          // stages per group
+    static_assert(NG * NV * 8 * 4 <= SM::kStagesBytes, "dw combine reuses the stages");
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int g = threadIdx.x / GT;
+    const int t = threadIdx.x % GT;
+    const int wg = t / 32;
+    const uint32_t stage0 = smem_addr(smem) + g * NSE * SM::kStageBytes;
+    const uint32_t bar0 = smem_addr(smem) + SM::kBarOff + g * NSE * 8;
+    float *red = reinterpret_cast<float *>(smem + SM::kRedOff) + g * 2 * GW * NR;  // [2][GW][NR]
+
+    if (t == 0)
+        for (int s = 0; s < NSE; ++s)
+            mbar_init(bar0 + 8 * s, 1);
+    mbar_init_fence();
+    __syncthreads();
+    griddep_wait();
+
+    P wp[V];        // weight kept packed (registers are the constraint here)
+    X acc[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        wp[j] = P::load_cached(p.w, t + j * GT);
+        acc[j] = X::zero();
+    }
+
+    const int64_t gg = (int64_t)blockIdx.x * NG + g;
+    const int64_t TG = (int64_t)gridDim.x * NG;
+    const int64_t nk = gg < p.M ? (p.M - 1 - gg) / TG + 1 : 0;
+    const float fH = (float)p.H;
+
+    auto issue = [&](int64_t k) {
+        const int64_t row = gg + k * TG;
+        const int s = (int)(k % NSE);
+        const uint32_t st = stage0 + s * SM::kStageBytes;
+        const uint32_t bar = bar0 + 8 * s;
+        mbar_expect_tx(bar, SM::kStageBytes);
+        bulk_g2s(st, static_cast<const uint4 *>(p.x) + row * NV, SM::kRowBytes, bar);
+        bulk_g2s(st + SM::kRowBytes, static_cast<const uint4 *>(p.dy) + row * NV,
+                 SM::kRowBytes, bar);
+        if constexpr (DH)
+            bulk_g2s(st + 2 * SM::kRowBytes, static_cast<const uint4 *>(p.dh) + row * NV,
+                     SM::kRowBytes, bar);
+    };
+    if (t == 0) {
+        fence_proxy_async_smem();
+        for (int64_t k = 0; k < NSE && k < nk; ++k)
+            issue(k);
+    }
+
+    float r_next = 0.f;
+    if constexpr (LOADR)
+        r_next = nk > 0 ? p.rstd[gg] : 0.f;
+
+    int64_t k = 0;
+    bool failed = false;
+    for (; k < nk; ++k) {
+        const int64_t row = gg + k * TG;
+        const uint32_t st = stage0 + (int)(k % NSE) * SM::kStageBytes;
+        float r_cur = 0.f;
+        if constexpr (LOADR) {
+            r_cur = r_next;                 // loaded one row ahead
+            if (k + 1 < nk)
+                r_next = p.rstd[row + TG];
+        }
+        const bool ok = mbar_wait_bounded(bar0 + 8 * (int)(k % NSE), (uint32_t)((k / NSE) & 1));
+
+        F cs = splat<F>(0.f), ss = splat<F>(0.f);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            X a, b, wv;
+            as_pack<8>(lds128(st + (t + j * GT) * 16)).widen(a);
+            as_pack<8>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+            wp[j].widen(wv);
+#pragma unroll
+            for (int i = 0; i < X::N; ++i) {
+                cs = vfma(vmul(wv.v[i], b.v[i]), a.v[i], cs);
+                if constexpr (!LOADR)
+                    ss = vfma(a.v[i], a.v[i], ss);
+            }
+        }
+        float sums[NR];
+        sums[0] = group_allreduce<32>(hsum(cs));
+        if constexpr (!LOADR)
+            sums[1] = group_allreduce<32>(hsum(ss));
+        float *rb = red + (k & 1) * GW * NR;   // double buffer
+        if ((t & 31) == 0)
+#pragma unroll
+            for (int i = 0; i < NR; ++i)
+                rb[wg * NR + i] = sums[i];
+        // Every thread of the group has posted its sums and finished the
+        // previous iteration (whose stage is refilled below).
+        if (bar_red_or(1 + g, GT, !ok)) {
+            failed = true;
+            break;
+        }
+        if (t == 0 && k >= 1 && k - 1 + NSE < nk) {
+            fence_proxy_async_smem();
+            issue(k - 1 + NSE);
+        }
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            float v = 0.f;
+#pragma unroll
+            for (int q = 0; q < GW; ++q)
+                v += rb[q * NR + i];
+            sums[i] = v;
+        }
+        float r;
+        if constexpr (LOADR)
+            r = r_cur;
+        else
+            r = rsqrtf(sums[1] / fH + p.eps);
+        const float c = sums[0] / fH;
+        const F r2 = splat<F>(r);
+        const F negm = splat<F>(-(r * r * r * c));
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            X a, b, o, wv;
+            as_pack<8>(lds128(st + (t + j * GT) * 16)).widen(a);
+            as_pack<8>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+            wp[j].widen(wv);
+#pragma unroll
+            for (int i = 0; i < X::N; ++i) {
+                o.v[i] = vfma(a.v[i], negm, vmul(r2, vmul(wv.v[i], b.v[i])));
+                acc[j].v[i] = vfma(vmul(b.v[i], a.v[i]), r2, acc[j].v[i]);
+            }
+            if constexpr (DH) {
+                X d;
+                as_pack<8>(lds128(st + 2 * SM::kRowBytes + (t + j * GT) * 16)).widen(d);
+#pragma unroll
+                for (int i = 0; i < X::N; ++i)
+                    o.v[i] = vadd(o.v[i], d.v[i]);
+            }
+            P::narrow(o).store(p.dx, row * NV + t + j * GT);
+        }
+    }
+    if (failed && t == 0) {
+        atomicAdd(timeouts, 1u);
+        // rows k .. k+NSE-2 were issued and not consumed
+        for (int64_t q = k; q < k + NSE - 1 && q < nk; ++q)
+            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1));
+    }
+    griddep_launch_dependents();
+
+    // Fold the NG groups' dw accumulators (same columns) in group order into
+    // one partial row; the stage memory is free now.
+    __syncthreads();
+    float *comb = reinterpret_cast<float *>(smem);
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        float4 *d = reinterpret_cast<float4 *>(comb + (size_t)g * NV * 8 + (t + j * GT) * 8);
+        d[0] = make_float4(acc[j].v[0].x, acc[j].v[0].y, acc[j].v[1].x, acc[j].v[1].y);
+        d[1] = make_float4(acc[j].v[2].x, acc[j].v[2].y, acc[j].v[3].x, acc[j].v[3].y);
+    }
+    __syncthreads();
+    float *part = p.part + (int64_t)blockIdx.x * p.H;
+    for (int c = threadIdx.x; c < NV * 8; c += NG * GT) {
+        float v = 0.f;
+#pragma unroll
+        for (int q = 0; q < NG; ++q)
+            v += comb[q * NV * 8 + c];
+        part[c] = v;
+    }
+}
+
+} // namespace rmsk

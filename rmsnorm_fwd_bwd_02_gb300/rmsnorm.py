@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG, "librmsnorm.so")
 RMSNORM_F32, RMSNORM_BF16 = 0, 1
 DTYPES = {torch.float32: RMSNORM_F32, torch.bfloat16: RMSNORM_BF16}
 MAX_H = 16384
-PATH_AUTO, PATH_ROWS, PATH_SPLIT, PATH_SCALAR = 0, 1, 2, 3
+PATH_AUTO, PATH_ROWS, PATH_SPLIT, PATH_SCALAR, PATH_STREAM = 0, 1, 2, 3, 4
 
 # Entry points of include/rmsnorm.h with their ctypes signatures.
 _i64, _vp, _sz, _int, _f = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
@@ -38,6 +38,7 @@ SIGNATURES = {
     "rmsnorm_last_path": (_int, []),
     "rmsnorm_bwd_static_scratch": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                           _i64, _f, _int, _vp]),
+    "rmsnorm_wait_timeouts": (_int, [ctypes.POINTER(ctypes.c_uint), _int]),
 }
 
 
@@ -109,6 +110,15 @@ def set_path_override(path: int):
 
 def last_path() -> int:
     return lib().rmsnorm_last_path()
+
+
+def wait_timeouts(reset: bool = False) -> int:
+    """Streamed-kernel waits that ran out on the current device (0 when all
+    is well); synchronous diagnostic."""
+    c = ctypes.c_uint(0)
+    _check(lib().rmsnorm_wait_timeouts(ctypes.byref(c), int(reset)),
+           "rmsnorm_wait_timeouts")
+    return int(c.value)
 
 
 def bwd_workspace_bytes(M: int, H: int, dtype: torch.dtype) -> int:

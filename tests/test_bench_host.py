@@ -1,0 +1,91 @@
+"""CPU tier: host-side logic of bench.py — algorithmic bytes, buffer-set
+sizing, the reference (oracle) arm, and the multi-rank reduction used when
+bench.py runs one replica per GPU (two gloo ranks on the CPU)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+from rmsnorm_fwd_bwd_02_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_algorithmic_bytes_of_the_workloads():
+    # Qwen3-8B: fwd reads x and w, writes y and rstd; bwd reads x, dy, w and
+    # writes dx and dw (rstd read and workspace not counted)
+    assert bench.step_bytes(W.WORKLOADS["qwen3-8b-train"]) == (537010176, 805330944)
+    assert bench.step_bytes(W.WORKLOADS["qwen3-qknorm"]) == (270532864, 402653952)
+    # residual: x, r in and h, y out; dy, h, dh in and dx out
+    assert bench.step_bytes(W.WORKLOADS["residual-14b"]) == (671164416, 671119360)
+    # decode, one token: x, w in; y, rstd out
+    assert bench.step_bytes(W.WORKLOADS["decode-m1"]) == (3 * 1792 + 4, 0)
+
+
+def test_buffer_sets_defeat_l2():
+    for name, wl in W.WORKLOADS.items():
+        n = bench.buffer_sets(wl)
+        x_bytes = wl.M * wl.H * wl.elem_bytes
+        assert 3 <= n <= 64
+        if bench.streams_from_hbm(wl):
+            assert n == 3 and x_bytes > 100e6
+        else:
+            assert n * x_bytes >= min(2 * bench.L2_BYTES, 64 * x_bytes)
+    assert bench.streams_from_hbm(W.WORKLOADS["qwen3-8b-train"].with_rows(16384))
+
+
+def test_whole_job_value():
+    assert bench.whole_job_gbs(1e9, 1, 1.0) == pytest.approx(1000.0)
+    assert bench.whole_job_gbs(1e9, 4, 2.0) == pytest.approx(2000.0)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local = 1.0 + 2.5 * rank                  # this replica's step time, ms
+    q.put((rank, bench.reduce_max(local, dist)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == {0: 3.5, 1: 3.5}
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl",
+                        "reference", "--steps", "3", "--warmup", "3", "--workload",
+                        "tiny-fp32"], capture_output=True, text=True, timeout=600,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup",
+              "ms_per_step", "higher_is_better", "config", "cpu_baseline", "e2e"):
+        assert k in d
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["value"] > 0

@@ -187,7 +187,11 @@ def test_edge_shapes(orc, M, H, dtype):
         compare_all(f"M={M} H={H} {dtype} res={residual}", wl, got, o)
 
 
-@pytest.mark.parametrize("path", [rn.PATH_ROWS, rn.PATH_SPLIT, rn.PATH_SCALAR])
+STREAM_H = (4096, 5120)     # bf16 feature counts with a streamed layout
+
+
+@pytest.mark.parametrize("path", [rn.PATH_ROWS, rn.PATH_SPLIT, rn.PATH_SCALAR,
+                                  rn.PATH_STREAM])
 @pytest.mark.parametrize("H", [1, 7, 128, 896, 4096, 5120, 16384])
 def test_forced_paths_agree_with_oracle(orc, path, H):
     M = 5
@@ -202,9 +206,61 @@ def test_forced_paths_agree_with_oracle(orc, path, H):
             vec_ok = (H * inp["x"].element_size()) % 16 == 0
             if path == rn.PATH_SCALAR or not vec_ok:
                 assert used == rn.PATH_SCALAR
+            elif path == rn.PATH_STREAM and dtype == torch.bfloat16 and H in STREAM_H:
+                assert used == rn.PATH_STREAM
             else:
                 assert used == rn.PATH_ROWS   # the backward reports last
             compare_all(f"path={path} H={H} {dtype} res={residual}", wl, got, o)
+
+
+@pytest.mark.parametrize("name,M", [("qwen3-8b-train", 1), ("qwen3-8b-train", 7),
+                                    ("qwen3-8b-train", 1037), ("residual-14b", 3),
+                                    ("residual-14b", 517)])
+def test_stream_path_ragged(orc, name, M):
+    """Streamed kernels: every variant (residual, dh_out given or not, rstd
+    given or recomputed) on row counts that leave groups idle or uneven."""
+    wl = W.WORKLOADS[name].with_rows(M)
+    inp = W.make_inputs(wl)
+    g = to_dev(inp)
+    with forced_path(rn.PATH_STREAM):
+        for dh in ((True, False) if wl.residual else (True,)):
+            for with_rstd in (True, False):
+                o = oracle_all(orc, wl, inp, dh=dh)
+                got = gpu_fwd_bwd(wl, g, dh=dh, with_rstd=with_rstd)
+                assert rn.last_path() == rn.PATH_STREAM
+                compare_all(f"stream {name} M={M} dh={dh} rstd={with_rstd}", wl, got, o)
+
+
+@pytest.mark.parametrize("name", ["qwen3-8b-train", "residual-14b"])
+def test_stream_path_full_size_sampled(orc, name):
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl)
+    with forced_path(rn.PATH_STREAM):
+        got = gpu_fwd_bwd(wl, to_dev(inp))
+        assert rn.last_path() == rn.PATH_STREAM
+    if wl.residual:
+        h_full, _, _ = orc.residual_fwd(inp["x"], inp["r"], inp["w"], wl.eps)
+        check_bits(f"stream {name} h (all rows)", got["h"], h_full)
+        _, dw, _, tdw = orc.residual_bwd(inp["dy"], inp["dh"], h_full, inp["w"],
+                                         wl.eps, want_dx=False, want_terms=True)
+        del h_full
+    else:
+        _, dw, _, tdw = orc.bwd(inp["dy"], inp["x"], inp["w"], wl.eps,
+                                want_dx=False, want_terms=True)
+    check_dw(f"stream {name} dw (all rows)", got["dw"], dw, tdw)
+    rows = W.random_rows(wl.M, 64, seed=wl.seed + 1)
+    sub = {k: (v[rows].contiguous() if v.dim() == 2 else v) for k, v in inp.items()}
+    o = oracle_all(orc, wl.with_rows(len(rows)), sub)
+    check_rows(f"stream {name} y", got["y"][rows], o["y"], wl.dtype)
+    check_rstd(f"stream {name} rstd", got["rstd"][rows], o["rstd"])
+    check_rows(f"stream {name} dx", got["dx"][rows], o["dx"], wl.dtype, o["tdx"])
+    if wl.residual:
+        check_bits(f"stream {name} h", got["h"][rows], o["h"])
+    # deterministic run to run
+    with forced_path(rn.PATH_STREAM):
+        again = gpu_fwd_bwd(wl, to_dev(inp))
+    for k in got:
+        check_bits(f"stream {name} {k} run-to-run", again[k], got[k])
 
 
 def test_auto_path_choice():
@@ -218,6 +274,14 @@ def test_auto_path_choice():
     x = torch.randn(65, 895, device=DEV, dtype=torch.bfloat16)
     rn.rmsnorm_fwd(x, torch.ones(895, device=DEV, dtype=torch.bfloat16))
     assert rn.last_path() == rn.PATH_SCALAR
+    # bf16 rows of 4096 / 5120: the forward row-wise, the backward streamed
+    for H in STREAM_H:
+        x = torch.randn(100, H, device=DEV, dtype=torch.bfloat16)
+        w = torch.ones(H, device=DEV, dtype=torch.bfloat16)
+        _, rstd = rn.rmsnorm_fwd(x, w)
+        assert rn.last_path() == rn.PATH_ROWS
+        rn.rmsnorm_bwd(x, x, w, rstd)
+        assert rn.last_path() == rn.PATH_STREAM
     torch.cuda.synchronize()
 
 
@@ -464,3 +528,8 @@ def test_side_stream():
     s.synchronize()
     for k, v in (("y", y), ("rstd", rstd), ("dx", dx), ("dw", dw)):
         check_bits(f"side stream {k}", v, ref[k])
+
+
+def test_no_stream_wait_ran_out():
+    """Every bounded wait in the streamed kernels completed during this module."""
+    assert rn.wait_timeouts() == 0
