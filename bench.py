@@ -569,16 +569,38 @@ def run_e2e(rn, wl, src, dev, ws, args, dist):
             "rows_per_s": round(wl.M * world / (ms * 1e-3), 1)}
 
 
+# Sources of the kernels whose DRAM traffic profiles/traffic.json records;
+# a change to any of them makes the recorded figure stale (reported null).
+TRAFFIC_SOURCES = {
+    "bwd": ["stream.cuh", "stream.cu", "reduce.cuh", "common.cuh", "params.h",
+            "rows.cuh", "rows_bf16_shaped.cu"],
+    "fwd": ["rows.cuh", "rows_bf16_shaped.cu", "common.cuh", "params.h"],
+}
+
+
+def kernel_src_hash(which):
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "rmsnorm_fwd_bwd_02_gb300", "csrc")
+    for f in TRAFFIC_SOURCES[which]:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(wl, which):
-    """DRAM bytes per launch of the dominant call from the committed ncu
-    summary, when one exists for this workload and the current kernels."""
+    """DRAM bytes per launch of the dominant call, from the committed ncu
+    summary, when one exists for this workload and the kernels' sources are
+    unchanged since it was taken; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        v = d.get(wl.name, {}).get(which)
-        return None if v is None else int(v)
-    except (OSError, ValueError):
+        e = d.get(wl.name, {}).get(which)
+        if not e or e.get("src") != kernel_src_hash(which):
+            return None
+        return int(e["bytes"])
+    except (OSError, ValueError, KeyError):
         return None
 
 

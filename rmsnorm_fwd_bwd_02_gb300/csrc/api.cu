@@ -185,15 +185,17 @@ cudaError_t launch2(const void *fn, dim3 grid, dim3 block, int smem, cudaStream_
 }
 
 // -------------------------------------------------------- kernel choice
-const RowKernels &pick_rows(int dtype, int64_t H, bool vec)
+// wide: every row pointer 32-byte aligned and H * element size a multiple
+// of 32, so a forward with 32-byte packs may run.
+const RowKernels &pick_rows(int dtype, int64_t H, bool vec, bool wide)
 {
     if (dtype == RMSNORM_BF16) {
         if (!vec)
             return H <= b_s32.max_cols() ? b_s32 : b_s1024;
-        if (H == 128) return b_h128;
+        if (H == 128) return wide ? b_h128w : b_h128;
         if (H == 896) return b_h896;
-        if (H == 4096) return b_h4096;
-        if (H == 5120) return b_h5120;
+        if (H == 4096) return wide ? b_h4096w : b_h4096;
+        if (H == 5120) return wide ? b_h5120w : b_h5120;
         if (H <= b_g32.max_cols()) return b_g32;
         if (H <= b_g128.max_cols()) return b_g128;
         return b_g512;
@@ -251,6 +253,8 @@ int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, floa
                        aligned(y, 16) && aligned(r, 16) && aligned(h, 16);
     const int ov = g_path_override.load(std::memory_order_relaxed);
     const bool vec = vec16 && ov != kPathScalar;
+    const bool wide = vec && (H * (int64_t)es) % 32 == 0 && aligned(x, 32) && aligned(w, 32) &&
+                      aligned(y, 32) && aligned(r, 32) && aligned(h, 32);
     const bool split = M <= 65535 && (ov == kPathSplit || (ov == kPathAuto && M <= kSplitMaxRows));
 
     if (split) {
@@ -294,7 +298,7 @@ int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, floa
         return RMSNORM_OK;
     }
 
-    const RowKernels &k = pick_rows(dtype, H, vec);
+    const RowKernels &k = pick_rows(dtype, H, vec, wide);
     const void *fn = k.fwd[res ? 1 : 0];
     int64_t grid;
     int st = rows_grid(k.f, fn, M, &grid);
@@ -343,7 +347,7 @@ int bwd_plan(int dtype, int64_t M, int64_t H, bool vec, bool dh, bool have_rstd,
         pl->timeouts = stream_timeout_counter(dev);
         return pl->timeouts ? RMSNORM_OK : cuda_fail(cudaErrorInvalidSymbol);
     }
-    const RowKernels &k = pick_rows(dtype, H, vec);
+    const RowKernels &k = pick_rows(dtype, H, vec, false);   // 16-byte packs
     pl->fn = k.bwd[dh ? 1 : 0][have_rstd ? 1 : 0];
     pl->threads = k.b.threads();
     pl->smem = 0;

@@ -60,6 +60,40 @@ __device__ __forceinline__ void st_row_b16(void *p, uint16_t v)
     asm volatile("st.global.b16 [%0], %1;" : : "l"(p), "h"(v) : "memory");
 }
 
+// 32-byte accesses (sm_100 family: one instruction moves 8 words per
+// thread). RMSK_L2_EVICT_FIRST marks streamed row data as first to leave L2.
+#ifndef RMSK_L2_EVICT_FIRST
+#define RMSK_L2_EVICT_FIRST 0
+#endif
+#if RMSK_L2_EVICT_FIRST
+#define RMSK_L2_HINT ".L2::evict_first"
+#else
+#define RMSK_L2_HINT ""
+#endif
+
+struct u32x8 {
+    uint32_t w[8];
+};
+
+__device__ __forceinline__ u32x8 ld_row_v8(const void *p)
+{
+    u32x8 v;
+    asm volatile("ld.global.L1::no_allocate" RMSK_L2_HINT ".v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]),
+                   "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_row_v8(void *p, const u32x8 &v)
+{
+    asm volatile("st.global" RMSK_L2_HINT ".v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :
+                 : "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]),
+                   "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                 : "memory");
+}
+
 // ------------------------------------------------------------ bf16 <-> fp32
 // bf16 is the upper half of an fp32 word, so widening is a shift.
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -164,6 +198,96 @@ template <> struct Pack<bf16, 8> {
         Pack p;
         p.u.x = pack_bf16x2(f.v[0].x, f.v[0].y); p.u.y = pack_bf16x2(f.v[1].x, f.v[1].y);
         p.u.z = pack_bf16x2(f.v[2].x, f.v[2].y); p.u.w = pack_bf16x2(f.v[3].x, f.v[3].y);
+        return p;
+    }
+};
+
+template <> struct Pack<bf16, 16> {
+    u32x8 u;
+    static constexpr int E = 16;
+    __device__ __forceinline__ static Pack zero()
+    {
+        Pack p;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            p.u.w[i] = 0;
+        return p;
+    }
+    __device__ __forceinline__ static Pack load(const void *base, int64_t idx)
+    {
+        Pack p; p.u = ld_row_v8(static_cast<const uint4 *>(base) + 2 * idx); return p;
+    }
+    __device__ __forceinline__ static Pack load_cached(const void *base, int64_t idx)
+    {
+        Pack p;
+        const uint4 *q = static_cast<const uint4 *>(base) + 2 * idx;
+        const uint4 a = __ldg(q), b = __ldg(q + 1);
+        p.u.w[0] = a.x; p.u.w[1] = a.y; p.u.w[2] = a.z; p.u.w[3] = a.w;
+        p.u.w[4] = b.x; p.u.w[5] = b.y; p.u.w[6] = b.z; p.u.w[7] = b.w;
+        return p;
+    }
+    __device__ __forceinline__ void store(void *base, int64_t idx) const
+    {
+        st_row_v8(static_cast<uint4 *>(base) + 2 * idx, u);
+    }
+    __device__ __forceinline__ void widen(Vals<16> &f) const
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            f.v[i] = make_float2(bf16lo(u.w[i]), bf16hi(u.w[i]));
+    }
+    __device__ __forceinline__ static Pack narrow(const Vals<16> &f)
+    {
+        Pack p;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            p.u.w[i] = pack_bf16x2(f.v[i].x, f.v[i].y);
+        return p;
+    }
+};
+
+template <> struct Pack<float, 8> {
+    u32x8 u;
+    static constexpr int E = 8;
+    __device__ __forceinline__ static Pack zero()
+    {
+        Pack p;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            p.u.w[i] = 0;
+        return p;
+    }
+    __device__ __forceinline__ static Pack load(const void *base, int64_t idx)
+    {
+        Pack p; p.u = ld_row_v8(static_cast<const uint4 *>(base) + 2 * idx); return p;
+    }
+    __device__ __forceinline__ static Pack load_cached(const void *base, int64_t idx)
+    {
+        Pack p;
+        const uint4 *q = static_cast<const uint4 *>(base) + 2 * idx;
+        const uint4 a = __ldg(q), b = __ldg(q + 1);
+        p.u.w[0] = a.x; p.u.w[1] = a.y; p.u.w[2] = a.z; p.u.w[3] = a.w;
+        p.u.w[4] = b.x; p.u.w[5] = b.y; p.u.w[6] = b.z; p.u.w[7] = b.w;
+        return p;
+    }
+    __device__ __forceinline__ void store(void *base, int64_t idx) const
+    {
+        st_row_v8(static_cast<uint4 *>(base) + 2 * idx, u);
+    }
+    __device__ __forceinline__ void widen(Vals<8> &f) const
+    {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            f.v[i] = make_float2(__uint_as_float(u.w[2 * i]), __uint_as_float(u.w[2 * i + 1]));
+    }
+    __device__ __forceinline__ static Pack narrow(const Vals<8> &f)
+    {
+        Pack p;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            p.u.w[2 * i] = __float_as_uint(f.v[i].x);
+            p.u.w[2 * i + 1] = __float_as_uint(f.v[i].y);
+        }
         return p;
     }
 };

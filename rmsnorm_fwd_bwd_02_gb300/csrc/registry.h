@@ -7,6 +7,7 @@
 namespace rmsk {
 
 struct RowShape {
+    int E;       // elements per pack (16/8 bf16 or 8/4 fp32 vectorised, 1 scalar)
     int L;       // lanes per row group
     int V;       // packs per lane
     int G;       // rows per group per iteration
@@ -14,18 +15,20 @@ struct RowShape {
     bool exact;  // H == L * V * E (no column masking)
     int threads() const { return L * S; }
     int tile_rows() const { return S * G; }
+    long long cols() const { return (long long)L * V * E; }
 };
 
 struct RowKernels {
     const char *name;
-    int E;               // elements per pack (8 bf16 / 4 fp32 vectorised, 1 scalar)
-    RowShape f, b;       // forward and backward layouts
+    RowShape f, b;           // forward and backward layouts
     const void *fwd[2];      // [residual]
     const void *bwd[2][2];   // [dh_out given][rstd given]
-    long long max_cols() const
+    long long max_cols() const { return f.cols() < b.cols() ? f.cols() : b.cols(); }
+    // bytes of one pack, for the alignment a call needs
+    int align(int elem_bytes) const
     {
-        const long long cf = (long long)f.L * f.V * E, cb = (long long)b.L * b.V * E;
-        return cf < cb ? cf : cb;
+        const int a = f.E > b.E ? f.E : b.E;
+        return a * elem_bytes;
     }
 };
 
@@ -55,6 +58,8 @@ struct SplitKernels {
 // bf16, 16-byte packs. Named for the feature count they are shaped for
 // (hNNN, exact) or the lanes of their masked layouts (gNNN).
 extern const RowKernels b_h128, b_h896, b_h4096, b_h5120, b_g32, b_g128, b_g512;
+// bf16 shaped layouts whose forward moves 32-byte packs (rows 32-byte aligned)
+extern const RowKernels b_h128w, b_h4096w, b_h5120w;
 // bf16, one element per access (rows not 16-byte aligned, odd H)
 extern const RowKernels b_s32, b_s1024;
 // fp32, 16-byte packs
@@ -70,16 +75,20 @@ unsigned int *stream_timeout_counter(int dev);
 
 } // namespace rmsk
 
-// RMSK_ROWS(name, type, E, forward L V G S MINB exact, backward L V G S MINB exact)
-#define RMSK_ROWS(NAME, T, E, FL, FV, FG, FS, FMB, FEX, BL, BV, BG, BS, BMB, BEX)      \
-    const RowKernels NAME = {                                                        \
-        #NAME, E, {FL, FV, FG, FS, FEX}, {BL, BV, BG, BS, BEX},                      \
-        {(const void *)&rms_fwd_rows<T, E, FL, FV, FG, FS, FMB, FEX, false>,         \
-         (const void *)&rms_fwd_rows<T, E, FL, FV, FG, FS, FMB, FEX, true>},         \
-        {{(const void *)&rms_bwd_rows<T, E, BL, BV, BG, BS, BMB, BEX, false, false>, \
-          (const void *)&rms_bwd_rows<T, E, BL, BV, BG, BS, BMB, BEX, false, true>}, \
-         {(const void *)&rms_bwd_rows<T, E, BL, BV, BG, BS, BMB, BEX, true, false>,  \
-          (const void *)&rms_bwd_rows<T, E, BL, BV, BG, BS, BMB, BEX, true, true>}}};
+// RMSK_ROWS2(name, type, forward E L V G S MINB exact, backward E L V G S MINB exact)
+#define RMSK_ROWS2(NAME, T, FE, FL, FV, FG, FS, FMB, FEX, BE, BL, BV, BG, BS, BMB, BEX)    \
+    const RowKernels NAME = {                                                            \
+        #NAME, {FE, FL, FV, FG, FS, FEX}, {BE, BL, BV, BG, BS, BEX},                     \
+        {(const void *)&rms_fwd_rows<T, FE, FL, FV, FG, FS, FMB, FEX, false>,            \
+         (const void *)&rms_fwd_rows<T, FE, FL, FV, FG, FS, FMB, FEX, true>},            \
+        {{(const void *)&rms_bwd_rows<T, BE, BL, BV, BG, BS, BMB, BEX, false, false>,    \
+          (const void *)&rms_bwd_rows<T, BE, BL, BV, BG, BS, BMB, BEX, false, true>},    \
+         {(const void *)&rms_bwd_rows<T, BE, BL, BV, BG, BS, BMB, BEX, true, false>,     \
+          (const void *)&rms_bwd_rows<T, BE, BL, BV, BG, BS, BMB, BEX, true, true>}}};
+
+// Same pack width in both directions.
+#define RMSK_ROWS(NAME, T, E, FL, FV, FG, FS, FMB, FEX, BL, BV, BG, BS, BMB, BEX)          \
+    RMSK_ROWS2(NAME, T, E, FL, FV, FG, FS, FMB, FEX, E, BL, BV, BG, BS, BMB, BEX)
 
 #define RMSK_STREAM(NAME, H, FGW, FV, FNG, FNS, BGW, BV, BNG, BNS)                       \
     static_assert(32 * FGW * FV * 8 == H && 32 * BGW * BV * 8 == H, "stream layout");    \

@@ -306,6 +306,26 @@ def test_misaligned_rows_take_scalar_path(orc):
                     {"y": y, "rstd": rstd, "dx": dx, "dw": dw}, o)
 
 
+@pytest.mark.parametrize("H", [128, 4096, 5120])
+def test_rows_16_byte_aligned_only(orc, H):
+    """Row starts on a 16-byte but not a 32-byte boundary: the forward cannot
+    use its 32-byte packs and falls back to 16-byte ones, with the same
+    results."""
+    M, dt = 301, torch.bfloat16
+    for residual in (False, True):
+        wl = W.Workload("a16", M, H, dt, residual=residual)
+        inp = synth(M, H, dt, seed=H, residual=residual)
+        o = oracle_all(orc, wl, inp)
+        g = {}
+        for k, v in inp.items():
+            b = torch.empty(v.numel() + 8, device=DEV, dtype=dt)
+            t = b[8:].view(v.shape)            # 16 bytes past a 256-byte boundary
+            t.copy_(v.to(DEV))
+            g[k] = t
+        got = gpu_fwd_bwd(wl, g)
+        compare_all(f"16B-aligned H={H} res={residual}", wl, got, o)
+
+
 def test_in_place(orc):
     M, H, dt = 300, 4096, torch.bfloat16
     inp = synth(M, H, dt, seed=7, residual=True)
