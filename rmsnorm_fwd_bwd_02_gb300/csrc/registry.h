@@ -32,11 +32,13 @@ struct RowKernels {
     }
 };
 
-// A streamed (bulk-copy fed) layout: NG groups of GW warps per CTA, each
-// thread V packs of a row, NS stages per group (stream.cuh). bf16 only.
+// A streamed (bulk-copy fed) layout, bf16 only: the CTA's threads and the
+// rows a CTA takes per round (stream.cuh: NG groups, one row each;
+// stream_small.cuh: NW warps, one block of rows each).
 struct StreamShape {
-    int GW, V, NG, NS;
-    int threads() const { return NG * GW * 32; }
+    int threads_;
+    int rows;
+    int threads() const { return threads_; }
 };
 
 struct StreamKernels {
@@ -69,7 +71,7 @@ extern const RowKernels f_s32, f_s1024;
 
 extern const SplitKernels split_bf16_v, split_bf16_s, split_f32_v, split_f32_s;
 
-extern const StreamKernels s_h4096, s_h5120;
+extern const StreamKernels s_h4096, s_h5120, s_h128;
 // Device address of the counter of streamed-kernel waits that ran out.
 unsigned int *stream_timeout_counter(int dev);
 
@@ -93,7 +95,7 @@ unsigned int *stream_timeout_counter(int dev);
 #define RMSK_STREAM(NAME, H, FGW, FV, FNG, FNS, BGW, BV, BNG, BNS)                       \
     static_assert(32 * FGW * FV * 8 == H && 32 * BGW * BV * 8 == H, "stream layout");    \
     const StreamKernels NAME = {                                                         \
-        #NAME, H, {FGW, FV, FNG, FNS}, {BGW, BV, BNG, BNS},                              \
+        #NAME, H, {FNG * FGW * 32, FNG}, {BNG * BGW * 32, BNG},                          \
         {(const void *)&rms_fwd_stream<FGW, FV, FNG, FNS, false>,                        \
          (const void *)&rms_fwd_stream<FGW, FV, FNG, FNS, true>},                        \
         {StreamSmem<FGW, FV, FNG, FNS, 1, 1>::kBytes,                                    \
@@ -106,6 +108,23 @@ unsigned int *stream_timeout_counter(int dev);
           StreamSmem<BGW, BV, BNG, BNS, 2, 1>::kBytes},                                  \
          {StreamSmem<BGW, BV, BNG, BNS, 3, 2>::kBytes,                                   \
           StreamSmem<BGW, BV, BNG, BNS, 3, 1>::kBytes}}};
+
+// Short rows (stream_small.cuh): H = 8 * NVP, NW warps, RPT rows per lane per stage.
+#define RMSK_SMALL(NAME, H, FRPT, FNW, FNS, BRPT, BNW, BNS)                               \
+    const StreamKernels NAME = {                                                         \
+        #NAME, H, {FNW * 32, FNW * (256 / H) * FRPT}, {BNW * 32, BNW * (256 / H) * BRPT}, \
+        {(const void *)&rms_fwd_stream_small<H / 8, FRPT, FNW, FNS, false>,              \
+         (const void *)&rms_fwd_stream_small<H / 8, FRPT, FNW, FNS, true>},              \
+        {SmallSmem<H / 8, FRPT, FNW, FNS, 1>::kBytes,                                    \
+         SmallSmem<H / 8, FRPT, FNW, FNS, 2>::kBytes},                                   \
+        {{(const void *)&rms_bwd_stream_small<H / 8, BRPT, BNW, BNS, false, false>,      \
+          (const void *)&rms_bwd_stream_small<H / 8, BRPT, BNW, BNS, false, true>},      \
+         {(const void *)&rms_bwd_stream_small<H / 8, BRPT, BNW, BNS, true, false>,       \
+          (const void *)&rms_bwd_stream_small<H / 8, BRPT, BNW, BNS, true, true>}},      \
+        {{SmallSmem<H / 8, BRPT, BNW, BNS, 2>::kBytes,                                   \
+          SmallSmem<H / 8, BRPT, BNW, BNS, 2>::kBytes},                                  \
+         {SmallSmem<H / 8, BRPT, BNW, BNS, 3>::kBytes,                                   \
+          SmallSmem<H / 8, BRPT, BNW, BNS, 3>::kBytes}}};
 
 #define RMSK_SPLIT(NAME, T, E)                                                    \
     const SplitKernels NAME = {                                                   \

@@ -6,6 +6,7 @@
 
 #include "registry.h"
 #include "stream.cuh"
+#include "stream_small.cuh"
 
 namespace rmsk {
 
@@ -34,5 +35,9 @@ unsigned int *stream_timeout_counter(int dev)
 //           name     H     |-- forward: GW V NG NS --| |-- backward: GW V NG NS --|
 RMSK_STREAM(s_h4096, 4096,   4, 4, 4, 4,               8, 2, 2, 6)
 RMSK_STREAM(s_h5120, 5120,   4, 5, 3, 3,              10, 2, 2, 3)
+
+// 128-wide rows (QK-norm): warps with their own rings of row blocks.
+//          name    H    |- forward: RPT NW NS -| |- backward: RPT NW NS -|
+RMSK_SMALL(s_h128, 128,       4,   16,  4,              8,   8,  3)
 
 } // namespace rmsk

@@ -187,7 +187,7 @@ def test_edge_shapes(orc, M, H, dtype):
         compare_all(f"M={M} H={H} {dtype} res={residual}", wl, got, o)
 
 
-STREAM_H = (4096, 5120)     # bf16 feature counts with a streamed layout
+STREAM_H = (128, 4096, 5120)     # bf16 feature counts with a streamed layout
 
 
 @pytest.mark.parametrize("path", [rn.PATH_ROWS, rn.PATH_SPLIT, rn.PATH_SCALAR,
@@ -215,23 +215,32 @@ def test_forced_paths_agree_with_oracle(orc, path, H):
 
 @pytest.mark.parametrize("name,M", [("qwen3-8b-train", 1), ("qwen3-8b-train", 7),
                                     ("qwen3-8b-train", 1037), ("residual-14b", 3),
-                                    ("residual-14b", 517)])
+                                    ("residual-14b", 517), ("qwen3-qknorm", 1),
+                                    ("qwen3-qknorm", 7), ("qwen3-qknorm", 33),
+                                    ("qwen3-qknorm", 40961)])
 def test_stream_path_ragged(orc, name, M):
     """Streamed kernels: every variant (residual, dh_out given or not, rstd
     given or recomputed) on row counts that leave groups idle or uneven."""
     wl = W.WORKLOADS[name].with_rows(M)
     inp = W.make_inputs(wl)
     g = to_dev(inp)
-    with forced_path(rn.PATH_STREAM):
+    variants = [(wl, inp, g)]
+    if name == "qwen3-qknorm":       # the residual variant on short rows too
+        rw = W.Workload("qk-res", M, 128, torch.bfloat16, residual=True, dy_std=1e-2)
+        ri = synth(M, 128, torch.bfloat16, seed=M, residual=True)
+        variants.append((rw, ri, to_dev(ri)))
+    for wl, inp, g in variants:
         for dh in ((True, False) if wl.residual else (True,)):
             for with_rstd in (True, False):
                 o = oracle_all(orc, wl, inp, dh=dh)
-                got = gpu_fwd_bwd(wl, g, dh=dh, with_rstd=with_rstd)
-                assert rn.last_path() == rn.PATH_STREAM
-                compare_all(f"stream {name} M={M} dh={dh} rstd={with_rstd}", wl, got, o)
+                with forced_path(rn.PATH_STREAM):
+                    got = gpu_fwd_bwd(wl, g, dh=dh, with_rstd=with_rstd)
+                    assert rn.last_path() == rn.PATH_STREAM
+                compare_all(f"stream {wl.name} M={M} dh={dh} rstd={with_rstd}",
+                            wl, got, o)
 
 
-@pytest.mark.parametrize("name", ["qwen3-8b-train", "residual-14b"])
+@pytest.mark.parametrize("name", ["qwen3-8b-train", "residual-14b", "qwen3-qknorm"])
 def test_stream_path_full_size_sampled(orc, name):
     wl = W.WORKLOADS[name]
     inp = W.make_inputs(wl)
