@@ -179,6 +179,19 @@ int rmsnorm_last_path(void);
 int rmsnorm_wait_timeouts(unsigned int *count, int reset);
 
 /*
+ * Test hook for the bounded waits of the streamed kernels, process-wide, not
+ * thread-safe against concurrent calls: later streamed launches make every
+ * stage wait for extra_tx_bytes more than its copies deliver (so each wait
+ * runs out) and give up after wait_limit_us microseconds (0 = the default of
+ * about one second). (0, 0) restores normal operation. With a non-zero
+ * extra_tx_bytes the results of those calls are left incomplete and
+ * rmsnorm_wait_timeouts counts the waits that ran out; the kernels still end
+ * and the CUDA context stays usable.
+ */
+void rmsnorm_set_stream_test_fault(unsigned int extra_tx_bytes,
+                                   unsigned int wait_limit_us);
+
+/*
  * Backward that allocates nothing and needs no workspace from the caller.
  * The pages have no counterpart to this entry point; it exists for callers
  * that cannot call cudaMalloc at all: plug-ins hosted by a runtime that owns

@@ -27,6 +27,8 @@ constexpr int kReduceCols = 32, kReduceRows = 16;
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_path = 0;
 std::atomic<int> g_path_override{kPathAuto};
+// Test hook for the streamed kernels' bounded waits (see rmsnorm.h).
+std::atomic<unsigned> g_test_extra_tx{0}, g_test_wait_us{0};
 
 int cuda_fail(cudaError_t e)
 {
@@ -294,6 +296,8 @@ int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, floa
         if (tmo == nullptr)
             return cuda_fail(cudaErrorInvalidSymbol);
         FwdParams p = {x, r, w, y, h, rstd, M, (int)H, eps};
+        p.extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
+        p.wait_limit_us = g_test_wait_us.load(std::memory_order_relaxed);
         cudaError_t e = launch2(fn, dim3((unsigned)grid), dim3(k.f.threads()), smem, stream, &p,
                                 &tmo);
         if (e != cudaSuccess)
@@ -405,6 +409,10 @@ int bwd_impl(const void *dy, const void *dh, const void *x, const void *w, const
 
     if (M > 0) {
         BwdParams p = {dy, x, w, rstd, dh, dx, static_cast<float *>(ws), M, (int)H, eps};
+        if (pl.stream) {
+            p.extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
+            p.wait_limit_us = g_test_wait_us.load(std::memory_order_relaxed);
+        }
         cudaError_t e =
             pl.stream ? launch2(pl.fn, dim3((unsigned)pl.grid), dim3(pl.threads), pl.smem, stream,
                                 &p, &pl.timeouts)
@@ -553,6 +561,12 @@ int rmsnorm_last_cuda_error(void) { return t_last_cuda_error; }
 void rmsnorm_set_path_override(int path)
 {
     g_path_override.store(path >= kPathAuto && path <= kPathStream ? path : kPathAuto);
+}
+
+void rmsnorm_set_stream_test_fault(unsigned int extra_tx_bytes, unsigned int wait_limit_us)
+{
+    g_test_extra_tx.store(extra_tx_bytes);
+    g_test_wait_us.store(wait_limit_us);
 }
 
 int rmsnorm_wait_timeouts(unsigned int *count, int reset)

@@ -17,6 +17,11 @@ struct FwdParams {
     int64_t M;
     int H;
     float eps;
+    // Streamed kernels only: bytes a stage waits for beyond what its copies
+    // deliver (0; a test sets it to make waits run out) and the wait limit
+    // in microseconds (0 = the default of about one second).
+    uint32_t extra_tx;
+    uint32_t wait_limit_us;
 };
 
 // Row-wise backward (rows.cuh).
@@ -31,6 +36,8 @@ struct BwdParams {
     int64_t M;
     int H;
     float eps;
+    uint32_t extra_tx;       // as in FwdParams
+    uint32_t wait_limit_us;
 };
 
 // Split-row forward (split.cuh).

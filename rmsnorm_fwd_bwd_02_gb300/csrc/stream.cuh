@@ -26,6 +26,11 @@ namespace rmsk {
 
 constexpr unsigned long long kStageWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
+__device__ __forceinline__ unsigned long long wait_limit_ns(uint32_t us)
+{
+    return us ? 1000ull * us : kStageWaitLimitNs;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -68,14 +73,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait for the phase with this parity to complete; false if it has not
-// within kStageWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+// within limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kStageWaitLimitNs)
+        if (global_ns() - t0 > limit_ns)
             return false;
     return true;
 }
@@ -181,6 +187,7 @@ rms_fwd_stream(const FwdParams p, unsigned int *timeouts)
     mbar_init_fence();
     __syncthreads();
     griddep_wait();
+    const unsigned long long limit = wait_limit_ns(p.wait_limit_us);
 
     P wp[V];
 #pragma unroll
@@ -197,7 +204,7 @@ rms_fwd_stream(const FwdParams p, unsigned int *timeouts)
         const int s = (int)(k % NSE);
         const uint32_t st = stage0 + s * SM::kStageBytes;
         const uint32_t bar = bar0 + 8 * s;
-        mbar_expect_tx(bar, SM::kStageBytes);
+        mbar_expect_tx(bar, SM::kStageBytes + p.extra_tx);
         bulk_g2s(st, static_cast<const uint4 *>(p.x) + row * NV, SM::kRowBytes, bar);
         if constexpr (RES)
             bulk_g2s(st + SM::kRowBytes, static_cast<const uint4 *>(p.r) + row * NV,
@@ -229,7 +236,7 @@ rms_fwd_stream(const FwdParams p, unsigned int *timeouts)
     for (; k < nk; ++k) {
         const int64_t row = gg + k * TG;
         const uint32_t st = stage0 + (int)(k % NSE) * SM::kStageBytes;
-        const bool ok = mbar_wait_bounded(bar0 + 8 * (int)(k % NSE), (uint32_t)((k / NSE) & 1));
+        const bool ok = mbar_wait_bounded(bar0 + 8 * (int)(k % NSE), (uint32_t)((k / NSE) & 1), limit);
 
         F acc = splat<F>(0.f);
 #pragma unroll
@@ -278,9 +285,11 @@ rms_fwd_stream(const FwdParams p, unsigned int *timeouts)
     if (failed && t == 0) {
         atomicAdd(timeouts, 1u);
         // drain this group's copies still in flight (bounded):
-        // rows k .. k+NSE-2 were issued and not consumed
-        for (int64_t q = k; q < k + NSE - 1 && q < nk; ++q)
-            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1));
+        // issued and not consumed: rows k .. k+NSE-2, or all NSE of the
+        // prologue when the first wait ran out
+        const int64_t last = k == 0 ? NSE - 1 : k + NSE - 2;
+        for (int64_t q = k; q <= last && q < nk; ++q)
+            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1), limit);
     }
     griddep_launch_dependents();
 }
@@ -315,6 +324,7 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
     mbar_init_fence();
     __syncthreads();
     griddep_wait();
+    const unsigned long long limit = wait_limit_ns(p.wait_limit_us);
 
     P wp[V];        // weight kept packed (registers are the constraint here)
     X acc[V];
@@ -334,7 +344,7 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
         const int s = (int)(k % NSE);
         const uint32_t st = stage0 + s * SM::kStageBytes;
         const uint32_t bar = bar0 + 8 * s;
-        mbar_expect_tx(bar, SM::kStageBytes);
+        mbar_expect_tx(bar, SM::kStageBytes + p.extra_tx);
         bulk_g2s(st, static_cast<const uint4 *>(p.x) + row * NV, SM::kRowBytes, bar);
         bulk_g2s(st + SM::kRowBytes, static_cast<const uint4 *>(p.dy) + row * NV,
                  SM::kRowBytes, bar);
@@ -363,7 +373,7 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
             if (k + 1 < nk)
                 r_next = p.rstd[row + TG];
         }
-        const bool ok = mbar_wait_bounded(bar0 + 8 * (int)(k % NSE), (uint32_t)((k / NSE) & 1));
+        const bool ok = mbar_wait_bounded(bar0 + 8 * (int)(k % NSE), (uint32_t)((k / NSE) & 1), limit);
 
         F cs = splat<F>(0.f), ss = splat<F>(0.f);
 #pragma unroll
@@ -437,9 +447,11 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
     }
     if (failed && t == 0) {
         atomicAdd(timeouts, 1u);
-        // rows k .. k+NSE-2 were issued and not consumed
-        for (int64_t q = k; q < k + NSE - 1 && q < nk; ++q)
-            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1));
+        // issued and not consumed: rows k .. k+NSE-2, or all NSE of the
+        // prologue when the first wait ran out
+        const int64_t last = k == 0 ? NSE - 1 : k + NSE - 2;
+        for (int64_t q = k; q <= last && q < nk; ++q)
+            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1), limit);
     }
     griddep_launch_dependents();
 

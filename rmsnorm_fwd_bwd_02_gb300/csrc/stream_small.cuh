@@ -64,6 +64,7 @@ rms_fwd_stream_small(const FwdParams p, unsigned int *timeouts)
     mbar_init_fence();
     __syncwarp();
     griddep_wait();
+    const unsigned long long limit = wait_limit_ns(p.wait_limit_us);
 
     X wv;
     P::load_cached(p.w, pk).widen(wv);
@@ -80,7 +81,7 @@ rms_fwd_stream_small(const FwdParams p, unsigned int *timeouts)
         const int s = (int)(k % NSE);
         const uint32_t st = stage0 + s * SM::kStageBytes;
         const uint32_t bar = bar0 + 8 * s;
-        mbar_expect_tx(bar, NTEN * bytes);
+        mbar_expect_tx(bar, NTEN * bytes + p.extra_tx);
         bulk_g2s(st, static_cast<const uint4 *>(p.x) + row0 * NVP, bytes, bar);
         if constexpr (RES)
             bulk_g2s(st + SM::kTenBytes, static_cast<const uint4 *>(p.r) + row0 * NVP, bytes,
@@ -99,7 +100,7 @@ rms_fwd_stream_small(const FwdParams p, unsigned int *timeouts)
         const int64_t row0 = (wgid + k * TW) * SM::kRows;
         const int s = (int)(k % NSE);
         const uint32_t st = stage0 + s * SM::kStageBytes;
-        const bool ok = mbar_wait_bounded(bar0 + 8 * s, (uint32_t)((k / NSE) & 1));
+        const bool ok = mbar_wait_bounded(bar0 + 8 * s, (uint32_t)((k / NSE) & 1), limit);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
             failed = true;
             break;
@@ -150,7 +151,7 @@ rms_fwd_stream_small(const FwdParams p, unsigned int *timeouts)
     if (failed && lane == 0) {
         atomicAdd(timeouts, 1u);
         for (int64_t q = k; q < k + NSE && q < nk; ++q)
-            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1));
+            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1), limit);
     }
     griddep_launch_dependents();
 }
@@ -183,6 +184,7 @@ rms_bwd_stream_small(const BwdParams p, unsigned int *timeouts)
     mbar_init_fence();
     __syncwarp();
     griddep_wait();
+    const unsigned long long limit = wait_limit_ns(p.wait_limit_us);
 
     X wv, acc = X::zero();
     P::load_cached(p.w, pk).widen(wv);
@@ -199,7 +201,7 @@ rms_bwd_stream_small(const BwdParams p, unsigned int *timeouts)
         const int s = (int)(k % NSE);
         const uint32_t st = stage0 + s * SM::kStageBytes;
         const uint32_t bar = bar0 + 8 * s;
-        mbar_expect_tx(bar, NTEN * bytes);
+        mbar_expect_tx(bar, NTEN * bytes + p.extra_tx);
         bulk_g2s(st, static_cast<const uint4 *>(p.x) + row0 * NVP, bytes, bar);
         bulk_g2s(st + SM::kTenBytes, static_cast<const uint4 *>(p.dy) + row0 * NVP, bytes, bar);
         if constexpr (DH)
@@ -228,7 +230,7 @@ rms_bwd_stream_small(const BwdParams p, unsigned int *timeouts)
                 rs[j] = row < p.M ? p.rstd[row] : 0.f;
             }
         }
-        const bool ok = mbar_wait_bounded(bar0 + 8 * s, (uint32_t)((k / NSE) & 1));
+        const bool ok = mbar_wait_bounded(bar0 + 8 * s, (uint32_t)((k / NSE) & 1), limit);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
             failed = true;
             break;
@@ -301,7 +303,7 @@ rms_bwd_stream_small(const BwdParams p, unsigned int *timeouts)
     if (failed && lane == 0) {
         atomicAdd(timeouts, 1u);
         for (int64_t q = k; q < k + NSE && q < nk; ++q)
-            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1));
+            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1), limit);
     }
     griddep_launch_dependents();
 

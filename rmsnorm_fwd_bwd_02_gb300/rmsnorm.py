@@ -39,6 +39,7 @@ SIGNATURES = {
     "rmsnorm_bwd_static_scratch": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                           _i64, _f, _int, _vp]),
     "rmsnorm_wait_timeouts": (_int, [ctypes.POINTER(ctypes.c_uint), _int]),
+    "rmsnorm_set_stream_test_fault": (None, [ctypes.c_uint, ctypes.c_uint]),
 }
 
 
@@ -119,6 +120,11 @@ def wait_timeouts(reset: bool = False) -> int:
     _check(lib().rmsnorm_wait_timeouts(ctypes.byref(c), int(reset)),
            "rmsnorm_wait_timeouts")
     return int(c.value)
+
+
+def set_stream_test_fault(extra_tx_bytes: int, wait_limit_us: int):
+    """Test hook: make the streamed kernels' waits run out (see rmsnorm.h)."""
+    lib().rmsnorm_set_stream_test_fault(int(extra_tx_bytes), int(wait_limit_us))
 
 
 def bwd_workspace_bytes(M: int, H: int, dtype: torch.dtype) -> int:

@@ -559,6 +559,31 @@ def test_side_stream():
         check_bits(f"side stream {k}", v, ref[k])
 
 
+@pytest.mark.parametrize("name,M", [("qwen3-8b-train", 257), ("residual-14b", 129),
+                                    ("qwen3-qknorm", 1000)])
+def test_stream_wait_runs_out_and_context_survives(orc, name, M):
+    """Make every streamed wait run out (each stage expects 16 bytes that no
+    copy delivers, 20 ms limit): the kernels record it, drain their copies,
+    end, and the next normal calls are right."""
+    wl = W.WORKLOADS[name].with_rows(M)
+    inp = W.make_inputs(wl)
+    g = to_dev(inp)
+    before = rn.wait_timeouts(reset=True)
+    assert before == 0
+    rn.set_stream_test_fault(16, 20000)
+    try:
+        with forced_path(rn.PATH_STREAM):
+            gpu_fwd_bwd(wl, g)          # results incomplete by design
+        torch.cuda.synchronize()
+    finally:
+        rn.set_stream_test_fault(0, 0)
+    assert rn.wait_timeouts(reset=True) > 0
+    with forced_path(rn.PATH_STREAM):
+        got = gpu_fwd_bwd(wl, g)
+    compare_all(f"after timeouts {name}", wl, got, oracle_all(orc, wl, inp))
+    assert rn.wait_timeouts() == 0
+
+
 def test_no_stream_wait_ran_out():
     """Every bounded wait in the streamed kernels completed during this module."""
     assert rn.wait_timeouts() == 0
