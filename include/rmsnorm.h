@@ -63,9 +63,10 @@ typedef enum {
     RMSNORM_ERR_UNSUPPORTED = -7, /* H > RMSNORM_MAX_H */
     RMSNORM_ERR_CUDA = -8,        /* a CUDA runtime call failed */
     RMSNORM_ERR_ALIAS = -9,       /* buffers overlap in a way not allowed */
-    RMSNORM_ERR_SCRATCH_LIMIT = -10 /* rmsnorm_bwd_static_scratch: the problem
+    RMSNORM_ERR_SCRATCH_LIMIT = -10, /* rmsnorm_bwd_static_scratch: the problem
                                        needs more scratch than the library's
                                        built-in RMSNORM_STATIC_SCRATCH_BYTES */
+    RMSNORM_ERR_BAD_FLAGS = -11   /* rmsnorm_bwd_ex: unknown flag bits */
 } rmsnorm_status;
 
 /* Largest feature count the kernels hold in registers ([P1 §7.1] puts the
@@ -137,6 +138,22 @@ int rmsnorm_residual_bwd(const void *dy, const void *dh_out, const void *h,
                          const void *w, const float *rstd, void *dx, float *dw,
                          void *workspace, size_t workspace_bytes, int64_t M,
                          int64_t H, float eps, int dtype, void *stream);
+
+/*
+ * Backward with options: the plain backward when dh_out is NULL, the
+ * residual backward otherwise (x then holds h), with the same arguments,
+ * results, aliasing and errors as rmsnorm_bwd / rmsnorm_residual_bwd, plus
+ *   flags: 0, or RMSNORM_BWD_ACCUMULATE_DW to add this call's dw to the dw
+ *   already in the buffer (gradient accumulation over micro-batches or over
+ *   chunks of rows) instead of overwriting it. The addition follows the
+ *   fixed-order sum of this call, so a sequence of calls in stream order is
+ *   reproducible. Unknown bits give RMSNORM_ERR_BAD_FLAGS.
+ */
+#define RMSNORM_BWD_ACCUMULATE_DW 1
+int rmsnorm_bwd_ex(const void *dy, const void *dh_out, const void *x,
+                   const void *w, const float *rstd, void *dx, float *dw,
+                   void *workspace, size_t workspace_bytes, int64_t M,
+                   int64_t H, float eps, int dtype, int flags, void *stream);
 
 /*
  * Bytes of workspace rmsnorm_bwd / rmsnorm_residual_bwd need for (M, H,

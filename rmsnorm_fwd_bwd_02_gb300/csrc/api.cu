@@ -369,7 +369,7 @@ int bwd_plan(int dtype, int64_t M, int64_t H, bool vec, bool dh, bool have_rstd,
 
 int bwd_impl(const void *dy, const void *dh, const void *x, const void *w, const float *rstd,
              void *dx, float *dw, void *ws, size_t ws_bytes, int64_t M, int64_t H, float eps,
-             int dtype, cudaStream_t stream)
+             int dtype, cudaStream_t stream, int flags = 0)
 {
     int st = check_common(M, H, eps, dtype);
     if (st)
@@ -422,13 +422,14 @@ int bwd_impl(const void *dy, const void *dh, const void *x, const void *w, const
             return cuda_fail(e);
     }
     const float *part = static_cast<const float *>(ws);
-    int P = (int)pl.grid, Hi = (int)H;
+    int P = (int)pl.grid, Hi = (int)H, acc = (flags & RMSNORM_BWD_ACCUMULATE_DW) ? 1 : 0;
     struct {
         const float *part;
         int P, H;
         float *dw;
-    } a = {part, P, Hi, dw};
-    void *args[4] = {&a.part, &a.P, &a.H, &a.dw};
+        int acc;
+    } a = {part, P, Hi, dw, acc};
+    void *args[5] = {&a.part, &a.P, &a.H, &a.dw, &a.acc};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((H + kReduceCols - 1) / kReduceCols));
     cfg.blockDim = dim3(kReduceCols * kReduceRows);
@@ -519,6 +520,17 @@ int rmsnorm_residual_bwd(const void *dy, const void *dh_out, const void *h, cons
                     dtype, static_cast<cudaStream_t>(stream));
 }
 
+int rmsnorm_bwd_ex(const void *dy, const void *dh_out, const void *x, const void *w,
+                   const float *rstd, void *dx, float *dw, void *workspace,
+                   size_t workspace_bytes, int64_t M, int64_t H, float eps, int dtype, int flags,
+                   void *stream)
+{
+    if (flags & ~RMSNORM_BWD_ACCUMULATE_DW)
+        return RMSNORM_ERR_BAD_FLAGS;
+    return bwd_impl(dy, dh_out, x, w, rstd, dx, dw, workspace, workspace_bytes, M, H, eps,
+                    dtype, static_cast<cudaStream_t>(stream), flags);
+}
+
 size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype)
 {
     if (check_common(M, H, 0.f, dtype) != RMSNORM_OK)
@@ -550,6 +562,7 @@ const char *rmsnorm_status_string(int status)
     case RMSNORM_ERR_UNSUPPORTED: return "H exceeds RMSNORM_MAX_H";
     case RMSNORM_ERR_CUDA: return "a CUDA runtime call failed (see rmsnorm_last_cuda_error)";
     case RMSNORM_ERR_ALIAS: return "output buffers overlap inputs or each other in a way not allowed";
+    case RMSNORM_ERR_BAD_FLAGS: return "unknown bits in flags";
     case RMSNORM_ERR_SCRATCH_LIMIT:
         return "problem needs more scratch than RMSNORM_STATIC_SCRATCH_BYTES (use rmsnorm_bwd with a workspace)";
     default: return "unknown status";

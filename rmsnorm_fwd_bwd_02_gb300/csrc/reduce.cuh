@@ -11,10 +11,12 @@ namespace rmsk {
 
 // CW columns per CTA, RY threads per column. Thread (tx, ty) adds partial
 // rows ty, ty+RY, ty+2RY, ... of column blockIdx.x*CW+tx; the RY sums are
-// then added in ty order. With P == 0 (no rows) dw is all zeros.
+// then added in ty order. With P == 0 (no rows) dw is all zeros. With
+// accumulate != 0 the total is added to the dw already there (gradient
+// accumulation over micro-batches), after the fixed-order sum.
 template <int CW, int RY>
 __global__ void __launch_bounds__(CW * RY)
-dw_reduce(const float *__restrict__ part, int P, int H, float *__restrict__ dw)
+dw_reduce(const float *__restrict__ part, int P, int H, float *__restrict__ dw, int accumulate)
 {
     __shared__ float sm[RY][CW + 1];
     // Launched with programmatic serialization after the backward kernel:
@@ -37,7 +39,7 @@ dw_reduce(const float *__restrict__ part, int P, int H, float *__restrict__ dw)
 #pragma unroll
         for (int q = 0; q < RY; ++q)
             t += sm[q][tx];
-        dw[col] = t;
+        dw[col] = accumulate ? dw[col] + t : t;
     }
 }
 

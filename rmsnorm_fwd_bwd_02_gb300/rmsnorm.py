@@ -40,7 +40,11 @@ SIGNATURES = {
                                           _i64, _f, _int, _vp]),
     "rmsnorm_wait_timeouts": (_int, [ctypes.POINTER(ctypes.c_uint), _int]),
     "rmsnorm_set_stream_test_fault": (None, [ctypes.c_uint, ctypes.c_uint]),
+    "rmsnorm_bwd_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64,
+                              _i64, _f, _int, _int, _vp]),
 }
+
+BWD_ACCUMULATE_DW = 1
 
 
 class RmsNormError(RuntimeError):
@@ -209,6 +213,32 @@ def rmsnorm_residual_bwd(dy, dh_out, h, w, rstd=None, dx=None, dw=None,
         _ptr(dw), _ptr(workspace), workspace.numel() * workspace.element_size(),
         M, H, float(eps), _dtype_code(h), _stream(stream)),
         "rmsnorm_residual_bwd")
+    return dx, dw
+
+
+def rmsnorm_bwd_ex(dy, x, w, rstd=None, dh_out=None, dx=None, dw=None,
+                   workspace=None, eps=1e-6, accumulate_dw=False, stream=None):
+    """(dx, dw) of the plain (dh_out None) or residual backward; with
+    accumulate_dw the call adds its dw into the given dw buffer."""
+    H = w.numel()
+    M = _rows("x", x, H)
+    _rows("dy", dy, H, x.dtype)
+    if dh_out is not None:
+        _rows("dh_out", dh_out, H, x.dtype)
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        if accumulate_dw:
+            raise ValueError("accumulate_dw needs the dw buffer to add into")
+        dw = torch.empty(H, device=x.device, dtype=torch.float32)
+    need = bwd_workspace_bytes(M, H, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=x.device, dtype=torch.uint8)
+    _check(lib().rmsnorm_bwd_ex(
+        _ptr(dy), _ptr(dh_out), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), M, H,
+        float(eps), _dtype_code(x), BWD_ACCUMULATE_DW if accumulate_dw else 0,
+        _stream(stream)), "rmsnorm_bwd_ex")
     return dx, dw
 
 

@@ -119,6 +119,15 @@ def test_bwd_argument_checks(lib):
              None) == BAD_SHAPE
 
 
+def test_bwd_ex_rejects_unknown_flags(lib):
+    f = lib.rmsnorm_bwd_ex
+    E = 0x7f0400000000
+    W = 0x7f0500000000
+    assert f(A, None, B, C, D, E, 0x7f0600000000, W, 1 << 20, 4, 8, 1e-6, BF16,
+             2, None) == -11
+    assert lib.rmsnorm_status_string(-11).decode() != "unknown status"
+
+
 def test_workspace_query_without_device(lib):
     import torch
     if torch.cuda.is_available():

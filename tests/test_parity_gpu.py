@@ -363,6 +363,50 @@ def test_in_place(orc):
     check_rows("in-place resid dx", dx, o["dx"], dt, o["tdx"])
 
 
+@pytest.mark.parametrize("name", ["qwen3-8b-train", "qwen3-qknorm", "residual-14b"])
+def test_bwd_ex_accumulates_dw_over_chunks(orc, name):
+    """dw accumulated over chunks of rows equals the dw of all rows (within
+    the dw tolerance), dx of each chunk is right, and flags = 0 gives the
+    bits of the plain entry point."""
+    wl = W.WORKLOADS[name].with_rows(2051)
+    inp = W.make_inputs(wl)
+    g = to_dev(inp)
+    o = oracle_all(orc, wl, inp)
+    xk = "x"
+    if wl.residual:
+        h, _, rstd = rn.rmsnorm_residual_fwd(g["x"], g["r"], g["w"], eps=wl.eps)
+        g["h"] = h
+        xk = "h"
+    else:
+        _, rstd = rn.rmsnorm_fwd(g["x"], g["w"], eps=wl.eps)
+    dh = g.get("dh")
+    dw = torch.full((wl.H,), float("nan"), device=DEV)
+    dx = torch.empty_like(g[xk])
+    bounds = [0, 1, 700, 1500, 2051]          # uneven chunks, one of one row
+    for i, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
+        rn.rmsnorm_bwd_ex(g["dy"][a:b], g[xk][a:b], g["w"], rstd[a:b],
+                          dh_out=None if dh is None else dh[a:b], dx=dx[a:b], dw=dw,
+                          eps=wl.eps, accumulate_dw=i > 0)
+    torch.cuda.synchronize()
+    check_rows(f"{name} chunked dx", dx, o["dx"], wl.dtype, o["tdx"])
+    check_dw(f"{name} accumulated dw", dw, o["dw"], o["tdw"])
+    # M == 0 with accumulation leaves dw as it is
+    before = dw.clone()
+    rn.rmsnorm_bwd_ex(g["dy"][:0], g[xk][:0], g["w"], rstd[:0], dw=dw,
+                      accumulate_dw=True)
+    torch.cuda.synchronize()
+    check_bits(f"{name} M=0 accumulate", dw, before)
+    # flags = 0: same bits as the plain entry points
+    dx1, dw1 = rn.rmsnorm_bwd_ex(g["dy"], g[xk], g["w"], rstd, dh_out=dh, eps=wl.eps)
+    if wl.residual:
+        dx2, dw2 = rn.rmsnorm_residual_bwd(g["dy"], dh, g[xk], g["w"], rstd, eps=wl.eps)
+    else:
+        dx2, dw2 = rn.rmsnorm_bwd(g["dy"], g[xk], g["w"], rstd, eps=wl.eps)
+    torch.cuda.synchronize()
+    check_bits(f"{name} bwd_ex dx", dx1, dx2)
+    check_bits(f"{name} bwd_ex dw", dw1, dw2)
+
+
 def test_rstd_recompute_matches_saved(orc):
     wl = W.WORKLOADS["qwen3-8b-train"].with_rows(513)
     inp = W.make_inputs(wl)
