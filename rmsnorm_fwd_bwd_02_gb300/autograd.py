@@ -1,0 +1,120 @@
+"""PyTorch autograd functions and modules over the C ABI.
+
+[P1] "训推加速 Qwen3 实战：从“调包”到手写 Triton Kernel（含 backward）" §5.5 wraps
+its kernels in a torch.autograd.Function (saving x and the weight, returning
+(dx, dw, None)) and exposes an nn.Module; §5.6 lists the backward gotchas:
+make dy contiguous, save tensors with save_for_backward, return one gradient
+per forward input (None for eps), take eps as a float, and raise on double
+backward unless it is implemented. These wrappers follow that shape over the
+CUDA kernels of librmsnorm.so; the forward also saves rstd, so the backward
+does not recompute it. Every arithmetic step runs in the CUDA kernels;
+there is no CPU fallback (CPU tensors raise).
+"""
+import torch
+from torch.autograd.function import once_differentiable
+
+from . import rmsnorm as _rn
+
+
+def _rows2d(t, H):
+    """A contiguous [M, H] view (a copy only when t is not contiguous)."""
+    return t.contiguous().view(-1, H)
+
+
+class RMSNormFunction(torch.autograd.Function):
+    """y = w * x / sqrt(mean(x^2) + eps) over the last dimension."""
+
+    @staticmethod
+    def forward(ctx, x, weight, eps: float = 1e-6):
+        H = weight.numel()
+        x2 = _rows2d(x, H)
+        y, rstd = _rn.rmsnorm_fwd(x2, weight, eps=float(eps))
+        ctx.save_for_backward(x2, weight, rstd)
+        ctx.eps = float(eps)
+        ctx.shape = x.shape
+        return y.view(x.shape)
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, dy):
+        x2, weight, rstd = ctx.saved_tensors
+        H = weight.numel()
+        dx, dw = _rn.rmsnorm_bwd(_rows2d(dy, H), x2, weight, rstd, eps=ctx.eps)
+        dx = dx.view(ctx.shape) if ctx.needs_input_grad[0] else None
+        dw = dw.to(weight.dtype) if ctx.needs_input_grad[1] else None
+        return dx, dw, None
+
+
+class ResidualRMSNormFunction(torch.autograd.Function):
+    """h = x + r (rounded to the dtype), y = RMSNorm(h); returns (y, h). The
+    gradient of x and of r is the same tensor: the norm's backward at h
+    plus the gradient arriving on h."""
+
+    @staticmethod
+    def forward(ctx, x, residual, weight, eps: float = 1e-6):
+        H = weight.numel()
+        x2, r2 = _rows2d(x, H), _rows2d(residual, H)
+        h, y, rstd = _rn.rmsnorm_residual_fwd(x2, r2, weight, eps=float(eps))
+        ctx.save_for_backward(h, weight, rstd)
+        ctx.eps = float(eps)
+        ctx.shape = x.shape
+        return y.view(x.shape), h.view(x.shape)
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, dy, dh):
+        h, weight, rstd = ctx.saved_tensors
+        H = weight.numel()
+        if dy is None:
+            dy = torch.zeros_like(h)
+        dh2 = None if dh is None else _rows2d(dh, H)
+        dx, dw = _rn.rmsnorm_residual_bwd(_rows2d(dy, H), dh2, h, weight, rstd,
+                                          eps=ctx.eps)
+        dx = dx.view(ctx.shape)
+        dw = dw.to(weight.dtype) if ctx.needs_input_grad[2] else None
+        gx = dx if ctx.needs_input_grad[0] else None
+        gr = dx if ctx.needs_input_grad[1] else None
+        return gx, gr, dw, None
+
+
+def rms_norm(x, weight, eps: float = 1e-6):
+    return RMSNormFunction.apply(x, weight, eps)
+
+
+def residual_rms_norm(x, residual, weight, eps: float = 1e-6):
+    return ResidualRMSNormFunction.apply(x, residual, weight, eps)
+
+
+class RMSNorm(torch.nn.Module):
+    """Qwen3-style RMSNorm over the last dimension (weight initialised to 1)."""
+
+    def __init__(self, hidden_size: int, eps: float = 1e-6, device=None,
+                 dtype=torch.bfloat16):
+        super().__init__()
+        self.weight = torch.nn.Parameter(
+            torch.ones(hidden_size, device=device, dtype=dtype))
+        self.eps = float(eps)
+
+    def forward(self, x):
+        return RMSNormFunction.apply(x, self.weight, self.eps)
+
+    def extra_repr(self):
+        return f"{self.weight.numel()}, eps={self.eps}"
+
+
+class ResidualRMSNorm(torch.nn.Module):
+    """The residual add fused with the norm: forward(x, residual) returns
+    (RMSNorm(x + residual), x + residual)."""
+
+    def __init__(self, hidden_size: int, eps: float = 1e-6, device=None,
+                 dtype=torch.bfloat16):
+        super().__init__()
+        self.weight = torch.nn.Parameter(
+            torch.ones(hidden_size, device=device, dtype=dtype))
+        self.eps = float(eps)
+
+    def forward(self, x, residual):
+        return ResidualRMSNormFunction.apply(x, residual, self.weight, self.eps)
+
+    def extra_repr(self):
+        return f"{self.weight.numel()}, eps={self.eps}"
