@@ -6,7 +6,7 @@ baseline leg of ``bench.py`` use this module; the CUDA product path
 the product. What the oracle computes, and which passage of the pages each
 function follows, is documented in oracle.c.
 
-Inputs are torch CPU tensors (float32, bfloat16 or float64), contiguous,
+Inputs are torch CPU tensors (float32, bfloat16, float16 or float64), contiguous,
 row-major ``[M, H]`` with a ``[H]`` weight. Outputs are float64 tensors, except
 the residual sum ``h``, which is stored in the input dtype as the method does.
 """
@@ -17,8 +17,9 @@ import torch
 
 from . import build as _build
 
-F32, BF16, F64 = 0, 1, 2
-_CODES = {torch.float32: F32, torch.bfloat16: BF16, torch.float64: F64}
+F32, BF16, F64, F16 = 0, 1, 2, 3
+_CODES = {torch.float32: F32, torch.bfloat16: BF16, torch.float64: F64,
+          torch.float16: F16}
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -42,6 +43,10 @@ def _declare(lib):
     lib.oracle_bf16_to_double.restype = _dbl
     lib.oracle_bf16_from_double.argtypes = [_dbl]
     lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+    lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_to_double.restype = _dbl
+    lib.oracle_f16_from_double.argtypes = [_dbl]
+    lib.oracle_f16_from_double.restype = ctypes.c_uint16
     return lib
 
 
@@ -71,6 +76,12 @@ class Oracle:
 
     def bf16_from_double(self, v: float) -> int:
         return self.lib.oracle_bf16_from_double(float(v))
+
+    def f16_to_double(self, bits: int) -> float:
+        return self.lib.oracle_f16_to_double(bits & 0xFFFF)
+
+    def f16_from_double(self, v: float) -> int:
+        return self.lib.oracle_f16_from_double(float(v))
 
     # -- forward
     def fwd(self, x, w, eps):

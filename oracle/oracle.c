@@ -18,7 +18,8 @@
  * Every function writes its definition out with plain loops in double
  * precision: no blocking, no fusion, no reordering beyond what the definition
  * states, so that it can be checked against the pages by eye. Inputs are read
- * in their stored format (fp32, bf16 bit patterns or fp64) and decoded here,
+ * in their stored format (fp32, bf16 or fp16 bit patterns, or fp64) and
+ * decoded here,
  * exactly, to double. Results stay in double and are never rounded, except the
  * residual sum h, which the method stores in the input dtype.
  *
@@ -33,6 +34,7 @@
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
 #define ORACLE_F64 2
+#define ORACLE_F16 3
 
 /* ---------------------------------------------------------------- formats */
 
@@ -74,6 +76,56 @@ uint16_t oracle_bf16_from_double(double v)
     return (uint16_t)(u >> 16);
 }
 
+/* IEEE binary16: sign, 5-bit exponent with bias 15, 10 stored fraction
+ * bits; exponent 0 holds subnormals (fraction * 2^-24), 31 infinities and
+ * NaNs. Widening to double is exact. */
+double oracle_f16_to_double(uint16_t bits)
+{
+    const int sign = bits >> 15;
+    const int exp = (bits >> 10) & 0x1F;
+    const int frac = bits & 0x3FF;
+    double v;
+    if (exp == 0)
+        v = ldexp((double)frac, -24);
+    else if (exp == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), exp - 25);
+    return sign ? -v : v;
+}
+
+/*
+ * Round a double to the nearest binary16, ties to even, in one step: 11
+ * significant bits for normal numbers (exponents -14..15), spacing 2^-24 for
+ * subnormals, infinity beyond the largest finite value 65504 (the tie at
+ * 65520 goes to infinity, whose significand is even).
+ */
+uint16_t oracle_f16_from_double(double v)
+{
+    if (isnan(v))
+        return (uint16_t)(signbit(v) ? 0xFE00u : 0x7E00u);
+    const uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);            /* a in [2^(e-1), 2^e) */
+    int q = e - 11;                /* spacing of 11-bit significands there */
+    if (q < -24)
+        q = -24;                   /* subnormal spacing */
+    double r = ldexp(nearbyint(ldexp(a, -q)), q);
+    if (r > 65504.0)
+        return (uint16_t)(sign | 0x7C00u);
+    /* encode the representable r */
+    if (r < ldexp(1.0, -14))
+        return (uint16_t)(sign | (uint16_t)ldexp(r, 24));          /* subnormal */
+    int re;
+    double m = frexp(r, &re);      /* r = m 2^re, m in [0.5, 1) */
+    int exp = re - 1 + 15;
+    int frac = (int)ldexp(m, 11) - 1024;
+    return (uint16_t)(sign | (exp << 10) | frac);
+}
+
 static double dec(const void *p, int dtype, int64_t i)
 {
     switch (dtype) {
@@ -81,6 +133,8 @@ static double dec(const void *p, int dtype, int64_t i)
         return (double)((const float *)p)[i];
     case ORACLE_BF16:
         return oracle_bf16_to_double(((const uint16_t *)p)[i]);
+    case ORACLE_F16:
+        return oracle_f16_to_double(((const uint16_t *)p)[i]);
     default:
         return ((const double *)p)[i];
     }
@@ -100,6 +154,11 @@ static double store_rounded(void *p, int dtype, int64_t i, double v)
         uint16_t b = oracle_bf16_from_double(v);
         ((uint16_t *)p)[i] = b;
         return oracle_bf16_to_double(b);
+    }
+    case ORACLE_F16: {
+        uint16_t b = oracle_f16_from_double(v);
+        ((uint16_t *)p)[i] = b;
+        return oracle_f16_to_double(b);
     }
     default:
         ((double *)p)[i] = v;

@@ -102,6 +102,92 @@ def pin_bf16_round_vs_library(o):
         assert got == w, f"round({v!r}) = {got:#06x}, library {w:#06x}"
 
 
+def pin_f16_decode(o):
+    """IEEE binary16 bit patterns decode to the values of their layout (sign,
+    5-bit exponent with bias 15, 10 stored fraction bits, subnormals at
+    multiples of 2^-24), worked by hand."""
+    cases = {
+        0x3C00: 1.0, 0xBC00: -1.0, 0x4248: 3.140625, 0xD7B8: -123.5,
+        0x0400: 2.0 ** -14, 0x0001: 2.0 ** -24, 0x03FF: 1023 * 2.0 ** -24,
+        0x8000: -0.0, 0x7BFF: 65504.0, 0x3555: 1365 * 2.0 ** -12,
+        0x7C00: math.inf, 0xFC00: -math.inf,
+    }
+    for bits, want in cases.items():
+        got = o.f16_to_double(bits)
+        assert got == want, f"f16 decode {bits:#06x}: {got!r} != {want!r}"
+    assert math.copysign(1.0, o.f16_to_double(0x8000)) == -1.0
+    assert math.isnan(o.f16_to_double(0x7E00))
+
+
+def pin_f16_round_hand_cases(o):
+    """Round-to-nearest-even to binary16 on ties and edges worked by hand."""
+    u = 2.0 ** -10                    # f16 spacing just above 1.0
+    cases = [
+        (1.0 + u / 2, 0x3C00),        # tie between 1 and 1+u: even is 1
+        (1.0 + 3 * u / 2, 0x3C02),    # tie between 1+u and 1+2u: 1+2u
+        (1.0 + u / 2 + 2.0 ** -40, 0x3C01),
+        (1.0 + u / 2 - 2.0 ** -40, 0x3C00),
+        (-(1.0 + 3 * u / 2), 0xBC02),
+        (2.0 ** -25, 0x0000),         # half the smallest subnormal: tie to 0
+        (3 * 2.0 ** -25, 0x0002),     # 1.5 x smallest subnormal: tie to 2
+        (2.0 ** -25 + 2.0 ** -50, 0x0001),
+        (1023.5 * 2.0 ** -24, 0x0400),  # largest subnormal + half: to 2^-14
+        (65504.0, 0x7BFF), (65519.99, 0x7BFF),
+        (65520.0, 0x7C00),            # tie between 65504 and 2^16: inf
+        (1e300, 0x7C00), (-1e300, 0xFC00),
+        (2049.0, 0x6800),             # tie between 2048 and 2050: 2048
+        (2051.0, 0x6802),             # tie between 2050 and 2052: 2052
+        (0.0, 0x0000), (-0.0, 0x8000),
+    ]
+    for v, want in cases:
+        got = o.f16_from_double(v)
+        assert got == want, f"f16 round({v!r}) = {got:#06x}, want {want:#06x}"
+
+
+def pin_f16_round_vs_library(o):
+    """On binary32 inputs the oracle's binary16 rounding equals torch's
+    float32 -> float16 conversion (round-to-nearest-even): normals,
+    subnormals, values near the overflow threshold and exact ties."""
+    g = _gen(16)
+    parts = [
+        torch.randn(4000, generator=g),
+        torch.randn(2000, generator=g) * 3e-6,           # f16 subnormals
+        torch.randn(2000, generator=g) * 6e4,            # near overflow
+        (torch.randint(0, 0x7C00, (3000,), generator=g, dtype=torch.int32)
+         .to(torch.int16).view(torch.float16).float()
+         * (1 + torch.randn(3000, generator=g) * 1e-3)),
+    ]
+    # exact ties: an f16 value + half its spacing (13 float32 bits below)
+    base = (torch.randn(2000, generator=g) * 100).to(torch.float16).float()
+    base = base[base.abs() >= 2.0 ** -14]                 # normals only
+    bits = base.view(torch.int32) | 0x1000
+    parts.append(bits.view(torch.float32))
+    xs = torch.cat(parts)
+    xs = xs[torch.isfinite(xs)]
+    want = xs.to(torch.float16).view(torch.int16).to(torch.int32) & 0xFFFF
+    for v, w in zip(xs.tolist(), want.tolist()):
+        got = o.f16_from_double(v)
+        assert got == w, f"f16 round({v!r}) = {got:#06x}, library {w:#06x}"
+
+
+def pin_f16_fwd_reads_f16(o):
+    """The forward decodes fp16 storage: on fp16 inputs it equals the fp64
+    forward applied to the same values widened (exactly) by torch."""
+    g = _gen(17)
+    x = (torch.randn(5, 96, generator=g) * 3).to(torch.float16)
+    x.view(-1)[::31] = torch.tensor(6e-6, dtype=torch.float16)   # subnormals
+    w = (1.0 + 0.1 * torch.randn(96, generator=g)).to(torch.float16)
+    y, rstd = o.fwd(x, w, 1e-6)
+    yd, rd = o.fwd(x.double(), w.double(), 1e-6)
+    _close(y, yd, 0.0, what="f16 y")
+    _close(rstd, rd, 0.0, what="f16 rstd")
+    dy = torch.randn(5, 96, generator=g).to(torch.float16)
+    dx, dw = o.bwd(dy, x, w, 1e-6)
+    dxd, dwd = o.bwd(dy.double(), x.double(), w.double(), 1e-6)
+    _close(dx, dxd, 0.0, what="f16 dx")
+    _close(dw, dwd, 0.0, what="f16 dw")
+
+
 # ----------------------------------------------------------------- forward
 
 def pin_fwd_constant_row(o):
@@ -340,10 +426,12 @@ def pin_residual_h_exact(o):
     """h = round(x + r) in the stored dtype: for bf16 it equals torch's
     float32 add followed by its round-to-nearest-even bf16 conversion (the
     float32 add of two bf16 values cannot round to a different bf16 result);
-    for float32 it equals torch's float32 add; for float64 it is x + r."""
+    the same holds for fp16 (binary32 carries at least 2 x 11 + 2 bits, so
+    rounding the float32 sum again to binary16 is the single rounding); for
+    float32 it equals torch's float32 add; for float64 it is x + r."""
     g = _gen(12)
     M, H = 8, 200
-    for dt in (torch.bfloat16, torch.float32):
+    for dt in (torch.bfloat16, torch.float16, torch.float32):
         x = torch.randn(M, H, generator=g)
         r = torch.randn(M, H, generator=g)
         x.view(-1)[::97] *= 100.0                  # outliers
@@ -352,9 +440,10 @@ def pin_residual_h_exact(o):
         w = (1.0 + 0.1 * torch.randn(H, generator=g)).to(dt)
         h, _, _ = o.residual_fwd(x, r, w, 1e-6)
         want = (x.float() + r.float()).to(dt)
-        assert torch.equal(h.view(torch.int16) if dt == torch.bfloat16 else h,
-                           want.view(torch.int16) if dt == torch.bfloat16
-                           else want), f"h not exact for {dt}"
+        half = dt in (torch.bfloat16, torch.float16)
+        assert torch.equal(h.view(torch.int16) if half else h,
+                           want.view(torch.int16) if half else want), \
+            f"h not exact for {dt}"
     x = torch.randn(2, 9, generator=g, dtype=F64)
     r = torch.randn(2, 9, generator=g, dtype=F64)
     h, _, _ = o.residual_fwd(x, r, torch.ones(9, dtype=F64), 0.0)

@@ -61,6 +61,19 @@ MUTANTS = [
      "v = (double)(float)v;\n    (void)frexp(v, &e);"),
     ("bf16_no_subnormal_clamp", "if (q < -133)\n        q = -133;", ""),
     ("bf16_decode_shift", "((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
+    ("f16_ties_away", "double r = ldexp(nearbyint(ldexp(a, -q)), q);",
+     "double r = ldexp(round(ldexp(a, -q)), q);"),
+    ("f16_truncate", "double r = ldexp(nearbyint(ldexp(a, -q)), q);",
+     "double r = ldexp(trunc(ldexp(a, -q)), q);"),
+    ("f16_10_bit_significand", "int q = e - 11;", "int q = e - 10;"),
+    ("f16_no_subnormal_clamp", "if (q < -24)\n        q = -24;", ""),
+    ("f16_overflow_at_max", "if (r > 65504.0)", "if (r >= 65504.0)"),
+    ("f16_decode_bias", "v = ldexp((double)(1024 + frac), exp - 25);",
+     "v = ldexp((double)(1024 + frac), exp - 24);"),
+    ("f16_decode_subnormal_scale", "v = ldexp((double)frac, -24);",
+     "v = ldexp((double)frac, -25);"),
+    ("f16_decode_as_bf16", "return oracle_f16_to_double(((const uint16_t *)p)[i]);",
+     "return oracle_bf16_to_double(((const uint16_t *)p)[i]);"),
     ("resid_subtract",
      "double s = dec(x, dtype, i * H + j) + dec(res, dtype, i * H + j);",
      "double s = dec(x, dtype, i * H + j) - dec(res, dtype, i * H + j);"),
