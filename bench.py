@@ -92,9 +92,12 @@ def buffer_sets(wl):
 
 
 def base_config(wl):
-    return {"workload": wl.name, "M": wl.M, "H": wl.H, "eps": wl.eps,
-            "dtype": str(wl.dtype).replace("torch.", ""),
-            "step": "fwd+bwd" if wl.backward else "fwd"}
+    c = {"workload": wl.name, "M": wl.M, "H": wl.H, "eps": wl.eps,
+         "dtype": str(wl.dtype).replace("torch.", ""),
+         "step": "fwd+bwd" if wl.backward else "fwd"}
+    if wl.ld:
+        c["row_stride"] = wl.ld
+    return c
 
 
 def reduce_max(value, dist):
@@ -264,11 +267,15 @@ class Calls:
 
     def __init__(self, rn, wl, src, dev, ws, w):
         self.rn, self.wl = rn, wl
-        e = lambda: torch.empty(wl.M, wl.H, device=dev, dtype=wl.dtype)  # noqa: E731
-        self.x = src["x"].to(dev)
-        self.dy = src["dy"].to(dev) if wl.backward else None
-        self.r = src["r"].to(dev) if wl.residual else None
-        self.dh = src["dh"].to(dev) if wl.residual else None
+        if wl.ld:        # every [M, H] tensor a column window of an [M, ld] buffer
+            place = lambda t: W.in_strided(t, wl.ld, 0.0)  # noqa: E731
+        else:
+            place = lambda t: t  # noqa: E731
+        e = lambda: place(torch.empty(wl.M, wl.H, device=dev, dtype=wl.dtype))  # noqa: E731
+        self.x = place(src["x"].to(dev))
+        self.dy = place(src["dy"].to(dev)) if wl.backward else None
+        self.r = place(src["r"].to(dev)) if wl.residual else None
+        self.dh = place(src["dh"].to(dev)) if wl.residual else None
         self.y, self.h = e(), (e() if wl.residual else None)
         self.dx = e() if wl.backward else None
         self.rstd = torch.empty(wl.M, device=dev)
@@ -284,7 +291,17 @@ class Calls:
         code = self.rn.DTYPES[wl.dtype]
         s = stream.cuda_stream
         ws_bytes = self.ws.numel()
-        if wl.residual:
+        if wl.ld:
+            ld = wl.ld
+            self._f = (lib.rmsnorm_fwd_strided,
+                       (P(self.x), ld, P(self.r), ld, P(self.w), P(self.y), ld,
+                        P(self.h), ld, P(self.rstd), wl.M, wl.H, wl.eps, code, s))
+            self._b = (lib.rmsnorm_bwd_strided,
+                       (P(self.dy), ld, P(self.dh), ld,
+                        P(self.h if wl.residual else self.x), ld, P(self.w),
+                        P(self.rstd), P(self.dx), ld, P(self.dw), P(self.ws),
+                        ws_bytes, wl.M, wl.H, wl.eps, code, 0, s))
+        elif wl.residual:
             self._f = (lib.rmsnorm_residual_fwd,
                        (P(self.x), P(self.r), P(self.w), P(self.h), P(self.y),
                         P(self.rstd), wl.M, wl.H, wl.eps, code, s))
@@ -472,9 +489,12 @@ def run_ours(args, wl):
                 "frac_of_nominal_8TBs": round(a / NOMINAL_HBM_GBS, 4)}
 
     fam = {1: "rows", 2: "split", 3: "rows, scalar", 4: "stream"}
-    fwd_kernel = ("rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd") + \
-        f" (rms_fwd_{fam.get(path_f, 'rows').split(',')[0]})"
-    bwd_kernel = ("rmsnorm_residual_bwd" if wl.residual else "rmsnorm_bwd") + \
+    fwd_api = "rmsnorm_fwd_strided" if wl.ld else (
+        "rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd")
+    bwd_api = "rmsnorm_bwd_strided" if wl.ld else (
+        "rmsnorm_residual_bwd" if wl.residual else "rmsnorm_bwd")
+    fwd_kernel = fwd_api + f" (rms_fwd_{fam.get(path_f, 'rows').split(',')[0]})"
+    bwd_kernel = bwd_api + \
         f" (rms_bwd_{fam.get(path_b, 'rows').split(',')[0]} + dw_reduce)"
     roofline = roof(dom_bytes, dom_ms, bwd_kernel if dom_is_bwd else fwd_kernel)
     roofline["achieved"] = round(achieved, 1)
@@ -483,8 +503,9 @@ def run_ours(args, wl):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
-        if wl.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {torch.bfloat16: "bf16", torch.float16: "f16"}.get(wl.dtype, "f32"),
+        "data": "synthetic",
         "config": dict(base_config(wl), **{
             "l2": (f"inputs larger than L2: {n_sets} rotating buffer sets, "
                    f"{x_bytes / 1e6:.0f} MB per row tensor"
@@ -538,9 +559,13 @@ def run_e2e(rn, wl, src, dev, ws, args, dist):
     dtypes = {"rstd": torch.float32, "dw": torch.float32}
 
     def dev_set():
-        return {k: torch.empty(shapes.get(k, (M, H)), device=dev,
-                               dtype=dtypes.get(k, wl.dtype))
-                for k in set(in_keys) | set(out_keys)}
+        d = {k: torch.empty(shapes.get(k, (M, H)), device=dev,
+                            dtype=dtypes.get(k, wl.dtype))
+             for k in set(in_keys) | set(out_keys)}
+        if wl.ld:        # row tensors as column windows of [M, ld] buffers
+            d = {k: (W.in_strided(v, wl.ld, 0.0) if k not in shapes else v)
+                 for k, v in d.items()}
+        return d
     sets = [dev_set(), dev_set()]
     host_out = {k: torch.empty(shapes.get(k, (M, H)), dtype=dtypes.get(k, wl.dtype),
                                pin_memory=True) for k in out_keys}
@@ -573,7 +598,13 @@ def run_e2e(rn, wl, src, dev, ws, args, dist):
                 if c == 0 and used[si]:
                     # ... and its results have been copied out
                     s_c.wait_event(ev_out[si][chunks - 1])
-                if wl.residual:
+                if wl.ld:
+                    rn.rmsnorm_fwd_strided(
+                        d["x"][a:b], d["w"], y=d["y"][a:b],
+                        r=d["r"][a:b] if wl.residual else None,
+                        h=d["h"][a:b] if wl.residual else None,
+                        rstd=d["rstd"][a:b], eps=wl.eps, stream=s_c)
+                elif wl.residual:
                     rn.rmsnorm_residual_fwd(d["x"][a:b], d["r"][a:b], d["w"],
                                             h=d["h"][a:b], y=d["y"][a:b],
                                             rstd=d["rstd"][a:b], eps=wl.eps, stream=s_c)
@@ -582,10 +613,11 @@ def run_e2e(rn, wl, src, dev, ws, args, dist):
                                    rstd=d["rstd"][a:b], eps=wl.eps, stream=s_c)
                 if wl.backward:
                     xin = d["h"] if wl.residual else d["x"]
-                    rn.rmsnorm_bwd_ex(d["dy"][a:b], xin[a:b], d["w"], d["rstd"][a:b],
-                                      dh_out=d["dh"][a:b] if wl.residual else None,
-                                      dx=d["dx"][a:b], dw=d["dw"], workspace=ws,
-                                      eps=wl.eps, accumulate_dw=c > 0, stream=s_c)
+                    bwd = rn.rmsnorm_bwd_strided if wl.ld else rn.rmsnorm_bwd_ex
+                    bwd(d["dy"][a:b], xin[a:b], d["w"], d["rstd"][a:b],
+                        dh_out=d["dh"][a:b] if wl.residual else None,
+                        dx=d["dx"][a:b], dw=d["dw"], workspace=ws,
+                        eps=wl.eps, accumulate_dw=c > 0, stream=s_c)
                 ev_c[si][c].record(s_c)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_c[si][c])

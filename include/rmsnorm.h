@@ -11,15 +11,17 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Tensors are dense, row-major [M, H] (M rows of H features), owned by the
- *    caller, in device memory (or memory the device can address). The
- *    weight w has H entries. x, r, w, y, h, dy, dh_out and dx share one
- *    dtype (RMSNORM_F32 or RMSNORM_BF16); rstd, dw and the workspace are
- *    always fp32.
+ *  - Tensors are row-major [M, H] (M rows of H features), owned by the
+ *    caller, in device memory (or memory the device can address); dense
+ *    (row stride H) except through the *_strided entry points, where each
+ *    [M, H] tensor has its own row stride. The weight w has H entries. x, r,
+ *    w, y, h, dy, dh_out and dx share one dtype (RMSNORM_F32, RMSNORM_BF16
+ *    or RMSNORM_F16); rstd, dw and the workspace are always fp32.
  *  - Every pointer must be aligned to its element size. Rows whose start is
- *    16-byte aligned (aligned base pointer and H * element size a multiple of
- *    16) take the 128-bit vectorised kernels; anything else takes a scalar
- *    kernel with the same results up to fp32 summation order.
+ *    16-byte aligned (aligned base pointer, H * element size and every row
+ *    stride * element size multiples of 16) take the 128-bit vectorised
+ *    kernels; anything else takes a scalar kernel with the same results up
+ *    to fp32 summation order.
  *  - 1 <= H <= RMSNORM_MAX_H, 0 <= M. eps is a finite float >= 0 (a plain
  *    float, never a tensor: [P1 §5.6] gotcha table).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
@@ -46,8 +48,9 @@
 extern "C" {
 #endif
 
-/* Element type of the row tensors and the weight. */
-typedef enum { RMSNORM_F32 = 0, RMSNORM_BF16 = 1 } rmsnorm_dtype;
+/* Element type of the row tensors and the weight ([P1 §4.2]: the forward
+ * stores its result as fp16 or bf16; fp32 for reference runs). */
+typedef enum { RMSNORM_F32 = 0, RMSNORM_BF16 = 1, RMSNORM_F16 = 2 } rmsnorm_dtype;
 
 /* Return codes. */
 typedef enum {
@@ -66,7 +69,10 @@ typedef enum {
     RMSNORM_ERR_SCRATCH_LIMIT = -10, /* rmsnorm_bwd_static_scratch: the problem
                                        needs more scratch than the library's
                                        built-in RMSNORM_STATIC_SCRATCH_BYTES */
-    RMSNORM_ERR_BAD_FLAGS = -11   /* rmsnorm_bwd_ex: unknown flag bits */
+    RMSNORM_ERR_BAD_FLAGS = -11,  /* rmsnorm_bwd_ex: unknown flag bits */
+    RMSNORM_ERR_BAD_STRIDE = -12  /* *_strided: a row stride below H, above
+                                     2^31 - 1, or so large that the tensor's
+                                     last element lies beyond 2^63 bytes */
 } rmsnorm_status;
 
 /* Largest feature count the kernels hold in registers ([P1 §7.1] puts the
@@ -78,7 +84,7 @@ typedef enum {
  *   rstd_i = 1 / sqrt( (1/H) sum_j x_ij^2 + eps )
  *   y_ij   = round( x_ij * rstd_i * w_j )
  * summed and scaled in fp32, rounded once to the dtype (round-to-nearest-
- * even for bf16).
+ * even for bf16 and fp16; fp16 results beyond 65504 become infinite).
  *   x    [M,H] in, w [H] in, y [M,H] out (y may equal x: in place)
  *   rstd [M] fp32 out, or NULL when not wanted (the backward can recompute it)
  * M <= 64 rows take the split-row kernel ([P2 §3.2]): each row is spread over
@@ -156,6 +162,53 @@ int rmsnorm_bwd_ex(const void *dy, const void *dh_out, const void *x,
                    int64_t H, float eps, int dtype, int flags, void *stream);
 
 /*
+ * Strided rows ([P1 §4.2]: the forward kernel takes the row stride of its
+ * input and of its output, so a row-major view with padded or interleaved
+ * rows needs no copy). Each [M, H] tensor t is given with its row stride
+ * ld_t in ELEMENTS (H <= ld_t <= 2^31 - 1): row i starts at t + i * ld_t.
+ * ld_t == H is the dense layout of the entry points above, with identical
+ * results; the results do not depend on the strides.
+ *
+ * Forward, plain or fused with the residual add: r and h both NULL gives
+ * rmsnorm_fwd; both non-NULL gives rmsnorm_residual_fwd. The ld of a NULL
+ * tensor is ignored.
+ *   x [M,H] (ldx), r [M,H] (ldr) in; w [H] in;
+ *   y [M,H] (ldy) out, h [M,H] (ldh) out; rstd [M] out or NULL.
+ * Aliasing as for the dense calls, applied element by element: y (or h) may
+ * be exactly x (same pointer and stride); two tensors that share memory but
+ * touch disjoint columns of rows with the same stride (e.g. two column
+ * windows of one [M, ld] buffer) do not overlap; anything else that shares
+ * an element is RMSNORM_ERR_ALIAS.
+ * Errors: those of rmsnorm_fwd / rmsnorm_residual_fwd; RMSNORM_ERR_NULLPTR
+ * when only one of r and h is NULL; RMSNORM_ERR_BAD_STRIDE as defined above.
+ * Kernel choice: as for the dense calls, except that the streamed kernels of
+ * 128-wide rows (which copy blocks of consecutive rows) need every stride
+ * equal to H, and the 256-bit forward needs every stride * element size to
+ * be a multiple of 32.
+ */
+int rmsnorm_fwd_strided(const void *x, int64_t ldx, const void *r, int64_t ldr,
+                        const void *w, void *y, int64_t ldy, void *h,
+                        int64_t ldh, float *rstd, int64_t M, int64_t H,
+                        float eps, int dtype, void *stream);
+
+/*
+ * Backward with strided rows: rmsnorm_bwd_ex with a row stride (in
+ * elements, >= H) for dy, dh_out, x (h for the residual backward) and dx.
+ *   dy [M,H] (lddy) in; dh_out [M,H] (lddh) in or NULL; x [M,H] (ldx) in;
+ *   w [H] in; rstd [M] in or NULL; dx [M,H] (lddx) out; dw [H] fp32 out;
+ *   workspace, flags: as for rmsnorm_bwd_ex (the workspace size does not
+ *   depend on the strides).
+ * Aliasing element by element as for rmsnorm_fwd_strided: dx may be exactly
+ * dy or dh_out. Errors: those of rmsnorm_bwd_ex and RMSNORM_ERR_BAD_STRIDE.
+ */
+int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
+                        int64_t lddh, const void *x, int64_t ldx,
+                        const void *w, const float *rstd, void *dx,
+                        int64_t lddx, float *dw, void *workspace,
+                        size_t workspace_bytes, int64_t M, int64_t H,
+                        float eps, int dtype, int flags, void *stream);
+
+/*
  * Bytes of workspace rmsnorm_bwd / rmsnorm_residual_bwd need for (M, H,
  * dtype) on the current CUDA device (one fp32 row of H per CTA of the
  * backward grid; the grid is sized from the device's SM count). Returns 0 on
@@ -174,10 +227,11 @@ int rmsnorm_last_cuda_error(void);
  * Test hook: force the kernel family for later calls in this process.
  * 0 = automatic (default), 1 = row-wise vectorised, 2 = split-row (forward
  * only; the backward then takes row-wise), 3 = row-wise scalar, 4 = streamed
- * (rows staged through shared memory by bulk asynchronous copies; bf16 with
- * H = 4096 or 5120 only, row-wise elsewhere). Forcing a vectorised family on
- * rows that are not 16-byte aligned still takes the scalar one. Not
- * thread-safe against concurrent calls; intended for tests only.
+ * (rows staged through shared memory by bulk asynchronous copies; bf16 or
+ * fp16 with H = 128 (dense rows only), 4096 or 5120; row-wise elsewhere).
+ * Forcing a vectorised family on rows that are not 16-byte aligned still
+ * takes the scalar one. Not thread-safe against concurrent calls; intended
+ * for tests only.
  */
 void rmsnorm_set_path_override(int path);
 

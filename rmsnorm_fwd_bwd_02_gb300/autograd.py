@@ -7,8 +7,11 @@ make dy contiguous, save tensors with save_for_backward, return one gradient
 per forward input (None for eps), take eps as a float, and raise on double
 backward unless it is implemented. These wrappers follow that shape over the
 CUDA kernels of librmsnorm.so; the forward also saves rstd, so the backward
-does not recompute it. Every arithmetic step runs in the CUDA kernels;
-there is no CPU fallback (CPU tensors raise).
+does not recompute it. Inputs and incoming gradients whose rows are evenly
+strided (a column window of a wider buffer, a slice along the leading dims)
+go to the kernels as they are, through the strided entry points; only
+layouts that no row stride describes are copied first. Every arithmetic step
+runs in the CUDA kernels; there is no CPU fallback (CPU tensors raise).
 """
 import torch
 from torch.autograd.function import once_differentiable
@@ -17,8 +20,11 @@ from . import rmsnorm as _rn
 
 
 def _rows2d(t, H):
-    """A contiguous [M, H] view (a copy only when t is not contiguous)."""
-    return t.contiguous().view(-1, H)
+    """t as [M, H] rows: a view with its own row stride when t's layout has
+    one, else a contiguous copy."""
+    if not t.is_cuda:
+        raise ValueError("RMSNorm: tensors must be on a CUDA device")
+    return _rn.as_rows(t, H)
 
 
 class RMSNormFunction(torch.autograd.Function):
@@ -28,7 +34,7 @@ class RMSNormFunction(torch.autograd.Function):
     def forward(ctx, x, weight, eps: float = 1e-6):
         H = weight.numel()
         x2 = _rows2d(x, H)
-        y, rstd = _rn.rmsnorm_fwd(x2, weight, eps=float(eps))
+        y, rstd = _rn.rmsnorm_fwd_strided(x2, weight, eps=float(eps))
         ctx.save_for_backward(x2, weight, rstd)
         ctx.eps = float(eps)
         ctx.shape = x.shape
@@ -39,7 +45,8 @@ class RMSNormFunction(torch.autograd.Function):
     def backward(ctx, dy):
         x2, weight, rstd = ctx.saved_tensors
         H = weight.numel()
-        dx, dw = _rn.rmsnorm_bwd(_rows2d(dy, H), x2, weight, rstd, eps=ctx.eps)
+        dx, dw = _rn.rmsnorm_bwd_strided(_rows2d(dy, H), x2, weight, rstd,
+                                         eps=ctx.eps)
         dx = dx.view(ctx.shape) if ctx.needs_input_grad[0] else None
         dw = dw.to(weight.dtype) if ctx.needs_input_grad[1] else None
         return dx, dw, None
@@ -54,7 +61,7 @@ class ResidualRMSNormFunction(torch.autograd.Function):
     def forward(ctx, x, residual, weight, eps: float = 1e-6):
         H = weight.numel()
         x2, r2 = _rows2d(x, H), _rows2d(residual, H)
-        h, y, rstd = _rn.rmsnorm_residual_fwd(x2, r2, weight, eps=float(eps))
+        h, y, rstd = _rn.rmsnorm_fwd_strided(x2, weight, r=r2, eps=float(eps))
         ctx.save_for_backward(h, weight, rstd)
         ctx.eps = float(eps)
         ctx.shape = x.shape
@@ -68,8 +75,8 @@ class ResidualRMSNormFunction(torch.autograd.Function):
         if dy is None:
             dy = torch.zeros_like(h)
         dh2 = None if dh is None else _rows2d(dh, H)
-        dx, dw = _rn.rmsnorm_residual_bwd(_rows2d(dy, H), dh2, h, weight, rstd,
-                                          eps=ctx.eps)
+        dx, dw = _rn.rmsnorm_bwd_strided(_rows2d(dy, H), h, weight, rstd,
+                                         dh_out=dh2, eps=ctx.eps)
         dx = dx.view(ctx.shape)
         dw = dw.to(weight.dtype) if ctx.needs_input_grad[2] else None
         gx = dx if ctx.needs_input_grad[0] else None

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <map>
 #include <mutex>
+#include <initializer_list>
 #include <utility>
 
 #include "rmsnorm.h"
@@ -36,32 +37,61 @@ int cuda_fail(cudaError_t e)
     return RMSNORM_ERR_CUDA;
 }
 
-size_t elem_size(int dtype) { return dtype == RMSNORM_BF16 ? 2 : 4; }
+size_t elem_size(int dtype) { return dtype == RMSNORM_F32 ? 4 : 2; }
 
 bool aligned(const void *p, size_t a) { return p == nullptr || (uintptr_t)p % a == 0; }
 
-struct Buf {
+// A tensor argument as the bytes it touches: `rows` rows of `row_bytes`
+// bytes whose starts are `ld_bytes` apart (a flat buffer is one row).
+struct Span {
     const void *p;
-    size_t n;
+    int64_t rows, row_bytes, ld_bytes;
+    bool empty() const { return p == nullptr || rows <= 0 || row_bytes <= 0; }
+    uintptr_t begin() const { return (uintptr_t)p; }
+    uintptr_t end() const { return (uintptr_t)p + (rows - 1) * ld_bytes + row_bytes; }
 };
 
-bool overlap(Buf a, Buf b)
+Span flat(const void *p, size_t n) { return {p, 1, (int64_t)n, (int64_t)n}; }
+
+Span rows_span(const void *p, int64_t M, int64_t H, int64_t ld, size_t es)
 {
-    if (!a.p || !b.p || !a.n || !b.n)
-        return false;
-    const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
-    return a0 < b0 + b.n && b0 < a0 + a.n;
+    return {p, M, H * (int64_t)es, ld * (int64_t)es};
 }
 
-// Allowed: the same buffer exactly, or no overlap at all.
-bool same_or_disjoint(Buf a, Buf b)
+// Whether two arguments may share a byte. Exact for disjoint address
+// ranges and for row windows of one stride that never meet (the rows of b
+// fall, modulo the stride, after the end of a's rows and before the next
+// row of a starts); any other pair whose ranges intersect counts as
+// overlapping.
+bool overlap(Span a, Span b)
 {
-    return (a.p == b.p && a.n == b.n) || !overlap(a, b);
+    if (a.empty() || b.empty())
+        return false;
+    if (!(a.begin() < b.end() && b.begin() < a.end()))
+        return false;
+    if (a.ld_bytes == b.ld_bytes && a.ld_bytes > 0) {
+        const int64_t ld = a.ld_bytes;
+        const int64_t d = (int64_t)(b.begin() - a.begin());
+        const int64_t s = ((d % ld) + ld) % ld;   // b's row offset within a's row frame
+        if (s >= a.row_bytes && s + b.row_bytes <= ld)
+            return false;
+    }
+    return true;
 }
+
+bool same(Span a, Span b)
+{
+    return a.p == b.p && a.rows == b.rows && a.row_bytes == b.row_bytes &&
+           (a.rows == 1 || a.ld_bytes == b.ld_bytes);
+}
+
+// Allowed: the same tensor exactly (same start, shape and stride), or no
+// shared byte at all.
+bool same_or_disjoint(Span a, Span b) { return same(a, b) || !overlap(a, b); }
 
 int check_common(int64_t M, int64_t H, float eps, int dtype)
 {
-    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16)
+    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16 && dtype != RMSNORM_F16)
         return RMSNORM_ERR_BAD_DTYPE;
     if (M < 0 || H < 1)
         return RMSNORM_ERR_BAD_SHAPE;
@@ -72,6 +102,25 @@ int check_common(int64_t M, int64_t H, float eps, int dtype)
     if (!(eps >= 0.f) || !std::isfinite(eps))
         return RMSNORM_ERR_BAD_EPS;
     return RMSNORM_OK;
+}
+
+// A row stride is at least H and below 2^31 (the row kernels hold strides in
+// 32 bits), and the tensor's last byte stays far below 2^63 (so every byte
+// offset the kernels form fits an int64).
+bool stride_ok(int64_t ld, int64_t M, int64_t H)
+{
+    if (ld < H || ld > INT32_MAX)
+        return false;
+    return M <= 1 || ld <= (INT64_MAX / 8 - H) / (M - 1);
+}
+
+// Row strides (elements) whose byte size is a multiple of `a`.
+bool strides_multiple(size_t a, size_t es, std::initializer_list<int64_t> lds)
+{
+    for (int64_t ld : lds)
+        if ((ld * (int64_t)es) % (int64_t)a != 0)
+            return false;
+    return true;
 }
 
 // ------------------------------------------------------- device properties
@@ -157,19 +206,25 @@ struct StreamPolicy {
     bool auto_fwd, auto_bwd;
 };
 
-const StreamPolicy *pick_stream(int dtype, int64_t H, bool vec)
+// dense: every row stride equals H (the 128-wide kernels copy blocks of
+// consecutive rows). fp16 takes the bf16 choices (same bytes, same layouts).
+const StreamPolicy *pick_stream(int dtype, int64_t H, bool vec, bool dense)
 {
-    static const StreamPolicy h4096 = {&s_h4096, false, true};
-    static const StreamPolicy h5120 = {&s_h5120, false, true};
-    static const StreamPolicy h128 = {&s_h128, false, true};
-    if (dtype != RMSNORM_BF16 || !vec)
+    static const StreamPolicy b4096 = {&s_h4096, false, true};
+    static const StreamPolicy b5120 = {&s_h5120, false, true};
+    static const StreamPolicy b128 = {&s_h128, false, true};
+    static const StreamPolicy h4096 = {&sh_h4096, false, true};
+    static const StreamPolicy h5120 = {&sh_h5120, false, true};
+    static const StreamPolicy h128 = {&sh_h128, false, true};
+    if (dtype == RMSNORM_F32 || !vec)
         return nullptr;
-    if (H == 128)
-        return &h128;
+    const bool b = dtype == RMSNORM_BF16;
+    if (H == 128 && dense)
+        return b ? &b128 : &h128;
     if (H == 4096)
-        return &h4096;
+        return b ? &b4096 : &h4096;
     if (H == 5120)
-        return &h5120;
+        return b ? &b5120 : &h5120;
     return nullptr;
 }
 
@@ -191,21 +246,37 @@ cudaError_t launch2(const void *fn, dim3 grid, dim3 block, int smem, cudaStream_
 }
 
 // -------------------------------------------------------- kernel choice
-// wide: every row pointer 32-byte aligned and H * element size a multiple
-// of 32, so a forward with 32-byte packs may run.
+// The row-wise layouts of one 16-bit format.
+struct HalfSet {
+    const RowKernels &s32, &s1024, &h128, &h128w, &h896, &h4096, &h4096w, &h5120, &h5120w,
+        &g32, &g128, &g512;
+};
+
+const RowKernels &pick_half(const HalfSet &k, int64_t H, bool vec, bool wide)
+{
+    if (!vec)
+        return H <= k.s32.max_cols() ? k.s32 : k.s1024;
+    if (H == 128) return wide ? k.h128w : k.h128;
+    if (H == 896) return k.h896;
+    if (H == 4096) return wide ? k.h4096w : k.h4096;
+    if (H == 5120) return wide ? k.h5120w : k.h5120;
+    if (H <= k.g32.max_cols()) return k.g32;
+    if (H <= k.g128.max_cols()) return k.g128;
+    return k.g512;
+}
+
+// wide: every row start 32-byte aligned (pointers, H * element size and the
+// row strides), so a forward with 32-byte packs may run.
 const RowKernels &pick_rows(int dtype, int64_t H, bool vec, bool wide)
 {
-    if (dtype == RMSNORM_BF16) {
-        if (!vec)
-            return H <= b_s32.max_cols() ? b_s32 : b_s1024;
-        if (H == 128) return wide ? b_h128w : b_h128;
-        if (H == 896) return b_h896;
-        if (H == 4096) return wide ? b_h4096w : b_h4096;
-        if (H == 5120) return wide ? b_h5120w : b_h5120;
-        if (H <= b_g32.max_cols()) return b_g32;
-        if (H <= b_g128.max_cols()) return b_g128;
-        return b_g512;
-    }
+    static const HalfSet bf = {b_s32, b_s1024, b_h128, b_h128w, b_h896, b_h4096,
+                               b_h4096w, b_h5120, b_h5120w, b_g32, b_g128, b_g512};
+    static const HalfSet hf = {h_s32, h_s1024, h_h128, h_h128w, h_h896, h_h4096,
+                               h_h4096w, h_h5120, h_h5120w, h_g32, h_g128, h_g512};
+    if (dtype == RMSNORM_BF16)
+        return pick_half(bf, H, vec, wide);
+    if (dtype == RMSNORM_F16)
+        return pick_half(hf, H, vec, wide);
     if (!vec)
         return H <= f_s32.max_cols() ? f_s32 : f_s1024;
     if (H == 896) return f_h896;
@@ -218,6 +289,8 @@ const SplitKernels &pick_split(int dtype, bool vec)
 {
     if (dtype == RMSNORM_BF16)
         return vec ? split_bf16_v : split_bf16_s;
+    if (dtype == RMSNORM_F16)
+        return vec ? split_f16_v : split_f16_s;
     return vec ? split_f32_v : split_f32_s;
 }
 
@@ -250,17 +323,24 @@ cudaError_t launch(const void *fn, dim3 grid, dim3 block, cudaStream_t s, void *
 }
 
 // ------------------------------------------------------------- forward
-int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, float *rstd,
-             int64_t M, int64_t H, float eps, int dtype, cudaStream_t stream)
+// Arguments already checked; ld* are row strides in elements (H if dense).
+int fwd_impl(const void *x, int64_t ldx, const void *r, int64_t ldr, const void *w, void *y,
+             int64_t ldy, void *h, int64_t ldh, float *rstd, int64_t M, int64_t H, float eps,
+             int dtype, cudaStream_t stream)
 {
     const bool res = r != nullptr;
+    if (!res)
+        ldr = ldh = H;
     const size_t es = elem_size(dtype);
     const bool vec16 = (H * (int64_t)es) % 16 == 0 && aligned(x, 16) && aligned(w, 16) &&
-                       aligned(y, 16) && aligned(r, 16) && aligned(h, 16);
+                       aligned(y, 16) && aligned(r, 16) && aligned(h, 16) &&
+                       strides_multiple(16, es, {ldx, ldr, ldy, ldh});
     const int ov = g_path_override.load(std::memory_order_relaxed);
     const bool vec = vec16 && ov != kPathScalar;
     const bool wide = vec && (H * (int64_t)es) % 32 == 0 && aligned(x, 32) && aligned(w, 32) &&
-                      aligned(y, 32) && aligned(r, 32) && aligned(h, 32);
+                      aligned(y, 32) && aligned(r, 32) && aligned(h, 32) &&
+                      strides_multiple(32, es, {ldx, ldr, ldy, ldh});
+    const bool dense = ldx == H && ldr == H && ldy == H && ldh == H;
     const bool split = M <= 65535 && (ov == kPathSplit || (ov == kPathAuto && M <= kSplitMaxRows));
 
     if (split) {
@@ -274,7 +354,7 @@ int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, floa
         NT = NT > 256 ? 256 : NT;
         const int V = (SV + NT - 1) / NT;   // <= 8 for H <= RMSNORM_MAX_H
         const void *fn = V == 1 ? (res ? k.v1_res : k.v1) : (res ? k.v8_res : k.v8);
-        SplitParams p = {x, r, w, y, h, rstd, (int)H, NV, SV, eps};
+        SplitParams p = {x, r, w, y, h, rstd, (int)H, NV, SV, eps, ldx, ldr, ldy, ldh};
         cudaError_t e = launch(fn, dim3(K, (unsigned)M), dim3(NT), stream, &p, true, K);
         if (e != cudaSuccess)
             return cuda_fail(e);
@@ -282,7 +362,8 @@ int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, floa
         return RMSNORM_OK;
     }
 
-    const StreamPolicy *sp = pick_stream(dtype, H, vec);
+    FwdParams p = {x, r, w, y, h, rstd, M, (int)H, eps, ldx, ldr, ldy, ldh, 0, 0};
+    const StreamPolicy *sp = pick_stream(dtype, H, vec, dense);
     if (sp && (ov == kPathStream || (ov == kPathAuto && sp->auto_fwd))) {
         const StreamKernels &k = *sp->k;
         const void *fn = k.fwd[res ? 1 : 0];
@@ -295,7 +376,6 @@ int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, floa
         unsigned int *tmo = stream_timeout_counter(dev);
         if (tmo == nullptr)
             return cuda_fail(cudaErrorInvalidSymbol);
-        FwdParams p = {x, r, w, y, h, rstd, M, (int)H, eps};
         p.extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
         p.wait_limit_us = g_test_wait_us.load(std::memory_order_relaxed);
         cudaError_t e = launch2(fn, dim3((unsigned)grid), dim3(k.f.threads()), smem, stream, &p,
@@ -312,12 +392,55 @@ int fwd_impl(const void *x, const void *r, const void *w, void *y, void *h, floa
     int st = rows_grid(k.f, fn, M, &grid);
     if (st)
         return st;
-    FwdParams p = {x, r, w, y, h, rstd, M, (int)H, eps};
     cudaError_t e = launch(fn, dim3((unsigned)grid), dim3(k.f.threads()), stream, &p, true, 0);
     if (e != cudaSuccess)
         return cuda_fail(e);
     t_last_path = vec ? kPathRows : kPathScalar;
     return RMSNORM_OK;
+}
+
+// Checks shared by the dense and strided forward entry points, then the
+// launch. r and h are both NULL (plain) or both given (residual).
+int fwd_checked(const void *x, int64_t ldx, const void *r, int64_t ldr, const void *w, void *y,
+                int64_t ldy, void *h, int64_t ldh, float *rstd, int64_t M, int64_t H, float eps,
+                int dtype, cudaStream_t stream)
+{
+    int st = check_common(M, H, eps, dtype);
+    if (st)
+        return st;
+    const bool res = r != nullptr || h != nullptr;
+    if (res && (r == nullptr || h == nullptr))
+        return RMSNORM_ERR_NULLPTR;
+    if (!stride_ok(ldx, M, H) || !stride_ok(ldy, M, H) ||
+        (res && (!stride_ok(ldr, M, H) || !stride_ok(ldh, M, H))))
+        return RMSNORM_ERR_BAD_STRIDE;
+    if (M == 0)
+        return RMSNORM_OK;
+    if (!x || !w || !y)
+        return RMSNORM_ERR_NULLPTR;
+    const size_t es = elem_size(dtype);
+    if (!aligned(x, es) || !aligned(r, es) || !aligned(w, es) || !aligned(h, es) ||
+        !aligned(y, es) || !aligned(rstd, 4))
+        return RMSNORM_ERR_MISALIGNED;
+    const Span sx = rows_span(x, M, H, ldx, es), sw = flat(w, (size_t)H * es),
+               sy = rows_span(y, M, H, ldy, es), ss = flat(rstd, (size_t)M * 4);
+    if (!res) {
+        if (!same_or_disjoint(sy, sx) || overlap(sy, sw) || overlap(ss, sx) ||
+            overlap(ss, sw) || overlap(ss, sy))
+            return RMSNORM_ERR_ALIAS;
+    } else {
+        const Span sr = rows_span(r, M, H, ldr, es), sh = rows_span(h, M, H, ldh, es);
+        if (!same_or_disjoint(sh, sx) || !same_or_disjoint(sh, sr) || overlap(sh, sw) ||
+            overlap(sh, ss))
+            return RMSNORM_ERR_ALIAS;
+        for (Span b : {sx, sr, sw, sh, ss})
+            if (overlap(sy, b))
+                return RMSNORM_ERR_ALIAS;
+        for (Span b : {sx, sr, sw})
+            if (overlap(ss, b))
+                return RMSNORM_ERR_ALIAS;
+    }
+    return fwd_impl(x, ldx, r, ldr, w, y, ldy, h, ldh, rstd, M, H, eps, dtype, stream);
 }
 
 // ------------------------------------------------------------ backward
@@ -332,10 +455,10 @@ struct BwdPlan {
 };
 
 // Kernel, grid (and so partial-row count) of the backward for these args.
-int bwd_plan(int dtype, int64_t M, int64_t H, bool vec, bool dh, bool have_rstd, int ov,
-             BwdPlan *pl)
+int bwd_plan(int dtype, int64_t M, int64_t H, bool vec, bool dense, bool dh, bool have_rstd,
+             int ov, BwdPlan *pl)
 {
-    const StreamPolicy *sp = pick_stream(dtype, H, vec);
+    const StreamPolicy *sp = pick_stream(dtype, H, vec, dense);
     pl->vec = vec;
     pl->timeouts = nullptr;
     if (sp && (ov == kPathStream || (ov == kPathAuto && sp->auto_bwd))) {
@@ -367,13 +490,20 @@ int bwd_plan(int dtype, int64_t M, int64_t H, bool vec, bool dh, bool have_rstd,
     return rows_grid(k.b, pl->fn, M, &pl->grid);
 }
 
-int bwd_impl(const void *dy, const void *dh, const void *x, const void *w, const float *rstd,
-             void *dx, float *dw, void *ws, size_t ws_bytes, int64_t M, int64_t H, float eps,
-             int dtype, cudaStream_t stream, int flags = 0)
+// ld* are row strides in elements (H if dense); a NULL dh's stride is ignored.
+int bwd_impl(const void *dy, int64_t lddy, const void *dh, int64_t lddh, const void *x,
+             int64_t ldx, const void *w, const float *rstd, void *dx, int64_t lddx, float *dw,
+             void *ws, size_t ws_bytes, int64_t M, int64_t H, float eps, int dtype,
+             cudaStream_t stream, int flags = 0)
 {
     int st = check_common(M, H, eps, dtype);
     if (st)
         return st;
+    if (dh == nullptr)
+        lddh = H;
+    if (!stride_ok(lddy, M, H) || !stride_ok(lddh, M, H) || !stride_ok(ldx, M, H) ||
+        !stride_ok(lddx, M, H))
+        return RMSNORM_ERR_BAD_STRIDE;
     if (dw == nullptr)
         return RMSNORM_ERR_NULLPTR;
     if (M > 0 && (!dy || !x || !w || !dx))
@@ -383,32 +513,38 @@ int bwd_impl(const void *dy, const void *dh, const void *x, const void *w, const
         !aligned(dh, es) || !aligned(rstd, 4) || !aligned(dw, 4) || !aligned(ws, 16))
         return RMSNORM_ERR_MISALIGNED;
 
+    const Span sdy = rows_span(dy, M, H, lddy, es), sdh = rows_span(dh, M, H, lddh, es),
+               sx = rows_span(x, M, H, ldx, es), sw = flat(w, (size_t)H * es),
+               sr = flat(rstd, (size_t)M * 4), sdx = rows_span(dx, M, H, lddx, es),
+               sdw = flat(dw, (size_t)H * 4);
+    if (!same_or_disjoint(sdx, sdy) || !same_or_disjoint(sdx, sdh) || overlap(sdx, sx) ||
+        overlap(sdx, sw) || overlap(sdx, sr) || overlap(sdx, sdw))
+        return RMSNORM_ERR_ALIAS;
+    for (Span b : {sdy, sdh, sx, sw, sr})
+        if (overlap(sdw, b))
+            return RMSNORM_ERR_ALIAS;
+
     const bool vec16 = (H * (int64_t)es) % 16 == 0 && aligned(dy, 16) && aligned(x, 16) &&
-                       aligned(w, 16) && aligned(dx, 16) && aligned(dh, 16);
+                       aligned(w, 16) && aligned(dx, 16) && aligned(dh, 16) &&
+                       strides_multiple(16, es, {lddy, lddh, ldx, lddx});
+    const bool dense = lddy == H && lddh == H && ldx == H && lddx == H;
     const int ov = g_path_override.load(std::memory_order_relaxed);
     const bool vec = vec16 && ov != kPathScalar;
     BwdPlan pl;
-    if ((st = bwd_plan(dtype, M, H, vec, dh != nullptr, rstd != nullptr, ov, &pl)))
+    if ((st = bwd_plan(dtype, M, H, vec, dense, dh != nullptr, rstd != nullptr, ov, &pl)))
         return st;
     const size_t need = (size_t)pl.grid * (size_t)H * sizeof(float);
     if (need > 0 && (ws == nullptr || ws_bytes < need))
         return RMSNORM_ERR_WORKSPACE;
-
-    const size_t rows = (size_t)M * (size_t)H * es;
-    const Buf bdy{dy, rows}, bdh{dh, rows}, bx{x, rows}, bw{w, (size_t)H * es},
-        br{rstd, (size_t)M * 4}, bdx{dx, rows}, bdw{dw, (size_t)H * 4}, bws{ws, need};
-    if (!same_or_disjoint(bdx, bdy) || !same_or_disjoint(bdx, bdh) || overlap(bdx, bx) ||
-        overlap(bdx, bw) || overlap(bdx, br) || overlap(bdx, bdw) || overlap(bdx, bws))
-        return RMSNORM_ERR_ALIAS;
-    for (Buf b : {bdy, bdh, bx, bw, br, bws})
-        if (overlap(bdw, b))
-            return RMSNORM_ERR_ALIAS;
-    for (Buf b : {bdy, bdh, bx, bw, br})
-        if (overlap(bws, b))
+    const Span sws = flat(ws, need);
+    for (Span b : {sdy, sdh, sx, sw, sr, sdx, sdw})
+        if (overlap(sws, b))
             return RMSNORM_ERR_ALIAS;
 
     if (M > 0) {
-        BwdParams p = {dy, x, w, rstd, dh, dx, static_cast<float *>(ws), M, (int)H, eps};
+        BwdParams p = {dy,  x,        w,    rstd, dh,  dx,   static_cast<float *>(ws),
+                       M,   (int)H,   eps,  lddy, ldx, lddh, lddx,
+                       0,   0};
         if (pl.stream) {
             p.extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
             p.wait_limit_us = g_test_wait_us.load(std::memory_order_relaxed);
@@ -455,60 +591,33 @@ extern "C" {
 int rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd, int64_t M, int64_t H,
                 float eps, int dtype, void *stream)
 {
-    int st = check_common(M, H, eps, dtype);
-    if (st)
-        return st;
-    if (M == 0)
-        return RMSNORM_OK;
-    if (!x || !w || !y)
-        return RMSNORM_ERR_NULLPTR;
-    const size_t es = elem_size(dtype);
-    if (!aligned(x, es) || !aligned(w, es) || !aligned(y, es) || !aligned(rstd, 4))
-        return RMSNORM_ERR_MISALIGNED;
-    const size_t rows = (size_t)M * (size_t)H * es;
-    const Buf bx{x, rows}, bw{w, (size_t)H * es}, by{y, rows}, br{rstd, (size_t)M * 4};
-    if (!same_or_disjoint(by, bx) || overlap(by, bw) || overlap(br, bx) || overlap(br, bw) ||
-        overlap(br, by))
-        return RMSNORM_ERR_ALIAS;
-    return fwd_impl(x, nullptr, w, y, nullptr, rstd, M, H, eps, dtype,
-                    static_cast<cudaStream_t>(stream));
+    return fwd_checked(x, H, nullptr, H, w, y, H, nullptr, H, rstd, M, H, eps, dtype,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int rmsnorm_residual_fwd(const void *x, const void *r, const void *w, void *h, void *y,
                          float *rstd, int64_t M, int64_t H, float eps, int dtype, void *stream)
 {
-    int st = check_common(M, H, eps, dtype);
-    if (st)
-        return st;
-    if (M == 0)
-        return RMSNORM_OK;
-    if (!x || !r || !w || !h || !y)
+    if (check_common(M, H, eps, dtype) == RMSNORM_OK && M > 0 && (!r || !h))
         return RMSNORM_ERR_NULLPTR;
-    const size_t es = elem_size(dtype);
-    if (!aligned(x, es) || !aligned(r, es) || !aligned(w, es) || !aligned(h, es) ||
-        !aligned(y, es) || !aligned(rstd, 4))
-        return RMSNORM_ERR_MISALIGNED;
-    const size_t rows = (size_t)M * (size_t)H * es;
-    const Buf bx{x, rows}, br{r, rows}, bw{w, (size_t)H * es}, bh{h, rows}, by{y, rows},
-        bs{rstd, (size_t)M * 4};
-    if (!same_or_disjoint(bh, bx) || !same_or_disjoint(bh, br) || overlap(bh, bw) ||
-        overlap(bh, bs))
-        return RMSNORM_ERR_ALIAS;
-    for (Buf b : {bx, br, bw, bh, bs})
-        if (overlap(by, b))
-            return RMSNORM_ERR_ALIAS;
-    for (Buf b : {bx, br, bw})
-        if (overlap(bs, b))
-            return RMSNORM_ERR_ALIAS;
-    return fwd_impl(x, r, w, y, h, rstd, M, H, eps, dtype, static_cast<cudaStream_t>(stream));
+    return fwd_checked(x, H, r, H, w, y, H, h, H, rstd, M, H, eps, dtype,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int rmsnorm_fwd_strided(const void *x, int64_t ldx, const void *r, int64_t ldr, const void *w,
+                        void *y, int64_t ldy, void *h, int64_t ldh, float *rstd, int64_t M,
+                        int64_t H, float eps, int dtype, void *stream)
+{
+    return fwd_checked(x, ldx, r, ldr, w, y, ldy, h, ldh, rstd, M, H, eps, dtype,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int rmsnorm_bwd(const void *dy, const void *x, const void *w, const float *rstd, void *dx,
                 float *dw, void *workspace, size_t workspace_bytes, int64_t M, int64_t H,
                 float eps, int dtype, void *stream)
 {
-    return bwd_impl(dy, nullptr, x, w, rstd, dx, dw, workspace, workspace_bytes, M, H, eps,
-                    dtype, static_cast<cudaStream_t>(stream));
+    return bwd_impl(dy, H, nullptr, H, x, H, w, rstd, dx, H, dw, workspace, workspace_bytes, M,
+                    H, eps, dtype, static_cast<cudaStream_t>(stream));
 }
 
 int rmsnorm_residual_bwd(const void *dy, const void *dh_out, const void *h, const void *w,
@@ -516,8 +625,8 @@ int rmsnorm_residual_bwd(const void *dy, const void *dh_out, const void *h, cons
                          size_t workspace_bytes, int64_t M, int64_t H, float eps, int dtype,
                          void *stream)
 {
-    return bwd_impl(dy, dh_out, h, w, rstd, dx, dw, workspace, workspace_bytes, M, H, eps,
-                    dtype, static_cast<cudaStream_t>(stream));
+    return bwd_impl(dy, H, dh_out, H, h, H, w, rstd, dx, H, dw, workspace, workspace_bytes, M,
+                    H, eps, dtype, static_cast<cudaStream_t>(stream));
 }
 
 int rmsnorm_bwd_ex(const void *dy, const void *dh_out, const void *x, const void *w,
@@ -527,8 +636,19 @@ int rmsnorm_bwd_ex(const void *dy, const void *dh_out, const void *x, const void
 {
     if (flags & ~RMSNORM_BWD_ACCUMULATE_DW)
         return RMSNORM_ERR_BAD_FLAGS;
-    return bwd_impl(dy, dh_out, x, w, rstd, dx, dw, workspace, workspace_bytes, M, H, eps,
-                    dtype, static_cast<cudaStream_t>(stream), flags);
+    return bwd_impl(dy, H, dh_out, H, x, H, w, rstd, dx, H, dw, workspace, workspace_bytes, M,
+                    H, eps, dtype, static_cast<cudaStream_t>(stream), flags);
+}
+
+int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out, int64_t lddh,
+                        const void *x, int64_t ldx, const void *w, const float *rstd, void *dx,
+                        int64_t lddx, float *dw, void *workspace, size_t workspace_bytes,
+                        int64_t M, int64_t H, float eps, int dtype, int flags, void *stream)
+{
+    if (flags & ~RMSNORM_BWD_ACCUMULATE_DW)
+        return RMSNORM_ERR_BAD_FLAGS;
+    return bwd_impl(dy, lddy, dh_out, lddh, x, ldx, w, rstd, dx, lddx, dw, workspace,
+                    workspace_bytes, M, H, eps, dtype, static_cast<cudaStream_t>(stream), flags);
 }
 
 size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype)
@@ -541,7 +661,8 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype)
             for (int dh = 0; dh < 2; ++dh)
                 for (int hr = 0; hr < 2; ++hr) {
                     BwdPlan pl;
-                    if (bwd_plan(dtype, M, H, vec != 0, dh != 0, hr != 0, ov, &pl) != RMSNORM_OK)
+                    if (bwd_plan(dtype, M, H, vec != 0, true, dh != 0, hr != 0, ov, &pl) !=
+                        RMSNORM_OK)
                         return 0;
                     const size_t need = (size_t)pl.grid * (size_t)H * sizeof(float);
                     most = need > most ? need : most;
@@ -555,7 +676,7 @@ const char *rmsnorm_status_string(int status)
     case RMSNORM_OK: return "ok";
     case RMSNORM_ERR_NULLPTR: return "a required pointer is NULL";
     case RMSNORM_ERR_BAD_SHAPE: return "bad shape (M < 0, H < 1 or M*H too large)";
-    case RMSNORM_ERR_BAD_DTYPE: return "dtype is not RMSNORM_F32 or RMSNORM_BF16";
+    case RMSNORM_ERR_BAD_DTYPE: return "dtype is not RMSNORM_F32, RMSNORM_BF16 or RMSNORM_F16";
     case RMSNORM_ERR_BAD_EPS: return "eps must be finite and >= 0";
     case RMSNORM_ERR_MISALIGNED: return "pointer not aligned to its element size (workspace: 16 bytes)";
     case RMSNORM_ERR_WORKSPACE: return "workspace missing or smaller than rmsnorm_bwd_workspace_bytes()";
@@ -563,6 +684,7 @@ const char *rmsnorm_status_string(int status)
     case RMSNORM_ERR_CUDA: return "a CUDA runtime call failed (see rmsnorm_last_cuda_error)";
     case RMSNORM_ERR_ALIAS: return "output buffers overlap inputs or each other in a way not allowed";
     case RMSNORM_ERR_BAD_FLAGS: return "unknown bits in flags";
+    case RMSNORM_ERR_BAD_STRIDE: return "a row stride is below H, above 2^31-1 or too large for the row count";
     case RMSNORM_ERR_SCRATCH_LIMIT:
         return "problem needs more scratch than RMSNORM_STATIC_SCRATCH_BYTES (use rmsnorm_bwd with a workspace)";
     default: return "unknown status";
@@ -652,6 +774,7 @@ extern "C" int rmsnorm_bwd_static_scratch(const void *dy, const void *x, const v
     void *scratch = nullptr;
     if ((st = static_scratch_address(&scratch)))
         return st;
-    return bwd_impl(dy, nullptr, x, w, rstd, dx, dw, scratch, RMSNORM_STATIC_SCRATCH_BYTES, M,
-                    H, eps, dtype, static_cast<cudaStream_t>(stream));
+    return bwd_impl(dy, H, nullptr, H, x, H, w, rstd, dx, H, dw, scratch,
+                    RMSNORM_STATIC_SCRATCH_BYTES, M, H, eps, dtype,
+                    static_cast<cudaStream_t>(stream));
 }

@@ -1,9 +1,10 @@
 // common.cuh -- device helpers shared by the RMSNorm kernels: element packs
-// moved with one memory instruction, streaming loads/stores, bf16 <-> fp32,
-// lane-group reductions.
+// moved with one memory instruction, streaming loads/stores, bf16/fp16 <->
+// fp32, lane-group reductions.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -12,6 +13,7 @@
 namespace rmsk {
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 // ---------------------------------------------------------------- memory ops
 // Row data is touched once per kernel: loads skip L1 allocation so the
@@ -94,23 +96,57 @@ __device__ __forceinline__ void st_row_v8(void *p, const u32x8 &v)
                  : "memory");
 }
 
-// ------------------------------------------------------------ bf16 <-> fp32
-// bf16 is the upper half of an fp32 word, so widening is a shift.
-__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+// ------------------------------------------------ 16-bit formats <-> fp32
+// Half16<T>: conversions of a 16-bit storage format (bf16 or fp16) to and
+// from fp32, on one element or on a 32-bit word holding two (the lower
+// address in the low half). Widening is exact in both formats; narrowing
+// rounds to nearest even (including fp16 subnormals and overflow to inf).
+template <typename T> struct Half16;
 
-// Two fp32 -> packed bf16x2 (lo in the low half), round to nearest even.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
-{
-    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&b);
-}
+template <> struct Half16<bf16> {
+    using Tag = void;
+    // bf16 is the upper half of an fp32 word, so widening is a shift.
+    __device__ __forceinline__ static float2 wide2(uint32_t u)
+    {
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    }
+    __device__ __forceinline__ static float wide1(uint16_t u)
+    {
+        return __uint_as_float((uint32_t)u << 16);
+    }
+    __device__ __forceinline__ static uint32_t narrow2(float lo, float hi)
+    {
+        __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&b);
+    }
+    __device__ __forceinline__ static uint16_t narrow1(float v)
+    {
+        __nv_bfloat16 b = __float2bfloat16_rn(v);
+        return *reinterpret_cast<uint16_t *>(&b);
+    }
+};
 
-__device__ __forceinline__ uint16_t pack_bf16(float v)
-{
-    __nv_bfloat16 b = __float2bfloat16_rn(v);
-    return *reinterpret_cast<uint16_t *>(&b);
-}
+template <> struct Half16<f16> {
+    using Tag = void;
+    __device__ __forceinline__ static float2 wide2(uint32_t u)
+    {
+        __half2 h = *reinterpret_cast<__half2 *>(&u);
+        return __half22float2(h);
+    }
+    __device__ __forceinline__ static float wide1(uint16_t u)
+    {
+        return __half2float(__ushort_as_half(u));
+    }
+    __device__ __forceinline__ static uint32_t narrow2(float lo, float hi)
+    {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ __forceinline__ static uint16_t narrow1(float v)
+    {
+        return __half_as_ushort(__float2half_rn(v));
+    }
+};
 
 // ------------------------------------------------------- packed fp32 math
 // The sm_100 family issues two fp32 operations per FFMA2 / FMUL2 / FADD2
@@ -154,11 +190,14 @@ struct Vals {
 
 // ----------------------------------------------------------------- packs
 // Pack<T, E>: E consecutive elements of T moved by one memory instruction
-// (E * sizeof(T) == 16 for the vectorised kernels, E == 1 for the scalar
-// ones). idx counts packs from `base`.
-template <typename T, int E> struct Pack;
+// (E * sizeof(T) == 16 or 32 for the vectorised kernels, E == 1 for the
+// scalar ones). idx counts packs from `base`. The 16-bit formats share one
+// definition per width (selected through Half16<T>::Tag).
+template <typename T, int E, typename Enable = void> struct Pack;
 
-template <> struct Pack<bf16, 8> {
+// 16-bit formats (bf16, fp16), 16-byte packs.
+template <typename T> struct Pack<T, 8, typename Half16<T>::Tag> {
+    using C = Half16<T>;
     uint4 u;
     static constexpr int E = 8;
     __device__ __forceinline__ static Pack zero() { Pack p; p.u = make_uint4(0, 0, 0, 0); return p; }
@@ -176,33 +215,40 @@ template <> struct Pack<bf16, 8> {
     }
     __device__ __forceinline__ void to_float(float (&f)[8]) const
     {
-        f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
-        f[4] = bf16lo(u.z); f[5] = bf16hi(u.z); f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 t = C::wide2(w[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
     }
     __device__ __forceinline__ static Pack from_float(const float (&f)[8])
     {
         Pack p;
-        p.u.x = pack_bf16x2(f[0], f[1]); p.u.y = pack_bf16x2(f[2], f[3]);
-        p.u.z = pack_bf16x2(f[4], f[5]); p.u.w = pack_bf16x2(f[6], f[7]);
+        p.u.x = C::narrow2(f[0], f[1]); p.u.y = C::narrow2(f[2], f[3]);
+        p.u.z = C::narrow2(f[4], f[5]); p.u.w = C::narrow2(f[6], f[7]);
         return p;
     }
     __device__ __forceinline__ void widen(Vals<8> &f) const
     {
-        f.v[0] = make_float2(bf16lo(u.x), bf16hi(u.x));
-        f.v[1] = make_float2(bf16lo(u.y), bf16hi(u.y));
-        f.v[2] = make_float2(bf16lo(u.z), bf16hi(u.z));
-        f.v[3] = make_float2(bf16lo(u.w), bf16hi(u.w));
+        f.v[0] = C::wide2(u.x);
+        f.v[1] = C::wide2(u.y);
+        f.v[2] = C::wide2(u.z);
+        f.v[3] = C::wide2(u.w);
     }
     __device__ __forceinline__ static Pack narrow(const Vals<8> &f)
     {
         Pack p;
-        p.u.x = pack_bf16x2(f.v[0].x, f.v[0].y); p.u.y = pack_bf16x2(f.v[1].x, f.v[1].y);
-        p.u.z = pack_bf16x2(f.v[2].x, f.v[2].y); p.u.w = pack_bf16x2(f.v[3].x, f.v[3].y);
+        p.u.x = C::narrow2(f.v[0].x, f.v[0].y); p.u.y = C::narrow2(f.v[1].x, f.v[1].y);
+        p.u.z = C::narrow2(f.v[2].x, f.v[2].y); p.u.w = C::narrow2(f.v[3].x, f.v[3].y);
         return p;
     }
 };
 
-template <> struct Pack<bf16, 16> {
+// 16-bit formats, 32-byte packs (one 256-bit access).
+template <typename T> struct Pack<T, 16, typename Half16<T>::Tag> {
+    using C = Half16<T>;
     u32x8 u;
     static constexpr int E = 16;
     __device__ __forceinline__ static Pack zero()
@@ -234,14 +280,14 @@ template <> struct Pack<bf16, 16> {
     {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            f.v[i] = make_float2(bf16lo(u.w[i]), bf16hi(u.w[i]));
+            f.v[i] = C::wide2(u.w[i]);
     }
     __device__ __forceinline__ static Pack narrow(const Vals<16> &f)
     {
         Pack p;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            p.u.w[i] = pack_bf16x2(f.v[i].x, f.v[i].y);
+            p.u.w[i] = C::narrow2(f.v[i].x, f.v[i].y);
         return p;
     }
 };
@@ -292,7 +338,9 @@ template <> struct Pack<float, 8> {
     }
 };
 
-template <> struct Pack<bf16, 1> {
+// 16-bit formats, one element per access.
+template <typename T> struct Pack<T, 1, typename Half16<T>::Tag> {
+    using C = Half16<T>;
     uint16_t u;
     static constexpr int E = 1;
     __device__ __forceinline__ static Pack zero() { Pack p; p.u = 0; return p; }
@@ -308,15 +356,15 @@ template <> struct Pack<bf16, 1> {
     {
         st_row_b16(static_cast<uint16_t *>(base) + idx, u);
     }
-    __device__ __forceinline__ void to_float(float (&f)[1]) const { f[0] = bf16lo(u); }
+    __device__ __forceinline__ void to_float(float (&f)[1]) const { f[0] = C::wide1(u); }
     __device__ __forceinline__ static Pack from_float(const float (&f)[1])
     {
-        Pack p; p.u = pack_bf16(f[0]); return p;
+        Pack p; p.u = C::narrow1(f[0]); return p;
     }
-    __device__ __forceinline__ void widen(Vals<1> &f) const { f.v[0] = bf16lo(u); }
+    __device__ __forceinline__ void widen(Vals<1> &f) const { f.v[0] = C::wide1(u); }
     __device__ __forceinline__ static Pack narrow(const Vals<1> &f)
     {
-        Pack p; p.u = pack_bf16(f.v[0]); return p;
+        Pack p; p.u = C::narrow1(f.v[0]); return p;
     }
 };
 

@@ -1,5 +1,7 @@
 // params.h -- kernel argument blocks, passed by value; shared by the
-// kernels and the host code that launches them.
+// kernels and the host code that launches them. Every [M,H] tensor has its
+// own row stride ld (elements between the starts of consecutive rows, >= H;
+// H for contiguous rows); a kernel's pack width divides every stride it gets.
 #pragma once
 
 #include <stdint.h>
@@ -17,6 +19,7 @@ struct FwdParams {
     int64_t M;
     int H;
     float eps;
+    int64_t ldx, ldr, ldy, ldh;   // row strides of x, r, y, h
     // Streamed kernels only: bytes a stage waits for beyond what its copies
     // deliver (0; a test sets it to make waits run out) and the wait limit
     // in microseconds (0 = the default of about one second).
@@ -36,6 +39,7 @@ struct BwdParams {
     int64_t M;
     int H;
     float eps;
+    int64_t lddy, ldx, lddh, lddx;   // row strides of dy, x, dh, dx
     uint32_t extra_tx;       // as in FwdParams
     uint32_t wait_limit_us;
 };
@@ -52,6 +56,7 @@ struct SplitParams {
     int NV;          // packs per row
     int SV;          // packs per CTA (the last ranks may hold fewer or none)
     float eps;
+    int64_t ldx, ldr, ldy, ldh;   // row strides of x, r, y, h
 };
 
 } // namespace rmsk

@@ -32,7 +32,7 @@ struct RowKernels {
     }
 };
 
-// A streamed (bulk-copy fed) layout, bf16 only: the CTA's threads and the
+// A streamed (bulk-copy fed) layout, 16-bit formats only: the CTA's threads and the
 // rows a CTA takes per round (stream.cuh: NG groups, one row each;
 // stream_small.cuh: NW warps, one block of rows each).
 struct StreamShape {
@@ -64,14 +64,21 @@ extern const RowKernels b_h128, b_h896, b_h4096, b_h5120, b_g32, b_g128, b_g512;
 extern const RowKernels b_h128w, b_h4096w, b_h5120w;
 // bf16, one element per access (rows not 16-byte aligned, odd H)
 extern const RowKernels b_s32, b_s1024;
+// fp16: the same layouts as bf16
+extern const RowKernels h_h128, h_h896, h_h4096, h_h5120, h_g32, h_g128, h_g512;
+extern const RowKernels h_h128w, h_h4096w, h_h5120w;
+extern const RowKernels h_s32, h_s1024;
 // fp32, 16-byte packs
 extern const RowKernels f_h896, f_g32, f_g128, f_g512;
 // fp32, one element per access
 extern const RowKernels f_s32, f_s1024;
 
 extern const SplitKernels split_bf16_v, split_bf16_s, split_f32_v, split_f32_s;
+extern const SplitKernels split_f16_v, split_f16_s;
 
+// streamed layouts: bf16 (s_) and fp16 (sh_)
 extern const StreamKernels s_h4096, s_h5120, s_h128;
+extern const StreamKernels sh_h4096, sh_h5120, sh_h128;
 // Device address of the counter of streamed-kernel waits that ran out.
 unsigned int *stream_timeout_counter(int dev);
 
@@ -92,35 +99,36 @@ unsigned int *stream_timeout_counter(int dev);
 #define RMSK_ROWS(NAME, T, E, FL, FV, FG, FS, FMB, FEX, BL, BV, BG, BS, BMB, BEX)          \
     RMSK_ROWS2(NAME, T, E, FL, FV, FG, FS, FMB, FEX, E, BL, BV, BG, BS, BMB, BEX)
 
-#define RMSK_STREAM(NAME, H, FGW, FV, FNG, FNS, BGW, BV, BNG, BNS)                       \
+#define RMSK_STREAM(NAME, T, H, FGW, FV, FNG, FNS, BGW, BV, BNG, BNS)                    \
     static_assert(32 * FGW * FV * 8 == H && 32 * BGW * BV * 8 == H, "stream layout");    \
     const StreamKernels NAME = {                                                         \
         #NAME, H, {FNG * FGW * 32, FNG}, {BNG * BGW * 32, BNG},                          \
-        {(const void *)&rms_fwd_stream<FGW, FV, FNG, FNS, false>,                        \
-         (const void *)&rms_fwd_stream<FGW, FV, FNG, FNS, true>},                        \
+        {(const void *)&rms_fwd_stream<T, FGW, FV, FNG, FNS, false>,                     \
+         (const void *)&rms_fwd_stream<T, FGW, FV, FNG, FNS, true>},                     \
         {StreamSmem<FGW, FV, FNG, FNS, 1, 1>::kBytes,                                    \
          StreamSmem<FGW, FV, FNG, FNS, 2, 1>::kBytes},                                   \
-        {{(const void *)&rms_bwd_stream<BGW, BV, BNG, BNS, false, false>,                \
-          (const void *)&rms_bwd_stream<BGW, BV, BNG, BNS, false, true>},                \
-         {(const void *)&rms_bwd_stream<BGW, BV, BNG, BNS, true, false>,                 \
-          (const void *)&rms_bwd_stream<BGW, BV, BNG, BNS, true, true>}},                \
+        {{(const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, false, false>,             \
+          (const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, false, true>},             \
+         {(const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, true, false>,              \
+          (const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, true, true>}},             \
         {{StreamSmem<BGW, BV, BNG, BNS, 2, 2>::kBytes,                                   \
           StreamSmem<BGW, BV, BNG, BNS, 2, 1>::kBytes},                                  \
          {StreamSmem<BGW, BV, BNG, BNS, 3, 2>::kBytes,                                   \
           StreamSmem<BGW, BV, BNG, BNS, 3, 1>::kBytes}}};
 
 // Short rows (stream_small.cuh): H = 8 * NVP, NW warps, RPT rows per lane per stage.
-#define RMSK_SMALL(NAME, H, FRPT, FNW, FNS, BRPT, BNW, BNS)                               \
+// T is the 16-bit storage format.
+#define RMSK_SMALL(NAME, T, H, FRPT, FNW, FNS, BRPT, BNW, BNS)                            \
     const StreamKernels NAME = {                                                         \
         #NAME, H, {FNW * 32, FNW * (256 / H) * FRPT}, {BNW * 32, BNW * (256 / H) * BRPT}, \
-        {(const void *)&rms_fwd_stream_small<H / 8, FRPT, FNW, FNS, false>,              \
-         (const void *)&rms_fwd_stream_small<H / 8, FRPT, FNW, FNS, true>},              \
+        {(const void *)&rms_fwd_stream_small<T, H / 8, FRPT, FNW, FNS, false>,           \
+         (const void *)&rms_fwd_stream_small<T, H / 8, FRPT, FNW, FNS, true>},           \
         {SmallSmem<H / 8, FRPT, FNW, FNS, 1>::kBytes,                                    \
          SmallSmem<H / 8, FRPT, FNW, FNS, 2>::kBytes},                                   \
-        {{(const void *)&rms_bwd_stream_small<H / 8, BRPT, BNW, BNS, false, false>,      \
-          (const void *)&rms_bwd_stream_small<H / 8, BRPT, BNW, BNS, false, true>},      \
-         {(const void *)&rms_bwd_stream_small<H / 8, BRPT, BNW, BNS, true, false>,       \
-          (const void *)&rms_bwd_stream_small<H / 8, BRPT, BNW, BNS, true, true>}},      \
+        {{(const void *)&rms_bwd_stream_small<T, H / 8, BRPT, BNW, BNS, false, false>,   \
+          (const void *)&rms_bwd_stream_small<T, H / 8, BRPT, BNW, BNS, false, true>},   \
+         {(const void *)&rms_bwd_stream_small<T, H / 8, BRPT, BNW, BNS, true, false>,    \
+          (const void *)&rms_bwd_stream_small<T, H / 8, BRPT, BNW, BNS, true, true>}},   \
         {{SmallSmem<H / 8, BRPT, BNW, BNS, 2>::kBytes,                                   \
           SmallSmem<H / 8, BRPT, BNW, BNS, 2>::kBytes},                                  \
          {SmallSmem<H / 8, BRPT, BNW, BNS, 3>::kBytes,                                   \

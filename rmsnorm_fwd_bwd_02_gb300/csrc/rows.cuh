@@ -159,6 +159,9 @@ rms_fwd_rows(const FwdParams p)
     const int grp = threadIdx.x / L;
     const int NV = p.H / E;                 // packs per row
     const float fH = (float)p.H;
+    // row strides in packs (the host keeps strides below 2^31)
+    const uint32_t sx = (uint32_t)p.ldx / E, sr = (uint32_t)p.ldr / E;
+    const uint32_t sy = (uint32_t)p.ldy / E, sh = (uint32_t)p.ldh / E;
 
     griddep_wait();
     LaneWeight<T, E, L, V, EXACT, Lay::kWideW> wt;
@@ -177,7 +180,7 @@ rms_fwd_rows(const FwdParams p)
             for (int k = 0; k < V; ++k) {
                 const int vi = lane + k * L;
                 const bool ok = row < p.M && (EXACT || vi < NV);
-                xv[g][k] = ok ? P::load(p.x, row * NV + vi) : P::zero();
+                xv[g][k] = ok ? P::load(p.x, row * sx + vi) : P::zero();
             }
         }
         if constexpr (RES) {
@@ -189,7 +192,7 @@ rms_fwd_rows(const FwdParams p)
                 for (int k = 0; k < V; ++k) {
                     const int vi = lane + k * L;
                     const bool ok = row < p.M && (EXACT || vi < NV);
-                    rv[g][k] = ok ? P::load(p.r, row * NV + vi) : P::zero();
+                    rv[g][k] = ok ? P::load(p.r, row * sr + vi) : P::zero();
                 }
             }
             // h = round(x + r): the stored h is what the norm sees
@@ -207,7 +210,7 @@ rms_fwd_rows(const FwdParams p)
                         a.v[i] = vadd(a.v[i], b.v[i]);
                     xv[g][k] = P::narrow(a);
                     if (row < p.M && (EXACT || vi < NV))
-                        xv[g][k].store(p.h, row * NV + vi);
+                        xv[g][k].store(p.h, row * sh + vi);
                 }
             }
         }
@@ -249,7 +252,7 @@ rms_fwd_rows(const FwdParams p)
 #pragma unroll
                 for (int i = 0; i < X::N; ++i)
                     a.v[i] = vmul(vmul(a.v[i], r2), w.v[i]);
-                P::narrow(a).store(p.y, row * NV + vi);
+                P::narrow(a).store(p.y, row * sy + vi);
             }
         }
     }
@@ -294,6 +297,9 @@ rms_bwd_rows(const BwdParams p)
     const int grp = threadIdx.x / L;
     const int NV = p.H / E;
     const float fH = (float)p.H;
+    // row strides in packs (the host keeps strides below 2^31)
+    const uint32_t sdy = (uint32_t)p.lddy / E, sx = (uint32_t)p.ldx / E;
+    const uint32_t sdh = (uint32_t)p.lddh / E, sdx = (uint32_t)p.lddx / E;
 
     griddep_wait();
     LaneWeight<T, E, L, V, EXACT, Lay::kWideW> wt;
@@ -320,8 +326,8 @@ rms_bwd_rows(const BwdParams p)
             for (int k = 0; k < V; ++k) {
                 const int vi = lane + k * L;
                 const bool ok = row < p.M && (EXACT || vi < NV);
-                xv[g][k] = ok ? P::load(p.x, row * NV + vi) : P::zero();
-                dyv[g][k] = ok ? P::load(p.dy, row * NV + vi) : P::zero();
+                xv[g][k] = ok ? P::load(p.x, row * sx + vi) : P::zero();
+                dyv[g][k] = ok ? P::load(p.dy, row * sdy + vi) : P::zero();
             }
         }
 
@@ -380,12 +386,12 @@ rms_bwd_rows(const BwdParams p)
                 }
                 if constexpr (DH) {
                     X d;
-                    P::load(p.dh, row * NV + vi).widen(d);
+                    P::load(p.dh, row * sdh + vi).widen(d);
 #pragma unroll
                     for (int i = 0; i < X::N; ++i)
                         o.v[i] = vadd(o.v[i], d.v[i]);
                 }
-                P::narrow(o).store(p.dx, row * NV + vi);
+                P::narrow(o).store(p.dx, row * sdx + vi);
             }
         }
     }

@@ -70,20 +70,23 @@ rms_fwd_split(const SplitParams p)
     const int64_t row = blockIdx.y;
     const int v0 = (int)rank * p.SV;
     const int v1 = min(v0 + p.SV, p.NV);
+    // first pack of this row in each tensor
+    const int64_t bx = row * (p.ldx / E), br = row * (p.ldr / E);
+    const int64_t by = row * (p.ldy / E), bh = row * (p.ldh / E);
 
     griddep_wait();
     P xv[V];
 #pragma unroll
     for (int k = 0; k < V; ++k) {
         const int vi = v0 + tid + k * nt;
-        xv[k] = vi < v1 ? P::load(p.x, row * p.NV + vi) : P::zero();
+        xv[k] = vi < v1 ? P::load(p.x, bx + vi) : P::zero();
     }
     if constexpr (RES) {
         P rv[V];
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int vi = v0 + tid + k * nt;
-            rv[k] = vi < v1 ? P::load(p.r, row * p.NV + vi) : P::zero();
+            rv[k] = vi < v1 ? P::load(p.r, br + vi) : P::zero();
         }
 #pragma unroll
         for (int k = 0; k < V; ++k) {
@@ -96,7 +99,7 @@ rms_fwd_split(const SplitParams p)
                 a[e] += b[e];
             xv[k] = P::from_float(a);
             if (vi < v1)
-                xv[k].store(p.h, row * p.NV + vi);
+                xv[k].store(p.h, bh + vi);
         }
     }
 
@@ -142,7 +145,7 @@ rms_fwd_split(const SplitParams p)
 #pragma unroll
         for (int e = 0; e < E; ++e)
             f[e] = f[e] * rs * fw[e];
-        P::from_float(f).store(p.y, row * p.NV + vi);
+        P::from_float(f).store(p.y, by + vi);
     }
     // Keep this CTA's shared memory alive until every CTA has read cta_sum.
     cluster_wait_acquire();

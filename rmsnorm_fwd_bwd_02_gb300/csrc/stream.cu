@@ -1,5 +1,6 @@
 // Streamed (bulk-copy fed) row kernels for the shaped bf16 feature counts,
-// and the device counter of bounded waits that ran out.
+// and the device counter of bounded waits that ran out (the fp16 kernels,
+// in stream_f16.cu, count into the same one).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -32,12 +33,12 @@ unsigned int *stream_timeout_counter(int dev)
 
 // Stage counts are upper bounds: variants that stage more tensors per row get
 // as many stages as fit in shared memory (StreamSmem).
-//           name     H     |-- forward: GW V NG NS --| |-- backward: GW V NG NS --|
-RMSK_STREAM(s_h4096, 4096,   4, 4, 4, 4,               8, 2, 2, 6)
-RMSK_STREAM(s_h5120, 5120,   4, 5, 3, 3,              10, 2, 2, 3)
+//           name    type   H     |-- forward: GW V NG NS --| |-- backward: GW V NG NS --|
+RMSK_STREAM(s_h4096, bf16, 4096,   4, 4, 4, 4,               8, 2, 2, 6)
+RMSK_STREAM(s_h5120, bf16, 5120,   4, 5, 3, 3,              10, 2, 2, 3)
 
 // 128-wide rows (QK-norm): warps with their own rings of row blocks.
-//          name    H    |- forward: RPT NW NS -| |- backward: RPT NW NS -|
-RMSK_SMALL(s_h128, 128,       4,   16,  4,              8,   8,  3)
+//          name    type   H    |- forward: RPT NW NS -| |- backward: RPT NW NS -|
+RMSK_SMALL(s_h128, bf16, 128,       4,   16,  4,              8,   8,  3)
 
 } // namespace rmsk

@@ -12,6 +12,8 @@
 // reads a stage into registers (conflict-free 16-byte shared loads), reduces
 // over its warps with one named barrier per row, and that barrier also
 // releases the stage for the next copy. Outputs are stored from registers.
+// Each tensor has its own row stride, a multiple of 8 elements, so every
+// row copy starts on a 16-byte boundary.
 //
 // Every wait on an mbarrier is bounded in time (%globaltimer). A wait that
 // runs out means a copy never landed: the group records it in a device
@@ -127,10 +129,11 @@ __device__ __forceinline__ bool bar_red_or(int id, int count, bool pred)
     return r != 0;
 }
 
-template <int E>
-__device__ __forceinline__ Pack<bf16, 8> as_pack(uint4 u)
+// A 16-byte pack of a 16-bit format read from shared memory.
+template <typename T>
+__device__ __forceinline__ Pack<T, 8> as_pack(uint4 u)
 {
-    Pack<bf16, 8> p;
+    Pack<T, 8> p;
     p.u = u;
     return p;
 }
@@ -159,12 +162,12 @@ struct StreamSmem {
 // row NS-1 ahead. NS stages therefore keep NS-1 rows in flight per group.
 
 // ------------------------------------------------------------------ forward
-// The bf16 shaped rows only (E = 8).
-template <int GW, int V, int NG, int NS, bool RES>
+// Shaped rows of a 16-bit format (bf16 or fp16; 16-byte packs, E = 8).
+template <typename T, int GW, int V, int NG, int NS, bool RES>
 __global__ void __launch_bounds__(NG * GW * 32, 1)
 rms_fwd_stream(const FwdParams p, unsigned int *timeouts)
 {
-    using P = Pack<bf16, 8>;
+    using P = Pack<T, 8>;
     using X = Vals<8>;
     using F = float2;
     constexpr int GT = GW * 32;
@@ -205,24 +208,24 @@ rms_fwd_stream(const FwdParams p, unsigned int *timeouts)
         const uint32_t st = stage0 + s * SM::kStageBytes;
         const uint32_t bar = bar0 + 8 * s;
         mbar_expect_tx(bar, SM::kStageBytes + p.extra_tx);
-        bulk_g2s(st, static_cast<const uint4 *>(p.x) + row * NV, SM::kRowBytes, bar);
+        bulk_g2s(st, static_cast<const uint4 *>(p.x) + row * (p.ldx / 8), SM::kRowBytes, bar);
         if constexpr (RES)
-            bulk_g2s(st + SM::kRowBytes, static_cast<const uint4 *>(p.r) + row * NV,
+            bulk_g2s(st + SM::kRowBytes, static_cast<const uint4 *>(p.r) + row * (p.ldr / 8),
                      SM::kRowBytes, bar);
     };
     // x (+ r) of pack j of the current stage, widened; with the residual,
-    // rounded to bf16 first (h as stored).
+    // rounded to the storage format first (h as stored).
     auto row_pack = [&](uint32_t st, int j, X &a) {
         if constexpr (RES) {
             X b;
-            as_pack<8>(lds128(st + (t + j * GT) * 16)).widen(a);
-            as_pack<8>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+            as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
+            as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
 #pragma unroll
             for (int i = 0; i < X::N; ++i)
                 a.v[i] = vadd(a.v[i], b.v[i]);
             P::narrow(a).widen(a);
         } else {
-            as_pack<8>(lds128(st + (t + j * GT) * 16)).widen(a);
+            as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
         }
     };
     if (t == 0) {
@@ -274,12 +277,12 @@ rms_fwd_stream(const FwdParams p, unsigned int *timeouts)
             X a, wv;
             row_pack(st, j, a);
             if constexpr (RES)
-                P::narrow(a).store(p.h, row * NV + t + j * GT);
+                P::narrow(a).store(p.h, row * (p.ldh / 8) + t + j * GT);
             wp[j].widen(wv);
 #pragma unroll
             for (int i = 0; i < X::N; ++i)
                 a.v[i] = vmul(vmul(a.v[i], r2), wv.v[i]);
-            P::narrow(a).store(p.y, row * NV + t + j * GT);
+            P::narrow(a).store(p.y, row * (p.ldy / 8) + t + j * GT);
         }
     }
     if (failed && t == 0) {
@@ -295,11 +298,11 @@ rms_fwd_stream(const FwdParams p, unsigned int *timeouts)
 }
 
 // ----------------------------------------------------------------- backward
-template <int GW, int V, int NG, int NS, bool DH, bool LOADR>
+template <typename T, int GW, int V, int NG, int NS, bool DH, bool LOADR>
 __global__ void __launch_bounds__(NG * GW * 32, 1)
 rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
 {
-    using P = Pack<bf16, 8>;
+    using P = Pack<T, 8>;
     using X = Vals<8>;
     using F = float2;
     constexpr int GT = GW * 32;
@@ -345,11 +348,11 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
         const uint32_t st = stage0 + s * SM::kStageBytes;
         const uint32_t bar = bar0 + 8 * s;
         mbar_expect_tx(bar, SM::kStageBytes + p.extra_tx);
-        bulk_g2s(st, static_cast<const uint4 *>(p.x) + row * NV, SM::kRowBytes, bar);
-        bulk_g2s(st + SM::kRowBytes, static_cast<const uint4 *>(p.dy) + row * NV,
+        bulk_g2s(st, static_cast<const uint4 *>(p.x) + row * (p.ldx / 8), SM::kRowBytes, bar);
+        bulk_g2s(st + SM::kRowBytes, static_cast<const uint4 *>(p.dy) + row * (p.lddy / 8),
                  SM::kRowBytes, bar);
         if constexpr (DH)
-            bulk_g2s(st + 2 * SM::kRowBytes, static_cast<const uint4 *>(p.dh) + row * NV,
+            bulk_g2s(st + 2 * SM::kRowBytes, static_cast<const uint4 *>(p.dh) + row * (p.lddh / 8),
                      SM::kRowBytes, bar);
     };
     if (t == 0) {
@@ -379,8 +382,8 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             X a, b, wv;
-            as_pack<8>(lds128(st + (t + j * GT) * 16)).widen(a);
-            as_pack<8>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+            as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
+            as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
             wp[j].widen(wv);
 #pragma unroll
             for (int i = 0; i < X::N; ++i) {
@@ -427,8 +430,8 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             X a, b, o, wv;
-            as_pack<8>(lds128(st + (t + j * GT) * 16)).widen(a);
-            as_pack<8>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+            as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
+            as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
             wp[j].widen(wv);
 #pragma unroll
             for (int i = 0; i < X::N; ++i) {
@@ -437,12 +440,12 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
             }
             if constexpr (DH) {
                 X d;
-                as_pack<8>(lds128(st + 2 * SM::kRowBytes + (t + j * GT) * 16)).widen(d);
+                as_pack<T>(lds128(st + 2 * SM::kRowBytes + (t + j * GT) * 16)).widen(d);
 #pragma unroll
                 for (int i = 0; i < X::N; ++i)
                     o.v[i] = vadd(o.v[i], d.v[i]);
             }
-            P::narrow(o).store(p.dx, row * NV + t + j * GT);
+            P::narrow(o).store(p.dx, row * (p.lddx / 8) + t + j * GT);
         }
     }
     if (failed && t == 0) {

@@ -1,6 +1,7 @@
-// stream_small.cuh -- streamed kernels for short rows (H = 8 * NVP bf16, NVP
-// packs of 16 bytes per row, NVP a power of two <= 32), e.g. the 128-wide
-// rows of Qwen3's QK-norm.
+// stream_small.cuh -- streamed kernels for short rows (H = 8 * NVP elements of
+// a 16-bit format, NVP packs of 16 bytes per row, NVP a power of two <= 32),
+// e.g. the 128-wide rows of Qwen3's QK-norm. Rows must be contiguous (row
+// stride H in every tensor): one bulk copy moves a block of rows.
 //
 // Same arithmetic as rows.cuh ([P1] "训推加速 Qwen3 实战：从“调包”到手写 Triton
 // Kernel（含 backward）" §4.1-4.2, §5.3-5.4). A row is NVP lanes, so a warp
@@ -38,11 +39,11 @@ struct SmallSmem {
 };
 
 // ------------------------------------------------------------------ forward
-template <int NVP, int RPT, int NW, int NS, bool RES>
+template <typename T, int NVP, int RPT, int NW, int NS, bool RES>
 __global__ void __launch_bounds__(NW * 32, 1)
 rms_fwd_stream_small(const FwdParams p, unsigned int *timeouts)
 {
-    using P = Pack<bf16, 8>;
+    using P = Pack<T, 8>;
     using X = Vals<8>;
     using F = float2;
     constexpr int NTEN = RES ? 2 : 1;
@@ -110,10 +111,10 @@ rms_fwd_stream_small(const FwdParams p, unsigned int *timeouts)
 #pragma unroll
         for (int j = 0; j < RPT; ++j) {
             const int rs = j * RW + sub;
-            as_pack<8>(lds128(st + rs * SM::kRowBytes + pk * 16)).widen(a[j]);
+            as_pack<T>(lds128(st + rs * SM::kRowBytes + pk * 16)).widen(a[j]);
             if constexpr (RES) {
                 X b;
-                as_pack<8>(lds128(st + SM::kTenBytes + rs * SM::kRowBytes + pk * 16)).widen(b);
+                as_pack<T>(lds128(st + SM::kTenBytes + rs * SM::kRowBytes + pk * 16)).widen(b);
 #pragma unroll
                 for (int i = 0; i < X::N; ++i)
                     a[j].v[i] = vadd(a[j].v[i], b.v[i]);
@@ -157,11 +158,11 @@ rms_fwd_stream_small(const FwdParams p, unsigned int *timeouts)
 }
 
 // ----------------------------------------------------------------- backward
-template <int NVP, int RPT, int NW, int NS, bool DH, bool LOADR>
+template <typename T, int NVP, int RPT, int NW, int NS, bool DH, bool LOADR>
 __global__ void __launch_bounds__(NW * 32, 1)
 rms_bwd_stream_small(const BwdParams p, unsigned int *timeouts)
 {
-    using P = Pack<bf16, 8>;
+    using P = Pack<T, 8>;
     using X = Vals<8>;
     using F = float2;
     constexpr int NTEN = DH ? 3 : 2;      // x, dy, [dh]
@@ -240,8 +241,8 @@ rms_bwd_stream_small(const BwdParams p, unsigned int *timeouts)
 #pragma unroll
         for (int j = 0; j < RPT; ++j) {
             const int rs_ = j * RW + sub;
-            xv[j] = as_pack<8>(lds128(st + rs_ * SM::kRowBytes + pk * 16));
-            dyv[j] = as_pack<8>(lds128(st + SM::kTenBytes + rs_ * SM::kRowBytes + pk * 16));
+            xv[j] = as_pack<T>(lds128(st + rs_ * SM::kRowBytes + pk * 16));
+            dyv[j] = as_pack<T>(lds128(st + SM::kTenBytes + rs_ * SM::kRowBytes + pk * 16));
             X a, b;
             xv[j].widen(a);
             dyv[j].widen(b);
@@ -260,7 +261,7 @@ rms_bwd_stream_small(const BwdParams p, unsigned int *timeouts)
         if constexpr (DH) {
 #pragma unroll
             for (int j = 0; j < RPT; ++j)
-                dhv[j] = as_pack<8>(lds128(st + 2 * SM::kTenBytes +
+                dhv[j] = as_pack<T>(lds128(st + 2 * SM::kTenBytes +
                                            (j * RW + sub) * SM::kRowBytes + pk * 16));
         }
         // every lane has its data in registers: release the stage

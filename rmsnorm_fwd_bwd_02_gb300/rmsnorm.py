@@ -1,9 +1,9 @@
 """Thin ctypes binding over librmsnorm.so (C ABI in include/rmsnorm.h).
 
 Same entry-point names as the C ABI. Argument marshalling only: tensors are
-checked (CUDA, contiguous, dtype, shape), outputs that the caller did not
-pass are allocated with torch, and raw device pointers plus the current torch
-CUDA stream are handed to the library. Every arithmetic step runs in the
+checked (CUDA, contiguous or row-strided, dtype, shape), outputs that the
+caller did not pass are allocated with torch, and raw device pointers, row
+strides and the current torch CUDA stream are handed to the library. Every arithmetic step runs in the
 CUDA kernels. If the library has not been built this module raises at load
 time; there is no fallback.
 """
@@ -15,8 +15,9 @@ import torch
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "librmsnorm.so")
 
-RMSNORM_F32, RMSNORM_BF16 = 0, 1
-DTYPES = {torch.float32: RMSNORM_F32, torch.bfloat16: RMSNORM_BF16}
+RMSNORM_F32, RMSNORM_BF16, RMSNORM_F16 = 0, 1, 2
+DTYPES = {torch.float32: RMSNORM_F32, torch.bfloat16: RMSNORM_BF16,
+          torch.float16: RMSNORM_F16}
 MAX_H = 16384
 PATH_AUTO, PATH_ROWS, PATH_SPLIT, PATH_SCALAR, PATH_STREAM = 0, 1, 2, 3, 4
 
@@ -42,6 +43,11 @@ SIGNATURES = {
     "rmsnorm_set_stream_test_fault": (None, [ctypes.c_uint, ctypes.c_uint]),
     "rmsnorm_bwd_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64,
                               _i64, _f, _int, _int, _vp]),
+    "rmsnorm_fwd_strided": (_int, [_vp, _i64, _vp, _i64, _vp, _vp, _i64, _vp,
+                                   _i64, _vp, _i64, _i64, _f, _int, _vp]),
+    "rmsnorm_bwd_strided": (_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp,
+                                   _vp, _i64, _vp, _vp, _sz, _i64, _i64, _f,
+                                   _int, _int, _vp]),
 }
 
 BWD_ACCUMULATE_DW = 1
@@ -101,6 +107,33 @@ def _rows(name, t, H, dtype=None):
     if t.shape[-1] != H:
         raise ValueError(f"{name} last dim must be {H}")
     return t.numel() // H if H else 0
+
+
+def _strided(name, t, H, dtype=None):
+    """(M, ld) of a 2-D [M, H] CUDA tensor with unit column stride; ld is its
+    row stride in elements (H for one row)."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2 or t.shape[1] != H:
+        raise ValueError(f"{name} must be 2-D [M, {H}]")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    M = t.shape[0]
+    if H > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit column stride")
+    ld = t.stride(0) if M > 1 else H
+    return M, ld
+
+
+def as_rows(t, H):
+    """t viewed as [M, H] rows without a copy when its strides allow it
+    (any row stride, unit column stride), else a contiguous copy."""
+    if t.shape[-1] == H and (H == 1 or t.stride(-1) == 1):
+        try:
+            return t.view(-1, H)
+        except RuntimeError:
+            pass
+    return t.contiguous().view(-1, H)
 
 
 def _dtype_code(t):
@@ -239,6 +272,64 @@ def rmsnorm_bwd_ex(dy, x, w, rstd=None, dh_out=None, dx=None, dw=None,
         _ptr(workspace), workspace.numel() * workspace.element_size(), M, H,
         float(eps), _dtype_code(x), BWD_ACCUMULATE_DW if accumulate_dw else 0,
         _stream(stream)), "rmsnorm_bwd_ex")
+    return dx, dw
+
+
+def rmsnorm_fwd_strided(x, w, y=None, r=None, h=None, rstd=None, eps=1e-6,
+                        want_rstd=True, stream=None):
+    """Forward on row-strided 2-D tensors (each with its own row stride).
+    Without r: returns (y, rstd); with r (residual variant): (h, y, rstd).
+    Outputs the caller does not pass are allocated dense."""
+    H = w.numel()
+    M, ldx = _strided("x", x, H)
+    _rows("w", w.view(-1), H, x.dtype)
+    if y is None:
+        y = torch.empty(M, H, device=x.device, dtype=x.dtype)
+    _, ldy = _strided("y", y, H, x.dtype)
+    ldr = ldh = H
+    if r is not None:
+        _, ldr = _strided("r", r, H, x.dtype)
+        if h is None:
+            h = torch.empty(M, H, device=x.device, dtype=x.dtype)
+        _, ldh = _strided("h", h, H, x.dtype)
+    elif h is not None:
+        raise ValueError("h is the residual variant's output: pass r too")
+    if rstd is None and want_rstd:
+        rstd = torch.empty(M, device=x.device, dtype=torch.float32)
+    _check(lib().rmsnorm_fwd_strided(
+        _ptr(x), ldx, _ptr(r), ldr, _ptr(w), _ptr(y), ldy, _ptr(h), ldh,
+        _ptr(rstd), M, H, float(eps), _dtype_code(x), _stream(stream)),
+        "rmsnorm_fwd_strided")
+    return (y, rstd) if r is None else (h, y, rstd)
+
+
+def rmsnorm_bwd_strided(dy, x, w, rstd=None, dh_out=None, dx=None, dw=None,
+                        workspace=None, eps=1e-6, accumulate_dw=False,
+                        stream=None):
+    """(dx, dw) of the plain (dh_out None) or residual backward on row-strided
+    2-D tensors; dx is allocated dense unless given."""
+    H = w.numel()
+    M, ldx = _strided("x", x, H)
+    _, lddy = _strided("dy", dy, H, x.dtype)
+    lddh = H
+    if dh_out is not None:
+        _, lddh = _strided("dh_out", dh_out, H, x.dtype)
+    if dx is None:
+        dx = torch.empty(M, H, device=x.device, dtype=x.dtype)
+    _, lddx = _strided("dx", dx, H, x.dtype)
+    if dw is None:
+        if accumulate_dw:
+            raise ValueError("accumulate_dw needs the dw buffer to add into")
+        dw = torch.empty(H, device=x.device, dtype=torch.float32)
+    need = bwd_workspace_bytes(M, H, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=x.device, dtype=torch.uint8)
+    _check(lib().rmsnorm_bwd_strided(
+        _ptr(dy), lddy, _ptr(dh_out), lddh, _ptr(x), ldx, _ptr(w), _ptr(rstd),
+        _ptr(dx), lddx, _ptr(dw), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), M, H, float(eps),
+        _dtype_code(x), BWD_ACCUMULATE_DW if accumulate_dw else 0,
+        _stream(stream)), "rmsnorm_bwd_strided")
     return dx, dw
 
 

@@ -33,6 +33,7 @@ class Workload:
     outlier_scale: float = 1.0
     residual: bool = False         # also draw r (residual) and dh_out
     backward: bool = True          # the workload runs the backward too
+    ld: int = 0                    # row stride of every [M, H] tensor (0: H)
     note: str = ""
 
     def with_rows(self, M: int) -> "Workload":
@@ -41,6 +42,10 @@ class Workload:
     @property
     def elem_bytes(self) -> int:
         return torch.empty(0, dtype=self.dtype).element_size()
+
+    @property
+    def row_stride(self) -> int:
+        return self.ld or self.H
 
 
 WORKLOADS = {
@@ -67,6 +72,13 @@ WORKLOADS = {
                  dy_std=1e-2, outlier_frac=1e-3, outlier_scale=100.0,
                  residual=True,
                  note="fused residual-add + RMSNorm at Qwen3-14B width"),
+        Workload("qwen3-8b-train-fp16", 32768, 4096, torch.float16, seed=2,
+                 dy_std=1e-2,
+                 note="the Qwen3-8B training shape with fp16 storage"),
+        Workload("qwen3-8b-train-strided", 32768, 4096, torch.bfloat16, seed=2,
+                 dy_std=1e-2, ld=4608,
+                 note="the Qwen3-8B training shape, every [M, H] tensor the "
+                      "first 4096 columns of an [M, 4608] buffer"),
     ]
 }
 
@@ -113,6 +125,17 @@ def make_inputs(w: Workload) -> dict:
         out["r"] = r
         out["dh"] = _normal(shape, base + 5, std=w.dy_std)
     return {k: v.to(w.dtype).contiguous() for k, v in out.items()}
+
+
+def in_strided(t, ld: int, fill=float("nan")):
+    """A copy of the [M, H] tensor t (on t's device) as the first H columns
+    of a new [M, ld] buffer whose other columns hold ``fill``; returns the
+    [M, H] view (row stride ld)."""
+    M, H = t.shape
+    buf = torch.full((M, ld), fill, dtype=t.dtype, device=t.device)
+    view = buf[:, :H]
+    view.copy_(t)
+    return view
 
 
 def random_rows(M: int, k: int, seed: int = 0):

@@ -14,7 +14,8 @@ HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
 
 OK, NULLPTR, BAD_SHAPE, BAD_DTYPE, BAD_EPS, MISALIGNED, WORKSPACE, \
     UNSUPPORTED, CUDA, ALIAS = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
+BAD_STRIDE = -12
 NAN = float("nan")
 
 
@@ -49,7 +50,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings(lib):
     for code in (OK, NULLPTR, BAD_SHAPE, BAD_DTYPE, BAD_EPS, MISALIGNED,
-                 WORKSPACE, UNSUPPORTED, CUDA, ALIAS):
+                 WORKSPACE, UNSUPPORTED, CUDA, ALIAS, BAD_STRIDE):
         s = lib.rmsnorm_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.rmsnorm_status_string(12345).decode() == "unknown status"
@@ -87,6 +88,82 @@ def test_fwd_argument_checks(lib):
     assert fwd(lib, rstd=C + 4) == ALIAS
     # nothing to do for M == 0, even with NULL pointers
     assert fwd(lib, x=None, w=None, y=None, rstd=None, M=0) == OK
+
+
+def test_fp16_is_a_dtype(lib):
+    # fp16 passes the dtype check and is checked as a 2-byte type
+    assert fwd(lib, x=A + 1, dtype=F16) == MISALIGNED
+    assert fwd(lib, dtype=3) == BAD_DTYPE
+    assert fwd(lib, x=None, w=None, y=None, rstd=None, M=0, dtype=F16) == OK
+
+
+def no_gpu():
+    import torch
+    return not torch.cuda.is_available()
+
+
+def fwd_s(lib, x=A, ldx=256, r=None, ldr=256, w=B, y=C, ldy=256, h=None,
+          ldh=256, rstd=D, M=4, H=128, dtype=BF16):
+    return lib.rmsnorm_fwd_strided(x, ldx, r, ldr, w, y, ldy, h, ldh, rstd, M,
+                                   H, 1e-6, dtype, None)
+
+
+def test_fwd_strided_argument_checks(lib):
+    assert fwd_s(lib, ldx=127) == BAD_STRIDE
+    assert fwd_s(lib, ldy=0) == BAD_STRIDE
+    assert fwd_s(lib, ldx=2 ** 31) == BAD_STRIDE
+    assert fwd_s(lib, M=2 ** 40, ldx=2 ** 30) == BAD_STRIDE   # past 2^63 bytes
+    assert fwd_s(lib, r=0x7f0400000000) == NULLPTR            # r without h
+    assert fwd_s(lib, h=0x7f0400000000) == NULLPTR            # h without r
+    # y at the same start as x but another stride: not the same tensor
+    assert fwd_s(lib, y=A, ldy=128) == ALIAS
+    # y's columns start 127 elements into x's rows: they meet x's window
+    assert fwd_s(lib, y=A + 254) == ALIAS
+    # rstd in the gap between x's rows still counts as inside x's range
+    assert fwd_s(lib, rstd=A + 256) == ALIAS
+
+
+@pytest.mark.skipif("not no_gpu()")
+def test_fwd_strided_allowed_layouts_reach_the_device(lib):
+    """Layouts the alias rule allows pass every host check; without a GPU
+    the first CUDA call then fails (status CUDA), which shows it."""
+    # y in the other half of x's 256-wide rows: disjoint windows
+    assert fwd_s(lib, y=A + 256) == CUDA
+    # in place: same start and stride
+    assert fwd_s(lib, y=A) == CUDA
+    # one row: the stride does not matter
+    assert fwd_s(lib, y=A, ldy=128, M=1) == CUDA
+    # residual, h in place of r, everything interleaved in one buffer
+    assert fwd_s(lib, x=A, r=A + 256, h=A + 256, y=A + 512, ldx=384, ldr=384,
+                 ldh=384, ldy=384) == CUDA
+    assert fwd_s(lib, dtype=F16) == CUDA
+
+
+def bwd_s(lib, dy=A, lddy=256, dh=None, lddh=256, x=B, ldx=256, w=C, rstd=D,
+          dx=0x7f0400000000, lddx=256, dw=0x7f0500000000, ws=0x7f0600000000,
+          wsb=1 << 24, M=4, H=128, flags=0, dtype=BF16):
+    return lib.rmsnorm_bwd_strided(dy, lddy, dh, lddh, x, ldx, w, rstd, dx,
+                                   lddx, dw, ws, wsb, M, H, 1e-6, dtype,
+                                   flags, None)
+
+
+def test_bwd_strided_argument_checks(lib):
+    assert bwd_s(lib, lddy=100) == BAD_STRIDE
+    assert bwd_s(lib, ldx=100) == BAD_STRIDE
+    assert bwd_s(lib, lddx=2 ** 31) == BAD_STRIDE
+    assert bwd_s(lib, dh=0x7f0700000000, lddh=1) == BAD_STRIDE
+    assert bwd_s(lib, flags=4) == -11
+    assert bwd_s(lib, dx=A + 2) == ALIAS          # dx partially over dy
+    assert bwd_s(lib, dx=B + 2) == ALIAS          # dx over x's columns
+    assert bwd_s(lib, dw=B + 256) == ALIAS        # dw between x's rows (in its range)
+
+
+@pytest.mark.skipif("not no_gpu()")
+def test_bwd_strided_allowed_layouts_reach_the_device(lib):
+    assert bwd_s(lib, dx=A) == CUDA               # in place over dy
+    assert bwd_s(lib, dx=A + 256) == CUDA         # other half of dy's rows
+    assert bwd_s(lib, dx=B + 256) == CUDA         # other half of x's rows
+    assert bwd_s(lib, dtype=F16) == CUDA
 
 
 def test_residual_fwd_argument_checks(lib):

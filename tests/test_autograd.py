@@ -143,3 +143,53 @@ def test_training_step_in_a_cuda_graph():
     torch.cuda.synchronize()
     assert torch.equal(x.grad, ref_dx)
     assert torch.equal(mod.weight.grad, ref_dw)
+
+
+@pytest.mark.gpu
+def test_fp16_module_grads_match_oracle(orc):
+    M, H = 515, 4096
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(M, H, generator=g).to(torch.float16)
+    dy = (torch.randn(M, H, generator=g) * 1e-2).to(torch.float16)
+    w = (1 + 0.1 * torch.randn(H, generator=g)).to(torch.float16)
+    mod = A.RMSNorm(H, device=DEV, dtype=torch.float16)
+    with torch.no_grad():
+        mod.weight.copy_(w.to(DEV))
+    xd = x.to(DEV).requires_grad_()
+    y = mod(xd)
+    assert y.dtype == torch.float16
+    y.backward(dy.to(DEV))
+    torch.cuda.synchronize()
+    oy, _ = orc.fwd(x, w, 1e-6)
+    odx, odw, tdx, tdw = orc.bwd(dy, x, w, 1e-6, want_terms=True)
+    check_rows("f16 module y", y.detach(), oy, torch.float16)
+    check_rows("f16 module dx", xd.grad, odx, torch.float16, tdx)
+    got = mod.weight.grad.double().cpu()
+    assert bool(((got - odw).abs() <= 1e-3 * tdw + 2.0 ** -10 * odw.abs()
+                 + 2.0 ** -24).all())
+
+
+@pytest.mark.gpu
+def test_column_window_input_is_not_copied():
+    """x = the first H columns of a (B, T, ld) buffer: the rows go to the
+    kernels in place (a view with row stride ld), with the same bits as a
+    contiguous copy."""
+    from rmsnorm_fwd_bwd_02_gb300 import rmsnorm as rn
+    B, T, H, ld = 3, 70, 4096, 4096 + 512
+    buf = torch.randn(B, T, ld, device=DEV, dtype=torch.bfloat16)
+    x = buf[:, :, :H]
+    rows = rn.as_rows(x, H)
+    assert rows.data_ptr() == x.data_ptr() and rows.stride() == (ld, 1)
+    w = (1 + 0.1 * torch.randn(H, device=DEV)).to(torch.bfloat16).requires_grad_()
+    xr = x.detach().requires_grad_()
+    y = A.rms_norm(xr, w)
+    dy = torch.randn(B, T, ld, device=DEV, dtype=torch.bfloat16)[:, :, :H]
+    y.backward(dy)
+    wc = w.detach().clone().requires_grad_()
+    xc = x.detach().contiguous().requires_grad_()
+    yc = A.rms_norm(xc, wc)
+    yc.backward(dy.contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(y, yc)
+    assert torch.equal(xr.grad, xc.grad)
+    assert torch.equal(w.grad, wc.grad)

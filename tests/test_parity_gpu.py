@@ -105,6 +105,7 @@ def compare_all(name, wl, got, o):
 REDUCED = {
     "tiny-fp32": 64, "decode-m1": 1, "decode-m8": 8, "decode-m64": 64,
     "qwen3-8b-train": 1037, "qwen3-qknorm": 4099, "residual-14b": 517,
+    "qwen3-8b-train-fp16": 1037,
 }
 
 
@@ -123,7 +124,8 @@ def test_workload_reduced_all_elements(orc, name):
         compare_all(name + " dh=None", wl, got2, o2)
 
 
-@pytest.mark.parametrize("name", ["qwen3-8b-train", "qwen3-qknorm", "residual-14b"])
+@pytest.mark.parametrize("name", ["qwen3-8b-train", "qwen3-qknorm", "residual-14b",
+                                  "qwen3-8b-train-fp16"])
 def test_workload_full_size_sampled(orc, name):
     wl = W.WORKLOADS[name]
     inp = W.make_inputs(wl)
@@ -173,7 +175,8 @@ EDGE_H = [1, 2, 7, 8, 9, 64, 127, 128, 129, 512, 895, 896, 1000, 1024, 2048,
           4095, 4096, 4104, 5120, 8192, 16384]
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, torch.float16],
+                         ids=["bf16", "f32", "f16"])
 @pytest.mark.parametrize("H", EDGE_H)
 @pytest.mark.parametrize("M", [1, 67, 300])
 def test_edge_shapes(orc, M, H, dtype):
@@ -187,7 +190,8 @@ def test_edge_shapes(orc, M, H, dtype):
         compare_all(f"M={M} H={H} {dtype} res={residual}", wl, got, o)
 
 
-STREAM_H = (128, 4096, 5120)     # bf16 feature counts with a streamed layout
+STREAM_H = (128, 4096, 5120)     # 16-bit feature counts with a streamed layout
+HALF = (torch.bfloat16, torch.float16)
 
 
 @pytest.mark.parametrize("path", [rn.PATH_ROWS, rn.PATH_SPLIT, rn.PATH_SCALAR,
@@ -195,7 +199,7 @@ STREAM_H = (128, 4096, 5120)     # bf16 feature counts with a streamed layout
 @pytest.mark.parametrize("H", [1, 7, 128, 896, 4096, 5120, 16384])
 def test_forced_paths_agree_with_oracle(orc, path, H):
     M = 5
-    for dtype in (torch.bfloat16, torch.float32):
+    for dtype in (torch.bfloat16, torch.float32, torch.float16):
         for residual in (False, True):
             wl = W.Workload(f"forced-{path}", M, H, dtype, residual=residual)
             inp = synth(M, H, dtype, seed=3, residual=residual)
@@ -206,7 +210,7 @@ def test_forced_paths_agree_with_oracle(orc, path, H):
             vec_ok = (H * inp["x"].element_size()) % 16 == 0
             if path == rn.PATH_SCALAR or not vec_ok:
                 assert used == rn.PATH_SCALAR
-            elif path == rn.PATH_STREAM and dtype == torch.bfloat16 and H in STREAM_H:
+            elif path == rn.PATH_STREAM and dtype in HALF and H in STREAM_H:
                 assert used == rn.PATH_STREAM
             else:
                 assert used == rn.PATH_ROWS   # the backward reports last
@@ -272,6 +276,50 @@ def test_stream_path_full_size_sampled(orc, name):
         check_bits(f"stream {name} {k} run-to-run", again[k], got[k])
 
 
+@pytest.mark.parametrize("H,M", [(128, 1), (128, 33), (128, 4099), (4096, 7),
+                                 (4096, 1037), (5120, 3), (5120, 517)])
+def test_stream_path_fp16(orc, H, M):
+    """The streamed kernels with fp16 storage: plain and residual, dh_out
+    given or not, rstd given or recomputed, ragged row counts."""
+    for residual in (False, True):
+        wl = W.Workload("stream-f16", M, H, torch.float16, residual=residual,
+                        dy_std=1e-2)
+        inp = synth(M, H, torch.float16, seed=M + H, residual=residual)
+        g = to_dev(inp)
+        for dh in ((True, False) if residual else (True,)):
+            for with_rstd in (True, False):
+                o = oracle_all(orc, wl, inp, dh=dh)
+                with forced_path(rn.PATH_STREAM):
+                    got = gpu_fwd_bwd(wl, g, dh=dh, with_rstd=with_rstd)
+                    assert rn.last_path() == rn.PATH_STREAM
+                compare_all(f"stream f16 H={H} M={M} res={residual} dh={dh} "
+                            f"rstd={with_rstd}", wl, got, o)
+
+
+def test_fp16_overflow_and_subnormal_results(orc):
+    """fp16 results beyond 65504 are infinite with the right sign; tiny
+    results land on the subnormal grid as the one-step rounding puts them."""
+    H = 4
+    # a spike row: x r = +-sqrt(H) = +-2 at the spike, y = 2 w there
+    x = torch.tensor([[3.0, 0, 0, 0], [0, -5.0, 0, 0]], dtype=torch.float16)
+    w = torch.tensor([60000.0, 40000.0, 1.0, 1.0], dtype=torch.float16)
+    y, rstd = rn.rmsnorm_fwd(x.to(DEV), w.to(DEV), eps=0.0)
+    torch.cuda.synchronize()
+    oy, _ = orc.fwd(x, w, 0.0)
+    yc = y.cpu().double()
+    assert yc[0, 0] == float("inf") and oy[0, 0] > 65520
+    assert yc[1, 1] == float("-inf") and oy[1, 1] < -65520
+    # tiny weights: results in the fp16 subnormal range
+    M, H = 300, 1024
+    inp = synth(M, H, torch.float16, seed=9)
+    inp["w"] = (inp["w"].float() * 1e-6).to(torch.float16)
+    wl = W.Workload("f16-tiny", M, H, torch.float16)
+    o = oracle_all(orc, wl, inp)
+    got = gpu_fwd_bwd(wl, to_dev(inp))
+    assert bool((o["y"].abs() < 2.0 ** -14).any())
+    compare_all("f16 subnormal y", wl, got, o)
+
+
 def test_auto_path_choice():
     x = torch.randn(64, 896, device=DEV, dtype=torch.bfloat16)
     w = torch.ones(896, device=DEV, dtype=torch.bfloat16)
@@ -283,14 +331,16 @@ def test_auto_path_choice():
     x = torch.randn(65, 895, device=DEV, dtype=torch.bfloat16)
     rn.rmsnorm_fwd(x, torch.ones(895, device=DEV, dtype=torch.bfloat16))
     assert rn.last_path() == rn.PATH_SCALAR
-    # bf16 rows of 4096 / 5120: the forward row-wise, the backward streamed
-    for H in STREAM_H:
-        x = torch.randn(100, H, device=DEV, dtype=torch.bfloat16)
-        w = torch.ones(H, device=DEV, dtype=torch.bfloat16)
-        _, rstd = rn.rmsnorm_fwd(x, w)
-        assert rn.last_path() == rn.PATH_ROWS
-        rn.rmsnorm_bwd(x, x, w, rstd)
-        assert rn.last_path() == rn.PATH_STREAM
+    # 16-bit rows of 128 / 4096 / 5120: the forward row-wise, the backward
+    # streamed
+    for dt in HALF:
+        for H in STREAM_H:
+            x = torch.randn(100, H, device=DEV, dtype=dt)
+            w = torch.ones(H, device=DEV, dtype=dt)
+            _, rstd = rn.rmsnorm_fwd(x, w)
+            assert rn.last_path() == rn.PATH_ROWS
+            rn.rmsnorm_bwd(x, x, w, rstd)
+            assert rn.last_path() == rn.PATH_STREAM
     torch.cuda.synchronize()
 
 
@@ -298,7 +348,7 @@ def test_misaligned_rows_take_scalar_path(orc):
     """Row pointers offset by one element (not 16-byte aligned); M > 64 so
     the row-wise kernels run (M <= 64 takes the split-row kernel)."""
     M, H = 337, 4096
-    for dtype in (torch.bfloat16, torch.float32):
+    for dtype in (torch.bfloat16, torch.float32, torch.float16):
         inp = synth(M, H, dtype, seed=5)
         o = oracle_all(orc, W.Workload("mis", M, H, dtype), inp)
         bx = torch.empty(M * H + 1, device=DEV, dtype=dtype)

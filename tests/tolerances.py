@@ -16,6 +16,13 @@ result is within 2^-8 |o| of the oracle plus the fp32 error of its terms,
 bounded generously by 1e-3 T (y has a single term, T = |o|). These catch
 errors the contract's 1e-2 absolute floor would hide when the values are
 small (dy ~ N(0, 1e-2) makes dx ~ 1e-2).
+
+fp16 outputs (no contract figure is fixed for fp16; derived the same way):
+one rounding to binary16 costs at most half an ulp, 2^-11 relative for
+normal results and 2^-25 absolute below 2^-14 (subnormal spacing 2^-24), on
+top of the fp32 error of the terms. Contract: 2^-10 |o| + 1e-3 T + 2^-24;
+strict: 2^-10 |o| + 1e-4 T + 2^-25. Results beyond 65504 must be infinite
+with the oracle's sign (checked separately where a test provokes them).
 """
 import torch
 
@@ -47,6 +54,11 @@ def check_rows(name, got, want, dtype, terms=None):
         _report(name + " (contract)", err, 1e-2 + 1.6e-2 * want.abs(), g, want)
         _report(name + " (strict)", err, 2.0 ** -8 * want.abs() + 1e-3 * T + 1e-30,
                 g, want)
+    elif dtype == torch.float16:
+        _report(name + " (contract)", err,
+                2.0 ** -10 * want.abs() + 1e-3 * T + 2.0 ** -24, g, want)
+        _report(name + " (strict)", err,
+                2.0 ** -10 * want.abs() + 1e-4 * T + 2.0 ** -25, g, want)
     else:
         _report(name + " (contract)", err, 1e-3 * T + 1e-30, g, want)
         _report(name + " (strict)", err, 2e-5 * T + 1e-30, g, want)
@@ -69,7 +81,7 @@ def check_dw(name, got, want, tdw):
 def check_bits(name, got, want):
     a = got.detach().cpu().contiguous()
     b = want.detach().cpu().contiguous()
-    if a.dtype == torch.bfloat16:
+    if a.dtype in (torch.bfloat16, torch.float16):
         a, b = a.view(torch.int16), b.view(torch.int16)
     elif a.dtype == torch.float32:
         a, b = a.view(torch.int32), b.view(torch.int32)
