@@ -659,22 +659,18 @@ def run_e2e(rn, wl, src, dev, ws, args, dist):
             "pipeline": f"{chunks} row chunks on 3 streams (copy in / compute / copy out)"}
 
 
-# Sources of the kernels whose DRAM traffic profiles/traffic.json records;
-# a change to any of them makes the recorded figure stale (reported null).
-TRAFFIC_SOURCES = {
-    "bwd": ["stream.cuh", "stream.cu", "reduce.cuh", "common.cuh", "params.h",
-            "rows.cuh", "rows_bf16_shaped.cu"],
-    "fwd": ["rows.cuh", "rows_bf16_shaped.cu", "common.cuh", "params.h"],
-}
-
-
-def kernel_src_hash(which):
+def kernel_src_hash(which=None):
+    """Hash of every source under csrc/ (kernels, their headers and the
+    dispatch that picks them): the DRAM traffic recorded in
+    profiles/traffic.json holds only while it is unchanged."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "rmsnorm_fwd_bwd_02_gb300", "csrc")
-    for f in TRAFFIC_SOURCES[which]:
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(fh.read())
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 
