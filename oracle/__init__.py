@@ -43,6 +43,10 @@ def _declare(lib):
     lib.oracle_bf16_to_double.restype = _dbl
     lib.oracle_bf16_from_double.argtypes = [_dbl]
     lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+    lib.oracle_rmsnorm_gemv.argtypes = [_i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                        ctypes.c_int, _dbl, _vp, _vp, _vp, _vp,
+                                        _vp]
+    lib.oracle_rmsnorm_gemv.restype = ctypes.c_int
     lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_f16_to_double.restype = _dbl
     lib.oracle_f16_from_double.argtypes = [_dbl]
@@ -153,6 +157,32 @@ class Oracle:
         if want_terms:
             return dx, dw, tdx, tdw
         return dx, dw
+
+    # -- norm followed by the projection GEMV (decode chain)
+    def rmsnorm_gemv(self, x, w, A, eps, r=None):
+        """dict with out [M,N] (float64, unrounded), y (the stored norm
+        output, input dtype), h (residual variant, else None), rstd and the
+        error scale tout [M,N]."""
+        M, H = x.shape
+        N = A.shape[0]
+        code = _CODES[x.dtype]
+        _check_rows("x", x, x.dtype, M, H)
+        _check_rows("w", w, x.dtype, 1, H)
+        _check_rows("A", A, x.dtype, N, H)
+        if r is not None:
+            _check_rows("r", r, x.dtype, M, H)
+        h = torch.empty(M, H, dtype=x.dtype) if r is not None else None
+        y = torch.empty(M, H, dtype=x.dtype)
+        out = torch.empty(M, N, dtype=torch.float64)
+        rstd = torch.empty(M, dtype=torch.float64)
+        tout = torch.empty(M, N, dtype=torch.float64)
+        st = self.lib.oracle_rmsnorm_gemv(M, H, N, _ptr(x), _ptr(r), _ptr(w),
+                                          _ptr(A), code, float(eps), _ptr(h),
+                                          _ptr(y), _ptr(out), _ptr(rstd),
+                                          _ptr(tout))
+        if st != 0:
+            raise MemoryError("oracle_rmsnorm_gemv: out of memory")
+        return {"out": out, "y": y, "h": h, "rstd": rstd, "tout": tout}
 
 
 _default = None

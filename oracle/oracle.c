@@ -29,6 +29,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORACLE_F32 0
@@ -302,4 +303,70 @@ void oracle_residual_bwd(int64_t M, int64_t H, const void *dy,
                 if (tdx)
                     tdx[i * H + j] += fabs(g);
             }
+}
+
+/* ------------------------------------------------ norm, then projection */
+
+/* v rounded to the given storage format (nearest, ties to even). */
+static double round_to(int dtype, double v)
+{
+    switch (dtype) {
+    case ORACLE_F32:
+        return (double)(float)v;
+    case ORACLE_BF16:
+        return oracle_bf16_to_double(oracle_bf16_from_double(v));
+    case ORACLE_F16:
+        return oracle_f16_to_double(oracle_f16_from_double(v));
+    default:
+        return v;
+    }
+}
+
+/*
+ * The decode chain of [P2]: the norm (optionally after the residual add)
+ * feeds the projection GEMVs -- q/k/v_proj, gate/up_proj ([P2 §2.1] ops
+ * 3-5, 10-13; §3.1: a [1, 896] hidden state against the [1024, 896] q_proj
+ * weight) -- and [P2 §6] names fusing these steps as the next optimisation.
+ * The fused result is defined as the chain's: the norm's output y is stored
+ * in the dtype (the separate rms_norm kernel writes it, the GEMV reads it
+ * back), then, for a row-major weight A of N rows of H (a linear layer's
+ * weight),
+ *   out_in = sum_k y_ik A_nk          in double, unrounded.
+ * res and h: the residual variant (both NULL for the plain norm), h as in
+ * oracle_residual_fwd. y_store (may be NULL) receives the stored y; rstd
+ * (may be NULL) as for the forward; tout (may be NULL) receives the error
+ * scale sum_k |y_ik A_nk|. Returns 0, or -1 if scratch memory is short.
+ */
+int oracle_rmsnorm_gemv(int64_t M, int64_t H, int64_t N, const void *x,
+                        const void *res, const void *w, const void *A,
+                        int dtype, double eps, void *h, void *y_store,
+                        double *out, double *rstd, double *tout)
+{
+    double *y = (double *)malloc((size_t)(M * H > 0 ? M * H : 1) * sizeof(double));
+    if (!y)
+        return -1;
+    if (res)
+        oracle_residual_fwd(M, H, x, res, w, dtype, eps, h, y, rstd);
+    else
+        oracle_rmsnorm_fwd(M, H, x, w, dtype, eps, y, rstd);
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < H; ++j) {
+            y[i * H + j] = round_to(dtype, y[i * H + j]);
+            if (y_store)
+                (void)store_rounded(y_store, dtype, i * H + j, y[i * H + j]);
+        }
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < H; ++k) {
+                double term = y[i * H + k] * dec(A, dtype, n * H + k);
+                acc += term;
+                mag += fabs(term);
+            }
+            out[i * N + n] = acc;
+            if (tout)
+                tout[i * N + n] = mag;
+        }
+    free(y);
+    return 0;
 }

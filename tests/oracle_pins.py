@@ -512,6 +512,103 @@ def pin_residual_dh_none_is_zero(o):
     _close(a[0], c[0], 0.0, what="resid bwd = bwd on h")
 
 
+# ------------------------------------------- norm, then projection (decode)
+
+def _round_like(o, v, dtype):
+    """v (float64 tensor) rounded element by element to bf16/fp16 with the
+    oracle's pinned rounding, returned as float64."""
+    f = o.bf16_from_double if dtype == torch.bfloat16 else o.f16_from_double
+    d = o.bf16_to_double if dtype == torch.bfloat16 else o.f16_to_double
+    return torch.tensor([d(f(x)) for x in v.flatten().tolist()],
+                        dtype=F64).reshape(v.shape)
+
+
+def pin_gemv_closed_form(o):
+    """Rows x_i = a_i s_i with s_i in {-1, +1}^H and eps = 0 have rms a_i, so
+    y = w s exactly; with small-integer w and A the output is the integer
+    product (w s) A^T, computed here with torch int64 ([P2 §3.1] shapes
+    shrunk: M = 3 rows, N = 5 outputs, H = 32)."""
+    g = _gen(21)
+    M, H, N = 3, 32, 5
+    s = torch.randint(0, 2, (M, H), generator=g) * 2 - 1
+    a = torch.tensor([2.0, 0.5, 8.0])
+    x = (a[:, None] * s).to(torch.bfloat16)
+    wi = torch.randint(-4, 5, (H,), generator=g)
+    Ai = torch.randint(-3, 4, (N, H), generator=g)
+    d = o.rmsnorm_gemv(x, wi.to(torch.bfloat16), Ai.to(torch.bfloat16), 0.0)
+    want = ((wi[None, :] * s) @ Ai.T).to(F64)
+    _close(d["out"], want, 0.0, what="gemv closed form")
+    _close(d["y"].double(), (wi[None, :] * s).to(F64), 0.0, what="gemv y")
+    _close(d["rstd"], 1.0 / a.double(), 1e-15, what="gemv rstd")
+
+
+def pin_gemv_vs_library(o):
+    """out = round(y) A^T with y the (pinned) forward's output rounded by the
+    (pinned) rounding and the product taken by torch in float64; tout =
+    |round(y)| |A|^T; the stored y is that rounding; for bf16 and fp16."""
+    g = _gen(22)
+    M, H, N = 4, 48, 7
+    for dt in (torch.bfloat16, torch.float16):
+        x = (torch.randn(M, H, generator=g) * 3).to(dt)
+        w = (1.0 + 0.1 * torch.randn(H, generator=g)).to(dt)
+        A = (torch.randn(N, H, generator=g) * 0.05).to(dt)
+        d = o.rmsnorm_gemv(x, w, A, 1e-6)
+        y, _ = o.fwd(x, w, 1e-6)
+        yq = _round_like(o, y, dt)
+        _close(d["y"].double(), yq, 0.0, what=f"gemv stored y {dt}")
+        want = yq @ A.double().T
+        mag = yq.abs() @ A.double().abs().T
+        _close(d["out"], want, 1e-12, 1e-300, what=f"gemv out {dt}")
+        _close(d["tout"], mag, 1e-12, what=f"gemv tout {dt}")
+
+
+def pin_gemv_identity_weight(o):
+    """With A = I (N = H) the output is the stored y itself."""
+    g = _gen(23)
+    H = 40
+    x = torch.randn(3, H, generator=g).to(torch.float16)
+    w = (1.0 + 0.1 * torch.randn(H, generator=g)).to(torch.float16)
+    d = o.rmsnorm_gemv(x, w, torch.eye(H).to(torch.float16), 1e-6)
+    _close(d["out"], d["y"].double(), 0.0, what="gemv identity")
+    y, _ = o.fwd(x, w, 1e-6)
+    _close(d["out"], _round_like(o, y, torch.float16), 0.0,
+           what="gemv identity = rounded forward")
+
+
+def pin_gemv_residual_composes(o):
+    """The residual variant writes the residual forward's h and projects
+    the norm of that stored h: the same as the plain variant applied to h."""
+    g = _gen(24)
+    M, H, N = 3, 64, 6
+    x = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    r = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    w = (1.0 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    A = torch.randn(N, H, generator=g).to(torch.bfloat16)
+    d = o.rmsnorm_gemv(x, w, A, 1e-6, r=r)
+    h, _, _ = o.residual_fwd(x, r, w, 1e-6)
+    assert torch.equal(d["h"].view(torch.int16), h.view(torch.int16)), "gemv h"
+    e = o.rmsnorm_gemv(h, w, A, 1e-6)
+    _close(d["out"], e["out"], 0.0, what="gemv residual out")
+    _close(d["rstd"], e["rstd"], 0.0, what="gemv residual rstd")
+
+
+def pin_gemv_permutations(o):
+    """Permuting the rows of A permutes the output columns the same way;
+    rows of x are independent."""
+    g = _gen(25)
+    M, H, N = 4, 24, 9
+    x = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    w = (1.0 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    A = torch.randn(N, H, generator=g).to(torch.bfloat16)
+    d = o.rmsnorm_gemv(x, w, A, 1e-6)
+    p = torch.randperm(N, generator=g)
+    e = o.rmsnorm_gemv(x, w, A[p].contiguous(), 1e-6)
+    _close(e["out"], d["out"][:, p], 0.0, what="gemv column permutation")
+    q = torch.randperm(M, generator=g)
+    f = o.rmsnorm_gemv(x[q].contiguous(), w, A, 1e-6)
+    _close(f["out"], d["out"][q], 0.0, what="gemv row permutation")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

@@ -74,6 +74,16 @@ MUTANTS = [
      "v = ldexp((double)frac, -25);"),
     ("f16_decode_as_bf16", "return oracle_f16_to_double(((const uint16_t *)p)[i]);",
      "return oracle_bf16_to_double(((const uint16_t *)p)[i]);"),
+    ("gemv_unrounded_y", "            y[i * H + j] = round_to(dtype, y[i * H + j]);\n", ""),
+    ("gemv_A_transposed", "dec(A, dtype, n * H + k)", "dec(A, dtype, k * N + n)"),
+    ("gemv_x_not_h", "oracle_residual_fwd(M, H, x, res, w, dtype, eps, h, y, rstd);",
+     "oracle_rmsnorm_fwd(M, H, x, w, dtype, eps, y, rstd);"),
+    ("gemv_tout_signed", "mag += fabs(term);", "mag += term;"),
+    ("gemv_last_k_dropped", "for (int64_t k = 0; k < H; ++k) {\n                double term",
+     "for (int64_t k = 0; k < H - 1; ++k) {\n                double term"),
+    ("gemv_f16_rounded_as_bf16",
+     "return oracle_f16_to_double(oracle_f16_from_double(v));",
+     "return oracle_bf16_to_double(oracle_bf16_from_double(v));"),
     ("resid_subtract",
      "double s = dec(x, dtype, i * H + j) + dec(res, dtype, i * H + j);",
      "double s = dec(x, dtype, i * H + j) - dec(res, dtype, i * H + j);"),
