@@ -48,6 +48,11 @@ def step_bytes(wl):
     from x; the workspace is overhead)."""
     es = wl.elem_bytes
     MH, H, M = wl.M * wl.H, wl.H, wl.M
+    if wl.N:
+        # norm fused with the projection: x (r), w and A in; out (and h) out
+        ins = MH * es * (2 if wl.residual else 1) + H * es + wl.N * H * es
+        outs = M * wl.N * es + (MH * es if wl.residual else 0)
+        return ins + outs, 0
     if wl.residual:
         fwd = 4 * MH * es + H * es + 4 * M          # x, r in; h, y out; rstd
         bwd = 4 * MH * es + H * es + 4 * H          # dy, h, dh in; dx out; dw
@@ -87,6 +92,9 @@ def buffer_sets(wl):
     (decode-sized steps stay launch-bound)."""
     if streams_from_hbm(wl):
         return 3
+    if wl.N:         # the projection weight dominates: rotate copies of it
+        a_bytes = wl.N * wl.H * wl.elem_bytes
+        return int(min(128, max(3, -(-2 * L2_BYTES // a_bytes))))
     x_bytes = wl.M * wl.H * wl.elem_bytes
     return int(min(64, max(3, -(-2 * L2_BYTES // max(x_bytes, 1)))))
 
@@ -97,6 +105,10 @@ def base_config(wl):
          "step": "fwd+bwd" if wl.backward else "fwd"}
     if wl.ld:
         c["row_stride"] = wl.ld
+    if wl.N:
+        c["N"] = wl.N
+        c["step"] = ("residual add + " if wl.residual else "") + \
+            "RMSNorm + projection GEMV (one call)"
     return c
 
 
@@ -193,10 +205,14 @@ def time_oracle(wl, inp, rows, reps=1):
     backward on `rows` rows (single thread, the oracle as it stands)."""
     import oracle
     orc = oracle.get()
-    sub = {k: (v[:rows].contiguous() if v.dim() == 2 else v) for k, v in inp.items()}
+    sub = {k: (v[:rows].contiguous() if v.dim() == 2 and k != "A" else v)
+           for k, v in inp.items()}
     t0 = time.perf_counter()
     for _ in range(reps):
-        if wl.residual:
+        if wl.N:
+            orc.rmsnorm_gemv(sub["x"], sub["w"], sub["A"], wl.eps,
+                             r=sub["r"] if wl.residual else None)
+        elif wl.residual:
             h, _, _ = orc.residual_fwd(sub["x"], sub["r"], sub["w"], wl.eps)
             if wl.backward:
                 orc.residual_bwd(sub["dy"], sub["dh"], h, sub["w"], wl.eps)
@@ -282,6 +298,9 @@ class Calls:
         self.dw = torch.empty(wl.H, device=dev)
         self.ws = ws
         self.w = w
+        if wl.N:         # one copy of the projection weight per buffer set
+            self.A = src["A"].to(dev)
+            self.out = torch.empty(wl.M, wl.N, device=dev, dtype=wl.dtype)
         self.bind(torch.cuda.current_stream())
 
     def bind(self, stream):
@@ -291,6 +310,14 @@ class Calls:
         code = self.rn.DTYPES[wl.dtype]
         s = stream.cuda_stream
         ws_bytes = self.ws.numel()
+        if wl.N:
+            # decode: the weights are static while the step runs
+            self._f = (lib.rmsnorm_gemv_fwd,
+                       (P(self.x), P(self.r), P(self.w), P(self.A), P(self.out),
+                        P(self.h), None, None, wl.M, wl.H, wl.N, wl.eps, code,
+                        self.rn.GEMV_STATIC_WEIGHTS, s))
+            self._b = None
+            return
         if wl.ld:
             ld = wl.ld
             self._f = (lib.rmsnorm_fwd_strided,
@@ -362,6 +389,13 @@ def run_ours(args, wl):
     x_bytes = wl.M * wl.H * wl.elem_bytes
     n_sets = buffer_sets(wl)
     sets = [Calls(rn, wl, src, dev, ws, w) for _ in range(n_sets)]
+    if wl.N:
+        # decode: the activations (x, r and the outputs) are one small set
+        # that stays in L2, as the previous kernel's output would; only the
+        # projection weights rotate, so each call streams its weight from HBM
+        for c in sets[1:]:
+            c.x, c.r, c.h, c.out = sets[0].x, sets[0].r, sets[0].h, sets[0].out
+            c.bind(torch.cuda.current_stream())
     fwd_b, bwd_b = step_bytes(wl)
 
     def barrier():
@@ -372,7 +406,7 @@ def run_ours(args, wl):
     # Decode-sized steps are a few microseconds of GPU work, less than the
     # host needs to issue them one by one; they are timed the way a decoder
     # runs them, replayed from a CUDA graph of consecutive calls.
-    use_graph = fwd_b + bwd_b < 16 * 2 ** 20
+    use_graph = fwd_b + bwd_b < 64 * 2 ** 20
     graphs = []
     if use_graph:
         gstream = torch.cuda.Stream()
@@ -461,10 +495,13 @@ def run_ours(args, wl):
         bwd_ms = [e[1].elapsed_time(e[2]) for e in ev] if wl.backward else [0.0]
     ms_step = total_ms / args.steps
 
+    unfused = time_unfused_gemv(rn, wl, sets, args.steps) if wl.N else None
+
     # ---- e2e: host buffers, copies inside the timed region
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(rn, wl, src, dev, ws, args, dist)
+        e2e = (run_e2e_gemv(rn, wl, src, sets, args, dist) if wl.N else
+               run_e2e(rn, wl, src, dev, ws, args, dist))
 
     if rank != 0:
         if dist is not None:
@@ -488,12 +525,13 @@ def run_ours(args, wl):
                 "avg_ms": round(ms, 5),
                 "frac_of_nominal_8TBs": round(a / NOMINAL_HBM_GBS, 4)}
 
-    fam = {1: "rows", 2: "split", 3: "rows, scalar", 4: "stream"}
-    fwd_api = "rmsnorm_fwd_strided" if wl.ld else (
+    fam = {1: "rows", 2: "split", 3: "rows, scalar", 4: "stream", 5: "gemv"}
+    fwd_api = "rmsnorm_gemv_fwd" if wl.N else "rmsnorm_fwd_strided" if wl.ld else (
         "rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd")
     bwd_api = "rmsnorm_bwd_strided" if wl.ld else (
         "rmsnorm_residual_bwd" if wl.residual else "rmsnorm_bwd")
-    fwd_kernel = fwd_api + f" (rms_fwd_{fam.get(path_f, 'rows').split(',')[0]})"
+    fwd_kernel = fwd_api + (" (rms_gemv)" if wl.N else
+                            f" (rms_fwd_{fam.get(path_f, 'rows').split(',')[0]})")
     bwd_kernel = bwd_api + \
         f" (rms_bwd_{fam.get(path_b, 'rows').split(',')[0]} + dw_reduce)"
     roofline = roof(dom_bytes, dom_ms, bwd_kernel if dom_is_bwd else fwd_kernel)
@@ -510,6 +548,11 @@ def run_ours(args, wl):
             "l2": (f"inputs larger than L2: {n_sets} rotating buffer sets, "
                    f"{x_bytes / 1e6:.0f} MB per row tensor"
                    if streams_from_hbm(wl) else
+                   f"{n_sets} rotating copies of the {wl.N}x{wl.H} projection "
+                   f"weight ({n_sets * wl.N * wl.H * wl.elem_bytes / 1e6:.0f} MB, "
+                   f"more than twice L2: every call reads its weight from HBM); "
+                   f"one set of activations, L2-resident as a decode step's are"
+                   if wl.N else
                    f"{n_sets} rotating buffer sets of {x_bytes / 1e6:.3f} MB per "
                    f"row tensor (L2-resident; launch-bound)"),
             "parallelism": "replicas" if world > 1 else "single"}),
@@ -530,12 +573,107 @@ def run_ours(args, wl):
     }
     if wl.backward:
         line["roofline_bwd"] = roof(bwd_b, bwd_avg, bwd_kernel)
+    if wl.N:
+        line["unfused"] = unfused
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, src)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def time_unfused_gemv(rn, wl, sets, steps):
+    """Microseconds per call of the same work unfused: this library's norm
+    (rmsnorm_residual_fwd or rmsnorm_fwd, writing y) followed by a cuBLAS
+    product (torch.matmul) of y with A^T, replayed from a CUDA graph over
+    the same rotating buffers. Context for the fused call, not part of the
+    product."""
+    # one set of activations (L2-resident), as for the fused call
+    y1 = torch.empty(wl.M, wl.H, device=sets[0].x.device, dtype=wl.dtype)
+    o1 = torch.empty(wl.M, wl.N, device=sets[0].x.device, dtype=wl.dtype)
+    ys, outs = [y1] * len(sets), [o1] * len(sets)
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+
+    def call(i):
+        c, y = sets[i % len(sets)], ys[i % len(sets)]
+        if wl.residual:
+            rn.rmsnorm_residual_fwd(c.x, c.r, c.w, h=c.h, y=y, eps=wl.eps, stream=gs)
+        else:
+            rn.rmsnorm_fwd(c.x, c.w, y=y, want_rstd=False, eps=wl.eps, stream=gs)
+        torch.matmul(y, c.A.t(), out=outs[i % len(sets)])
+
+    with torch.cuda.stream(gs):
+        for i in range(len(sets)):
+            call(i)
+    torch.cuda.synchronize()
+    per = min(steps, 64)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=gs):
+        for i in range(per):
+            call(i)
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // per)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    return {"us_per_step": round(1e3 * s.elapsed_time(e) / (reps * per), 3),
+            "calls": ("rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd") +
+                     " + torch.matmul (cuBLAS), CUDA-graph replay"}
+
+
+def run_e2e_gemv(rn, wl, src, sets, args, dist):
+    """The fused norm + projection through the binding with host
+    activations: every step copies x and r from pinned host memory, runs
+    rmsnorm_gemv_fwd and copies out and h back, all inside the timed region
+    on one stream (a decode step's shape of work). The weights w and A stay
+    resident, as a model's do; the calls rotate over the benchmark's copies
+    of A, so each reads its weight from HBM."""
+    M, H, N = wl.M, wl.H, wl.N
+    pin = {k: src[k].pin_memory() for k in ("x", "r") if k in src}
+    host_out = torch.empty(M, N, dtype=wl.dtype, pin_memory=True)
+    host_h = torch.empty(M, H, dtype=wl.dtype, pin_memory=True) if wl.residual else None
+    main = torch.cuda.current_stream()
+
+    def step(i):
+        c = sets[i % len(sets)]
+        c.x.copy_(pin["x"], non_blocking=True)
+        if wl.residual:
+            c.r.copy_(pin["r"], non_blocking=True)
+        rn.rmsnorm_gemv_fwd(c.x, c.w, c.A, r=c.r, out=c.out, h=c.h, eps=wl.eps,
+                            static_weights=True, stream=main)
+        host_out.copy_(c.out, non_blocking=True)
+        if wl.residual:
+            host_h.copy_(c.h, non_blocking=True)
+
+    steps = max(1, min(args.steps, 2000))
+    for i in range(max(3, min(args.warmup, 20))):
+        step(i)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(main)
+    for i in range(steps):
+        step(i)
+    e.record(main)
+    torch.cuda.synchronize()
+    ms = reduce_max(s.elapsed_time(e) / steps, dist)
+    world = dist.get_world_size() if dist is not None else 1
+    fwd_b, _ = step_bytes(wl)
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = host_out.numel() * host_out.element_size() + \
+        (host_h.numel() * host_h.element_size() if host_h is not None else 0)
+    return {"value": round(whole_job_gbs(fwd_b, world, ms), 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms, 5), "steps": steps,
+            "pipeline": "one stream: copy x, r in; fused call; copy out, h back "
+                        "(weights resident)"}
 
 
 def run_e2e(rn, wl, src, dev, ws, args, dist):

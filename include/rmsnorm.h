@@ -209,6 +209,49 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
                         float eps, int dtype, int flags, void *stream);
 
 /*
+ * RMSNorm fused with the projection that follows it in decode ([P2 §2.1]:
+ * rms_norm, then the q/k/v_proj or gate/up_proj GEMVs; §3.1: a [1, 896]
+ * hidden state against the [1024, 896] q_proj weight, K split over several
+ * programs; §6: fusing the chain is the next step). For each row i:
+ *   (residual variant: h_ij = round(x_ij + r_ij), and the norm acts on h)
+ *   rstd_i = 1 / sqrt( (1/H) sum_j x_ij^2 + eps )
+ *   y_ij   = round( x_ij * rstd_i * w_j )            as rmsnorm_fwd stores it
+ *   out_in = round( sum_k y_ik A_nk )                fp32 accumulation
+ * i.e. the result of running the norm and then the GEMV on its stored
+ * output, in one launch.
+ *   x [M,H] in; r [M,H] in or NULL (plain norm); w [H] in;
+ *   A [N,H] in, row-major (a linear layer's weight; stack q|k|v or gate|up
+ *     rows to produce several projections in one call);
+ *   out [M,N] out; h [M,H] out or NULL (residual variant only);
+ *   y [M,H] out or NULL (the norm's output, when a caller needs it too);
+ *   rstd [M] fp32 out or NULL. All dense row-major.
+ * Limits (else RMSNORM_ERR_UNSUPPORTED): dtype RMSNORM_BF16 or RMSNORM_F16;
+ *   M <= 64 (decode batches); H a multiple of 32 with
+ *   ceil(M/16) * (16 * (2H + 64) + 2048) + 2H + 16 <= 227 KB, i.e.
+ *   H <= 6720 for M <= 16, 3424 for M <= 32, 2272 for M <= 48, 1664 for
+ *   M <= 64;
+ *   1 <= N < 2^30 (else RMSNORM_ERR_BAD_SHAPE).
+ * Alignment: x, r, w, A, h, y 16-byte aligned (RMSNORM_ERR_MISALIGNED).
+ * Aliasing: no output (out, h, y, rstd) may share a byte with an input or
+ *   with another output (every CTA reads x while one writes h and y), else
+ *   RMSNORM_ERR_ALIAS. h without r is RMSNORM_ERR_NULLPTR. M == 0 launches
+ *   nothing. Deterministic (fixed-order fp32 sums, no atomics).
+ * flags: 0, or RMSNORM_GEMV_STATIC_WEIGHTS: the caller guarantees that no
+ *   work still in flight on the stream when this call is enqueued writes w
+ *   or A (model weights during decoding). The kernel then fetches them while
+ *   the preceding kernel is still running (it starts early through
+ *   programmatic dependent launch), which takes their load latency off the
+ *   critical path; x and r are always read only after the preceding work is
+ *   complete. Breaking the guarantee gives results computed from stale
+ *   weights. Unknown bits give RMSNORM_ERR_BAD_FLAGS.
+ */
+#define RMSNORM_GEMV_STATIC_WEIGHTS 1
+int rmsnorm_gemv_fwd(const void *x, const void *r, const void *w,
+                     const void *A, void *out, void *h, void *y, float *rstd,
+                     int64_t M, int64_t H, int64_t N, float eps, int dtype,
+                     int flags, void *stream);
+
+/*
  * Bytes of workspace rmsnorm_bwd / rmsnorm_residual_bwd need for (M, H,
  * dtype) on the current CUDA device (one fp32 row of H per CTA of the
  * backward grid; the grid is sized from the device's SM count). Returns 0 on
@@ -235,8 +278,9 @@ int rmsnorm_last_cuda_error(void);
  */
 void rmsnorm_set_path_override(int path);
 
-/* Which kernel family the last forward/backward call on this thread used:
- * 1 row-wise vectorised, 2 split-row, 3 row-wise scalar, 4 streamed, 0 none. */
+/* Which kernel family the last call on this thread used: 1 row-wise
+ * vectorised, 2 split-row, 3 row-wise scalar, 4 streamed, 5 norm fused with
+ * the GEMV (rmsnorm_gemv_fwd), 0 none. */
 int rmsnorm_last_path(void);
 
 /*

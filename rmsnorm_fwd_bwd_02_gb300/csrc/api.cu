@@ -9,11 +9,13 @@
 #include <cstdint>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <initializer_list>
 #include <utility>
 
 #include "rmsnorm.h"
 #include "params.h"
+#include "gemv.cuh"
 #include "reduce.cuh"
 #include "registry.h"
 
@@ -22,6 +24,9 @@ using namespace rmsk;
 namespace {
 
 constexpr int kPathAuto = 0, kPathRows = 1, kPathSplit = 2, kPathScalar = 3, kPathStream = 4;
+constexpr int kPathGemv = 5;           // reported only: RMSNorm fused with the GEMV
+constexpr int kGemvMaxRows = 64;
+constexpr int64_t kGemvMaxSmem = 227 * 1024;
 constexpr int kSplitMaxRows = 64;      // decode-sized batches ([P2 §3.2])
 constexpr int kReduceCols = 32, kReduceRows = 16;
 
@@ -136,15 +141,18 @@ int sm_count(int dev, int *sms)
     return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e);
 }
 
-// Resident CTAs per SM for a kernel, cached per (kernel, device). Kernels
-// with dynamic shared memory above the default limit are opted in first.
+// Resident CTAs per SM for a kernel launched with `smem` bytes of dynamic
+// shared memory, cached per (kernel, device, smem). A kernel that needs more
+// than the default 48 KB is opted in to the device's maximum (not to this
+// size: a later call with more shared memory must still launch).
 int blocks_per_sm(const void *fn, int threads, int dev, int *out, int smem = 0)
 {
     static std::mutex mu;
-    static std::map<std::pair<const void *, int>, int> cache;
+    static std::map<std::tuple<const void *, int, int>, int> cache;
+    const auto key = std::make_tuple(fn, dev, smem);
     {
         std::lock_guard<std::mutex> g(mu);
-        auto it = cache.find({fn, dev});
+        auto it = cache.find(key);
         if (it != cache.end()) {
             *out = it->second;
             return RMSNORM_OK;
@@ -152,8 +160,14 @@ int blocks_per_sm(const void *fn, int threads, int dev, int *out, int smem = 0)
     }
     int n = 0;
     cudaError_t e = cudaSuccess;
-    if (smem > 48 * 1024)
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (smem > 48 * 1024) {
+        int most = 0;
+        e = cudaDeviceGetAttribute(&most, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess && smem > most)
+            return cuda_fail(cudaErrorInvalidValue);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    }
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
     if (e != cudaSuccess)
@@ -161,7 +175,7 @@ int blocks_per_sm(const void *fn, int threads, int dev, int *out, int smem = 0)
     if (n < 1)
         return cuda_fail(cudaErrorInvalidConfiguration);
     std::lock_guard<std::mutex> g(mu);
-    cache[{fn, dev}] = n;
+    cache[key] = n;
     *out = n;
     return RMSNORM_OK;
 }
@@ -583,6 +597,63 @@ int bwd_impl(const void *dy, int64_t lddy, const void *dh, int64_t lddh, const v
     return RMSNORM_OK;
 }
 
+// ------------------------------------------------- norm + projection GEMV
+int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *out, void *h,
+              void *y, float *rstd, int64_t M, int64_t H, int64_t N, float eps, int dtype,
+              int flags, cudaStream_t stream)
+{
+    const int MT = (int)((M + 15) / 16);
+    const bool half = M <= 8;
+    const int ysr = (int)(H * 2 + 64);     // padded: the two rows a quarter-warp reads
+                                           // fall in different halves of the banks
+    const void *const(&fns)[3] = gemv_kernels.fn[dtype == RMSNORM_F16 ? 1 : 0][half ? 0 : MT];
+    int dev, sms, st;
+    if ((st = current_device(&dev)) || (st = sm_count(dev, &sms)))
+        return st;
+    const int64_t tiles = (N + 7) / 8;
+    // Tiles per CTA so that every CTA is resident at once, for a variant.
+    auto plan = [&](int variant, int smem, int64_t *tn) {
+        int bps;
+        int s2 = blocks_per_sm(fns[variant], kGemvWarps * 32, dev, &bps, smem);
+        if (s2)
+            return s2;
+        const int64_t cap = (int64_t)bps * sms;
+        *tn = (tiles + cap - 1) / cap;
+        return (int)RMSNORM_OK;
+    };
+    // r is staged in shared memory with x and w whenever it fits (measured:
+    // staging beats reading r from L2 in the norm even when it costs the
+    // grid a second round of tiles)
+    const bool stage_r =
+        r != nullptr && gemv_smem_bytes(MT, half, (int)M, (int)H, true) <= kGemvMaxSmem;
+    const int variant = r == nullptr ? 0 : (stage_r ? 2 : 1);
+    const int smem = (int)gemv_smem_bytes(MT, half, (int)M, (int)H, stage_r);
+    int64_t TN;
+    if ((st = plan(variant, smem, &TN)))
+        return st;
+    const void *fn = fns[variant];
+    const int64_t grid = (tiles + TN - 1) / TN;
+    GemvParams p = {x,      r,      w,      A,       out, h,   y,
+                    rstd,   (int)M, (int)H, (int)N, (int)TN, ysr, eps,
+                    (flags & RMSNORM_GEMV_STATIC_WEIGHTS) ? 1 : 0};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kGemvWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    void *args[1] = {&p};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    t_last_path = kPathGemv;
+    return RMSNORM_OK;
+}
+
 } // namespace
 
 // =================================================================== C ABI
@@ -649,6 +720,50 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out, int64_
         return RMSNORM_ERR_BAD_FLAGS;
     return bwd_impl(dy, lddy, dh_out, lddh, x, ldx, w, rstd, dx, lddx, dw, workspace,
                     workspace_bytes, M, H, eps, dtype, static_cast<cudaStream_t>(stream), flags);
+}
+
+int rmsnorm_gemv_fwd(const void *x, const void *r, const void *w, const void *A, void *out,
+                     void *h, void *y, float *rstd, int64_t M, int64_t H, int64_t N, float eps,
+                     int dtype, int flags, void *stream)
+{
+    if (flags & ~RMSNORM_GEMV_STATIC_WEIGHTS)
+        return RMSNORM_ERR_BAD_FLAGS;
+    int st = check_common(M, H, eps, dtype);
+    if (st)
+        return st;
+    if (N < 1 || N > INT32_MAX / 2 || N * H > INT64_MAX / 8)
+        return RMSNORM_ERR_BAD_SHAPE;
+    if (dtype == RMSNORM_F32 || M > kGemvMaxRows || H % 32 != 0)
+        return RMSNORM_ERR_UNSUPPORTED;
+    const int MT = (int)((M + 15) / 16);
+    if (gemv_smem_bytes(MT > 0 ? MT : 1, false, (int)M, (int)H, false) > kGemvMaxSmem)
+        return RMSNORM_ERR_UNSUPPORTED;
+    if (h != nullptr && r == nullptr)
+        return RMSNORM_ERR_NULLPTR;
+    if (M == 0)
+        return RMSNORM_OK;
+    if (!x || !w || !A || !out)
+        return RMSNORM_ERR_NULLPTR;
+    if (!aligned(x, 16) || !aligned(r, 16) || !aligned(w, 16) || !aligned(A, 16) ||
+        !aligned(h, 16) || !aligned(y, 16) || !aligned(out, 2) || !aligned(rstd, 4))
+        return RMSNORM_ERR_MISALIGNED;
+    const size_t es = 2;
+    const Span sx = flat(x, (size_t)(M * H) * es), sr = flat(r, (size_t)(M * H) * es),
+               sw = flat(w, (size_t)H * es), sA = flat(A, (size_t)(N * H) * es),
+               so = flat(out, (size_t)(M * N) * es), sh = flat(h, (size_t)(M * H) * es),
+               sy = flat(y, (size_t)(M * H) * es), ss = flat(rstd, (size_t)M * 4);
+    // Every CTA reads x and r while CTA 0 writes h, y and rstd: no output may
+    // share a byte with an input or with another output.
+    for (Span o : {so, sh, sy, ss}) {
+        for (Span i : {sx, sr, sw, sA})
+            if (overlap(o, i))
+                return RMSNORM_ERR_ALIAS;
+    }
+    if (overlap(so, sh) || overlap(so, sy) || overlap(so, ss) || overlap(sh, sy) ||
+        overlap(sh, ss) || overlap(sy, ss))
+        return RMSNORM_ERR_ALIAS;
+    return gemv_impl(x, r, w, A, out, h, y, rstd, M, H, N, eps, dtype, flags,
+                     static_cast<cudaStream_t>(stream));
 }
 
 size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype)

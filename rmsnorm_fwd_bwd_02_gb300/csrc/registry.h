@@ -79,6 +79,14 @@ extern const SplitKernels split_f16_v, split_f16_s;
 // streamed layouts: bf16 (s_) and fp16 (sh_)
 extern const StreamKernels s_h4096, s_h5120, s_h128;
 extern const StreamKernels sh_h4096, sh_h5120, sh_h128;
+
+// RMSNorm fused with the projection GEMV (gemv.cuh):
+// fn[bf16 = 0, fp16 = 1][y tile: 0 = 8 rows (M <= 8), k = k 16-row tiles]
+//   [0 plain, 1 residual (r from L2), 2 residual (r staged in shared memory)]
+struct GemvKernels {
+    const void *fn[2][5][3];
+};
+extern const GemvKernels gemv_kernels;
 // Device address of the counter of streamed-kernel waits that ran out.
 unsigned int *stream_timeout_counter(int dev);
 

@@ -20,6 +20,7 @@ DTYPES = {torch.float32: RMSNORM_F32, torch.bfloat16: RMSNORM_BF16,
           torch.float16: RMSNORM_F16}
 MAX_H = 16384
 PATH_AUTO, PATH_ROWS, PATH_SPLIT, PATH_SCALAR, PATH_STREAM = 0, 1, 2, 3, 4
+PATH_GEMV = 5            # reported by last_path() after rmsnorm_gemv_fwd
 
 # Entry points of include/rmsnorm.h with their ctypes signatures.
 _i64, _vp, _sz, _int, _f = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
@@ -48,6 +49,8 @@ SIGNATURES = {
     "rmsnorm_bwd_strided": (_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp,
                                    _vp, _i64, _vp, _vp, _sz, _i64, _i64, _f,
                                    _int, _int, _vp]),
+    "rmsnorm_gemv_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                _i64, _i64, _f, _int, _int, _vp]),
 }
 
 BWD_ACCUMULATE_DW = 1
@@ -331,6 +334,42 @@ def rmsnorm_bwd_strided(dy, x, w, rstd=None, dh_out=None, dx=None, dw=None,
         _dtype_code(x), BWD_ACCUMULATE_DW if accumulate_dw else 0,
         _stream(stream)), "rmsnorm_bwd_strided")
     return dx, dw
+
+
+GEMV_STATIC_WEIGHTS = 1
+
+
+def rmsnorm_gemv_fwd(x, w, A, r=None, out=None, h=None, want_h=True, y=None,
+                     rstd=None, eps=1e-6, static_weights=False, stream=None):
+    """out = round(RMSNorm(x [+ r]) * w) @ A^T for decode-sized x [M, H]
+    (M <= 64) and a row-major weight A [N, H]. Returns (out, h or None,
+    rstd or None); y (the norm's output) is written only into a given
+    buffer. With r, h (the residual sum) is allocated unless want_h is
+    False. static_weights: nothing in flight on the stream writes w or A
+    (see RMSNORM_GEMV_STATIC_WEIGHTS)."""
+    H = w.numel()
+    M = _rows("x", x, H)
+    _rows("w", w.view(-1), H, x.dtype)
+    if A.dim() != 2:
+        raise ValueError("A must be 2-D [N, H]")
+    N = _rows("A", A, H, x.dtype)
+    if r is not None:
+        _rows("r", r, H, x.dtype)
+        if h is None and want_h:
+            h = torch.empty_like(x)
+    elif h is not None:
+        raise ValueError("h is the residual variant's output: pass r too")
+    if out is None:
+        out = torch.empty(x.shape[:-1] + (N,), device=x.device, dtype=x.dtype)
+    _rows("out", out, N, x.dtype)
+    if y is not None:
+        _rows("y", y, H, x.dtype)
+    _check(lib().rmsnorm_gemv_fwd(
+        _ptr(x), _ptr(r), _ptr(w), _ptr(A), _ptr(out), _ptr(h), _ptr(y),
+        _ptr(rstd), M, H, N, float(eps), _dtype_code(x),
+        GEMV_STATIC_WEIGHTS if static_weights else 0, _stream(stream)),
+        "rmsnorm_gemv_fwd")
+    return out, h, rstd
 
 
 STATIC_SCRATCH_BYTES = 16 << 20

@@ -34,6 +34,8 @@ class Workload:
     residual: bool = False         # also draw r (residual) and dh_out
     backward: bool = True          # the workload runs the backward too
     ld: int = 0                    # row stride of every [M, H] tensor (0: H)
+    N: int = 0                     # rows of a projection weight A [N, H] that
+                                   # the norm feeds (fused norm + GEMV); 0: none
     note: str = ""
 
     def with_rows(self, M: int) -> "Workload":
@@ -79,6 +81,16 @@ WORKLOADS = {
                  dy_std=1e-2, ld=4608,
                  note="the Qwen3-8B training shape, every [M, H] tensor the "
                       "first 4096 columns of an [M, 4608] buffer"),
+        Workload("decode-qkv-m1", 1, 896, torch.bfloat16, seed=5,
+                 outlier_frac=1e-3, outlier_scale=50.0, residual=True,
+                 backward=False, N=2048,
+                 note="one decode token: residual add + RMSNorm + the stacked "
+                      "q|k|v projection (1024 + 512 + 512 rows of 896)"),
+        Workload("decode-gateup-m1", 1, 896, torch.bfloat16, seed=6,
+                 outlier_frac=1e-3, outlier_scale=50.0, residual=True,
+                 backward=False, N=9728,
+                 note="one decode token: residual add + RMSNorm + the stacked "
+                      "gate|up projection (2 x 4864 rows of 896)"),
     ]
 }
 
@@ -106,9 +118,9 @@ def _outliers(t, seed, frac, scale):
 
 
 def make_inputs(w: Workload) -> dict:
-    """CPU tensors for workload ``w``: x, w (weight), dy, and with
+    """CPU tensors for workload ``w``: x, w (weight), dy, with
     ``w.residual`` also r and dh (the incoming gradient of the residual
-    stream). Same seed, same values, on every machine with the same torch
+    stream), and with ``w.N`` the projection weight A [N, H]. Same seed, same values, on every machine with the same torch
     random generator."""
     base = 1000 * w.seed
     shape = (w.M, w.H)
@@ -124,6 +136,9 @@ def make_inputs(w: Workload) -> dict:
             _outliers(r, base + 14, w.outlier_frac, w.outlier_scale)
         out["r"] = r
         out["dh"] = _normal(shape, base + 5, std=w.dy_std)
+    if w.N:
+        # a projection weight at the usual initialisation scale
+        out["A"] = _normal((w.N, w.H), base + 6, std=0.02)
     return {k: v.to(w.dtype).contiguous() for k, v in out.items()}
 
 

@@ -166,6 +166,32 @@ def test_bwd_strided_allowed_layouts_reach_the_device(lib):
     assert bwd_s(lib, dtype=F16) == CUDA
 
 
+def test_gemv_argument_checks(lib):
+    f = lib.rmsnorm_gemv_fwd
+    E = 0x7f0400000000
+    # x r w A out h y rstd M H N
+    args = dict(x=A, r=None, w=B, A=C, out=D, h=None, y=None, rstd=None, M=1,
+                H=896, N=64, dtype=BF16)
+
+    def call(flags=0, **kw):
+        a = dict(args, **kw)
+        return f(a["x"], a["r"], a["w"], a["A"], a["out"], a["h"], a["y"],
+                 a["rstd"], a["M"], a["H"], a["N"], 1e-6, a["dtype"], flags, None)
+    assert call(flags=4) == -11
+    assert call(M=65) == UNSUPPORTED
+    assert call(H=900) == UNSUPPORTED
+    assert call(M=64, H=4096) == UNSUPPORTED
+    assert call(dtype=F32) == UNSUPPORTED
+    assert call(N=0) == BAD_SHAPE
+    assert call(h=E) == NULLPTR
+    assert call(A=None) == NULLPTR
+    assert call(A=C + 8) == MISALIGNED
+    assert call(out=A) == ALIAS
+    assert call(r=E, h=A) == ALIAS
+    assert call(y=C) == ALIAS
+    assert call(M=0, x=None, w=None, A=None, out=None) == OK
+
+
 def test_residual_fwd_argument_checks(lib):
     f = lib.rmsnorm_residual_fwd
     E = 0x7f0400000000

@@ -32,6 +32,10 @@ def test_buffer_sets_defeat_l2():
     for name, wl in W.WORKLOADS.items():
         n = bench.buffer_sets(wl)
         x_bytes = wl.M * wl.H * wl.elem_bytes
+        if wl.N:      # the projection weight rotates: > 2 x L2 of weights
+            assert 3 <= n <= 128
+            assert n * wl.N * wl.H * wl.elem_bytes >= 2 * bench.L2_BYTES
+            continue
         assert 3 <= n <= 64
         if bench.streams_from_hbm(wl):
             assert n == 3 and x_bytes > 100e6
@@ -89,3 +93,11 @@ def test_reference_arm_prints_one_json_line():
         assert k in d
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["value"] > 0
+
+
+def test_gemv_step_bytes():
+    """Fused norm + projection: x, r, w and A read, out and h written."""
+    wl = W.WORKLOADS["decode-qkv-m1"]
+    f, b = bench.step_bytes(wl)
+    assert b == 0
+    assert f == (2 * 896 + 896 + 2048 * 896) * 2 + (2048 + 896) * 2

@@ -1,0 +1,242 @@
+"""GPU tier: RMSNorm fused with the projection GEMV (rmsnorm_gemv_fwd)
+against the fp64 oracle.
+
+The decode chain of the 0.8B Qwen decode article (trdm.cn news/483216,
+§2.1 and §3.1: rms_norm, then the q/k/v or gate/up projections of a
+[1, 896] hidden state; §6: fuse them) in one call: out = round(y) A^T with
+y the norm's output as the separate norm would store it. Compared element
+by element on every output (out, h, y, rstd) over dtypes, row counts that
+fill one to four 16-row MMA tiles (and leave them ragged), feature counts,
+output counts that leave the last 8-row tile of A ragged, with and without
+the residual add.
+"""
+import pytest
+import torch
+
+import oracle
+from rmsnorm_fwd_bwd_02_gb300 import rmsnorm as rn
+from rmsnorm_fwd_bwd_02_gb300 import workloads as W
+from tests.tolerances import check_bits, check_rows, check_rstd
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tier needs a CUDA device")
+    rn.lib()
+    yield
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+def synth(M, H, N, dtype, seed, residual):
+    g = torch.Generator().manual_seed(seed)
+    d = {"x": torch.randn(M, H, generator=g) * 2.0,
+         "w": 1.0 + 0.1 * torch.randn(H, generator=g),
+         "A": torch.randn(N, H, generator=g) * 0.05}
+    if residual:
+        d["r"] = torch.randn(M, H, generator=g)
+    if M > 1:
+        d["x"] *= torch.logspace(-2, 2, M).unsqueeze(1)
+    return {k: v.to(dtype).contiguous() for k, v in d.items()}
+
+
+def run(inp, residual, eps=1e-6, want_y=True, static=False):
+    g = {k: v.to(DEV) for k, v in inp.items()}
+    torch.cuda.synchronize()             # the weights are in place before the call
+    M, H = g["x"].shape
+    y = torch.empty(M, H, device=DEV, dtype=g["x"].dtype) if want_y else None
+    rstd = torch.empty(M, device=DEV)
+    out, h, _ = rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"],
+                                    r=g["r"] if residual else None, y=y,
+                                    rstd=rstd, eps=eps, static_weights=static)
+    assert rn.last_path() == rn.PATH_GEMV
+    torch.cuda.synchronize()
+    return {"out": out, "h": h, "y": y, "rstd": rstd}
+
+
+def oracle_all(orc, inp, residual, eps=1e-6):
+    """The oracle's fused result plus the norm's unrounded output (the
+    stored y is one rounding of it)."""
+    r = inp["r"] if residual else None
+    o = orc.rmsnorm_gemv(inp["x"], inp["w"], inp["A"], eps, r=r)
+    if residual:
+        _, o["y_exact"], _ = orc.residual_fwd(inp["x"], r, inp["w"], eps)
+    else:
+        o["y_exact"], _ = orc.fwd(inp["x"], inp["w"], eps)
+    return o
+
+
+def compare(name, got, o, dtype):
+    check_rows(f"{name} out", got["out"], o["out"], dtype, o["tout"])
+    check_rstd(f"{name} rstd", got["rstd"], o["rstd"])
+    if got.get("y") is not None:
+        check_rows(f"{name} y", got["y"], o["y_exact"], dtype)
+    if o["h"] is not None:
+        check_bits(f"{name} h", got["h"], o["h"])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 33, 64])
+@pytest.mark.parametrize("H,N", [(128, 1), (128, 9), (896, 1024), (896, 2051),
+                                 (1024, 13), (1664, 64)])
+def test_gemv_matches_oracle(orc, dtype, M, H, N):
+    for residual in (False, True):
+        inp = synth(M, H, N, dtype, seed=M * 7 + H + N, residual=residual)
+        o = oracle_all(orc, inp, residual)
+        for static in (False, True):
+            got = run(inp, residual, static=static)
+            compare(f"{dtype} M={M} H={H} N={N} res={residual} static={static}",
+                    got, o, dtype)
+
+
+@pytest.mark.parametrize("H,M", [(4096, 16), (6720, 1), (6720, 16), (3424, 32),
+                                 (2272, 48), (1664, 64)])
+def test_gemv_largest_shared_memory(orc, H, M):
+    """The largest y tile each row count allows (up to 227 KB of shared
+    memory), after smaller calls of the same kernels have run."""
+    small = synth(M, 128, 8, torch.bfloat16, seed=1, residual=False)
+    run(small, False)
+    inp = synth(M, H, 24, torch.bfloat16, seed=H, residual=True)
+    o = oracle_all(orc, inp, True)
+    compare(f"large H={H} M={M}", run(inp, True), o, torch.bfloat16)
+
+
+@pytest.mark.parametrize("name", ["decode-qkv-m1", "decode-gateup-m1"])
+def test_decode_workloads_full(orc, name):
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl)
+    o = oracle_all(orc, inp, True, wl.eps)
+    got = run(inp, True, eps=wl.eps, static=True)
+    compare(name, got, o, wl.dtype)
+    # the same at 8 and 64 decode rows
+    for M in (8, 64):
+        wm = wl.with_rows(M)
+        im = W.make_inputs(wm)
+        om = oracle_all(orc, im, True, wm.eps)
+        compare(f"{name} M={M}", run(im, True, eps=wm.eps), om, wm.dtype)
+
+
+def test_y_matches_the_unfused_norm():
+    """The fused kernel's y and h equal the residual forward's to within one
+    ulp of y (the fp32 sums of squares run in a different order) and
+    bit-exactly for h."""
+    for dt in (torch.bfloat16, torch.float16):
+        inp = synth(64, 896, 16, dt, seed=3, residual=True)
+        got = run(inp, True)
+        g = {k: v.to(DEV) for k, v in inp.items()}
+        h, y, rstd = rn.rmsnorm_residual_fwd(g["x"], g["r"], g["w"])
+        torch.cuda.synchronize()
+        check_bits(f"{dt} h fused vs unfused", got["h"], h)
+        a = got["y"].view(torch.int16).to(torch.int32).cpu()
+        b = y.view(torch.int16).to(torch.int32).cpu()
+        assert int((a - b).abs().max()) <= 1, f"{dt}: fused y > 1 ulp from unfused"
+
+
+def test_deterministic_and_optional_outputs(orc):
+    inp = synth(17, 896, 2048, torch.bfloat16, seed=5, residual=True)
+    a = run(inp, True)
+    b = run(inp, True)
+    c = run(inp, True, static=True)
+    for k in ("out", "h", "y", "rstd"):
+        check_bits(f"run-to-run {k}", a[k], b[k])
+        check_bits(f"static weights {k}", c[k], a[k])
+    # no y, no h, no rstd: out unchanged
+    g = {k: v.to(DEV) for k, v in inp.items()}
+    out, h, rstd = rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], want_h=False)
+    torch.cuda.synchronize()
+    assert h is None and rstd is None
+    check_bits("out without optional outputs", out, a["out"])
+
+
+def test_guard_words_untouched(orc):
+    M, H, N, G = 5, 896, 1003, 64
+    inp = synth(M, H, N, torch.float16, seed=8, residual=True)
+    g = {k: v.to(DEV) for k, v in inp.items()}
+
+    def guarded(n, dtype):
+        b = torch.empty(n + 2 * G, device=DEV, dtype=dtype)
+        b.view(torch.int16 if dtype != torch.float32 else torch.int32).fill_(0x7E5A)
+        return b, b[G:G + n]
+
+    bo, out = guarded(M * N, torch.float16)
+    bh, h = guarded(M * H, torch.float16)
+    by, y = guarded(M * H, torch.float16)
+    br, rstd = guarded(M, torch.float32)
+    rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], out=out.view(M, N),
+                        h=h.view(M, H), y=y.view(M, H), rstd=rstd)
+    torch.cuda.synchronize()
+    for b, n, nm in ((bo, M * N, "out"), (bh, M * H, "h"), (by, M * H, "y"),
+                     (br, M, "rstd")):
+        it = torch.int32 if b.dtype == torch.float32 else torch.int16
+        head, tail = b[:G].view(it), b[G + n:].view(it)
+        assert bool((head == 0x7E5A).all()) and bool((tail == 0x7E5A).all()), \
+            f"{nm}: guard words overwritten"
+    o = oracle_all(orc, inp, True)
+    compare("guarded", {"out": out.view(M, N), "h": h.view(M, H), "y": y.view(M, H),
+                        "rstd": rstd}, o, torch.float16)
+
+
+def test_cuda_graph_replay(orc):
+    """Captured once and replayed with new activations copied into the
+    static inputs (the decode loop of the article's §4)."""
+    wl = W.WORKLOADS["decode-qkv-m1"]
+    inp = W.make_inputs(wl)
+    g = {k: v.to(DEV) for k, v in inp.items()}
+    out = torch.empty(1, wl.N, device=DEV, dtype=wl.dtype)
+    h = torch.empty_like(g["x"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], out=out, h=h, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], out=out, h=h,
+                            static_weights=True)
+    for step in range(3):
+        x2 = (torch.randn(1, wl.H, generator=torch.Generator().manual_seed(step))
+              ).to(wl.dtype)
+        g["x"].copy_(x2.to(DEV))
+        graph.replay()
+        torch.cuda.synchronize()
+        o = orc.rmsnorm_gemv(x2, inp["w"], inp["A"], wl.eps, r=inp["r"])
+        check_rows(f"graph step {step} out", out, o["out"], wl.dtype, o["tout"])
+        check_bits(f"graph step {step} h", h, o["h"])
+
+
+def test_error_returns():
+    lib = rn.lib()
+    s = torch.cuda.current_stream().cuda_stream
+    x = torch.randn(65, 896, device=DEV, dtype=torch.bfloat16)
+    w = torch.ones(896, device=DEV, dtype=torch.bfloat16)
+    A = torch.randn(64, 896, device=DEV, dtype=torch.bfloat16)
+    out = torch.empty(65, 64, device=DEV, dtype=torch.bfloat16)
+    P = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+
+    def call(x=x, r=None, w=w, A=A, out=out, h=None, y=None, M=1, H=896, N=64,
+             dtype=rn.RMSNORM_BF16, flags=0):
+        return lib.rmsnorm_gemv_fwd(P(x) if hasattr(x, "data_ptr") else x, P(r),
+                                    P(w), P(A) if hasattr(A, "data_ptr") else A,
+                                    P(out) if hasattr(out, "data_ptr") else out,
+                                    P(h), P(y), None, M, H, N, 1e-6, dtype, flags, s)
+    assert call(flags=2) == -11
+    assert call(M=65) == -7                  # beyond 64 rows
+    assert call(H=900) == -7                 # H not a multiple of 32
+    assert call(M=64, H=4096) == -7          # y tile beyond shared memory
+    assert call(dtype=rn.RMSNORM_F32) == -7
+    assert call(N=0) == -2
+    assert call(h=x) == -1                   # h without r
+    assert call(A=A.data_ptr() + 2) == -5
+    assert call(out=x.data_ptr()) == -9      # out over x
+    assert call(r=x, h=x) == -9              # h over x (every CTA reads x)
+    assert call(M=0) == 0
+    torch.cuda.synchronize()
