@@ -43,6 +43,10 @@ def _declare(lib):
     lib.oracle_bf16_to_double.restype = _dbl
     lib.oracle_bf16_from_double.argtypes = [_dbl]
     lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+    lib.oracle_rmsnorm_bwd_bwd.argtypes = [_i64, _i64, _vp, _vp, _vp, _vp, _vp,
+                                           ctypes.c_int, _dbl, _vp, _vp, _vp, _vp,
+                                           _vp, _vp]
+    lib.oracle_rmsnorm_bwd_bwd.restype = None
     lib.oracle_rmsnorm_gemv.argtypes = [_i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                         ctypes.c_int, _dbl, _vp, _vp, _vp, _vp,
                                         _vp]
@@ -157,6 +161,33 @@ class Oracle:
         if want_terms:
             return dx, dw, tdx, tdw
         return dx, dw
+
+    # -- double backward
+    def bwd_bwd(self, dy, x, w, gx, gw, eps, want_terms=False):
+        """Gradients of sum(gx * dx) + sum(gw * dw) with respect to dy, x and
+        w (float64); gx [M,H] in the input dtype or None, gw [H] (any float
+        dtype, read as float64) or None. Returns (ddy, dx2, dw2) and with
+        want_terms also their error scales."""
+        M, H = x.shape
+        code = _CODES[x.dtype]
+        for name, t in (("dy", dy), ("x", x)):
+            _check_rows(name, t, x.dtype, M, H)
+        _check_rows("w", w, x.dtype, 1, H)
+        if gx is not None:
+            _check_rows("gx", gx, x.dtype, M, H)
+        gw64 = None if gw is None else gw.detach().to(torch.float64).contiguous()
+        ddy = torch.empty(M, H, dtype=torch.float64)
+        dx2 = torch.empty(M, H, dtype=torch.float64)
+        dw2 = torch.empty(H, dtype=torch.float64)
+        t = [torch.empty(M, H, dtype=torch.float64), torch.empty(M, H, dtype=torch.float64),
+             torch.empty(H, dtype=torch.float64)] if want_terms else [None] * 3
+        self.lib.oracle_rmsnorm_bwd_bwd(M, H, _ptr(dy), _ptr(x), _ptr(w), _ptr(gx),
+                                        _ptr(gw64), code, float(eps), _ptr(ddy),
+                                        _ptr(dx2), _ptr(dw2), _ptr(t[0]), _ptr(t[1]),
+                                        _ptr(t[2]))
+        if want_terms:
+            return ddy, dx2, dw2, t[0], t[1], t[2]
+        return ddy, dx2, dw2
 
     # -- norm followed by the projection GEMV (decode chain)
     def rmsnorm_gemv(self, x, w, A, eps, r=None):

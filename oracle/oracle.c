@@ -305,6 +305,91 @@ void oracle_residual_bwd(int64_t M, int64_t H, const void *dy,
             }
 }
 
+/* ---------------------------------------------------- double backward */
+
+/*
+ * Second derivatives ([P1 §5.6] lists double backward as what an autograd
+ * wrapper must either implement or refuse). The backward of [P1 §5.3] maps
+ * (dy, x, w) to dx and dw; given incoming gradients gx [M,H] on dx and gw [H]
+ * on dw (either may be NULL: zero), this returns the gradients of
+ *   L2 = sum_ij gx_ij dx_ij + sum_j gw_j dw_j
+ * with respect to dy, x and w. Per row, with r = 1/sqrt(mean(x^2) + eps)
+ * (a function of x), c = (1/H) sum_k w_k dy_k x_k and the row sums
+ *   A = sum_k gx_k w_k dy_k,  B = sum_k gx_k x_k,  D = sum_k gw_k dy_k x_k,
+ * differentiating dx_k = r w_k dy_k - r^3 c x_k and dw_k = sum dy_k x_k r
+ * term by term (dr/dx_k = -r^3 x_k / H, dc/dx_k = w_k dy_k / H,
+ * dc/ddy_k = w_k x_k / H, dc/dw_k = dy_k x_k / H) gives
+ *   ddy_k = r w_k gx_k - (r^3 B / H) w_k x_k + r gw_k x_k
+ *   dx2_k = (r^3 / H)(3 r^2 c B - A - D) x_k - (r^3 B / H) w_k dy_k
+ *           - r^3 c gx_k + r gw_k dy_k
+ *   dw2_k = sum over rows of  r gx_k dy_k - (r^3 B / H) dy_k x_k
+ * Inputs dy, x, w, gx in the stored format; gw in double. Outputs in double;
+ * t_* (each may be NULL) are the error scales, the sums of the absolute
+ * values of the terms.
+ */
+void oracle_rmsnorm_bwd_bwd(int64_t M, int64_t H, const void *dy, const void *x,
+                            const void *w, const void *gx, const double *gw,
+                            int dtype, double eps, double *ddy, double *dx2,
+                            double *dw2, double *t_ddy, double *t_dx2,
+                            double *t_dw2)
+{
+    for (int64_t j = 0; j < H; ++j) {
+        dw2[j] = 0.0;
+        if (t_dw2)
+            t_dw2[j] = 0.0;
+    }
+    for (int64_t i = 0; i < M; ++i) {
+        double ss = 0.0, cs = 0.0, A = 0.0, B = 0.0, D = 0.0;
+        double cabs = 0.0, Aabs = 0.0, Babs = 0.0, Dabs = 0.0;
+        for (int64_t k = 0; k < H; ++k) {
+            double xv = dec(x, dtype, i * H + k);
+            double dyv = dec(dy, dtype, i * H + k);
+            double wv = dec(w, dtype, k);
+            double g = gx ? dec(gx, dtype, i * H + k) : 0.0;
+            double gwv = gw ? gw[k] : 0.0;
+            ss += xv * xv;
+            cs += wv * dyv * xv;
+            A += g * wv * dyv;
+            B += g * xv;
+            D += gwv * dyv * xv;
+            cabs += fabs(wv * dyv * xv);
+            Aabs += fabs(g * wv * dyv);
+            Babs += fabs(g * xv);
+            Dabs += fabs(gwv * dyv * xv);
+        }
+        double mean_sq = ss / (double)H;
+        double r = 1.0 / sqrt(mean_sq + eps);
+        double c = cs / (double)H;
+        double r3 = r * r * r;
+        for (int64_t k = 0; k < H; ++k) {
+            double xv = dec(x, dtype, i * H + k);
+            double dyv = dec(dy, dtype, i * H + k);
+            double wv = dec(w, dtype, k);
+            double g = gx ? dec(gx, dtype, i * H + k) : 0.0;
+            double gwv = gw ? gw[k] : 0.0;
+            double t1 = r * wv * g, t2 = (r3 * B / (double)H) * wv * xv, t3 = r * gwv * xv;
+            ddy[i * H + k] = t1 - t2 + t3;
+            double u1 = (r3 / (double)H) * (3.0 * r * r * c * B - A - D) * xv;
+            double u2 = (r3 * B / (double)H) * wv * dyv;
+            double u3 = r3 * c * g;
+            double u4 = r * gwv * dyv;
+            dx2[i * H + k] = u1 - u2 - u3 + u4;
+            double v1 = r * g * dyv, v2 = (r3 * B / (double)H) * dyv * xv;
+            dw2[k] += v1 - v2;
+            if (t_ddy)
+                t_ddy[i * H + k] = fabs(t1) + (r3 * Babs / (double)H) * fabs(wv * xv) + fabs(t3);
+            if (t_dx2)
+                t_dx2[i * H + k] =
+                    (r3 / (double)H) * (3.0 * r * r * (cabs / (double)H) * Babs + Aabs + Dabs) *
+                        fabs(xv) +
+                    (r3 * Babs / (double)H) * fabs(wv * dyv) + r3 * (cabs / (double)H) * fabs(g) +
+                    fabs(u4);
+            if (t_dw2)
+                t_dw2[k] += fabs(v1) + (r3 * Babs / (double)H) * fabs(dyv * xv);
+        }
+    }
+}
+
 /* ------------------------------------------------ norm, then projection */
 
 /* v rounded to the given storage format (nearest, ties to even). */

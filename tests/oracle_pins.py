@@ -512,6 +512,82 @@ def pin_residual_dh_none_is_zero(o):
     _close(a[0], c[0], 0.0, what="resid bwd = bwd on h")
 
 
+# ------------------------------------------------------- double backward
+
+def _l2(o, dy, x, w, gx, gw, eps):
+    dx, dw = o.bwd(dy, x, w, eps)
+    return float((gx * dx).sum() + (gw * dw).sum())
+
+
+def pin_bwd_bwd_finite_differences(o):
+    """Central differences of L2 = sum(gx dx) + sum(gw dw), with (dx, dw)
+    from the (pinned) backward, in every element of dy, x and w."""
+    g = _gen(31)
+    M, H, eps = 2, 6, 0.1
+    dy = torch.randn(M, H, generator=g, dtype=F64)
+    x = torch.randn(M, H, generator=g, dtype=F64)
+    w = 1.0 + 0.3 * torch.randn(H, generator=g, dtype=F64)
+    gx = torch.randn(M, H, generator=g, dtype=F64)
+    gw = torch.randn(H, generator=g, dtype=F64)
+    ddy, dx2, dw2 = o.bwd_bwd(dy, x, w, gx, gw, eps)
+    step = 1e-6
+    for name, t, got in (("dy", dy, ddy), ("x", x, dx2), ("w", w, dw2)):
+        fd = torch.empty_like(t)
+        flat = t.view(-1)
+        for k in range(flat.numel()):
+            keep = float(flat[k])
+            flat[k] = keep + step
+            lp = _l2(o, dy, x, w, gx, gw, eps)
+            flat[k] = keep - step
+            lm = _l2(o, dy, x, w, gx, gw, eps)
+            flat[k] = keep
+            fd.view(-1)[k] = (lp - lm) / (2 * step)
+        _close(got, fd, 1e-6, 1e-8, what=f"double backward FD d{name}")
+
+
+def pin_bwd_bwd_vs_autograd(o):
+    """torch's float64 double backward of the definition y = w x r (r from
+    mean(x^2) + eps), through autograd with create_graph."""
+    g = _gen(32)
+    M, H, eps = 3, 32, 1e-6
+    dy = torch.randn(M, H, generator=g, dtype=F64)
+    x = torch.randn(M, H, generator=g, dtype=F64)
+    w = 1.0 + 0.1 * torch.randn(H, generator=g, dtype=F64)
+    gx = torch.randn(M, H, generator=g, dtype=F64)
+    gw = torch.randn(H, generator=g, dtype=F64)
+    dyr, xr, wr = (t.clone().requires_grad_() for t in (dy, x, w))
+    y = wr * xr / torch.sqrt((xr * xr).mean(dim=1, keepdim=True) + eps)
+    dx, dw = torch.autograd.grad(y, (xr, wr), dyr, create_graph=True)
+    l2 = (gx * dx).sum() + (gw * dw).sum()
+    a_dy, a_x, a_w = torch.autograd.grad(l2, (dyr, xr, wr))
+    ddy, dx2, dw2 = o.bwd_bwd(dy, x, w, gx, gw, eps)
+    _close(ddy, a_dy, 1e-11, 1e-13, what="double backward ddy vs autograd")
+    _close(dx2, a_x, 1e-11, 1e-13, what="double backward dx vs autograd")
+    _close(dw2, a_w, 1e-11, 1e-13, what="double backward dw vs autograd")
+
+
+def pin_bwd_bwd_linear_and_zero(o):
+    """The result is linear in (gx, gw) and zero without them; each error
+    scale bounds its value."""
+    g = _gen(33)
+    M, H = 3, 16
+    dy = torch.randn(M, H, generator=g, dtype=F64)
+    x = torch.randn(M, H, generator=g, dtype=F64)
+    w = torch.randn(H, generator=g, dtype=F64)
+    gx = torch.randn(M, H, generator=g, dtype=F64)
+    gw = torch.randn(H, generator=g, dtype=F64)
+    z = o.bwd_bwd(dy, x, w, None, None, 1e-6)
+    for t in z:
+        _close(t, torch.zeros_like(t), 0.0, what="double backward without gradients")
+    a = o.bwd_bwd(dy, x, w, gx, None, 1e-6)
+    b = o.bwd_bwd(dy, x, w, None, gw, 1e-6)
+    ab = o.bwd_bwd(dy, x, w, gx, gw, 1e-6, want_terms=True)
+    for i in range(3):
+        _close(ab[i], a[i] + b[i], 1e-12, 1e-15, what=f"double backward linearity {i}")
+        assert bool((ab[i].abs() <= ab[3 + i] * (1 + 1e-12) + 1e-300).all()), \
+            f"double backward error scale {i} below |value|"
+
+
 # ------------------------------------------- norm, then projection (decode)
 
 def _round_like(o, v, dtype):

@@ -84,6 +84,18 @@ MUTANTS = [
     ("gemv_f16_rounded_as_bf16",
      "return oracle_f16_to_double(oracle_f16_from_double(v));",
      "return oracle_bf16_to_double(oracle_bf16_from_double(v));"),
+    ("bwd2_eps_dropped", "double r = 1.0 / sqrt(mean_sq + eps);",
+     "double r = 1.0 / sqrt(mean_sq);"),
+    ("bwd2_r_power", "(3.0 * r * r * c * B - A - D)", "(3.0 * r * c * B - A - D)"),
+    ("bwd2_coeff_3", "(3.0 * r * r * c * B - A - D)", "(2.0 * r * r * c * B - A - D)"),
+    ("bwd2_D_dropped", "(3.0 * r * r * c * B - A - D)", "(3.0 * r * r * c * B - A)"),
+    ("bwd2_gx_term_sign", "dx2[i * H + k] = u1 - u2 - u3 + u4;",
+     "dx2[i * H + k] = u1 - u2 + u3 + u4;"),
+    ("bwd2_ddy_gw_dropped", "ddy[i * H + k] = t1 - t2 + t3;", "ddy[i * H + k] = t1 - t2;"),
+    ("bwd2_dw_second_term", "dw2[k] += v1 - v2;", "dw2[k] += v1;"),
+    ("bwd2_A_uses_x", "A += g * wv * dyv;", "A += g * wv * xv;"),
+    ("bwd2_B_over_H_missing", "double t1 = r * wv * g, t2 = (r3 * B / (double)H) * wv * xv",
+     "double t1 = r * wv * g, t2 = (r3 * B) * wv * xv"),
     ("resid_subtract",
      "double s = dec(x, dtype, i * H + j) + dec(res, dtype, i * H + j);",
      "double s = dec(x, dtype, i * H + j) - dec(res, dtype, i * H + j);"),
