@@ -53,6 +53,9 @@ def step_bytes(wl):
         ins = MH * es * (2 if wl.residual else 1) + H * es + wl.N * H * es
         outs = M * wl.N * es + (MH * es if wl.residual else 0)
         return ins + outs, 0
+    if wl.double_backward:
+        # dy, x, gx, w, gw (fp32), rstd in; ddy, dx2 and dw2 (fp32) out
+        return 3 * MH * es + H * es + 4 * H + 4 * M + 2 * MH * es + 4 * H, 0
     if wl.residual:
         fwd = 4 * MH * es + H * es + 4 * M          # x, r in; h, y out; rstd
         bwd = 4 * MH * es + H * es + 4 * H          # dy, h, dh in; dx out; dw
@@ -109,6 +112,8 @@ def base_config(wl):
         c["N"] = wl.N
         c["step"] = ("residual add + " if wl.residual else "") + \
             "RMSNorm + projection GEMV (one call)"
+    if wl.double_backward:
+        c["step"] = "double backward (rmsnorm_bwd_bwd: ddy, dx2, dw2)"
     return c
 
 
@@ -212,6 +217,8 @@ def time_oracle(wl, inp, rows, reps=1):
         if wl.N:
             orc.rmsnorm_gemv(sub["x"], sub["w"], sub["A"], wl.eps,
                              r=sub["r"] if wl.residual else None)
+        elif wl.double_backward:
+            orc.bwd_bwd(sub["dy"], sub["x"], sub["w"], sub["gx"], sub["gw"], wl.eps)
         elif wl.residual:
             h, _, _ = orc.residual_fwd(sub["x"], sub["r"], sub["w"], wl.eps)
             if wl.backward:
@@ -301,6 +308,12 @@ class Calls:
         if wl.N:         # one copy of the projection weight per buffer set
             self.A = src["A"].to(dev)
             self.out = torch.empty(wl.M, wl.N, device=dev, dtype=wl.dtype)
+        if wl.double_backward:
+            self.gx = src["gx"].to(dev)
+            self.gw = src["gw"].to(dev)
+            self.ddy, self.dx2 = e(), e()
+            self.dw2 = torch.empty(wl.H, device=dev)
+            rn.rmsnorm_fwd(self.x, self.w, rstd=self.rstd, eps=wl.eps)   # the saved rstd
         self.bind(torch.cuda.current_stream())
 
     def bind(self, stream):
@@ -310,6 +323,13 @@ class Calls:
         code = self.rn.DTYPES[wl.dtype]
         s = stream.cuda_stream
         ws_bytes = self.ws.numel()
+        if wl.double_backward:
+            self._f = (lib.rmsnorm_bwd_bwd,
+                       (P(self.dy), P(self.x), P(self.w), P(self.rstd), P(self.gx),
+                        P(self.gw), P(self.ddy), P(self.dx2), P(self.dw2), P(self.ws),
+                        ws_bytes, wl.M, wl.H, wl.eps, code, s))
+            self._b = None
+            return
         if wl.N:
             # decode: the weights are static while the step runs
             self._f = (lib.rmsnorm_gemv_fwd,
@@ -501,6 +521,7 @@ def run_ours(args, wl):
     e2e = None
     if not args.no_e2e:
         e2e = (run_e2e_gemv(rn, wl, src, sets, args, dist) if wl.N else
+               run_e2e_bwd2(rn, wl, src, sets[0], args, dist) if wl.double_backward else
                run_e2e(rn, wl, src, dev, ws, args, dist))
 
     if rank != 0:
@@ -526,11 +547,13 @@ def run_ours(args, wl):
                 "frac_of_nominal_8TBs": round(a / NOMINAL_HBM_GBS, 4)}
 
     fam = {1: "rows", 2: "split", 3: "rows, scalar", 4: "stream", 5: "gemv"}
-    fwd_api = "rmsnorm_gemv_fwd" if wl.N else "rmsnorm_fwd_strided" if wl.ld else (
-        "rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd")
+    fwd_api = "rmsnorm_bwd_bwd" if wl.double_backward else \
+        "rmsnorm_gemv_fwd" if wl.N else "rmsnorm_fwd_strided" if wl.ld else (
+            "rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd")
     bwd_api = "rmsnorm_bwd_strided" if wl.ld else (
         "rmsnorm_residual_bwd" if wl.residual else "rmsnorm_bwd")
     fwd_kernel = fwd_api + (" (rms_gemv)" if wl.N else
+                            " (rms_bwd2_rows + dw_reduce)" if wl.double_backward else
                             f" (rms_fwd_{fam.get(path_f, 'rows').split(',')[0]})")
     bwd_kernel = bwd_api + \
         f" (rms_bwd_{fam.get(path_b, 'rows').split(',')[0]} + dw_reduce)"
@@ -625,6 +648,48 @@ def time_unfused_gemv(rn, wl, sets, steps):
     return {"us_per_step": round(1e3 * s.elapsed_time(e) / (reps * per), 3),
             "calls": ("rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd") +
                      " + torch.matmul (cuBLAS), CUDA-graph replay"}
+
+
+def run_e2e_bwd2(rn, wl, src, c, args, dist):
+    """The double backward through the binding with host tensors: every step
+    copies dy, x, gx, w and gw from pinned host memory, runs
+    rmsnorm_bwd_bwd (with the saved rstd already on the device, as a
+    training step has it) and copies ddy, dx2 and dw2 back, on one stream."""
+    keys = ("dy", "x", "gx", "w", "gw")
+    pin = {k: src[k].pin_memory() for k in keys}
+    dev_in = {"dy": c.dy, "x": c.x, "gx": c.gx, "w": c.w, "gw": c.gw}
+    outs = {"ddy": c.ddy, "dx2": c.dx2, "dw2": c.dw2}
+    host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    main = torch.cuda.current_stream()
+
+    def step():
+        for k in keys:
+            dev_in[k].copy_(pin[k], non_blocking=True)
+        rn.rmsnorm_bwd_bwd(c.dy, c.x, c.w, c.rstd, c.gx, c.gw, ddy=c.ddy, dx2=c.dx2,
+                           dw2=c.dw2, workspace=c.ws, eps=wl.eps, stream=main)
+        for k, v in outs.items():
+            host[k].copy_(v, non_blocking=True)
+
+    steps = max(1, min(args.steps, 50))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(main)
+    for _ in range(steps):
+        step()
+    e.record(main)
+    torch.cuda.synchronize()
+    ms = reduce_max(s.elapsed_time(e) / steps, dist)
+    world = dist.get_world_size() if dist is not None else 1
+    fwd_b, _ = step_bytes(wl)
+    return {"value": round(whole_job_gbs(fwd_b, world, ms), 1), "unit": "GB/s",
+            "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in pin.values()),
+            "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "pipeline": "one stream: copies in, double backward, copies out"}
 
 
 def run_e2e_gemv(rn, wl, src, sets, args, dist):

@@ -252,10 +252,41 @@ int rmsnorm_gemv_fwd(const void *x, const void *r, const void *w,
                      int flags, void *stream);
 
 /*
- * Bytes of workspace rmsnorm_bwd / rmsnorm_residual_bwd need for (M, H,
- * dtype) on the current CUDA device (one fp32 row of H per CTA of the
- * backward grid; the grid is sized from the device's SM count). Returns 0 on
- * invalid arguments or when no device is available.
+ * Double backward ([P1 §5.6]: an autograd wrapper implements it or refuses
+ * it): given gradients gdx [M,H] arriving on the backward's dx and gdw [H]
+ * (fp32) arriving on its dw, the gradients of
+ *   L2 = sum_ij gdx_ij dx_ij + sum_j gdw_j dw_j
+ * with respect to the backward's inputs dy, x and w, the backward being
+ * that of rmsnorm_bwd ([P1 §5.3]) with r = rstd a function of x. Per row,
+ * with c = (1/H) sum w dy x and A = sum gdx w dy, B = sum gdx x,
+ * D = sum gdw dy x:
+ *   ddy = r w gdx - (r^3 B / H) w x + r gdw x
+ *   dx2 = (r^3 / H)(3 r^2 c B - A - D) x - (r^3 B / H) w dy - r^3 c gdx
+ *         + r gdw dy
+ *   dw2 = sum over rows of r gdx dy - (r^3 B / H) dy x        (fp32)
+ *   dy, x [M,H] in; w [H] in; rstd [M] fp32 in (as the forward saved it) or
+ *   NULL to recompute it; gdx [M,H] in or NULL (zero); gdw [H] fp32 in or
+ *   NULL (zero), 16-byte aligned; ddy, dx2 [M,H] out; dw2 [H] fp32 out
+ *   (overwritten; zeros when M == 0); workspace as for rmsnorm_bwd (at least
+ *   rmsnorm_bwd_workspace_bytes(M, H, dtype) bytes).
+ * For the residual variant pass h as x: dx2 is then the gradient on h, and
+ * the gradient on dh_out is gdx itself (dx depends on dh_out as the
+ * identity).
+ * Aliasing: no output may share a byte with an input or another output
+ * (RMSNORM_ERR_ALIAS). Errors otherwise as for rmsnorm_bwd. Deterministic.
+ */
+int rmsnorm_bwd_bwd(const void *dy, const void *x, const void *w,
+                    const float *rstd, const void *gdx, const float *gdw,
+                    void *ddy, void *dx2, float *dw2, void *workspace,
+                    size_t workspace_bytes, int64_t M, int64_t H, float eps,
+                    int dtype, void *stream);
+
+/*
+ * Bytes of workspace rmsnorm_bwd, rmsnorm_residual_bwd, rmsnorm_bwd_ex,
+ * rmsnorm_bwd_strided and rmsnorm_bwd_bwd need for (M, H, dtype) on the
+ * current CUDA device (one fp32 row of H per CTA of the backward grid; the
+ * grid is sized from the device's SM count). Returns 0 on invalid arguments
+ * or when no device is available.
  */
 size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype);
 

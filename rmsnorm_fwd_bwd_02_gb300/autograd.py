@@ -6,8 +6,11 @@ its kernels in a torch.autograd.Function (saving x and the weight, returning
 make dy contiguous, save tensors with save_for_backward, return one gradient
 per forward input (None for eps), take eps as a float, and raise on double
 backward unless it is implemented. These wrappers follow that shape over the
-CUDA kernels of librmsnorm.so; the forward also saves rstd, so the backward
-does not recompute it. Inputs and incoming gradients whose rows are evenly
+CUDA kernels of librmsnorm.so, and implement double backward: the backward
+is itself an autograd function of (dy, x, w) whose backward runs the double
+backward kernel (rmsnorm_bwd_bwd), so torch.autograd.grad(...,
+create_graph=True) followed by a second backward works; a third derivative
+raises. The forward also saves rstd, so the backward does not recompute it. Inputs and incoming gradients whose rows are evenly
 strided (a column window of a wider buffer, a slice along the leading dims)
 go to the kernels as they are, through the strided entry points; only
 layouts that no row stride describes are copied first. Every arithmetic step
@@ -27,29 +30,75 @@ def _rows2d(t, H):
     return _rn.as_rows(t, H)
 
 
+class RMSNormBackward(torch.autograd.Function):
+    """(dx, dw) of RMSNormFunction as a differentiable function of (dy, x,
+    w); its own backward is the double backward."""
+
+    @staticmethod
+    def forward(ctx, dy2, x2, weight, rstd, eps: float):
+        dx, dw = _rn.rmsnorm_bwd_strided(dy2, x2, weight, rstd, eps=eps)
+        ctx.save_for_backward(dy2, x2, weight, rstd)
+        ctx.eps = eps
+        return dx, dw
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, gdx, gdw):
+        dy2, x2, weight, rstd = ctx.saved_tensors
+        gx = None if gdx is None else gdx.contiguous()
+        gw = None if gdw is None else gdw.float().contiguous()
+        ddy, dx2, dw2 = _rn.rmsnorm_bwd_bwd(dy2.contiguous(), x2.contiguous(), weight,
+                                            rstd, gx, gw, eps=ctx.eps)
+        return ddy, dx2, dw2.to(weight.dtype), None, None
+
+
 class RMSNormFunction(torch.autograd.Function):
     """y = w * x / sqrt(mean(x^2) + eps) over the last dimension."""
 
     @staticmethod
     def forward(ctx, x, weight, eps: float = 1e-6):
         H = weight.numel()
-        x2 = _rows2d(x, H)
-        y, rstd = _rn.rmsnorm_fwd_strided(x2, weight, eps=float(eps))
-        ctx.save_for_backward(x2, weight, rstd)
+        y, rstd = _rn.rmsnorm_fwd_strided(_rows2d(x, H), weight, eps=float(eps))
+        # the input itself is saved (a view made here would carry no autograd
+        # history, and the double backward must reach x through it)
+        ctx.save_for_backward(x, weight, rstd)
         ctx.eps = float(eps)
         ctx.shape = x.shape
         return y.view(x.shape)
 
     @staticmethod
-    @once_differentiable
     def backward(ctx, dy):
-        x2, weight, rstd = ctx.saved_tensors
+        x, weight, rstd = ctx.saved_tensors
         H = weight.numel()
-        dx, dw = _rn.rmsnorm_bwd_strided(_rows2d(dy, H), x2, weight, rstd,
-                                         eps=ctx.eps)
+        dx, dw = RMSNormBackward.apply(_rows2d(dy, H), _rows2d(x, H), weight, rstd, ctx.eps)
         dx = dx.view(ctx.shape) if ctx.needs_input_grad[0] else None
         dw = dw.to(weight.dtype) if ctx.needs_input_grad[1] else None
         return dx, dw, None
+
+
+class ResidualRMSNormBackward(torch.autograd.Function):
+    """(dx, dw) of ResidualRMSNormFunction as a differentiable function of
+    (dy, dh, h, w); its own backward is the double backward at h, and the
+    gradient on dh is the incoming gradient on dx itself."""
+
+    @staticmethod
+    def forward(ctx, dy2, dh2, h, weight, rstd, eps: float):
+        dx, dw = _rn.rmsnorm_bwd_strided(dy2, h, weight, rstd, dh_out=dh2, eps=eps)
+        ctx.save_for_backward(dy2, h, weight, rstd)
+        ctx.has_dh = dh2 is not None
+        ctx.eps = eps
+        return dx, dw
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, gdx, gdw):
+        dy2, h, weight, rstd = ctx.saved_tensors
+        gx = None if gdx is None else gdx.contiguous()
+        gw = None if gdw is None else gdw.float().contiguous()
+        ddy, dh2, dw2 = _rn.rmsnorm_bwd_bwd(dy2.contiguous(), h.contiguous(), weight, rstd,
+                                            gx, gw, eps=ctx.eps)
+        g_dh = gdx if ctx.has_dh else None
+        return ddy, g_dh, dh2, dw2.to(weight.dtype), None, None
 
 
 class ResidualRMSNormFunction(torch.autograd.Function):
@@ -62,21 +111,23 @@ class ResidualRMSNormFunction(torch.autograd.Function):
         H = weight.numel()
         x2, r2 = _rows2d(x, H), _rows2d(residual, H)
         h, y, rstd = _rn.rmsnorm_fwd_strided(x2, weight, r=r2, eps=float(eps))
-        ctx.save_for_backward(h, weight, rstd)
+        hv = h.view(x.shape)
+        # the returned h itself is saved, so that a double backward reaches it
+        ctx.save_for_backward(hv, weight, rstd)
         ctx.eps = float(eps)
         ctx.shape = x.shape
-        return y.view(x.shape), h.view(x.shape)
+        return y.view(x.shape), hv
 
     @staticmethod
-    @once_differentiable
     def backward(ctx, dy, dh):
-        h, weight, rstd = ctx.saved_tensors
+        hv, weight, rstd = ctx.saved_tensors
         H = weight.numel()
+        h = _rows2d(hv, H)
         if dy is None:
             dy = torch.zeros_like(h)
         dh2 = None if dh is None else _rows2d(dh, H)
-        dx, dw = _rn.rmsnorm_bwd_strided(_rows2d(dy, H), h, weight, rstd,
-                                         dh_out=dh2, eps=ctx.eps)
+        dx, dw = ResidualRMSNormBackward.apply(_rows2d(dy, H), dh2, h, weight, rstd,
+                                               ctx.eps)
         dx = dx.view(ctx.shape)
         dw = dw.to(weight.dtype) if ctx.needs_input_grad[2] else None
         gx = dx if ctx.needs_input_grad[0] else None

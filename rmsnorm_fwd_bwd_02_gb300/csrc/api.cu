@@ -15,6 +15,7 @@
 
 #include "rmsnorm.h"
 #include "params.h"
+#include "bwd2.cuh"
 #include "gemv.cuh"
 #include "reduce.cuh"
 #include "registry.h"
@@ -597,6 +598,107 @@ int bwd_impl(const void *dy, int64_t lddy, const void *dh, int64_t lddh, const v
     return RMSNORM_OK;
 }
 
+// ------------------------------------------------------- double backward
+const Bwd2Kernel &pick_bwd2(int dtype, int64_t H, bool vec)
+{
+    struct Set {
+        const Bwd2Kernel &g32, &g128, &h4096, &g512, &s1024;
+    };
+    static const Set bf = {b2_bf_g32, b2_bf_g128, b2_bf_h4096, b2_bf_g512, b2_bf_s1024};
+    static const Set hf = {b2_h_g32, b2_h_g128, b2_h_h4096, b2_h_g512, b2_h_s1024};
+    static const Set f3 = {b2_f_g32, b2_f_g128, b2_f_g128, b2_f_g512, b2_f_s1024};
+    const Set &k = dtype == RMSNORM_BF16 ? bf : (dtype == RMSNORM_F16 ? hf : f3);
+    if (!vec)
+        return k.s1024;
+    if (H == 4096 && dtype != RMSNORM_F32)
+        return k.h4096;
+    if (H <= k.g32.s.cols()) return k.g32;
+    if (H <= k.g128.s.cols()) return k.g128;
+    return k.g512;
+}
+
+// Grid of the double backward (and so its partial-row count).
+int bwd2_grid(int dtype, int64_t M, int64_t H, bool vec, const Bwd2Kernel **k, int64_t *grid)
+{
+    *k = &pick_bwd2(dtype, H, vec);
+    if (M == 0) {
+        *grid = 0;
+        return RMSNORM_OK;
+    }
+    return rows_grid((*k)->s, (*k)->fn, M, grid);
+}
+
+int bwd2_impl(const void *dy, const void *x, const void *w, const float *rstd, const void *gx,
+              const float *gw, void *ddy, void *dx2, float *dw2, void *ws, size_t ws_bytes,
+              int64_t M, int64_t H, float eps, int dtype, cudaStream_t stream)
+{
+    int st = check_common(M, H, eps, dtype);
+    if (st)
+        return st;
+    if (dw2 == nullptr)
+        return RMSNORM_ERR_NULLPTR;
+    if (M > 0 && (!dy || !x || !w || !ddy || !dx2))
+        return RMSNORM_ERR_NULLPTR;
+    const size_t es = elem_size(dtype);
+    if (!aligned(dy, es) || !aligned(x, es) || !aligned(w, es) || !aligned(gx, es) ||
+        !aligned(ddy, es) || !aligned(dx2, es) || !aligned(rstd, 4) || !aligned(gw, 16) ||
+        !aligned(dw2, 4) || !aligned(ws, 16))
+        return RMSNORM_ERR_MISALIGNED;
+    const size_t rows = (size_t)M * (size_t)H * es;
+    const Span sdy = flat(dy, rows), sx = flat(x, rows), sw = flat(w, (size_t)H * es),
+               sr = flat(rstd, (size_t)M * 4), sgx = flat(gx, rows), sgw = flat(gw, (size_t)H * 4),
+               sddy = flat(ddy, rows), sdx2 = flat(dx2, rows), sdw2 = flat(dw2, (size_t)H * 4);
+    for (Span o : {sddy, sdx2, sdw2})
+        for (Span i : {sdy, sx, sw, sr, sgx, sgw})
+            if (overlap(o, i))
+                return RMSNORM_ERR_ALIAS;
+    if (overlap(sddy, sdx2) || overlap(sddy, sdw2) || overlap(sdx2, sdw2))
+        return RMSNORM_ERR_ALIAS;
+
+    const bool vec16 = (H * (int64_t)es) % 16 == 0 && aligned(dy, 16) && aligned(x, 16) &&
+                       aligned(w, 16) && aligned(gx, 16) && aligned(ddy, 16) && aligned(dx2, 16);
+    const int ov = g_path_override.load(std::memory_order_relaxed);
+    const bool vec = vec16 && ov != kPathScalar;
+    const Bwd2Kernel *k;
+    int64_t grid;
+    if ((st = bwd2_grid(dtype, M, H, vec, &k, &grid)))
+        return st;
+    const size_t need = (size_t)grid * (size_t)H * sizeof(float);
+    if (need > 0 && (ws == nullptr || ws_bytes < need))
+        return RMSNORM_ERR_WORKSPACE;
+    const Span sws = flat(ws, need);
+    for (Span b : {sdy, sx, sw, sr, sgx, sgw, sddy, sdx2, sdw2})
+        if (overlap(sws, b))
+            return RMSNORM_ERR_ALIAS;
+
+    if (M > 0) {
+        Bwd2Params p = {dy, x, w, rstd, gx, gw, ddy, dx2, static_cast<float *>(ws), M,
+                        (int)H, eps};
+        cudaError_t e = launch(k->fn, dim3((unsigned)grid), dim3(k->s.threads()), stream, &p,
+                               true, 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+    }
+    const float *part = static_cast<const float *>(ws);
+    int P = (int)grid, Hi = (int)H, acc = 0;
+    void *args[5] = {&part, &P, &Hi, &dw2, &acc};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((H + kReduceCols - 1) / kReduceCols));
+    cfg.blockDim = dim3(kReduceCols * kReduceRows);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelExC(
+        &cfg, (const void *)&dw_reduce<kReduceCols, kReduceRows>, args);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    t_last_path = M == 0 ? 0 : (vec ? kPathRows : kPathScalar);
+    return RMSNORM_OK;
+}
+
 // ------------------------------------------------- norm + projection GEMV
 int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *out, void *h,
               void *y, float *rstd, int64_t M, int64_t H, int64_t N, float eps, int dtype,
@@ -766,6 +868,15 @@ int rmsnorm_gemv_fwd(const void *x, const void *r, const void *w, const void *A,
                      static_cast<cudaStream_t>(stream));
 }
 
+int rmsnorm_bwd_bwd(const void *dy, const void *x, const void *w, const float *rstd,
+                    const void *gdx, const float *gdw, void *ddy, void *dx2, float *dw2,
+                    void *workspace, size_t workspace_bytes, int64_t M, int64_t H, float eps,
+                    int dtype, void *stream)
+{
+    return bwd2_impl(dy, x, w, rstd, gdx, gdw, ddy, dx2, dw2, workspace, workspace_bytes, M, H,
+                     eps, dtype, static_cast<cudaStream_t>(stream));
+}
+
 size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype)
 {
     if (check_common(M, H, 0.f, dtype) != RMSNORM_OK)
@@ -782,6 +893,14 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype)
                     const size_t need = (size_t)pl.grid * (size_t)H * sizeof(float);
                     most = need > most ? need : most;
                 }
+    for (int vec = 0; vec < 2; ++vec) {       // the double backward's grid too
+        const Bwd2Kernel *k;
+        int64_t grid;
+        if (bwd2_grid(dtype, M, H, vec != 0, &k, &grid) != RMSNORM_OK)
+            return 0;
+        const size_t need = (size_t)grid * (size_t)H * sizeof(float);
+        most = need > most ? need : most;
+    }
     return most;
 }
 

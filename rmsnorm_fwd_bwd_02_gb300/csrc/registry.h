@@ -80,6 +80,16 @@ extern const SplitKernels split_f16_v, split_f16_s;
 extern const StreamKernels s_h4096, s_h5120, s_h128;
 extern const StreamKernels sh_h4096, sh_h5120, sh_h128;
 
+// Double backward (bwd2.cuh): one layout and its kernel.
+struct Bwd2Kernel {
+    const char *name;
+    RowShape s;
+    const void *fn;
+};
+extern const Bwd2Kernel b2_bf_g32, b2_bf_g128, b2_bf_h4096, b2_bf_g512, b2_bf_s1024;
+extern const Bwd2Kernel b2_h_g32, b2_h_g128, b2_h_h4096, b2_h_g512, b2_h_s1024;
+extern const Bwd2Kernel b2_f_g32, b2_f_g128, b2_f_g512, b2_f_s1024;
+
 // RMSNorm fused with the projection GEMV (gemv.cuh):
 // fn[bf16 = 0, fp16 = 1][y tile: 0 = 8 rows (M <= 8), k = k 16-row tiles]
 //   [0 plain, 1 residual (r from L2), 2 residual (r staged in shared memory)]

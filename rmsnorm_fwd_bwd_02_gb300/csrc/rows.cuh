@@ -276,6 +276,63 @@ __device__ __forceinline__ void store_vals(float *dst, const Vals<E> &v)
     }
 }
 
+// The end of a backward CTA: the fp32 dw accumulators of the columns each
+// lane owns, summed over the CTA's groups in a fixed order, become one
+// partial row at `part` (H floats). Lanes of a warp that share columns
+// (L < 32) fold first by butterfly; groups then meet in `comb` (shared
+// memory, [kColGroups][kCols]) and are added in group order.
+template <int E, int L, int V, int S, bool EXACT>
+__device__ __forceinline__ void write_dw_partials(Vals<E> (&acc)[V], float *part, float *comb,
+                                                  int H, int lane, int grp)
+{
+    using X = Vals<E>;
+    using Lay = RowLayout<E, L, V, 1, S>;
+    const int NV = H / E;
+    if constexpr (Lay::kColGroups == 1) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int vi = lane + k * L;
+            if (EXACT || vi < NV)
+                store_vals<E>(part + (int64_t)vi * E, acc[k]);
+        }
+    } else {
+        if constexpr (L < 32) {
+            // lanes l, l+L, l+2L, ... of a warp own the same columns
+#pragma unroll
+            for (int k = 0; k < V; ++k)
+#pragma unroll
+                for (int i = 0; i < X::N; ++i)
+#pragma unroll
+                    for (int o = L; o < 32; o <<= 1) {
+                        if constexpr (E % 2 == 0) {
+                            acc[k].v[i].x += __shfl_xor_sync(0xFFFFFFFFu, acc[k].v[i].x, o);
+                            acc[k].v[i].y += __shfl_xor_sync(0xFFFFFFFFu, acc[k].v[i].y, o);
+                        } else {
+                            acc[k].v[i] += __shfl_xor_sync(0xFFFFFFFFu, acc[k].v[i], o);
+                        }
+                    }
+        }
+        const int cg = L < 32 ? (int)(threadIdx.x / 32) : grp;
+        if (L >= 32 || (threadIdx.x & 31) < L) {
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const int vi = lane + k * L;
+                if (EXACT || vi < NV)
+                    store_vals<E>(comb + cg * Lay::kCols + vi * E, acc[k]);
+            }
+        }
+        __syncthreads();
+        const int ncols = EXACT ? Lay::kCols : H;
+        for (int c = threadIdx.x; c < ncols; c += Lay::kThreads) {
+            float s = 0.f;
+#pragma unroll
+            for (int q = 0; q < Lay::kColGroups; ++q)
+                s += comb[q * Lay::kCols + c];
+            part[c] = s;
+        }
+    }
+}
+
 // LOADR: rstd is given (read it) instead of recomputed from x.
 template <typename T, int E, int L, int V, int G, int S, int MINB, bool EXACT, bool DH,
           bool LOADR>
@@ -400,50 +457,8 @@ rms_bwd_rows(const BwdParams p)
     // to finish before reading the partial rows.
     griddep_launch_dependents();
 
-    float *part = p.part + (int64_t)blockIdx.x * p.H;
-    if constexpr (Lay::kColGroups == 1) {
-#pragma unroll
-        for (int k = 0; k < V; ++k) {
-            const int vi = lane + k * L;
-            if (EXACT || vi < NV)
-                store_vals<E>(part + (int64_t)vi * E, acc[k]);
-        }
-    } else {
-        if constexpr (L < 32) {
-            // lanes l, l+L, l+2L, ... of a warp own the same columns
-#pragma unroll
-            for (int k = 0; k < V; ++k)
-#pragma unroll
-                for (int i = 0; i < X::N; ++i)
-#pragma unroll
-                    for (int o = L; o < 32; o <<= 1) {
-                        if constexpr (E % 2 == 0) {
-                            acc[k].v[i].x += __shfl_xor_sync(0xFFFFFFFFu, acc[k].v[i].x, o);
-                            acc[k].v[i].y += __shfl_xor_sync(0xFFFFFFFFu, acc[k].v[i].y, o);
-                        } else {
-                            acc[k].v[i] += __shfl_xor_sync(0xFFFFFFFFu, acc[k].v[i], o);
-                        }
-                    }
-        }
-        const int cg = L < 32 ? (int)(threadIdx.x / 32) : grp;
-        if (L >= 32 || (threadIdx.x & 31) < L) {
-#pragma unroll
-            for (int k = 0; k < V; ++k) {
-                const int vi = lane + k * L;
-                if (EXACT || vi < NV)
-                    store_vals<E>(comb + cg * Lay::kCols + vi * E, acc[k]);
-            }
-        }
-        __syncthreads();
-        const int ncols = EXACT ? Lay::kCols : p.H;
-        for (int c = threadIdx.x; c < ncols; c += Lay::kThreads) {
-            float s = 0.f;
-#pragma unroll
-            for (int q = 0; q < Lay::kColGroups; ++q)
-                s += comb[q * Lay::kCols + c];
-            part[c] = s;
-        }
-    }
+    write_dw_partials<E, L, V, S, EXACT>(acc, p.part + (int64_t)blockIdx.x * p.H, comb, p.H,
+                                         lane, grp);
 }
 
 } // namespace rmsk

@@ -49,6 +49,8 @@ SIGNATURES = {
     "rmsnorm_bwd_strided": (_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp,
                                    _vp, _i64, _vp, _vp, _sz, _i64, _i64, _f,
                                    _int, _int, _vp]),
+    "rmsnorm_bwd_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                               _sz, _i64, _i64, _f, _int, _vp]),
     "rmsnorm_gemv_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                 _i64, _i64, _f, _int, _int, _vp]),
 }
@@ -334,6 +336,35 @@ def rmsnorm_bwd_strided(dy, x, w, rstd=None, dh_out=None, dx=None, dw=None,
         _dtype_code(x), BWD_ACCUMULATE_DW if accumulate_dw else 0,
         _stream(stream)), "rmsnorm_bwd_strided")
     return dx, dw
+
+
+def rmsnorm_bwd_bwd(dy, x, w, rstd=None, gdx=None, gdw=None, ddy=None, dx2=None,
+                    dw2=None, workspace=None, eps=1e-6, stream=None):
+    """(ddy, dx2, dw2): gradients of sum(gdx * dx) + sum(gdw * dw) with
+    respect to the backward's dy, x and w (see rmsnorm.h). gdx in x's dtype
+    or None, gdw float32 or None; dw2 is float32."""
+    H = w.numel()
+    M = _rows("x", x, H)
+    _rows("dy", dy, H, x.dtype)
+    if gdx is not None:
+        _rows("gdx", gdx, H, x.dtype)
+    if gdw is not None and (gdw.dtype != torch.float32 or not gdw.is_contiguous()):
+        raise ValueError("gdw must be a contiguous float32 tensor")
+    if ddy is None:
+        ddy = torch.empty_like(x)
+    if dx2 is None:
+        dx2 = torch.empty_like(x)
+    if dw2 is None:
+        dw2 = torch.empty(H, device=x.device, dtype=torch.float32)
+    need = bwd_workspace_bytes(M, H, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=x.device, dtype=torch.uint8)
+    _check(lib().rmsnorm_bwd_bwd(
+        _ptr(dy), _ptr(x), _ptr(w), _ptr(rstd), _ptr(gdx), _ptr(gdw), _ptr(ddy),
+        _ptr(dx2), _ptr(dw2), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), M, H, float(eps),
+        _dtype_code(x), _stream(stream)), "rmsnorm_bwd_bwd")
+    return ddy, dx2, dw2
 
 
 GEMV_STATIC_WEIGHTS = 1

@@ -36,6 +36,7 @@ class Workload:
     ld: int = 0                    # row stride of every [M, H] tensor (0: H)
     N: int = 0                     # rows of a projection weight A [N, H] that
                                    # the norm feeds (fused norm + GEMV); 0: none
+    double_backward: bool = False  # the step is the double backward
     note: str = ""
 
     def with_rows(self, M: int) -> "Workload":
@@ -81,6 +82,10 @@ WORKLOADS = {
                  dy_std=1e-2, ld=4608,
                  note="the Qwen3-8B training shape, every [M, H] tensor the "
                       "first 4096 columns of an [M, 4608] buffer"),
+        Workload("qwen3-8b-train-bwd2", 32768, 4096, torch.bfloat16, seed=2,
+                 dy_std=1e-2, double_backward=True,
+                 note="double backward at the Qwen3-8B training shape: gradients "
+                      "gx ~ N(0, 1e-2) on dx and gw ~ N(0, 1e-3) (fp32) on dw"),
         Workload("decode-qkv-m1", 1, 896, torch.bfloat16, seed=5,
                  outlier_frac=1e-3, outlier_scale=50.0, residual=True,
                  backward=False, N=2048,
@@ -120,7 +125,9 @@ def _outliers(t, seed, frac, scale):
 def make_inputs(w: Workload) -> dict:
     """CPU tensors for workload ``w``: x, w (weight), dy, with
     ``w.residual`` also r and dh (the incoming gradient of the residual
-    stream), and with ``w.N`` the projection weight A [N, H]. Same seed, same values, on every machine with the same torch
+    stream), with ``w.N`` the projection weight A [N, H], and with
+    ``w.double_backward`` the incoming gradients gx [M, H] (dtype) and gw [H]
+    (float32). Same seed, same values, on every machine with the same torch
     random generator."""
     base = 1000 * w.seed
     shape = (w.M, w.H)
@@ -139,7 +146,12 @@ def make_inputs(w: Workload) -> dict:
     if w.N:
         # a projection weight at the usual initialisation scale
         out["A"] = _normal((w.N, w.H), base + 6, std=0.02)
-    return {k: v.to(w.dtype).contiguous() for k, v in out.items()}
+    if w.double_backward:
+        out["gx"] = _normal(shape, base + 7, std=w.dy_std)
+    res = {k: v.to(w.dtype).contiguous() for k, v in out.items()}
+    if w.double_backward:
+        res["gw"] = _normal((w.H,), base + 8, std=1e-3)      # fp32, as dw is
+    return res
 
 
 def in_strided(t, ld: int, fill=float("nan")):

@@ -1,15 +1,15 @@
 """The autograd wrappers (RMSNormFunction / RMSNorm and the residual variant)
 against the fp64 oracle, and their gotcha-table behaviour ([P1]
 "训推加速 Qwen3 实战：从“调包”到手写 Triton Kernel（含 backward）" §5.5-5.6):
-non-contiguous dy, one gradient per input, eps as a float, double backward
-raising."""
+non-contiguous dy, one gradient per input, eps as a float, the double
+backward (against the oracle) and a third derivative raising."""
 import pytest
 import torch
 
 import oracle
 from rmsnorm_fwd_bwd_02_gb300 import autograd as A
 from rmsnorm_fwd_bwd_02_gb300 import workloads as W
-from tests.tolerances import check_dw, check_rows, check_rstd  # noqa: F401
+from tests.tolerances import check_bits, check_dw, check_rows, check_rstd  # noqa: F401
 
 DEV = torch.device("cuda:0")
 
@@ -108,14 +108,61 @@ def test_residual_module_grads(orc):
 
 
 @pytest.mark.gpu
-def test_double_backward_raises():
-    H = 128
-    x = torch.randn(64, H, device=DEV, dtype=torch.bfloat16, requires_grad=True)
-    w = torch.ones(H, device=DEV, dtype=torch.bfloat16, requires_grad=True)
-    y = A.rms_norm(x, w)
-    (gx,) = torch.autograd.grad(y.float().sum(), x, create_graph=True)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_double_backward_matches_oracle(orc, dtype):
+    """grad of (sum(ga * dL/dx) + sum(gb * dL/dw)) with respect to x, w and dy,
+    through autograd with create_graph, against the oracle's double
+    backward; a third derivative raises."""
+    M, H = 67, 896
+    g = torch.Generator().manual_seed(21)
+    x = (torch.randn(M, H, generator=g) * 2).to(dtype)
+    w = (1 + 0.1 * torch.randn(H, generator=g)).to(dtype)
+    dy = torch.randn(M, H, generator=g).to(dtype)
+    ga = torch.randn(M, H, generator=g).to(dtype)
+    gb = torch.randn(H, generator=g).to(dtype)
+    xd = x.to(DEV).requires_grad_()
+    wd = w.to(DEV).requires_grad_()
+    dyd = dy.to(DEV).requires_grad_()
+    y = A.rms_norm(xd, wd)
+    gx_, gw_ = torch.autograd.grad(y, (xd, wd), dyd, create_graph=True)
+    l2 = (gx_.float() * ga.to(DEV).float()).sum() + (gw_.float() * gb.to(DEV).float()).sum()
+    d_x, d_w, d_dy = torch.autograd.grad(l2, (xd, wd, dyd), create_graph=True)
+    torch.cuda.synchronize()
+    ddy, dx2, dw2, tddy, tdx2, tdw2 = orc.bwd_bwd(dy, x, w, ga, gb.float(), 1e-6,
+                                                  want_terms=True)
+    check_rows("autograd d(dy)", d_dy, ddy, dtype, tddy)
+    check_rows("autograd d(x)", d_x, dx2, dtype, tdx2)
+    got = d_w.double().cpu()
+    ulp = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -23
+    assert bool(((got - dw2).abs() <= 1e-3 * tdw2 + ulp * dw2.abs() + 1e-30).all())
     with pytest.raises(RuntimeError):
-        gx.float().sum().backward()
+        d_x.float().sum().backward()
+
+
+@pytest.mark.gpu
+def test_residual_double_backward(orc):
+    """The residual module: the second derivative through h and dh_out."""
+    M, H = 33, 896
+    g = torch.Generator().manual_seed(22)
+    x = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    r = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    w = (1 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    dy = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    dh = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    ga = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    xd, rd, wd = (t.to(DEV).requires_grad_() for t in (x, r, w))
+    dyd, dhd = dy.to(DEV).requires_grad_(), dh.to(DEV).requires_grad_()
+    y, h = A.residual_rms_norm(xd, rd, wd)
+    gx_, = torch.autograd.grad((y, h), (xd,), (dyd, dhd), create_graph=True)
+    l2 = (gx_.float() * ga.to(DEV).float()).sum()
+    d_dy, d_dh, d_x, d_r = torch.autograd.grad(l2, (dyd, dhd, xd, rd))
+    torch.cuda.synchronize()
+    oh, _, _ = orc.residual_fwd(x, r, w, 1e-6)
+    ddy, dh2, _, tddy, tdh2, _ = orc.bwd_bwd(dy, oh, w, ga, None, 1e-6, want_terms=True)
+    check_rows("residual d(dy)", d_dy, ddy, torch.bfloat16, tddy)
+    check_bits("residual d(dh_out) = ga", d_dh, ga)
+    check_rows("residual d(x)", d_x, dh2, torch.bfloat16, tdh2)
+    check_rows("residual d(r)", d_r, dh2, torch.bfloat16, tdh2)
 
 
 @pytest.mark.gpu
