@@ -310,8 +310,10 @@ int rmsnorm_last_cuda_error(void);
 void rmsnorm_set_path_override(int path);
 
 /* Which kernel family the last call on this thread used: 1 row-wise
- * vectorised, 2 split-row, 3 row-wise scalar, 4 streamed, 5 norm fused with
- * the GEMV (rmsnorm_gemv_fwd), 0 none. */
+ * vectorised, 2 split-row, 3 row-wise scalar, 4 streamed, 5 and 6 the norm
+ * fused with the GEMV (rmsnorm_gemv_fwd; 5: the weight in registers, 6: the
+ * weight fed by bulk copies, the automatic choice, which override 1 turns
+ * off), 0 none. */
 int rmsnorm_last_path(void);
 
 /*

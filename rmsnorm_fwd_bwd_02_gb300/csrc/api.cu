@@ -17,6 +17,7 @@
 #include "params.h"
 #include "bwd2.cuh"
 #include "gemv.cuh"
+#include "gemv_tma.cuh"
 #include "reduce.cuh"
 #include "registry.h"
 
@@ -25,7 +26,8 @@ using namespace rmsk;
 namespace {
 
 constexpr int kPathAuto = 0, kPathRows = 1, kPathSplit = 2, kPathScalar = 3, kPathStream = 4;
-constexpr int kPathGemv = 5;           // reported only: RMSNorm fused with the GEMV
+constexpr int kPathGemv = 5;           // reported only: RMSNorm fused with the GEMV,
+constexpr int kPathGemvTma = 6;        // A in registers (5) or by bulk copies (6)
 constexpr int kGemvMaxRows = 64;
 constexpr int64_t kGemvMaxSmem = 227 * 1024;
 constexpr int kSplitMaxRows = 64;      // decode-sized batches ([P2 §3.2])
@@ -700,6 +702,54 @@ int bwd2_impl(const void *dy, const void *x, const void *w, const float *rstd, c
 }
 
 // ------------------------------------------------- norm + projection GEMV
+// The bulk-copy fed kernel's plan: tiles per warp, K slice, ring stages,
+// shared memory, or false when it does not fit (the register-fed kernel runs
+// then).
+struct GemvTmaPlan {
+    int TPW, KS, NSW, ctas;
+    bool stage_r;
+    int64_t smem;
+};
+
+bool gemv_tma_plan(int64_t M, int64_t H, int64_t N, bool res, int sms, GemvTmaPlan *pl)
+{
+    const int MT = (int)((M + 15) / 16);
+    const bool half = M <= 8;
+    const int64_t tiles = (N + 7) / 8;
+    for (int sr = res ? 1 : 0; sr >= 0; --sr) {
+        const bool stage_r = sr != 0;
+        const int64_t fixed = gemv_tma_fixed_bytes(MT, half, (int)M, (int)H, stage_r);
+        // Two CTAs per SM with half of its shared memory each when that
+        // leaves room for a ring (one call's CTA and the next call's can then
+        // share an SM), else one CTA per SM with all of it.
+        for (int cps : {2, 1}) {
+            const int64_t budget = cps == 2 ? (kGemvMaxSmem - 2048) / 2 : kGemvMaxSmem;
+            // every warp with a tile, no more CTAs than fit at once
+            int64_t ctas = (tiles + kGemvWarps - 1) / kGemvWarps;
+            if (ctas > (int64_t)cps * sms)
+                ctas = (int64_t)cps * sms;
+            const int64_t TPW = (tiles + kGemvWarps * ctas - 1) / (kGemvWarps * ctas);
+            ctas = (tiles + kGemvWarps * TPW - 1) / (kGemvWarps * TPW);
+            // whole rows first, in as many stages as there are tiles (<= 2)
+            int NSW = TPW < 2 ? 1 : 2;
+            int64_t bytes = gemv_tma_smem_bytes(MT, half, (int)M, (int)H, stage_r, (int)H, NSW);
+            int64_t KS = H;
+            if (bytes > budget) {              // else K slices, double-buffered
+                NSW = 2;
+                const int64_t room = budget - fixed - kGemvWarps * NSW * 8;
+                KS = (room / (kGemvWarps * NSW * 8) - 64) / 2;
+                KS = KS / 32 * 32;
+                if (KS < 64)
+                    continue;
+                bytes = gemv_tma_smem_bytes(MT, half, (int)M, (int)H, stage_r, (int)KS, NSW);
+            }
+            *pl = {(int)TPW, (int)KS, NSW, (int)ctas, stage_r, bytes};
+            return true;
+        }
+    }
+    return false;
+}
+
 int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *out, void *h,
               void *y, float *rstd, int64_t M, int64_t H, int64_t N, float eps, int dtype,
               int flags, cudaStream_t stream)
@@ -708,10 +758,40 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
     const bool half = M <= 8;
     const int ysr = (int)(H * 2 + 64);     // padded: the two rows a quarter-warp reads
                                            // fall in different halves of the banks
-    const void *const(&fns)[3] = gemv_kernels.fn[dtype == RMSNORM_F16 ? 1 : 0][half ? 0 : MT];
+    const int dt = dtype == RMSNORM_F16 ? 1 : 0;
+    const int ti = half ? 0 : MT;
     int dev, sms, st;
     if ((st = current_device(&dev)) || (st = sm_count(dev, &sms)))
         return st;
+    const uint32_t static_w = (flags & RMSNORM_GEMV_STATIC_WEIGHTS) ? 1 : 0;
+    const int ov = g_path_override.load(std::memory_order_relaxed);
+
+    GemvTmaPlan pl;
+    if (ov != kPathRows && gemv_tma_plan(M, H, N, r != nullptr, sms, &pl)) {
+        const void *fn = gemv_tma_kernels.fn[dt][ti][r == nullptr ? 0 : (pl.stage_r ? 2 : 1)];
+        int bps;
+        if ((st = blocks_per_sm(fn, kGemvWarps * 32, dev, &bps, (int)pl.smem)))
+            return st;
+        if (pl.ctas <= bps * sms) {
+            unsigned int *tmo = stream_timeout_counter(dev);
+            if (tmo == nullptr)
+                return cuda_fail(cudaErrorInvalidSymbol);
+            GemvParams p = {x,      r,      w,      A,      out,     h,   y,
+                            rstd,   (int)M, (int)H, (int)N, pl.TPW,  ysr, eps,
+                            (int)static_w, pl.KS, pl.NSW,
+                            g_test_extra_tx.load(std::memory_order_relaxed),
+                            g_test_wait_us.load(std::memory_order_relaxed)};
+            cudaError_t e = launch2(fn, dim3((unsigned)pl.ctas), dim3(kGemvWarps * 32),
+                                    (int)pl.smem, stream, &p, &tmo);
+            if (e != cudaSuccess)
+                return cuda_fail(e);
+            t_last_path = kPathGemvTma;
+            return RMSNORM_OK;
+        }
+    }
+
+    // A in registers: one 8-row tile per CTA at a time
+    const void *const(&fns)[3] = gemv_kernels.fn[dt][ti];
     const int64_t tiles = (N + 7) / 8;
     // Tiles per CTA so that every CTA is resident at once, for a variant.
     auto plan = [&](int variant, int smem, int64_t *tn) {
@@ -735,9 +815,9 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
         return st;
     const void *fn = fns[variant];
     const int64_t grid = (tiles + TN - 1) / TN;
-    GemvParams p = {x,      r,      w,      A,       out, h,   y,
+    GemvParams p = {x,      r,      w,      A,      out,     h,   y,
                     rstd,   (int)M, (int)H, (int)N, (int)TN, ysr, eps,
-                    (flags & RMSNORM_GEMV_STATIC_WEIGHTS) ? 1 : 0};
+                    (int)static_w, 0, 0, 0, 0};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kGemvWarps * 32);

@@ -1,7 +1,9 @@
-// RMSNorm fused with the projection GEMV (gemv.cuh): bf16 and fp16, an
+// RMSNorm fused with the projection GEMV: the register-fed kernel
+// (gemv.cuh) and the bulk-copy fed one (gemv_tma.cuh), bf16 and fp16, an
 // 8-row y tile (M <= 8) or one to four 16-row tiles, with and without the
 // residual add.
 #include "gemv.cuh"
+#include "gemv_tma.cuh"
 #include "registry.h"
 
 namespace rmsk {
@@ -18,5 +20,19 @@ const GemvKernels gemv_kernels = {
       RMSK_GEMV_MT(bf16, 3, false), RMSK_GEMV_MT(bf16, 4, false)},
      {RMSK_GEMV_MT(f16, 1, true), RMSK_GEMV_MT(f16, 1, false), RMSK_GEMV_MT(f16, 2, false),
       RMSK_GEMV_MT(f16, 3, false), RMSK_GEMV_MT(f16, 4, false)}}};
+
+#define RMSK_GEMV_TMA_MT(T, MT, HALF)                              \
+    {(const void *)&rms_gemv_tma<T, MT, HALF, false, false>,       \
+     (const void *)&rms_gemv_tma<T, MT, HALF, true, false>,        \
+     (const void *)&rms_gemv_tma<T, MT, HALF, true, true>}
+
+// the bulk-copy fed variants, same indexing
+const GemvKernels gemv_tma_kernels = {
+    {{RMSK_GEMV_TMA_MT(bf16, 1, true), RMSK_GEMV_TMA_MT(bf16, 1, false),
+      RMSK_GEMV_TMA_MT(bf16, 2, false), RMSK_GEMV_TMA_MT(bf16, 3, false),
+      RMSK_GEMV_TMA_MT(bf16, 4, false)},
+     {RMSK_GEMV_TMA_MT(f16, 1, true), RMSK_GEMV_TMA_MT(f16, 1, false),
+      RMSK_GEMV_TMA_MT(f16, 2, false), RMSK_GEMV_TMA_MT(f16, 3, false),
+      RMSK_GEMV_TMA_MT(f16, 4, false)}}};
 
 } // namespace rmsk

@@ -56,11 +56,16 @@ struct GemvParams {
     void *y;          // [M,H] stored norm output, or nullptr
     float *rstd;      // [M] or nullptr
     int M, H, N;
-    int TN;           // 8-row tiles of A per CTA
+    int TN;           // 8-row tiles of A per CTA (rms_gemv) or per warp (rms_gemv_tma)
     int ysr;          // shared-memory row stride of y in bytes
     float eps;
     int static_w;     // w and A are not written by work in flight before this
                       // kernel: they may be read before griddep_wait
+    // rms_gemv_tma only: columns of A per ring stage, stages per warp, and
+    // the test hook of the bounded waits (extra bytes a stage waits for,
+    // wait limit in microseconds, 0 = about one second)
+    int KS, NSW;
+    uint32_t extra_tx, wait_limit_us;
 };
 
 template <typename T> struct MmaOp;

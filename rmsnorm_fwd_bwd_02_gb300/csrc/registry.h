@@ -96,7 +96,8 @@ extern const Bwd2Kernel b2_f_g32, b2_f_g128, b2_f_g512, b2_f_s1024;
 struct GemvKernels {
     const void *fn[2][5][3];
 };
-extern const GemvKernels gemv_kernels;
+extern const GemvKernels gemv_kernels;       // A in registers (gemv.cuh)
+extern const GemvKernels gemv_tma_kernels;   // A by bulk copies (gemv_tma.cuh)
 // Device address of the counter of streamed-kernel waits that ran out.
 unsigned int *stream_timeout_counter(int dev);
 

@@ -8,7 +8,9 @@ y the norm's output as the separate norm would store it. Compared element
 by element on every output (out, h, y, rstd) over dtypes, row counts that
 fill one to four 16-row MMA tiles (and leave them ragged), feature counts,
 output counts that leave the last 8-row tile of A ragged, with and without
-the residual add.
+the residual add, for both kernels: the weight in registers (gemv.cuh,
+forced with the row-wise path override) and the weight fed by bulk copies
+(gemv_tma.cuh, the automatic choice).
 """
 import pytest
 import torch
@@ -21,6 +23,7 @@ from tests.tolerances import check_bits, check_rows, check_rstd
 pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
+KERNELS = {"regs": rn.PATH_ROWS, "tma": rn.PATH_AUTO}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -48,16 +51,24 @@ def synth(M, H, N, dtype, seed, residual):
     return {k: v.to(dtype).contiguous() for k, v in d.items()}
 
 
-def run(inp, residual, eps=1e-6, want_y=True, static=False):
+def run(inp, residual, eps=1e-6, want_y=True, static=False, kernel="tma"):
     g = {k: v.to(DEV) for k, v in inp.items()}
     torch.cuda.synchronize()             # the weights are in place before the call
     M, H = g["x"].shape
     y = torch.empty(M, H, device=DEV, dtype=g["x"].dtype) if want_y else None
     rstd = torch.empty(M, device=DEV)
-    out, h, _ = rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"],
-                                    r=g["r"] if residual else None, y=y,
-                                    rstd=rstd, eps=eps, static_weights=static)
-    assert rn.last_path() == rn.PATH_GEMV
+    rn.set_path_override(KERNELS[kernel])
+    try:
+        out, h, _ = rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"],
+                                        r=g["r"] if residual else None, y=y,
+                                        rstd=rstd, eps=eps, static_weights=static)
+        path = rn.last_path()
+    finally:
+        rn.set_path_override(rn.PATH_AUTO)
+    # the automatic choice takes the bulk-copy kernel where its ring fits in
+    # shared memory beside y, and the register kernel otherwise
+    assert path == rn.PATH_GEMV if kernel == "regs" else path in (rn.PATH_GEMV,
+                                                                   rn.PATH_GEMV_TMA), path
     torch.cuda.synchronize()
     return {"out": out, "h": h, "y": y, "rstd": rstd}
 
@@ -83,30 +94,34 @@ def compare(name, got, o, dtype):
         check_bits(f"{name} h", got["h"], o["h"])
 
 
+@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
 @pytest.mark.parametrize("M", [1, 7, 16, 17, 33, 64])
 @pytest.mark.parametrize("H,N", [(128, 1), (128, 9), (896, 1024), (896, 2051),
-                                 (1024, 13), (1664, 64)])
-def test_gemv_matches_oracle(orc, dtype, M, H, N):
+                                 (1024, 13), (1664, 64), (896, 9728)])
+def test_gemv_matches_oracle(orc, kernel, dtype, M, H, N):
     for residual in (False, True):
         inp = synth(M, H, N, dtype, seed=M * 7 + H + N, residual=residual)
         o = oracle_all(orc, inp, residual)
         for static in (False, True):
-            got = run(inp, residual, static=static)
-            compare(f"{dtype} M={M} H={H} N={N} res={residual} static={static}",
+            got = run(inp, residual, static=static, kernel=kernel)
+            compare(f"{kernel} {dtype} M={M} H={H} N={N} res={residual} static={static}",
                     got, o, dtype)
 
 
+@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("H,M", [(4096, 16), (6720, 1), (6720, 16), (3424, 32),
                                  (2272, 48), (1664, 64)])
-def test_gemv_largest_shared_memory(orc, H, M):
+def test_gemv_largest_shared_memory(orc, kernel, H, M):
     """The largest y tile each row count allows (up to 227 KB of shared
-    memory), after smaller calls of the same kernels have run."""
+    memory), after smaller calls of the same kernels have run; for the
+    bulk-copy kernel, K is then streamed in slices."""
     small = synth(M, 128, 8, torch.bfloat16, seed=1, residual=False)
-    run(small, False)
-    inp = synth(M, H, 24, torch.bfloat16, seed=H, residual=True)
+    run(small, False, kernel=kernel)
+    inp = synth(M, H, 200, torch.bfloat16, seed=H, residual=True)
     o = oracle_all(orc, inp, True)
-    compare(f"large H={H} M={M}", run(inp, True), o, torch.bfloat16)
+    compare(f"large {kernel} H={H} M={M}", run(inp, True, kernel=kernel), o,
+            torch.bfloat16)
 
 
 @pytest.mark.parametrize("name", ["decode-qkv-m1", "decode-gateup-m1"])
@@ -114,14 +129,27 @@ def test_decode_workloads_full(orc, name):
     wl = W.WORKLOADS[name]
     inp = W.make_inputs(wl)
     o = oracle_all(orc, inp, True, wl.eps)
-    got = run(inp, True, eps=wl.eps, static=True)
-    compare(name, got, o, wl.dtype)
+    for kernel in KERNELS:
+        got = run(inp, True, eps=wl.eps, static=True, kernel=kernel)
+        compare(f"{name} {kernel}", got, o, wl.dtype)
     # the same at 8 and 64 decode rows
     for M in (8, 64):
         wm = wl.with_rows(M)
         im = W.make_inputs(wm)
         om = oracle_all(orc, im, True, wm.eps)
-        compare(f"{name} M={M}", run(im, True, eps=wm.eps), om, wm.dtype)
+        for kernel in KERNELS:
+            compare(f"{name} M={M} {kernel}", run(im, True, eps=wm.eps, kernel=kernel),
+                    om, wm.dtype)
+
+
+def test_automatic_choice_is_the_bulk_copy_kernel_for_decode_shapes():
+    for M, H, N in ((1, 896, 2048), (8, 896, 9728), (64, 896, 2048), (16, 4096, 6144),
+                    (1, 6720, 64)):
+        inp = synth(M, H, N, torch.bfloat16, seed=2, residual=True)
+        g = {k: v.to(DEV) for k, v in inp.items()}
+        rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"])
+        assert rn.last_path() == rn.PATH_GEMV_TMA, (M, H, N)
+    torch.cuda.synchronize()
 
 
 def test_y_matches_the_unfused_norm():
@@ -148,6 +176,10 @@ def test_deterministic_and_optional_outputs(orc):
     for k in ("out", "h", "y", "rstd"):
         check_bits(f"run-to-run {k}", a[k], b[k])
         check_bits(f"static weights {k}", c[k], a[k])
+    # both kernels: the same y, h and rstd bits (same norm arithmetic)
+    d = run(inp, True, kernel="regs")
+    for k in ("h", "y", "rstd"):
+        check_bits(f"regs vs tma {k}", d[k], a[k])
     # no y, no h, no rstd: out unchanged
     g = {k: v.to(DEV) for k, v in inp.items()}
     out, h, rstd = rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], want_h=False)
@@ -240,3 +272,21 @@ def test_error_returns():
     assert call(r=x, h=x) == -9              # h over x (every CTA reads x)
     assert call(M=0) == 0
     torch.cuda.synchronize()
+
+
+def test_gemv_wait_runs_out_and_context_survives(orc):
+    """Every bulk-copy wait of the weight ring runs out (each stage expects 16
+    bytes that no copy delivers, 20 ms limit): the kernel records it, drains
+    its copies and ends, and the next normal call is right."""
+    inp = synth(3, 896, 1024, torch.bfloat16, seed=4, residual=True)
+    rn.wait_timeouts(reset=True)
+    rn.set_stream_test_fault(16, 20000)
+    try:
+        run(inp, True)                   # results incomplete by design
+        torch.cuda.synchronize()
+    finally:
+        rn.set_stream_test_fault(0, 0)
+    assert rn.wait_timeouts(reset=True) > 0
+    o = oracle_all(orc, inp, True)
+    compare("after timeouts", run(inp, True), o, torch.bfloat16)
+    assert rn.wait_timeouts() == 0
