@@ -706,7 +706,7 @@ int bwd2_impl(const void *dy, const void *x, const void *w, const float *rstd, c
 // shared memory, or false when it does not fit (the register-fed kernel runs
 // then).
 struct GemvTmaPlan {
-    int TPW, KS, NSW, ctas;
+    int TPW, KS, NSW, ctas, CS;
     bool stage_r;
     int64_t smem;
 };
@@ -715,10 +715,11 @@ bool gemv_tma_plan(int64_t M, int64_t H, int64_t N, bool res, int sms, GemvTmaPl
 {
     const int MT = (int)((M + 15) / 16);
     const bool half = M <= 8;
+    const int CS = MT > 1 ? kGemvCluster : 1;     // the norm shared by a cluster
     const int64_t tiles = (N + 7) / 8;
     for (int sr = res ? 1 : 0; sr >= 0; --sr) {
         const bool stage_r = sr != 0;
-        const int64_t fixed = gemv_tma_fixed_bytes(MT, half, (int)M, (int)H, stage_r);
+        const int64_t fixed = gemv_tma_fixed_bytes(MT, half, (int)M, (int)H, stage_r, CS);
         // Two CTAs per SM with half of its shared memory each when that
         // leaves room for a ring (one call's CTA and the next call's can then
         // share an SM), else one CTA per SM with all of it.
@@ -730,9 +731,11 @@ bool gemv_tma_plan(int64_t M, int64_t H, int64_t N, bool res, int sms, GemvTmaPl
                 ctas = (int64_t)cps * sms;
             const int64_t TPW = (tiles + kGemvWarps * ctas - 1) / (kGemvWarps * ctas);
             ctas = (tiles + kGemvWarps * TPW - 1) / (kGemvWarps * TPW);
+            ctas = (ctas + CS - 1) / CS * CS;        // whole clusters
             // whole rows first, in as many stages as there are tiles (<= 2)
             int NSW = TPW < 2 ? 1 : 2;
-            int64_t bytes = gemv_tma_smem_bytes(MT, half, (int)M, (int)H, stage_r, (int)H, NSW);
+            int64_t bytes =
+                gemv_tma_smem_bytes(MT, half, (int)M, (int)H, stage_r, CS, (int)H, NSW);
             int64_t KS = H;
             if (bytes > budget) {              // else K slices, double-buffered
                 NSW = 2;
@@ -741,9 +744,9 @@ bool gemv_tma_plan(int64_t M, int64_t H, int64_t N, bool res, int sms, GemvTmaPl
                 KS = KS / 32 * 32;
                 if (KS < 64)
                     continue;
-                bytes = gemv_tma_smem_bytes(MT, half, (int)M, (int)H, stage_r, (int)KS, NSW);
+                bytes = gemv_tma_smem_bytes(MT, half, (int)M, (int)H, stage_r, CS, (int)KS, NSW);
             }
-            *pl = {(int)TPW, (int)KS, NSW, (int)ctas, stage_r, bytes};
+            *pl = {(int)TPW, (int)KS, NSW, (int)ctas, CS, stage_r, bytes};
             return true;
         }
     }
@@ -781,8 +784,22 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
                             (int)static_w, pl.KS, pl.NSW,
                             g_test_extra_tx.load(std::memory_order_relaxed),
                             g_test_wait_us.load(std::memory_order_relaxed)};
-            cudaError_t e = launch2(fn, dim3((unsigned)pl.ctas), dim3(kGemvWarps * 32),
-                                    (int)pl.smem, stream, &p, &tmo);
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)pl.ctas);
+            cfg.blockDim = dim3(kGemvWarps * 32);
+            cfg.dynamicSmemBytes = (size_t)pl.smem;
+            cfg.stream = stream;
+            cudaLaunchAttribute attrs[2];
+            attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attrs[0].val.programmaticStreamSerializationAllowed = 1;
+            attrs[1].id = cudaLaunchAttributeClusterDimension;
+            attrs[1].val.clusterDim.x = (unsigned)pl.CS;
+            attrs[1].val.clusterDim.y = 1;
+            attrs[1].val.clusterDim.z = 1;
+            cfg.attrs = attrs;
+            cfg.numAttrs = pl.CS > 1 ? 2 : 1;
+            void *args[2] = {&p, &tmo};
+            cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
             if (e != cudaSuccess)
                 return cuda_fail(e);
             t_last_path = kPathGemvTma;

@@ -21,18 +21,21 @@ const GemvKernels gemv_kernels = {
      {RMSK_GEMV_MT(f16, 1, true), RMSK_GEMV_MT(f16, 1, false), RMSK_GEMV_MT(f16, 2, false),
       RMSK_GEMV_MT(f16, 3, false), RMSK_GEMV_MT(f16, 4, false)}}};
 
-#define RMSK_GEMV_TMA_MT(T, MT, HALF)                              \
-    {(const void *)&rms_gemv_tma<T, MT, HALF, false, false>,       \
-     (const void *)&rms_gemv_tma<T, MT, HALF, true, false>,        \
-     (const void *)&rms_gemv_tma<T, MT, HALF, true, true>}
+#define RMSK_GEMV_TMA_MT(T, MT, HALF, CS)                          \
+    {(const void *)&rms_gemv_tma<T, MT, HALF, false, false, CS>,   \
+     (const void *)&rms_gemv_tma<T, MT, HALF, true, false, CS>,    \
+     (const void *)&rms_gemv_tma<T, MT, HALF, true, true, CS>}
 
-// the bulk-copy fed variants, same indexing
+// the bulk-copy fed variants, same indexing; above 16 rows the norm is
+// shared by a cluster of kGemvCluster CTAs
 const GemvKernels gemv_tma_kernels = {
-    {{RMSK_GEMV_TMA_MT(bf16, 1, true), RMSK_GEMV_TMA_MT(bf16, 1, false),
-      RMSK_GEMV_TMA_MT(bf16, 2, false), RMSK_GEMV_TMA_MT(bf16, 3, false),
-      RMSK_GEMV_TMA_MT(bf16, 4, false)},
-     {RMSK_GEMV_TMA_MT(f16, 1, true), RMSK_GEMV_TMA_MT(f16, 1, false),
-      RMSK_GEMV_TMA_MT(f16, 2, false), RMSK_GEMV_TMA_MT(f16, 3, false),
-      RMSK_GEMV_TMA_MT(f16, 4, false)}}};
+    {{RMSK_GEMV_TMA_MT(bf16, 1, true, 1), RMSK_GEMV_TMA_MT(bf16, 1, false, 1),
+      RMSK_GEMV_TMA_MT(bf16, 2, false, kGemvCluster),
+      RMSK_GEMV_TMA_MT(bf16, 3, false, kGemvCluster),
+      RMSK_GEMV_TMA_MT(bf16, 4, false, kGemvCluster)},
+     {RMSK_GEMV_TMA_MT(f16, 1, true, 1), RMSK_GEMV_TMA_MT(f16, 1, false, 1),
+      RMSK_GEMV_TMA_MT(f16, 2, false, kGemvCluster),
+      RMSK_GEMV_TMA_MT(f16, 3, false, kGemvCluster),
+      RMSK_GEMV_TMA_MT(f16, 4, false, kGemvCluster)}}};
 
 } // namespace rmsk

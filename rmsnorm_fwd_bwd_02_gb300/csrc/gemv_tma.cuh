@@ -28,12 +28,37 @@
 //  4. A wait that runs out (about one second, or the test limit) counts in
 //     the device counter of streamed-kernel timeouts; the warp then waits,
 //     bounded again, for its copies still in flight and stops.
+//
+// Many rows (CS > 1): the CTAs of a thread-block cluster of CS share the
+// norm. Rank p stages, normalises and stores rows p, p + CS, ... and writes
+// each finished y pack into its own shared memory and, through distributed
+// shared memory, into every other CTA's of the cluster; one cluster barrier
+// (release / acquire) then gives every CTA all of y. A first barrier phase,
+// arrived at the start and waited on before the norm, makes sure every CTA
+// of the cluster runs before its shared memory is written. Nothing touches
+// another CTA's shared memory after the second barrier.
+
+// 16 bytes into the shared memory of CTA `rank` of the cluster, at the
+// offset `local` has in this CTA.
+__device__ __forceinline__ void st_cluster_v4(const void *local, uint32_t rank, uint4 v)
+{
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(ra), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
 #pragma once
 
 #include "gemv.cuh"
+#include "split.cuh"
 #include "stream.cuh"
 
 namespace rmsk {
+
+// CTAs of the cluster that share the norm when M > 16.
+constexpr int kGemvCluster = 8;
 
 // A ring stage: 8 rows of KS columns, each row padded by 64 bytes so that
 // the rows a quarter-warp reads fall in different halves of the banks.
@@ -42,20 +67,23 @@ __host__ __device__ constexpr int gemv_tma_stage_bytes(int KS) { return 8 * gemv
 
 // Bytes of the CTA's fixed shared memory (y, r, w, partial sums), then the
 // rings, then the mbarriers.
+// (With a cluster of CS, a CTA stages the r rows of its own (M + CS - 1) / CS
+// rows only.)
 __host__ __device__ constexpr int64_t gemv_tma_fixed_bytes(int MT, bool half, int M, int H,
-                                                           bool stage_r)
+                                                           bool stage_r, int CS)
 {
-    return (int64_t)gemv_y_rows(MT, half) * (2 * H + 64) + (stage_r ? (int64_t)M * 2 * H : 0) +
-           2 * H + 16;
+    return (int64_t)gemv_y_rows(MT, half) * (2 * H + 64) +
+           (stage_r ? (int64_t)((M + CS - 1) / CS) * 2 * H : 0) + 2 * H + 16;
 }
 __host__ __device__ constexpr int64_t gemv_tma_smem_bytes(int MT, bool half, int M, int H,
-                                                          bool stage_r, int KS, int NSW)
+                                                          bool stage_r, int CS, int KS,
+                                                          int NSW)
 {
-    return gemv_tma_fixed_bytes(MT, half, M, H, stage_r) +
+    return gemv_tma_fixed_bytes(MT, half, M, H, stage_r, CS) +
            (int64_t)kGemvWarps * NSW * gemv_tma_stage_bytes(KS) + kGemvWarps * NSW * 8;
 }
 
-template <typename T, int MT, bool HALF, bool RES, bool STAGER>
+template <typename T, int MT, bool HALF, bool RES, bool STAGER, int CS>
 __global__ void __launch_bounds__(kGemvWarps * 32)
 rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
 {
@@ -68,8 +96,10 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
     extern __shared__ __align__(128) unsigned char smem[];
     const int rbytes = 2 * p.H;
     unsigned char *ys = smem;                                      // [kYRows][ysr]
-    unsigned char *rsm = ys + kYRows * p.ysr;                      // [M][2H] if STAGER
-    unsigned char *wsm = rsm + (STAGER ? p.M * rbytes : 0);        // [2H]
+    const uint32_t rank = CS > 1 ? cluster_ctarank() : 0;
+    const int Mo = (p.M + CS - 1) / CS;                            // rows per rank
+    unsigned char *rsm = ys + kYRows * p.ysr;                      // [Mo][2H] if STAGER
+    unsigned char *wsm = rsm + (STAGER ? Mo * rbytes : 0);         // [2H]
     float *part = reinterpret_cast<float *>(wsm + rbytes);         // [4]
     const int stage_bytes = gemv_tma_stage_bytes(p.KS), asr = gemv_tma_row_bytes(p.KS);
     unsigned char *ring = reinterpret_cast<unsigned char *>(part + 4);   // [4][NSW][8][KS]
@@ -112,6 +142,10 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
             mbar_init(mybar + 8 * s, 1);
     mbar_init_fence();
     __syncwarp();
+    // A CTA's shared memory may be written by its peers only once every CTA
+    // of the cluster runs: arrive now, wait before the first such write.
+    if constexpr (CS > 1)
+        cluster_arrive_release();
     auto prologue = [&]() {
         if (lane == 0) {
             fence_proxy_async_smem();
@@ -132,12 +166,17 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
             cp_async16(wsm + j * 16, static_cast<const uint4 *>(p.w) + j);
     }
 
-    // 2. x (and r) into shared memory; the norm of every row, in place
-    for (int e = tid; e < p.M * NP; e += kGemvWarps * 32) {
-        const int m = e / NP, j = e - m * NP;
-        cp_async16(ys + m * p.ysr + j * 16, static_cast<const uint4 *>(p.x) + e);
+    // 2. x (and r) of this CTA's rows into shared memory; the norm of every
+    //    row, in place (row i of this rank is row rank + i CS)
+    for (int e = tid; e < Mo * NP; e += kGemvWarps * 32) {
+        const int i = e / NP, j = e - i * NP;
+        const int m = (int)rank + i * CS;
+        if (m >= p.M)
+            continue;
+        const int64_t src = (int64_t)m * NP + j;
+        cp_async16(ys + m * p.ysr + j * 16, static_cast<const uint4 *>(p.x) + src);
         if constexpr (STAGER)
-            cp_async16(rsm + m * rbytes + j * 16, static_cast<const uint4 *>(p.r) + e);
+            cp_async16(rsm + i * rbytes + j * 16, static_cast<const uint4 *>(p.r) + src);
     }
     for (int e = p.M * NP + tid; e < kYRows * NP; e += kGemvWarps * 32) {
         const int m = e / NP, j = e - m * NP;     // padding rows of y: zero
@@ -150,13 +189,17 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
     cp_async_wait_all();
     __syncthreads();
 
-    const bool writer = blockIdx.x == 0;
+    if constexpr (CS > 1)
+        cluster_wait_acquire();
+    // the first cluster (or CTA) writes h, y and rstd of the rows it owns
+    const bool writer = blockIdx.x < CS;
     int Mp = 1;
-    while (Mp < p.M)
+    while (Mp < Mo)
         Mp <<= 1;
     const int TPR = kGemvWarps * 32 / Mp;
-    const int m = tid / TPR, sub = tid % TPR;
-    const bool row_ok = m < p.M;
+    const int i_own = tid / TPR, sub = tid % TPR;
+    const int m = (int)rank + i_own * CS;
+    const bool row_ok = i_own < Mo && m < p.M;
     unsigned char *yrow = ys + m * p.ysr;
     const int64_t rb = (int64_t)m * NP;
     F acc = splat<F>(0.f);
@@ -175,7 +218,7 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
                     xv.widen(a);
                     if constexpr (STAGER) {
                         P rv;
-                        rv.u = lds_v4(rsm + m * rbytes + j * 16);
+                        rv.u = lds_v4(rsm + i_own * rbytes + j * 16);
                         rv.widen(b);
                     } else {
                         P::load_cached(p.r, rb + j).widen(b);
@@ -202,7 +245,7 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
         if (lane == 0)
             part[warp] = ss;
         __syncthreads();
-        const int w0 = m * (TPR / 32);
+        const int w0 = i_own * (TPR / 32);
         ss = 0.f;
         for (int v = 0; v < TPR / 32; ++v)
             ss += part[w0 + v];
@@ -229,12 +272,23 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
                     a.v[i] = vmul(vmul(a.v[i], r2), wv.v[i]);
                 const P yv = P::narrow(a);
                 *reinterpret_cast<uint4 *>(yrow + j * 16) = yv.u;
+                if constexpr (CS > 1) {
+#pragma unroll
+                    for (int d = 1; d < CS; ++d)
+                        st_cluster_v4(yrow + j * 16, (rank + d) % CS, yv.u);
+                }
                 if (writer && p.y != nullptr)
                     yv.store(p.y, rb + j);
             }
         }
     }
-    __syncthreads();
+    if constexpr (CS > 1) {
+        // every CTA of the cluster has written its rows everywhere
+        cluster_arrive_release();
+        cluster_wait_acquire();
+    } else {
+        __syncthreads();
+    }
     // every input but A is read: the next kernel may be scheduled
     griddep_launch_dependents();
 
