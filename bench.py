@@ -546,15 +546,17 @@ def run_ours(args, wl):
                 "avg_ms": round(ms, 5),
                 "frac_of_nominal_8TBs": round(a / NOMINAL_HBM_GBS, 4)}
 
-    fam = {1: "rows", 2: "split", 3: "rows, scalar", 4: "stream", 5: "gemv"}
+    fam = {1: "rows", 2: "split", 3: "rows, scalar", 4: "stream", 5: "gemv", 6: "gemv_tma"}
     fwd_api = "rmsnorm_bwd_bwd" if wl.double_backward else \
         "rmsnorm_gemv_fwd" if wl.N else "rmsnorm_fwd_strided" if wl.ld else (
             "rmsnorm_residual_fwd" if wl.residual else "rmsnorm_fwd")
     bwd_api = "rmsnorm_bwd_strided" if wl.ld else (
         "rmsnorm_residual_bwd" if wl.residual else "rmsnorm_bwd")
-    fwd_kernel = fwd_api + (" (rms_gemv)" if wl.N else
-                            " (rms_bwd2_rows + dw_reduce)" if wl.double_backward else
-                            f" (rms_fwd_{fam.get(path_f, 'rows').split(',')[0]})")
+    fwd_kernel = fwd_api + (
+        (" (rms_gemv_tma)" if path_f == 6 else " (rms_gemv)") if wl.N else
+        f" (rms_bwd2_{fam.get(path_f, 'rows').split(',')[0]} + dw_reduce)"
+        if wl.double_backward else
+        f" (rms_fwd_{fam.get(path_f, 'rows').split(',')[0]})")
     bwd_kernel = bwd_api + \
         f" (rms_bwd_{fam.get(path_b, 'rows').split(',')[0]} + dw_reduce)"
     roofline = roof(dom_bytes, dom_ms, bwd_kernel if dom_is_bwd else fwd_kernel)

@@ -619,15 +619,48 @@ const Bwd2Kernel &pick_bwd2(int dtype, int64_t H, bool vec)
     return k.g512;
 }
 
-// Grid of the double backward (and so its partial-row count).
-int bwd2_grid(int dtype, int64_t M, int64_t H, bool vec, const Bwd2Kernel **k, int64_t *grid)
+// The double backward's kernel and grid (and so its partial-row count):
+// streamed for the 16-bit feature counts with a streamed layout unless the
+// row-wise family is forced, row-wise otherwise.
+struct Bwd2Plan {
+    const void *fn;
+    int threads, smem;
+    int64_t grid;
+    bool stream;
+    unsigned int *timeouts;
+};
+
+int bwd2_plan(int dtype, int64_t M, int64_t H, bool vec, bool have_rstd, int ov, Bwd2Plan *pl)
 {
-    *k = &pick_bwd2(dtype, H, vec);
+    const StreamPolicy *sp = pick_stream(dtype, H, vec, true);
+    pl->timeouts = nullptr;
+    if (sp && sp->k->bwd2[0] != nullptr && (ov == kPathAuto || ov == kPathStream)) {
+        const StreamKernels &k = *sp->k;
+        pl->fn = k.bwd2[have_rstd ? 1 : 0];
+        pl->threads = k.b.threads();
+        pl->smem = k.bwd2_smem[have_rstd ? 1 : 0];
+        pl->stream = true;
+        if (M == 0) {
+            pl->grid = 0;
+            return RMSNORM_OK;
+        }
+        int dev;
+        int st = stream_grid(k.b, pl->fn, pl->smem, M, &pl->grid, &dev);
+        if (st)
+            return st;
+        pl->timeouts = stream_timeout_counter(dev);
+        return pl->timeouts ? RMSNORM_OK : cuda_fail(cudaErrorInvalidSymbol);
+    }
+    const Bwd2Kernel &k = pick_bwd2(dtype, H, vec);
+    pl->fn = k.fn;
+    pl->threads = k.s.threads();
+    pl->smem = 0;
+    pl->stream = false;
     if (M == 0) {
-        *grid = 0;
+        pl->grid = 0;
         return RMSNORM_OK;
     }
-    return rows_grid((*k)->s, (*k)->fn, M, grid);
+    return rows_grid(k.s, k.fn, M, &pl->grid);
 }
 
 int bwd2_impl(const void *dy, const void *x, const void *w, const float *rstd, const void *gx,
@@ -661,10 +694,10 @@ int bwd2_impl(const void *dy, const void *x, const void *w, const float *rstd, c
                        aligned(w, 16) && aligned(gx, 16) && aligned(ddy, 16) && aligned(dx2, 16);
     const int ov = g_path_override.load(std::memory_order_relaxed);
     const bool vec = vec16 && ov != kPathScalar;
-    const Bwd2Kernel *k;
-    int64_t grid;
-    if ((st = bwd2_grid(dtype, M, H, vec, &k, &grid)))
+    Bwd2Plan pl;
+    if ((st = bwd2_plan(dtype, M, H, vec, rstd != nullptr, ov, &pl)))
         return st;
+    const int64_t grid = pl.grid;
     const size_t need = (size_t)grid * (size_t)H * sizeof(float);
     if (need > 0 && (ws == nullptr || ws_bytes < need))
         return RMSNORM_ERR_WORKSPACE;
@@ -675,9 +708,16 @@ int bwd2_impl(const void *dy, const void *x, const void *w, const float *rstd, c
 
     if (M > 0) {
         Bwd2Params p = {dy, x, w, rstd, gx, gw, ddy, dx2, static_cast<float *>(ws), M,
-                        (int)H, eps};
-        cudaError_t e = launch(k->fn, dim3((unsigned)grid), dim3(k->s.threads()), stream, &p,
-                               true, 0);
+                        (int)H, eps, 0, 0};
+        cudaError_t e;
+        if (pl.stream) {
+            p.extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
+            p.wait_limit_us = g_test_wait_us.load(std::memory_order_relaxed);
+            e = launch2(pl.fn, dim3((unsigned)grid), dim3(pl.threads), pl.smem, stream, &p,
+                        &pl.timeouts);
+        } else {
+            e = launch(pl.fn, dim3((unsigned)grid), dim3(pl.threads), stream, &p, true, 0);
+        }
         if (e != cudaSuccess)
             return cuda_fail(e);
     }
@@ -697,7 +737,7 @@ int bwd2_impl(const void *dy, const void *x, const void *w, const float *rstd, c
         &cfg, (const void *)&dw_reduce<kReduceCols, kReduceRows>, args);
     if (e != cudaSuccess)
         return cuda_fail(e);
-    t_last_path = M == 0 ? 0 : (vec ? kPathRows : kPathScalar);
+    t_last_path = M == 0 ? 0 : (pl.stream ? kPathStream : (vec ? kPathRows : kPathScalar));
     return RMSNORM_OK;
 }
 
@@ -990,14 +1030,15 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t M, int64_t H, int dtype)
                     const size_t need = (size_t)pl.grid * (size_t)H * sizeof(float);
                     most = need > most ? need : most;
                 }
-    for (int vec = 0; vec < 2; ++vec) {       // the double backward's grid too
-        const Bwd2Kernel *k;
-        int64_t grid;
-        if (bwd2_grid(dtype, M, H, vec != 0, &k, &grid) != RMSNORM_OK)
-            return 0;
-        const size_t need = (size_t)grid * (size_t)H * sizeof(float);
-        most = need > most ? need : most;
-    }
+    for (int ov : {kPathAuto, kPathRows})     // the double backward's grids too
+        for (int vec = 0; vec < 2; ++vec)
+            for (int hr = 0; hr < 2; ++hr) {
+                Bwd2Plan pl;
+                if (bwd2_plan(dtype, M, H, vec != 0, hr != 0, ov, &pl) != RMSNORM_OK)
+                    return 0;
+                const size_t need = (size_t)pl.grid * (size_t)H * sizeof(float);
+                most = need > most ? need : most;
+            }
     return most;
 }
 

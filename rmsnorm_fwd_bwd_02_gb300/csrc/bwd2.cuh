@@ -22,21 +22,6 @@
 
 namespace rmsk {
 
-struct Bwd2Params {
-    const void *dy;     // [M,H]
-    const void *x;      // [M,H] (h for the residual variant)
-    const void *w;      // [H]
-    const float *rstd;  // [M] or nullptr (recompute)
-    const void *gx;     // [M,H] gradient arriving on dx, or nullptr (zero)
-    const float *gw;    // [H] gradient arriving on dw, or nullptr (zero)
-    void *ddy;          // [M,H]
-    void *dx2;          // [M,H]
-    float *part;        // [gridDim.x, H] fp32 partial rows of dw2
-    int64_t M;
-    int H;
-    float eps;
-};
-
 template <typename T, int E, int L, int V, int S, int MINB, bool EXACT>
 __global__ void __launch_bounds__(L * S, MINB)
 rms_bwd2_rows(const Bwd2Params p)

@@ -44,6 +44,24 @@ struct BwdParams {
     uint32_t wait_limit_us;
 };
 
+// Double backward (bwd2.cuh, stream.cuh).
+struct Bwd2Params {
+    const void *dy;     // [M,H]
+    const void *x;      // [M,H] (h for the residual variant)
+    const void *w;      // [H]
+    const float *rstd;  // [M] or nullptr (recompute)
+    const void *gx;     // [M,H] gradient arriving on dx, or nullptr (zero)
+    const float *gw;    // [H] gradient arriving on dw, or nullptr (zero)
+    void *ddy;          // [M,H]
+    void *dx2;          // [M,H]
+    float *part;        // [gridDim.x, H] fp32 partial rows of dw2
+    int64_t M;
+    int H;
+    float eps;
+    uint32_t extra_tx;       // streamed kernel only, as in FwdParams
+    uint32_t wait_limit_us;
+};
+
 // Split-row forward (split.cuh).
 struct SplitParams {
     const void *x;   // [M,H]

@@ -49,6 +49,8 @@ struct StreamKernels {
     int fwd_smem[2];
     const void *bwd[2][2];     // [dh_out given][rstd given]
     int bwd_smem[2][2];
+    const void *bwd2[2];       // double backward [rstd given], or nullptr
+    int bwd2_smem[2];
 };
 
 struct SplitKernels {
@@ -133,7 +135,11 @@ unsigned int *stream_timeout_counter(int dev);
         {{StreamSmem<BGW, BV, BNG, BNS, 2, 2>::kBytes,                                   \
           StreamSmem<BGW, BV, BNG, BNS, 2, 1>::kBytes},                                  \
          {StreamSmem<BGW, BV, BNG, BNS, 3, 2>::kBytes,                                   \
-          StreamSmem<BGW, BV, BNG, BNS, 3, 1>::kBytes}}};
+          StreamSmem<BGW, BV, BNG, BNS, 3, 1>::kBytes}},                                 \
+        {(const void *)&rms_bwd2_stream<T, BGW, BV, BNG, BNS, false>,                    \
+         (const void *)&rms_bwd2_stream<T, BGW, BV, BNG, BNS, true>},                    \
+        {StreamSmem<BGW, BV, BNG, BNS, 3, 5>::kBytes,                                    \
+         StreamSmem<BGW, BV, BNG, BNS, 3, 4>::kBytes}};
 
 // Short rows (stream_small.cuh): H = 8 * NVP, NW warps, RPT rows per lane per stage.
 // T is the 16-bit storage format.
@@ -151,7 +157,9 @@ unsigned int *stream_timeout_counter(int dev);
         {{SmallSmem<H / 8, BRPT, BNW, BNS, 2>::kBytes,                                   \
           SmallSmem<H / 8, BRPT, BNW, BNS, 2>::kBytes},                                  \
          {SmallSmem<H / 8, BRPT, BNW, BNS, 3>::kBytes,                                   \
-          SmallSmem<H / 8, BRPT, BNW, BNS, 3>::kBytes}}};
+          SmallSmem<H / 8, BRPT, BNW, BNS, 3>::kBytes}},                                 \
+        {nullptr, nullptr},                                                              \
+        {0, 0}};
 
 #define RMSK_SPLIT(NAME, T, E)                                                    \
     const SplitKernels NAME = {                                                   \

@@ -479,4 +479,220 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
     }
 }
 
+// ---------------------------------------------------------- double backward
+// The double backward of bwd2.cuh with rows staged like the backward above:
+// a stage holds one row of x, dy and gx (gx's copy is skipped, and read as
+// zero, when gx is absent); per row the four sums c = sum w dy x, A = sum
+// gx w dy, B = sum gx x, D = sum gw dy x (and sum x^2 when rstd is not
+// given) go through one group barrier, then ddy and dx2 are written and the
+// dw2 accumulators updated from a second read of the stage.
+template <typename T, int GW, int V, int NG, int NS, bool LOADR>
+__global__ void __launch_bounds__(NG * GW * 32, 1)
+rms_bwd2_stream(const Bwd2Params p, unsigned int *timeouts)
+{
+    using P = Pack<T, 8>;
+    using FP = Pack<float, 8>;
+    using X = Vals<8>;
+    using F = float2;
+    constexpr int GT = GW * 32;
+    constexpr int NV = GT * V;
+    constexpr int NTEN = 3;               // x, dy, gx
+    constexpr int NR = LOADR ? 4 : 5;     // c, A, B, D, [sum x^2]
+    using SM = StreamSmem<GW, V, NG, NS, NTEN, NR>;
+    constexpr int NSE = SM::kNS;
+    static_assert(NG * NV * 8 * 4 <= SM::kStagesBytes, "dw combine reuses the stages");
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int g = threadIdx.x / GT;
+    const int t = threadIdx.x % GT;
+    const int wg = t / 32;
+    const uint32_t stage0 = smem_addr(smem) + g * NSE * SM::kStageBytes;
+    const uint32_t bar0 = smem_addr(smem) + SM::kBarOff + g * NSE * 8;
+    float *red = reinterpret_cast<float *>(smem + SM::kRedOff) + g * 2 * GW * NR;
+    const bool has_gx = p.gx != nullptr;
+
+    if (t == 0)
+        for (int s = 0; s < NSE; ++s)
+            mbar_init(bar0 + 8 * s, 1);
+    mbar_init_fence();
+    __syncthreads();
+    griddep_wait();
+    const unsigned long long limit = wait_limit_ns(p.wait_limit_us);
+
+    P wp[V];        // the weight kept packed, gw widened, dw2 accumulators
+    X gwv[V], acc[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        wp[j] = P::load_cached(p.w, t + j * GT);
+        if (p.gw != nullptr)
+            FP::load_cached(p.gw, t + j * GT).widen(gwv[j]);
+        else
+            gwv[j] = X::zero();
+        acc[j] = X::zero();
+    }
+
+    const int64_t gg = (int64_t)blockIdx.x * NG + g;
+    const int64_t TG = (int64_t)gridDim.x * NG;
+    const int64_t nk = gg < p.M ? (p.M - 1 - gg) / TG + 1 : 0;
+    const float fH = (float)p.H;
+    const int64_t NVr = p.H / 8;          // packs per row (dense rows)
+
+    auto issue = [&](int64_t k) {
+        const int64_t row = gg + k * TG;
+        const int s = (int)(k % NSE);
+        const uint32_t st = stage0 + s * SM::kStageBytes;
+        const uint32_t bar = bar0 + 8 * s;
+        mbar_expect_tx(bar, (has_gx ? 3 : 2) * SM::kRowBytes + p.extra_tx);
+        bulk_g2s(st, static_cast<const uint4 *>(p.x) + row * NVr, SM::kRowBytes, bar);
+        bulk_g2s(st + SM::kRowBytes, static_cast<const uint4 *>(p.dy) + row * NVr,
+                 SM::kRowBytes, bar);
+        if (has_gx)
+            bulk_g2s(st + 2 * SM::kRowBytes, static_cast<const uint4 *>(p.gx) + row * NVr,
+                     SM::kRowBytes, bar);
+    };
+    if (t == 0) {
+        fence_proxy_async_smem();
+        for (int64_t k = 0; k < NSE && k < nk; ++k)
+            issue(k);
+    }
+    auto gx_at = [&](uint32_t st, int j, X &gv) {
+        if (has_gx)
+            as_pack<T>(lds128(st + 2 * SM::kRowBytes + (t + j * GT) * 16)).widen(gv);
+        else
+            gv = X::zero();
+    };
+
+    float r_next = 0.f;
+    if constexpr (LOADR)
+        r_next = nk > 0 ? p.rstd[gg] : 0.f;
+
+    int64_t k = 0;
+    bool failed = false;
+    for (; k < nk; ++k) {
+        const int64_t row = gg + k * TG;
+        const uint32_t st = stage0 + (int)(k % NSE) * SM::kStageBytes;
+        float r_cur = 0.f;
+        if constexpr (LOADR) {
+            r_cur = r_next;                 // loaded one row ahead
+            if (k + 1 < nk)
+                r_next = p.rstd[row + TG];
+        }
+        const bool ok = mbar_wait_bounded(bar0 + 8 * (int)(k % NSE), (uint32_t)((k / NSE) & 1), limit);
+
+        F s_c = splat<F>(0.f), s_a = splat<F>(0.f), s_b = splat<F>(0.f), s_d = splat<F>(0.f),
+          s_xx = splat<F>(0.f);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            X a, b, gv, wv;
+            as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
+            as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+            gx_at(st, j, gv);
+            wp[j].widen(wv);
+#pragma unroll
+            for (int i = 0; i < X::N; ++i) {
+                const F wdy = vmul(wv.v[i], b.v[i]);
+                s_c = vfma(wdy, a.v[i], s_c);
+                s_a = vfma(gv.v[i], wdy, s_a);
+                s_b = vfma(gv.v[i], a.v[i], s_b);
+                s_d = vfma(vmul(gwv[j].v[i], b.v[i]), a.v[i], s_d);
+                if constexpr (!LOADR)
+                    s_xx = vfma(a.v[i], a.v[i], s_xx);
+            }
+        }
+        float sums[NR];
+        sums[0] = group_allreduce<32>(hsum(s_c));
+        sums[1] = group_allreduce<32>(hsum(s_a));
+        sums[2] = group_allreduce<32>(hsum(s_b));
+        sums[3] = group_allreduce<32>(hsum(s_d));
+        if constexpr (!LOADR)
+            sums[4] = group_allreduce<32>(hsum(s_xx));
+        float *rb = red + (k & 1) * GW * NR;   // double buffer
+        if ((t & 31) == 0)
+#pragma unroll
+            for (int i = 0; i < NR; ++i)
+                rb[wg * NR + i] = sums[i];
+        // Every thread of the group has posted its sums and finished the
+        // previous iteration (whose stage is refilled below).
+        if (bar_red_or(1 + g, GT, !ok)) {
+            failed = true;
+            break;
+        }
+        if (t == 0 && k >= 1 && k - 1 + NSE < nk) {
+            fence_proxy_async_smem();
+            issue(k - 1 + NSE);
+        }
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            float v = 0.f;
+#pragma unroll
+            for (int q = 0; q < GW; ++q)
+                v += rb[q * NR + i];
+            sums[i] = v;
+        }
+        float r;
+        if constexpr (LOADR)
+            r = r_cur;
+        else
+            r = rsqrtf(sums[4] / fH + p.eps);
+        const float c = sums[0] / fH;
+        const float r3 = r * r * r;
+        const float a2 = r3 * sums[2] / fH;                                   // r^3 B / H
+        const float a3 = r3 * c;                                              // r^3 c
+        const float a1 = (r3 / fH) * (3.f * r * r * c * sums[2] - sums[1] - sums[3]);
+        const F r2 = splat<F>(r), A1 = splat<F>(a1), nA2 = splat<F>(-a2), nA3 = splat<F>(-a3);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            X a, b, gv, wv, o1, o2;
+            as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
+            as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+            gx_at(st, j, gv);
+            wp[j].widen(wv);
+#pragma unroll
+            for (int i = 0; i < X::N; ++i) {
+                // ddy = r (w gx + gw x) - a2 w x
+                const F u1 = vfma(wv.v[i], gv.v[i], vmul(gwv[j].v[i], a.v[i]));
+                o1.v[i] = vfma(nA2, vmul(wv.v[i], a.v[i]), vmul(r2, u1));
+                // dx2 = a1 x - a2 w dy - a3 gx + r gw dy
+                F u = vmul(A1, a.v[i]);
+                u = vfma(nA2, vmul(wv.v[i], b.v[i]), u);
+                u = vfma(nA3, gv.v[i], u);
+                o2.v[i] = vfma(r2, vmul(gwv[j].v[i], b.v[i]), u);
+                // dw2 += r gx dy - a2 dy x
+                acc[j].v[i] = vfma(r2, vmul(gv.v[i], b.v[i]), acc[j].v[i]);
+                acc[j].v[i] = vfma(nA2, vmul(b.v[i], a.v[i]), acc[j].v[i]);
+            }
+            P::narrow(o1).store(p.ddy, row * NVr + t + j * GT);
+            P::narrow(o2).store(p.dx2, row * NVr + t + j * GT);
+        }
+    }
+    if (failed && t == 0) {
+        atomicAdd(timeouts, 1u);
+        // issued and not consumed: rows k .. k+NSE-2, or all NSE of the
+        // prologue when the first wait ran out
+        const int64_t last = k == 0 ? NSE - 1 : k + NSE - 2;
+        for (int64_t q = k; q <= last && q < nk; ++q)
+            (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1), limit);
+    }
+    griddep_launch_dependents();
+
+    // the NG groups' dw2 accumulators, in group order, into one partial row
+    __syncthreads();
+    float *comb = reinterpret_cast<float *>(smem);
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        float4 *d = reinterpret_cast<float4 *>(comb + (size_t)g * NV * 8 + (t + j * GT) * 8);
+        d[0] = make_float4(acc[j].v[0].x, acc[j].v[0].y, acc[j].v[1].x, acc[j].v[1].y);
+        d[1] = make_float4(acc[j].v[2].x, acc[j].v[2].y, acc[j].v[3].x, acc[j].v[3].y);
+    }
+    __syncthreads();
+    float *part = p.part + (int64_t)blockIdx.x * p.H;
+    for (int c = threadIdx.x; c < NV * 8; c += NG * GT) {
+        float v = 0.f;
+#pragma unroll
+        for (int q = 0; q < NG; ++q)
+            v += comb[q * NV * 8 + c];
+        part[c] = v;
+    }
+}
+
 } // namespace rmsk

@@ -160,3 +160,47 @@ def test_error_returns():
     assert call(gw=gw.data_ptr() + 4) == -5   # gw must be 16-byte aligned
     assert call() == 0
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("H", [4096, 5120])
+@pytest.mark.parametrize("M", [1, 7, 1037])
+def test_streamed_and_row_wise_agree_with_oracle(orc, dtype, H, M):
+    """Rows of 4096 and 5120 take the streamed kernel automatically; both it
+    and the row-wise kernel (forced) against the oracle, with gx or gw
+    absent and rstd recomputed too."""
+    inp = synth(M, H, dtype, seed=M + H)
+    for use_gx, use_gw, with_rstd in ((True, True, True), (False, True, False),
+                                      (True, False, True)):
+        o = orc.bwd_bwd(inp["dy"], inp["x"], inp["w"], inp["gx"] if use_gx else None,
+                        inp["gw"] if use_gw else None, 1e-6, want_terms=True)
+        for path, expect in ((rn.PATH_AUTO, rn.PATH_STREAM), (rn.PATH_ROWS, rn.PATH_ROWS)):
+            rn.set_path_override(path)
+            try:
+                got, used = run(inp, use_gx, use_gw, with_rstd)
+            finally:
+                rn.set_path_override(rn.PATH_AUTO)
+            assert used == expect, (path, used)
+            compare(f"{dtype} H={H} M={M} path={path} gx={use_gx} gw={use_gw} "
+                    f"rstd={with_rstd}", got, o, dtype)
+
+
+def test_streamed_wait_runs_out_and_context_survives(orc):
+    """Every streamed wait of the double backward runs out (16 bytes that no
+    copy delivers, 20 ms limit): counted, drained, and the next call is
+    right."""
+    inp = synth(300, 4096, torch.bfloat16, seed=3)
+    rn.wait_timeouts(reset=True)
+    rn.set_stream_test_fault(16, 20000)
+    try:
+        run(inp, True, True, True)            # results incomplete by design
+        torch.cuda.synchronize()
+    finally:
+        rn.set_stream_test_fault(0, 0)
+    assert rn.wait_timeouts(reset=True) > 0
+    o = orc.bwd_bwd(inp["dy"], inp["x"], inp["w"], inp["gx"], inp["gw"], 1e-6,
+                    want_terms=True)
+    got, used = run(inp, True, True, True)
+    assert used == rn.PATH_STREAM
+    compare("after timeouts", got, o, torch.bfloat16)
+    assert rn.wait_timeouts() == 0
