@@ -681,3 +681,45 @@ def test_stream_wait_runs_out_and_context_survives(orc, name, M):
 def test_no_stream_wait_ran_out():
     """Every bounded wait in the streamed kernels completed during this module."""
     assert rn.wait_timeouts() == 0
+
+
+def test_tensors_beyond_2_31_elements(orc):
+    """M x H above 2^31 elements in every row tensor (524291 x 4096 bf16,
+    4.3 GB each): the forward and the (streamed) backward index rows with 64
+    bits. Sampled rows across the whole range, the last ones included,
+    against the oracle; dw over all rows."""
+    M, H = (1 << 31) // 4096 + 3, 4096
+    wl = W.Workload("big", M, H, torch.bfloat16, seed=6, dy_std=1e-2)
+    g = torch.Generator(device=DEV).manual_seed(6)
+    x = torch.randn(M, H, device=DEV, dtype=torch.bfloat16, generator=g)
+    dy = (torch.randn(M, H, device=DEV, generator=g) * 1e-2).to(torch.bfloat16)
+    w = (1 + 0.1 * torch.randn(H, device=DEV, generator=g)).to(torch.bfloat16)
+    y, rstd = rn.rmsnorm_fwd(x, w)
+    dx, dw = rn.rmsnorm_bwd(dy, x, w, rstd)
+    assert rn.last_path() == rn.PATH_STREAM
+    torch.cuda.synchronize()
+    rows = sorted(set(W.random_rows(M, 24, seed=1)) | {M - 2, (1 << 31) // H - 1,
+                                                        (1 << 31) // H})
+    xs, dys, ws = x[rows].cpu(), dy[rows].cpu(), w.cpu()
+    oy, orstd = orc.fwd(xs, ws, 1e-6)
+    odx, _, tdx, _ = orc.bwd(dys, xs, ws, 1e-6, want_terms=True)
+    check_rows("big y", y[rows], oy, torch.bfloat16)
+    check_rstd("big rstd", rstd[rows], orstd)
+    check_rows("big dx", dx[rows], odx, torch.bfloat16, tdx)
+    del y, dx
+    # dw over all rows, by a property that holds at any size: it equals the
+    # dw accumulated over chunks of rows below 2^31 elements (the chunked
+    # accumulation is pinned to the oracle at smaller sizes). Tolerance:
+    # 1e-4 of sum_i |dy x r| per column (fp32 on the GPU, a scale only).
+    dwc = torch.empty(H, device=DEV)
+    bounds = [0, M // 3, 2 * M // 3, M]
+    for i, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
+        rn.rmsnorm_bwd_ex(dy[a:b], x[a:b], w, rstd[a:b], dx=torch.empty_like(dy[a:b]),
+                          dw=dwc, accumulate_dw=i > 0)
+    scale = torch.zeros(H, device=DEV, dtype=torch.float64)
+    for a in range(0, M, 65536):
+        b = min(M, a + 65536)
+        scale += (dy[a:b].float() * x[a:b].float() * rstd[a:b, None]).abs().sum(0).double()
+    torch.cuda.synchronize()
+    err = (dw.double() - dwc.double()).abs()
+    assert bool((err <= 1e-4 * scale).all()), float((err / scale).max())
