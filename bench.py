@@ -205,60 +205,101 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle leg
-def time_oracle(wl, inp, rows, reps=1):
-    """Seconds for the fp64 CPU oracle to run the workload's forward and
-    backward on `rows` rows (single thread, the oracle as it stands)."""
+def host_cores():
+    """Host threads this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_pass(orc, wl, sub):
+    """One pass of the workload's calls on the oracle over the rows in `sub`."""
+    if wl.N:
+        orc.rmsnorm_gemv(sub["x"], sub["w"], sub["A"], wl.eps,
+                         r=sub["r"] if wl.residual else None)
+    elif wl.double_backward:
+        orc.bwd_bwd(sub["dy"], sub["x"], sub["w"], sub["gx"], sub["gw"], wl.eps)
+    elif wl.residual:
+        h, _, _ = orc.residual_fwd(sub["x"], sub["r"], sub["w"], wl.eps)
+        if wl.backward:
+            orc.residual_bwd(sub["dy"], sub["dh"], h, sub["w"], wl.eps)
+    else:
+        orc.fwd(sub["x"], sub["w"], wl.eps)
+        if wl.backward:
+            orc.bwd(sub["dy"], sub["x"], sub["w"], wl.eps)
+
+
+def time_oracle(wl, inp, rows, reps=1, threads=1):
+    """Wall seconds for the fp64 CPU oracle, as it stands, to run the
+    workload's calls on `rows` rows. With threads > 1 the rows are cut into
+    that many contiguous chunks, one per thread (the oracle's ctypes calls
+    release the GIL, so the chunks run in parallel); the per-chunk dw rows
+    are not summed afterwards (threads x H adds, negligible)."""
     import oracle
     orc = oracle.get()
-    sub = {k: (v[:rows].contiguous() if v.dim() == 2 and k != "A" else v)
-           for k, v in inp.items()}
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        if wl.N:
-            orc.rmsnorm_gemv(sub["x"], sub["w"], sub["A"], wl.eps,
-                             r=sub["r"] if wl.residual else None)
-        elif wl.double_backward:
-            orc.bwd_bwd(sub["dy"], sub["x"], sub["w"], sub["gx"], sub["gw"], wl.eps)
-        elif wl.residual:
-            h, _, _ = orc.residual_fwd(sub["x"], sub["r"], sub["w"], wl.eps)
-            if wl.backward:
-                orc.residual_bwd(sub["dy"], sub["dh"], h, sub["w"], wl.eps)
-        else:
-            orc.fwd(sub["x"], sub["w"], wl.eps)
-            if wl.backward:
-                orc.bwd(sub["dy"], sub["x"], sub["w"], wl.eps)
-    return (time.perf_counter() - t0) / reps
+    threads = max(1, min(threads, rows))
+    if wl.N:                        # one decode batch: not cut
+        threads = 1
+    cuts = [rows * i // threads for i in range(threads + 1)]
+    subs = [{k: (v[a:b].contiguous() if v.dim() == 2 and k != "A" else v)
+             for k, v in inp.items()} for a, b in zip(cuts, cuts[1:])]
+    if threads == 1:
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            _oracle_pass(orc, wl, subs[0])
+        return (time.perf_counter() - t0) / reps
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            list(pool.map(lambda sub: _oracle_pass(orc, wl, sub), subs))
+        return (time.perf_counter() - t0) / reps
 
 
-def cpu_baseline(wl, inp, budget_s=12.0):
-    """The oracle on a bounded sample of the workload's rows, scaled to GB/s
-    of the same algorithmic bytes per row."""
+def cpu_baseline(wl, inp, budget_s=8.0):
+    """The oracle on bounded samples of the workload's rows, scaled to GB/s
+    of the same algorithmic bytes per row: once on every host core (about
+    2 x budget_s of CPU work in all) and once on one thread (budget_s)."""
     probe = min(wl.M, 64)
-    t = time_oracle(wl, inp, probe)
-    rows = int(max(1, min(wl.M, budget_s / max(t / probe, 1e-9))))
+    t_row = time_oracle(wl, inp, probe) / probe
+    rows = int(max(1, min(wl.M, budget_s / max(t_row, 1e-9))))
     secs = time_oracle(wl, inp, rows)
     fwd_b, bwd_b = step_bytes(wl.with_rows(rows))
-    return {"value": round((fwd_b + bwd_b) / secs / 1e9, 4), "unit": "GB/s",
-            "cores": 1, "kind": "oracle",
-            "sample": f"{rows} of {wl.M} rows of {wl.name} (H={wl.H}), "
-                      f"{'fwd+bwd' if wl.backward else 'fwd'}, "
-                      f"single-threaded fp64 oracle, {secs:.2f} s",
-            "rows_per_s": round(rows / secs, 2)}
+    single = (fwd_b + bwd_b) / secs / 1e9
+    cores = host_cores()
+    rows_mt = int(max(1, min(wl.M, 2 * budget_s / max(t_row, 1e-9))))
+    secs_mt = time_oracle(wl, inp, rows_mt, threads=cores)
+    used = 1 if wl.N else max(1, min(cores, rows_mt))
+    fwd_b, bwd_b = step_bytes(wl.with_rows(rows_mt))
+    what = "fwd+bwd" if wl.backward else "fwd"
+    return {"value": round((fwd_b + bwd_b) / secs_mt / 1e9, 4), "unit": "GB/s",
+            "cores": used, "kind": "oracle",
+            "sample": f"{rows_mt} of {wl.M} rows of {wl.name} (H={wl.H}), {what}, "
+                      f"fp64 oracle on {used} threads (contiguous row chunks), "
+                      f"{secs_mt:.2f} s; single thread: {rows} rows, {secs:.2f} s",
+            "rows_per_s": round(rows_mt / secs_mt, 2),
+            "single_thread_value": round(single, 4)}
 
 
 def run_reference(args, wl):
-    """The oracle arm: the same metric on bounded CPU samples per step."""
+    """The oracle arm: the same metric on bounded CPU samples per step, the
+    oracle as it stands run on every host core (contiguous row chunks)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    cores = host_cores()
     inp = W.make_inputs(wl.with_rows(min(wl.M, 4096)))
-    probe = min(16, inp["x"].shape[0])
+    M_in = inp["x"].shape[0]
+    probe = min(16, M_in)
     t_row = time_oracle(wl, inp, probe) / probe
-    per_step = int(max(1, min(inp["x"].shape[0],
-                              90.0 / max(args.steps + args.warmup, 1) / t_row)))
+    threads = 1 if wl.N else cores
+    per_step = int(max(1, min(M_in, threads * 60.0 / max(args.steps + args.warmup, 1)
+                                    / t_row)))
+    used = 1 if wl.N else max(1, min(cores, per_step))
     for _ in range(args.warmup):
-        time_oracle(wl, inp, per_step)
-    times = [time_oracle(wl, inp, per_step) for _ in range(args.steps)]
+        time_oracle(wl, inp, per_step, threads=threads)
+    times = [time_oracle(wl, inp, per_step, threads=threads) for _ in range(args.steps)]
     total = sum(times)
     fwd_b, bwd_b = step_bytes(wl.with_rows(per_step))
     value = (fwd_b + bwd_b) * args.steps / total / 1e9
@@ -270,11 +311,11 @@ def run_reference(args, wl):
         "dtype": "f64", "data": "synthetic",
         "config": base_config(wl),
         "rows_per_s": round(per_step * args.steps / total, 2),
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used,
                          "kind": "oracle",
                          "sample": f"{per_step} rows of {wl.name} per step "
                                    f"({'fwd+bwd' if wl.backward else 'fwd'}), "
-                                   f"single-threaded fp64 oracle"},
+                                   f"fp64 oracle on {used} threads"},
         "e2e": {"value": round(value, 4), "unit": "GB/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -598,6 +639,10 @@ def run_ours(args, wl):
     }
     if wl.backward:
         line["roofline_bwd"] = roof(bwd_b, bwd_avg, bwd_kernel)
+    if not use_graph:
+        line["per_call_us"] = {"fwd": call_stats(fwd_ms)}
+        if wl.backward:
+            line["per_call_us"]["bwd"] = call_stats(bwd_ms)
     if wl.N:
         line["unfused"] = unfused
     if not args.no_cpu_baseline and world == 1:
@@ -606,6 +651,15 @@ def run_ours(args, wl):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def call_stats(ms):
+    """Mean, median and 95th percentile (nearest rank) of per-call times in
+    microseconds, over the event-instrumented steps."""
+    us = sorted(1e3 * m for m in ms)
+    p95 = us[min(len(us) - 1, max(0, -(-95 * len(us) // 100) - 1))]
+    return {"n": len(us), "mean": round(statistics.mean(us), 3),
+            "median": round(statistics.median(us), 3), "p95": round(p95, 3)}
 
 
 def time_unfused_gemv(rn, wl, sets, steps):

@@ -101,3 +101,21 @@ def test_gemv_step_bytes():
     f, b = bench.step_bytes(wl)
     assert b == 0
     assert f == (2 * 896 + 896 + 2048 * 896) * 2 + (2048 + 896) * 2
+
+
+def test_per_call_stats_nearest_rank():
+    # 1..20 us: median 10.5, p95 by nearest rank = the 19th value
+    s = bench.call_stats([1e-3 * i for i in range(1, 21)])
+    assert s["n"] == 20 and s["median"] == pytest.approx(10.5)
+    assert s["p95"] == pytest.approx(19.0) and s["mean"] == pytest.approx(10.5)
+    assert bench.call_stats([2e-3])["p95"] == pytest.approx(2.0)
+
+
+def test_threaded_oracle_timing_covers_every_row():
+    """The all-cores CPU baseline cuts the rows into contiguous chunks, one per
+    thread; with more threads than rows it uses one thread per row."""
+    wl = W.WORKLOADS["tiny-fp32"]
+    inp = W.make_inputs(wl)
+    assert bench.time_oracle(wl, inp, 5, threads=8) > 0
+    assert bench.time_oracle(wl, inp, 64, threads=3) > 0
+    assert bench.host_cores() >= 1
