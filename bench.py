@@ -102,6 +102,29 @@ def buffer_sets(wl):
     return int(min(64, max(3, -(-2 * L2_BYTES // max(x_bytes, 1)))))
 
 
+def has_bwd_call(wl):
+    """Whether a step makes a separate backward call after the forward one
+    (the double backward and the fused projection are one call each)."""
+    return wl.backward and not wl.double_backward and not wl.N
+
+
+def launches_per_step(wl):
+    """Kernels of this library launched by one step: the fused projection
+    one; the double backward its kernel and the dw reduce; forward +
+    backward three (forward, backward, dw reduce); forward only one."""
+    if wl.N:
+        return 1
+    if wl.double_backward:
+        return 2
+    return 3 if wl.backward else 1
+
+
+def step_name(wl):
+    if wl.double_backward:
+        return "double backward"
+    return "fwd+bwd" if wl.backward else "fwd"
+
+
 def base_config(wl):
     c = {"workload": wl.name, "M": wl.M, "H": wl.H, "eps": wl.eps,
          "dtype": str(wl.dtype).replace("torch.", ""),
@@ -272,7 +295,7 @@ def cpu_baseline(wl, inp, budget_s=8.0):
     secs_mt = time_oracle(wl, inp, rows_mt, threads=cores)
     used = 1 if wl.N else max(1, min(cores, rows_mt))
     fwd_b, bwd_b = step_bytes(wl.with_rows(rows_mt))
-    what = "fwd+bwd" if wl.backward else "fwd"
+    what = step_name(wl)
     return {"value": round((fwd_b + bwd_b) / secs_mt / 1e9, 4), "unit": "GB/s",
             "cores": used, "kind": "oracle",
             "sample": f"{rows_mt} of {wl.M} rows of {wl.name} (H={wl.H}), {what}, "
@@ -314,7 +337,7 @@ def run_reference(args, wl):
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used,
                          "kind": "oracle",
                          "sample": f"{per_step} rows of {wl.name} per step "
-                                   f"({'fwd+bwd' if wl.backward else 'fwd'}), "
+                                   f"({step_name(wl)}), "
                                    f"fp64 oracle on {used} threads"},
         "e2e": {"value": round(value, 4), "unit": "GB/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -550,10 +573,10 @@ def run_ours(args, wl):
     if use_graph:      # per-call times: the step time split by the byte shares
         step = total_ms / args.steps
         fwd_ms = [step * fwd_b / (fwd_b + bwd_b)]
-        bwd_ms = [step * bwd_b / (fwd_b + bwd_b)] if wl.backward else [0.0]
+        bwd_ms = [step * bwd_b / (fwd_b + bwd_b)] if has_bwd_call(wl) else [0.0]
     else:
         fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-        bwd_ms = [e[1].elapsed_time(e[2]) for e in ev] if wl.backward else [0.0]
+        bwd_ms = [e[1].elapsed_time(e[2]) for e in ev] if has_bwd_call(wl) else [0.0]
     ms_step = total_ms / args.steps
 
     unfused = time_unfused_gemv(rn, wl, sets, args.steps) if wl.N else None
@@ -574,7 +597,7 @@ def run_ours(args, wl):
     value = whole_job_gbs(fwd_b + bwd_b, world, ms_step)
     fwd_avg = statistics.mean(fwd_ms)
     bwd_avg = statistics.mean(bwd_ms)
-    dom_is_bwd = wl.backward and bwd_b >= fwd_b
+    dom_is_bwd = has_bwd_call(wl) and bwd_b >= fwd_b
     dom_bytes, dom_ms = (bwd_b, bwd_avg) if dom_is_bwd else (fwd_b, fwd_avg)
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = load_traffic(wl, "bwd" if dom_is_bwd else "fwd")
@@ -628,7 +651,7 @@ def run_ours(args, wl):
         "step_bytes": {"fwd": fwd_b, "bwd": bwd_b},
         "roofline": roofline,
         "roofline_fwd": roof(fwd_b, fwd_avg, fwd_kernel),
-        "gpu_launches": args.steps * (1 + (2 if wl.backward else 0)),
+        "gpu_launches": args.steps * launches_per_step(wl),
         "timing": ("CUDA-graph replay of consecutive calls (decode-sized step)"
                    if use_graph else
                    f"value from events around all {args.steps} steps; per-call "
@@ -637,11 +660,11 @@ def run_ours(args, wl):
         "e2e": e2e,
         "cpu_baseline": None,
     }
-    if wl.backward:
+    if has_bwd_call(wl):
         line["roofline_bwd"] = roof(bwd_b, bwd_avg, bwd_kernel)
     if not use_graph:
         line["per_call_us"] = {"fwd": call_stats(fwd_ms)}
-        if wl.backward:
+        if has_bwd_call(wl):
             line["per_call_us"]["bwd"] = call_stats(bwd_ms)
     if wl.N:
         line["unfused"] = unfused

@@ -637,7 +637,7 @@ int bwd2_plan(int dtype, int64_t M, int64_t H, bool vec, bool have_rstd, int ov,
     if (sp && sp->k->bwd2[0] != nullptr && (ov == kPathAuto || ov == kPathStream)) {
         const StreamKernels &k = *sp->k;
         pl->fn = k.bwd2[have_rstd ? 1 : 0];
-        pl->threads = k.b.threads();
+        pl->threads = k.d.threads();
         pl->smem = k.bwd2_smem[have_rstd ? 1 : 0];
         pl->stream = true;
         if (M == 0) {
@@ -645,7 +645,7 @@ int bwd2_plan(int dtype, int64_t M, int64_t H, bool vec, bool have_rstd, int ov,
             return RMSNORM_OK;
         }
         int dev;
-        int st = stream_grid(k.b, pl->fn, pl->smem, M, &pl->grid, &dev);
+        int st = stream_grid(k.d, pl->fn, pl->smem, M, &pl->grid, &dev);
         if (st)
             return st;
         pl->timeouts = stream_timeout_counter(dev);

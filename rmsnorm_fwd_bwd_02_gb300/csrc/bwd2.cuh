@@ -126,17 +126,17 @@ rms_bwd2_rows(const Bwd2Params p)
             const X gwk = gw_at(vi);
 #pragma unroll
             for (int i = 0; i < X::N; ++i) {
-                // ddy = r w gx - a2 w x + r gw x = r (w gx + gw x) - a2 w x
-                const F t = vfma(w.v[i], gg.v[i], vmul(gwk.v[i], a.v[i]));
-                o1.v[i] = vfma(nA2, vmul(w.v[i], a.v[i]), vmul(r2, t));
-                // dx2 = a1 x - a2 w dy - a3 gx + r gw dy
-                F u = vmul(A1, a.v[i]);
-                u = vfma(nA2, vmul(w.v[i], b.v[i]), u);
-                u = vfma(nA3, gg.v[i], u);
-                o2.v[i] = vfma(r2, vmul(gwk.v[i], b.v[i]), u);
-                // dw2 += r gx dy - a2 dy x
-                acc[k].v[i] = vfma(r2, vmul(gg.v[i], b.v[i]), acc[k].v[i]);
-                acc[k].v[i] = vfma(nA2, vmul(b.v[i], a.v[i]), acc[k].v[i]);
+                // with u = r gx - a2 x and rgw = r gw:
+                //   ddy = r w gx - a2 w x + r gw x    = w u + rgw x
+                //   dx2 = a1 x - a2 w dy - a3 gx + r gw dy
+                //       = a1 x - a3 gx + dy (rgw - a2 w)
+                //   dw2 += r gx dy - a2 dy x          = dy u
+                const F u = vfma(nA2, a.v[i], vmul(r2, gg.v[i]));
+                const F rgw = vmul(r2, gwk.v[i]);
+                o1.v[i] = vfma(w.v[i], u, vmul(rgw, a.v[i]));
+                o2.v[i] = vfma(b.v[i], vfma(nA2, w.v[i], rgw),
+                               vfma(nA3, gg.v[i], vmul(A1, a.v[i])));
+                acc[k].v[i] = vfma(b.v[i], u, acc[k].v[i]);
             }
             P::narrow(o1).store(p.ddy, row * NV + vi);
             P::narrow(o2).store(p.dx2, row * NV + vi);

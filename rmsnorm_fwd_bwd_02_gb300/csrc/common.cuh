@@ -451,6 +451,30 @@ __device__ __forceinline__ float group_allreduce(float v)
     return v;
 }
 
+// Sum of four values over a warp in six shuffles. Lane l ends with the warp
+// total of value number (l >> 3) & 3 (a, b, c, d in that order). The first
+// two exchanges halve the work: across 16 lanes each half keeps two of the
+// four values and hands the other two to its partner, across 8 lanes one of
+// the two; a butterfly over the 8 lanes that now hold the same value
+// finishes, so those 8 lanes end bit-identical. Needs all 32 lanes, with
+// lane = threadIdx.x % 32 (blocks of whole warps).
+__device__ __forceinline__ float warp_sum4_spread(float a, float b, float c, float d)
+{
+    const unsigned lane = threadIdx.x & 31u;
+    const bool h16 = (lane & 16u) != 0, h8 = (lane & 8u) != 0;
+    float k0 = h16 ? c : a, k1 = h16 ? d : b;
+    const float s0 = h16 ? a : c, s1 = h16 ? b : d;
+    k0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
+    k1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
+    float v = h8 ? k1 : k0;
+    const float s = h8 ? k0 : k1;
+    v += __shfl_xor_sync(0xFFFFFFFFu, s, 8);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    return v;
+}
+
 // ------------------------------------------------------- launch ordering
 // Programmatic dependent launch: a kernel launched with the
 // programmatic-serialization attribute may start while the previous kernel

@@ -44,7 +44,7 @@ struct StreamShape {
 struct StreamKernels {
     const char *name;
     int H;
-    StreamShape f, b;
+    StreamShape f, b, d;       // forward, backward, double backward
     const void *fwd[2];        // [residual]
     int fwd_smem[2];
     const void *bwd[2][2];     // [dh_out given][rstd given]
@@ -120,10 +120,12 @@ unsigned int *stream_timeout_counter(int dev);
 #define RMSK_ROWS(NAME, T, E, FL, FV, FG, FS, FMB, FEX, BL, BV, BG, BS, BMB, BEX)          \
     RMSK_ROWS2(NAME, T, E, FL, FV, FG, FS, FMB, FEX, E, BL, BV, BG, BS, BMB, BEX)
 
-#define RMSK_STREAM(NAME, T, H, FGW, FV, FNG, FNS, BGW, BV, BNG, BNS)                    \
-    static_assert(32 * FGW * FV * 8 == H && 32 * BGW * BV * 8 == H, "stream layout");    \
+#define RMSK_STREAM(NAME, T, H, FGW, FV, FNG, FNS, BGW, BV, BNG, BNS, DGW, DV, DNG, DNS)  \
+    static_assert(32 * FGW * FV * 8 == H && 32 * BGW * BV * 8 == H &&                    \
+                      32 * DGW * DV * 8 == H,                                            \
+                  "stream layout");                                                      \
     const StreamKernels NAME = {                                                         \
-        #NAME, H, {FNG * FGW * 32, FNG}, {BNG * BGW * 32, BNG},                          \
+        #NAME, H, {FNG * FGW * 32, FNG}, {BNG * BGW * 32, BNG}, {DNG * DGW * 32, DNG},   \
         {(const void *)&rms_fwd_stream<T, FGW, FV, FNG, FNS, false>,                     \
          (const void *)&rms_fwd_stream<T, FGW, FV, FNG, FNS, true>},                     \
         {StreamSmem<FGW, FV, FNG, FNS, 1, 1>::kBytes,                                    \
@@ -136,16 +138,17 @@ unsigned int *stream_timeout_counter(int dev);
           StreamSmem<BGW, BV, BNG, BNS, 2, 1>::kBytes},                                  \
          {StreamSmem<BGW, BV, BNG, BNS, 3, 2>::kBytes,                                   \
           StreamSmem<BGW, BV, BNG, BNS, 3, 1>::kBytes}},                                 \
-        {(const void *)&rms_bwd2_stream<T, BGW, BV, BNG, BNS, false>,                    \
-         (const void *)&rms_bwd2_stream<T, BGW, BV, BNG, BNS, true>},                    \
-        {StreamSmem<BGW, BV, BNG, BNS, 3, 5>::kBytes,                                    \
-         StreamSmem<BGW, BV, BNG, BNS, 3, 4>::kBytes}};
+        {(const void *)&rms_bwd2_stream<T, DGW, DV, DNG, DNS, false>,                    \
+         (const void *)&rms_bwd2_stream<T, DGW, DV, DNG, DNS, true>},                    \
+        {StreamSmem<DGW, DV, DNG, DNS, 3, bwd2_stream_slots(false)>::kBytes,              \
+         StreamSmem<DGW, DV, DNG, DNS, 3, bwd2_stream_slots(true)>::kBytes}};
 
 // Short rows (stream_small.cuh): H = 8 * NVP, NW warps, RPT rows per lane per stage.
 // T is the 16-bit storage format.
 #define RMSK_SMALL(NAME, T, H, FRPT, FNW, FNS, BRPT, BNW, BNS)                            \
     const StreamKernels NAME = {                                                         \
         #NAME, H, {FNW * 32, FNW * (256 / H) * FRPT}, {BNW * 32, BNW * (256 / H) * BRPT}, \
+        {0, 0},                                                                          \
         {(const void *)&rms_fwd_stream_small<T, H / 8, FRPT, FNW, FNS, false>,           \
          (const void *)&rms_fwd_stream_small<T, H / 8, FRPT, FNW, FNS, true>},           \
         {SmallSmem<H / 8, FRPT, FNW, FNS, 1>::kBytes,                                    \

@@ -149,14 +149,14 @@ struct StreamSmem {
     static constexpr int kNS = NS * NG * kStageBytes <= kBudget ? NS : (kFit > 0 ? kFit : 1);
     static constexpr int kStagesBytes = NG * kNS * kStageBytes;
     static constexpr int kBarOff = kStagesBytes;                 // NG*kNS mbarriers
-    static constexpr int kRedOff = kBarOff + NG * kNS * 8;       // [NG][2][GW][NR]
+    static constexpr int kRedOff = (kBarOff + NG * kNS * 8 + 15) / 16 * 16;  // [NG][2][GW][NR]
     static constexpr int kBytes = kRedOff + NG * 2 * GW * NR * 4;
     static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
     static_assert(kNS >= 2, "a stage is refilled one iteration after use: two at least");
 };
 
-// Both kernels read a stage twice (sums, then outputs) instead of holding the
-// row in registers across the group barrier. A stage is refilled one
+// The forward and backward read a stage twice (sums, then outputs) instead
+// of holding the row in registers across the group barrier. A stage is refilled one
 // iteration after it was consumed: the barrier of iteration k proves every
 // thread of the group has finished iteration k-1, whose stage then takes the
 // row NS-1 ahead. NS stages therefore keep NS-1 rows in flight per group.
@@ -480,14 +480,29 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
 }
 
 // ---------------------------------------------------------- double backward
+// Per-warp slots of the streamed double backward's reduction buffer: the
+// four sums as one float4, plus a second float4 holding sum x^2 when rstd is
+// recomputed (the registry sizes shared memory with the same count).
+__host__ __device__ constexpr int bwd2_stream_slots(bool loadr)
+{
+    return loadr ? 4 : 8;
+}
+
 // The double backward of bwd2.cuh with rows staged like the backward above:
 // a stage holds one row of x, dy and gx (gx's copy is skipped, and read as
 // zero, when gx is absent); per row the four sums c = sum w dy x, A = sum
 // gx w dy, B = sum gx x, D = sum gw dy x (and sum x^2 when rstd is not
 // given) go through one group barrier, then ddy and dx2 are written and the
-// dw2 accumulators updated from a second read of the stage.
-template <typename T, int GW, int V, int NG, int NS, bool LOADR>
-__global__ void __launch_bounds__(NG * GW * 32, 1)
+// dw2 accumulators updated. Unlike the kernels above, a thread keeps its
+// packs of the row in registers (widened) across the barrier, so the barrier
+// that completes row k also frees row k's stage: NS stages keep NS rows in
+// flight, and a deep ring per group (one group of 8 warps, 8 stages at
+// H = 4096) is what holds the copy engine at full rate with three tensors
+// read per row. The four sums cross a warp in one spread reduction
+// (warp_sum4_spread) and each warp posts them as one float4 slot (two when
+// sum x^2 rides along).
+template <typename T, int GW, int V, int NG, int NS, bool LOADR, int MINB = 1>
+__global__ void __launch_bounds__(NG * GW * 32, MINB)
 rms_bwd2_stream(const Bwd2Params p, unsigned int *timeouts)
 {
     using P = Pack<T, 8>;
@@ -497,7 +512,7 @@ rms_bwd2_stream(const Bwd2Params p, unsigned int *timeouts)
     constexpr int GT = GW * 32;
     constexpr int NV = GT * V;
     constexpr int NTEN = 3;               // x, dy, gx
-    constexpr int NR = LOADR ? 4 : 5;     // c, A, B, D, [sum x^2]
+    constexpr int NR = bwd2_stream_slots(LOADR);   // c, A, B, D, [sum x^2, pad]
     using SM = StreamSmem<GW, V, NG, NS, NTEN, NR>;
     constexpr int NSE = SM::kNS;
     static_assert(NG * NV * 8 * 4 <= SM::kStagesBytes, "dw combine reuses the stages");
@@ -555,13 +570,6 @@ rms_bwd2_stream(const Bwd2Params p, unsigned int *timeouts)
         for (int64_t k = 0; k < NSE && k < nk; ++k)
             issue(k);
     }
-    auto gx_at = [&](uint32_t st, int j, X &gv) {
-        if (has_gx)
-            as_pack<T>(lds128(st + 2 * SM::kRowBytes + (t + j * GT) * 16)).widen(gv);
-        else
-            gv = X::zero();
-    };
-
     float r_next = 0.f;
     if constexpr (LOADR)
         r_next = nk > 0 ? p.rstd[gg] : 0.f;
@@ -579,87 +587,93 @@ rms_bwd2_stream(const Bwd2Params p, unsigned int *timeouts)
         }
         const bool ok = mbar_wait_bounded(bar0 + 8 * (int)(k % NSE), (uint32_t)((k / NSE) & 1), limit);
 
+        // the row moves from the stage into registers, so the stage can be
+        // refilled as soon as the group barrier below has passed
+        X xa[V], dya[V], gxa[V];
         F s_c = splat<F>(0.f), s_a = splat<F>(0.f), s_b = splat<F>(0.f), s_d = splat<F>(0.f),
           s_xx = splat<F>(0.f);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-            X a, b, gv, wv;
-            as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
-            as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
-            gx_at(st, j, gv);
+            X wv;
+            as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(xa[j]);
+            as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(dya[j]);
+            if (has_gx)
+                as_pack<T>(lds128(st + 2 * SM::kRowBytes + (t + j * GT) * 16)).widen(gxa[j]);
+            else
+                gxa[j] = X::zero();
             wp[j].widen(wv);
 #pragma unroll
             for (int i = 0; i < X::N; ++i) {
-                const F wdy = vmul(wv.v[i], b.v[i]);
-                s_c = vfma(wdy, a.v[i], s_c);
-                s_a = vfma(gv.v[i], wdy, s_a);
-                s_b = vfma(gv.v[i], a.v[i], s_b);
-                s_d = vfma(vmul(gwv[j].v[i], b.v[i]), a.v[i], s_d);
+                const F wdy = vmul(wv.v[i], dya[j].v[i]);
+                s_c = vfma(wdy, xa[j].v[i], s_c);
+                s_a = vfma(gxa[j].v[i], wdy, s_a);
+                s_b = vfma(gxa[j].v[i], xa[j].v[i], s_b);
+                s_d = vfma(vmul(gwv[j].v[i], dya[j].v[i]), xa[j].v[i], s_d);
                 if constexpr (!LOADR)
-                    s_xx = vfma(a.v[i], a.v[i], s_xx);
+                    s_xx = vfma(xa[j].v[i], xa[j].v[i], s_xx);
             }
         }
-        float sums[NR];
-        sums[0] = group_allreduce<32>(hsum(s_c));
-        sums[1] = group_allreduce<32>(hsum(s_a));
-        sums[2] = group_allreduce<32>(hsum(s_b));
-        sums[3] = group_allreduce<32>(hsum(s_d));
-        if constexpr (!LOADR)
-            sums[4] = group_allreduce<32>(hsum(s_xx));
+        // lane l holds the warp's total of sum (l >> 3) & 3: c, A, B, D
+        const float tot = warp_sum4_spread(hsum(s_c), hsum(s_a), hsum(s_b), hsum(s_d));
         float *rb = red + (k & 1) * GW * NR;   // double buffer
-        if ((t & 31) == 0)
-#pragma unroll
-            for (int i = 0; i < NR; ++i)
-                rb[wg * NR + i] = sums[i];
-        // Every thread of the group has posted its sums and finished the
-        // previous iteration (whose stage is refilled below).
+        const int lane = t & 31;
+        if ((lane & 7) == 0)
+            rb[wg * NR + (lane >> 3)] = tot;
+        if constexpr (!LOADR) {
+            const float sxx = group_allreduce<32>(hsum(s_xx));
+            if (lane == 0)
+                rb[wg * NR + 4] = sxx;
+        }
+        // Every thread of the group has posted its sums and read this row's
+        // stage (refilled below with the row NSE ahead); the slots of the
+        // other buffer are free again.
         if (bar_red_or(1 + g, GT, !ok)) {
             failed = true;
             break;
         }
-        if (t == 0 && k >= 1 && k - 1 + NSE < nk) {
+        if (t == 0 && k + NSE < nk) {
             fence_proxy_async_smem();
-            issue(k - 1 + NSE);
+            issue(k + NSE);
         }
+        // the warps' slots summed in warp order
+        F cA = splat<F>(0.f), BD = splat<F>(0.f);
+        float xx = 0.f;
 #pragma unroll
-        for (int i = 0; i < NR; ++i) {
-            float v = 0.f;
-#pragma unroll
-            for (int q = 0; q < GW; ++q)
-                v += rb[q * NR + i];
-            sums[i] = v;
+        for (int q = 0; q < GW; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(rb + q * NR);
+            cA = vadd(cA, make_float2(v.x, v.y));
+            BD = vadd(BD, make_float2(v.z, v.w));
+            if constexpr (!LOADR)
+                xx += rb[q * NR + 4];
         }
         float r;
         if constexpr (LOADR)
             r = r_cur;
         else
-            r = rsqrtf(sums[4] / fH + p.eps);
-        const float c = sums[0] / fH;
+            r = rsqrtf(xx / fH + p.eps);
+        const float c = cA.x / fH;
         const float r3 = r * r * r;
-        const float a2 = r3 * sums[2] / fH;                                   // r^3 B / H
+        const float a2 = r3 * BD.x / fH;                                      // r^3 B / H
         const float a3 = r3 * c;                                              // r^3 c
-        const float a1 = (r3 / fH) * (3.f * r * r * c * sums[2] - sums[1] - sums[3]);
+        const float a1 = (r3 / fH) * (3.f * r * r * c * BD.x - cA.y - BD.y);
         const F r2 = splat<F>(r), A1 = splat<F>(a1), nA2 = splat<F>(-a2), nA3 = splat<F>(-a3);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-            X a, b, gv, wv, o1, o2;
-            as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
-            as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
-            gx_at(st, j, gv);
+            X wv, o1, o2;
             wp[j].widen(wv);
 #pragma unroll
             for (int i = 0; i < X::N; ++i) {
-                // ddy = r (w gx + gw x) - a2 w x
-                const F u1 = vfma(wv.v[i], gv.v[i], vmul(gwv[j].v[i], a.v[i]));
-                o1.v[i] = vfma(nA2, vmul(wv.v[i], a.v[i]), vmul(r2, u1));
-                // dx2 = a1 x - a2 w dy - a3 gx + r gw dy
-                F u = vmul(A1, a.v[i]);
-                u = vfma(nA2, vmul(wv.v[i], b.v[i]), u);
-                u = vfma(nA3, gv.v[i], u);
-                o2.v[i] = vfma(r2, vmul(gwv[j].v[i], b.v[i]), u);
-                // dw2 += r gx dy - a2 dy x
-                acc[j].v[i] = vfma(r2, vmul(gv.v[i], b.v[i]), acc[j].v[i]);
-                acc[j].v[i] = vfma(nA2, vmul(b.v[i], a.v[i]), acc[j].v[i]);
+                // with u = r gx - a2 x and rgw = r gw:
+                //   ddy = r w gx - a2 w x + r gw x    = w u + rgw x
+                //   dx2 = a1 x - a2 w dy - a3 gx + r gw dy
+                //       = a1 x - a3 gx + dy (rgw - a2 w)
+                //   dw2 += r gx dy - a2 dy x          = dy u
+                const F x = xa[j].v[i], dy = dya[j].v[i], gx = gxa[j].v[i];
+                const F u = vfma(nA2, x, vmul(r2, gx));
+                const F rgw = vmul(r2, gwv[j].v[i]);
+                o1.v[i] = vfma(wv.v[i], u, vmul(rgw, x));
+                o2.v[i] = vfma(dy, vfma(nA2, wv.v[i], rgw), vfma(nA3, gx, vmul(A1, x)));
+                acc[j].v[i] = vfma(dy, u, acc[j].v[i]);
             }
             P::narrow(o1).store(p.ddy, row * NVr + t + j * GT);
             P::narrow(o2).store(p.dx2, row * NVr + t + j * GT);
@@ -667,10 +681,8 @@ rms_bwd2_stream(const Bwd2Params p, unsigned int *timeouts)
     }
     if (failed && t == 0) {
         atomicAdd(timeouts, 1u);
-        // issued and not consumed: rows k .. k+NSE-2, or all NSE of the
-        // prologue when the first wait ran out
-        const int64_t last = k == 0 ? NSE - 1 : k + NSE - 2;
-        for (int64_t q = k; q <= last && q < nk; ++q)
+        // issued and not consumed: rows k .. k+NSE-1
+        for (int64_t q = k; q < k + NSE && q < nk; ++q)
             (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1), limit);
     }
     griddep_launch_dependents();

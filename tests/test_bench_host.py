@@ -119,3 +119,16 @@ def test_threaded_oracle_timing_covers_every_row():
     assert bench.time_oracle(wl, inp, 5, threads=8) > 0
     assert bench.time_oracle(wl, inp, 64, threads=3) > 0
     assert bench.host_cores() >= 1
+
+
+def test_launch_counts_and_step_calls():
+    """gpu_launches counts this library's kernels per step: forward, backward
+    and dw reduce for training; the double backward's kernel and dw reduce;
+    one fused projection kernel for decode."""
+    assert bench.launches_per_step(W.WORKLOADS["qwen3-8b-train"]) == 3
+    assert bench.has_bwd_call(W.WORKLOADS["qwen3-8b-train"])
+    bwd2 = W.WORKLOADS["qwen3-8b-train-bwd2"]
+    assert bench.launches_per_step(bwd2) == 2 and not bench.has_bwd_call(bwd2)
+    gemv = W.WORKLOADS["decode-qkv-m1"]
+    assert bench.launches_per_step(gemv) == 1 and not bench.has_bwd_call(gemv)
+    assert bench.step_name(bwd2) == "double backward"
