@@ -183,6 +183,49 @@ int blocks_per_sm(const void *fn, int threads, int dev, int *out, int smem = 0)
     return RMSNORM_OK;
 }
 
+// Clusters of `cs` CTAs of `fn` that can be resident at once on device
+// `dev` (a cluster must fit within one GPC, so fewer CTAs than SMs x
+// blocks_per_sm may run together).
+int max_active_clusters(const void *fn, int threads, int smem, int cs, int dev, int *out)
+{
+    static std::mutex mu;
+    static std::map<std::tuple<const void *, int, int, int>, int> cache;
+    const auto key = std::make_tuple(fn, dev, smem, cs);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *out = it->second;
+            return RMSNORM_OK;
+        }
+    }
+    int bps;
+    int st = blocks_per_sm(fn, threads, dev, &bps, smem);     // sets the smem limit
+    if (st)
+        return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = (unsigned)cs;
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+    cfg.attrs = &a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    if (n < 1)
+        return cuda_fail(cudaErrorInvalidConfiguration);
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = n;
+    *out = n;
+    return RMSNORM_OK;
+}
+
 // Persistent grid: no more CTAs than tiles, no more than fit at once.
 int rows_grid(const RowShape &k, const void *fn, int64_t M, int64_t *grid)
 {
@@ -751,7 +794,12 @@ struct GemvTmaPlan {
     int64_t smem;
 };
 
-bool gemv_tma_plan(int64_t M, int64_t H, int64_t N, bool res, int sms, GemvTmaPlan *pl)
+constexpr int64_t kGemvMinSliceTwoCtas = 256;
+
+// cap: most CTAs that may run at once (0: SMs x CTAs per SM), for clusters
+// the resident clusters x CS.
+bool gemv_tma_plan(int64_t M, int64_t H, int64_t N, bool res, int sms, int64_t cap,
+                   GemvTmaPlan *pl)
 {
     const int MT = (int)((M + 15) / 16);
     const bool half = M <= 8;
@@ -765,10 +813,17 @@ bool gemv_tma_plan(int64_t M, int64_t H, int64_t N, bool res, int sms, GemvTmaPl
         // share an SM), else one CTA per SM with all of it.
         for (int cps : {2, 1}) {
             const int64_t budget = cps == 2 ? (kGemvMaxSmem - 2048) / 2 : kGemvMaxSmem;
-            // every warp with a tile, no more CTAs than fit at once
+            // every warp with a tile, no more CTAs than fit at once (a whole
+            // number of clusters)
+            int64_t limit = (int64_t)cps * sms;
+            if (cap > 0 && cap < limit)
+                limit = cap;
+            limit = limit / CS * CS;
+            if (limit < CS)
+                continue;
             int64_t ctas = (tiles + kGemvWarps - 1) / kGemvWarps;
-            if (ctas > (int64_t)cps * sms)
-                ctas = (int64_t)cps * sms;
+            if (ctas > limit)
+                ctas = limit;
             const int64_t TPW = (tiles + kGemvWarps * ctas - 1) / (kGemvWarps * ctas);
             ctas = (tiles + kGemvWarps * TPW - 1) / (kGemvWarps * TPW);
             ctas = (ctas + CS - 1) / CS * CS;        // whole clusters
@@ -782,7 +837,12 @@ bool gemv_tma_plan(int64_t M, int64_t H, int64_t N, bool res, int sms, GemvTmaPl
                 const int64_t room = budget - fixed - kGemvWarps * NSW * 8;
                 KS = (room / (kGemvWarps * NSW * 8) - 64) / 2;
                 KS = KS / 32 * 32;
-                if (KS < 64)
+                // Two CTAs per SM only with slices of 256 columns or more:
+                // narrower ones make every step a few short copies through a
+                // two-stage ring (measured at 48 x 896 -> 9728: 64-column
+                // slices, two CTAs per SM, 40 us; whole rows, one CTA per SM,
+                // 18 us). One CTA per SM takes whatever fits, 64 at least.
+                if (KS < (cps == 2 ? kGemvMinSliceTwoCtas : 64))
                     continue;
                 bytes = gemv_tma_smem_bytes(MT, half, (int)M, (int)H, stage_r, CS, (int)KS, NSW);
             }
@@ -810,8 +870,24 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
     const int ov = g_path_override.load(std::memory_order_relaxed);
 
     GemvTmaPlan pl;
-    if (ov != kPathRows && gemv_tma_plan(M, H, N, r != nullptr, sms, &pl)) {
-        const void *fn = gemv_tma_kernels.fn[dt][ti][r == nullptr ? 0 : (pl.stage_r ? 2 : 1)];
+    bool tma = ov != kPathRows && gemv_tma_plan(M, H, N, r != nullptr, sms, 0, &pl);
+    auto tma_fn = [&]() {
+        return gemv_tma_kernels.fn[dt][ti][r == nullptr ? 0 : (pl.stage_r ? 2 : 1)];
+    };
+    // With clusters, plan again for the clusters that can be resident at
+    // once: a grid of more would run a second wave.
+    for (int pass = 0; tma && pl.CS > 1 && pass < 2; ++pass) {
+        int maxc;
+        if ((st = max_active_clusters(tma_fn(), kGemvWarps * 32, (int)pl.smem, pl.CS, dev,
+                                      &maxc)))
+            return st;
+        if (pl.ctas <= (int64_t)maxc * pl.CS)
+            break;
+        tma = pass == 0 &&
+              gemv_tma_plan(M, H, N, r != nullptr, sms, (int64_t)maxc * pl.CS, &pl);
+    }
+    if (tma) {
+        const void *fn = tma_fn();
         int bps;
         if ((st = blocks_per_sm(fn, kGemvWarps * 32, dev, &bps, (int)pl.smem)))
             return st;

@@ -68,6 +68,9 @@ struct GemvParams {
     uint32_t extra_tx, wait_limit_us;
 };
 
+// One m16n8k16 MMA, c += a b. Not volatile: it has no effect but its
+// outputs, so the compiler may interleave independent MMAs and the shared
+// loads that feed them.
 template <typename T> struct MmaOp;
 
 template <> struct MmaOp<bf16> {
@@ -75,7 +78,7 @@ template <> struct MmaOp<bf16> {
                                                uint32_t a2, uint32_t a3, uint32_t b0,
                                                uint32_t b1)
     {
-        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
                      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
                      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
                      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -87,7 +90,7 @@ template <> struct MmaOp<f16> {
                                                uint32_t a2, uint32_t a3, uint32_t b0,
                                                uint32_t b1)
     {
-        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
                      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
                      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
                      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -151,7 +154,7 @@ rms_gemv(const GemvParams p)
     static_assert(!HALF || MT == 1, "the 8-row tile is one MMA tile");
     static_assert(RES || !STAGER, "r is staged only in the residual variant");
     constexpr int kYRows = gemv_y_rows(MT, HALF);
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     const int rbytes = 2 * p.H;                                        // one row of T
     unsigned char *ys = smem;                                          // [kYRows][ysr]
     unsigned char *rsm = ys + kYRows * p.ysr;                          // [M][2H] if STAGER
@@ -327,10 +330,14 @@ rms_gemv(const GemvParams p)
         const int n0 = n_first + t * 8;
         if (n0 >= p.N)
             break;                            // uniform over the CTA
-        float c[MT][4];
+        // two accumulators per m-tile, one per half of a 32-wide chunk, so
+        // the two MMAs of a chunk do not wait on each other
+        float c[MT][2][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
-            c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                c[mt][hh][0] = c[mt][hh][1] = c[mt][hh][2] = c[mt][hh][3] = 0.f;
 
         for (int c0 = warp; c0 < nchunks; c0 += kGemvWarps * kGemvBatch) {
             if (t > 0 || c0 != warp)
@@ -346,15 +353,17 @@ rms_gemv(const GemvParams p)
                     const uint4 ya = lds_v4(ys + (mt * 16 + g) * p.ysr + kb);
                     const uint4 yb = HALF ? make_uint4(0, 0, 0, 0)
                                           : lds_v4(ys + (mt * 16 + g + 8) * p.ysr + kb);
-                    MmaOp<T>::run(c[mt], ya.x, yb.x, ya.y, yb.y, bf[b].x, bf[b].y);
-                    MmaOp<T>::run(c[mt], ya.z, yb.z, ya.w, yb.w, bf[b].z, bf[b].w);
+                    MmaOp<T>::run(c[mt][0], ya.x, yb.x, ya.y, yb.y, bf[b].x, bf[b].y);
+                    MmaOp<T>::run(c[mt][1], ya.z, yb.z, ya.w, yb.w, bf[b].z, bf[b].w);
                 }
             }
         }
 
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
-            red[(warp * MT + mt) * 32 + lane] = make_float4(c[mt][0], c[mt][1], c[mt][2], c[mt][3]);
+            red[(warp * MT + mt) * 32 + lane] =
+                make_float4(c[mt][0][0] + c[mt][1][0], c[mt][0][1] + c[mt][1][1],
+                            c[mt][0][2] + c[mt][1][2], c[mt][0][3] + c[mt][1][3]);
         __syncthreads();
         for (int e = tid; e < MT * 128; e += kGemvWarps * 32) {
             const int mt = e / 128, ln = (e % 128) / 4, i = e % 4;

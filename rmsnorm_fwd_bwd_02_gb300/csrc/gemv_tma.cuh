@@ -38,6 +38,14 @@
 // of the cluster runs before its shared memory is written. Nothing touches
 // another CTA's shared memory after the second barrier.
 
+#pragma once
+
+#include "gemv.cuh"
+#include "split.cuh"
+#include "stream.cuh"
+
+namespace rmsk {
+
 // 16 bytes into the shared memory of CTA `rank` of the cluster, at the
 // offset `local` has in this CTA.
 __device__ __forceinline__ void st_cluster_v4(const void *local, uint32_t rank, uint4 v)
@@ -49,13 +57,6 @@ __device__ __forceinline__ void st_cluster_v4(const void *local, uint32_t rank, 
                  "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
-#pragma once
-
-#include "gemv.cuh"
-#include "split.cuh"
-#include "stream.cuh"
-
-namespace rmsk {
 
 // CTAs of the cluster that share the norm when M > 16.
 constexpr int kGemvCluster = 8;
@@ -294,10 +295,14 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
 
     // 3. the warp's tiles, step by step through its ring
     const unsigned long long limit = wait_limit_ns(p.wait_limit_us);
-    float c[MT][4];
+    // two accumulators per m-tile, one per half of a 32-wide chunk, so the
+    // two MMAs of a chunk do not wait on each other
+    float c[MT][2][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
-        c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+            c[mt][hh][0] = c[mt][hh][1] = c[mt][hh][2] = c[mt][hh][3] = 0.f;
     int k = 0;
     bool failed = false;
     for (; k < steps; ++k) {
@@ -311,6 +316,7 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
         const int k0 = s * p.KS;
         const int kcols = min(p.KS, p.H - k0);
         const unsigned char *stg = myring + st * stage_bytes + g * asr;
+#pragma unroll 2
         for (int ch = 0; ch < kcols / 32; ++ch) {
             const uint4 bv = lds_v4(stg + (ch * 32 + q * 8) * 2);
             const int kb = (k0 + ch * 32 + q * 8) * 2;
@@ -319,8 +325,8 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
                 const uint4 ya = lds_v4(ys + (mt * 16 + g) * p.ysr + kb);
                 const uint4 yb = HALF ? make_uint4(0, 0, 0, 0)
                                       : lds_v4(ys + (mt * 16 + g + 8) * p.ysr + kb);
-                MmaOp<T>::run(c[mt], ya.x, yb.x, ya.y, yb.y, bv.x, bv.y);
-                MmaOp<T>::run(c[mt], ya.z, yb.z, ya.w, yb.w, bv.z, bv.w);
+                MmaOp<T>::run(c[mt][0], ya.x, yb.x, ya.y, yb.y, bv.x, bv.y);
+                MmaOp<T>::run(c[mt][1], ya.z, yb.z, ya.w, yb.w, bv.z, bv.w);
             }
         }
         // the warp is done reading this stage: refill it NSW steps ahead
@@ -339,10 +345,10 @@ rms_gemv_tma(const GemvParams p, unsigned int *timeouts)
                     const int nn = n0 + 2 * q + (i & 1);
                     if (mm < p.M && nn < p.N) {
                         Vals<1> o;
-                        o.v[0] = c[mt][i];
+                        o.v[0] = c[mt][0][i] + c[mt][1][i];
                         Pack<T, 1>::narrow(o).store(p.out, (int64_t)mm * p.N + nn);
                     }
-                    c[mt][i] = 0.f;
+                    c[mt][0][i] = c[mt][1][i] = 0.f;
                 }
             }
         }
