@@ -238,10 +238,9 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
  *   nothing. Deterministic (fixed-order fp32 sums, no atomics).
  * Performance: built for decode batches. Up to 16 rows the call is faster
  *   than the norm followed by a separate GEMM (measured on GB300 with the
- *   weights streaming from HBM); above 16 rows it stays correct but the
- *   tensor-core fragments of y are re-read from shared memory for every
- *   tile of A, and rmsnorm_fwd / rmsnorm_residual_fwd followed by a GEMM
- *   library call is faster.
+ *   weights streaming from HBM); above 16 rows it stays correct but its
+ *   warp-level MMAs (m16n8k16) bound it, and rmsnorm_fwd /
+ *   rmsnorm_residual_fwd followed by a GEMM library call is faster.
  * flags: 0, or RMSNORM_GEMV_STATIC_WEIGHTS: the caller guarantees that no
  *   work still in flight on the stream when this call is enqueued writes w
  *   or A (model weights during decoding). The kernel then fetches them while
