@@ -236,9 +236,9 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
  *   with another output (every CTA reads x while one writes h and y), else
  *   RMSNORM_ERR_ALIAS. h without r is RMSNORM_ERR_NULLPTR. M == 0 launches
  *   nothing. Deterministic (fixed-order fp32 sums, no atomics).
- * Performance: built for decode batches. Up to 16 rows the call is faster
+ * Performance: built for decode batches. Up to 8 rows the call is faster
  *   than the norm followed by a separate GEMM (measured on GB300 with the
- *   weights streaming from HBM); above 16 rows it stays correct but its
+ *   weights streaming from HBM); from 16 rows on it stays correct but its
  *   warp-level MMAs (m16n8k16) bound it, and rmsnorm_fwd /
  *   rmsnorm_residual_fwd followed by a GEMM library call is faster.
  * flags: 0, or RMSNORM_GEMV_STATIC_WEIGHTS: the caller guarantees that no
