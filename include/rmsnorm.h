@@ -308,6 +308,9 @@ int rmsnorm_last_cuda_error(void);
  * only; the backward then takes row-wise), 3 = row-wise scalar, 4 = streamed
  * (rows staged through shared memory by bulk asynchronous copies; bf16 or
  * fp16 with H = 128 (dense rows only), 4096 or 5120; row-wise elsewhere).
+ * For rmsnorm_gemv_fwd: 1 = the weight in registers, 6 = the weight by bulk
+ * copies (as automatic), 7 = the product on tcgen05 (H <= 2048 and y beside
+ * its ring in shared memory; else as automatic). Other values: automatic.
  * Forcing a vectorised family on rows that are not 16-byte aligned still
  * takes the scalar one. Not thread-safe against concurrent calls; intended
  * for tests only.
@@ -315,10 +318,10 @@ int rmsnorm_last_cuda_error(void);
 void rmsnorm_set_path_override(int path);
 
 /* Which kernel family the last call on this thread used: 1 row-wise
- * vectorised, 2 split-row, 3 row-wise scalar, 4 streamed, 5 and 6 the norm
+ * vectorised, 2 split-row, 3 row-wise scalar, 4 streamed, 5 to 7 the norm
  * fused with the GEMV (rmsnorm_gemv_fwd; 5: the weight in registers, 6: the
  * weight fed by bulk copies, the automatic choice, which override 1 turns
- * off), 0 none. */
+ * off; 7: the product on tcgen05, override 7 only), 0 none. */
 int rmsnorm_last_path(void);
 
 /*

@@ -2,6 +2,8 @@
 // checks, kernel choice, grid sizing and launches. No allocation, no
 // synchronisation, no host copies; everything is enqueued on the caller's
 // stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -18,6 +20,7 @@
 #include "bwd2.cuh"
 #include "gemv.cuh"
 #include "gemv_tma.cuh"
+#include "gemv_umma.cuh"
 #include "reduce.cuh"
 #include "registry.h"
 
@@ -26,8 +29,9 @@ using namespace rmsk;
 namespace {
 
 constexpr int kPathAuto = 0, kPathRows = 1, kPathSplit = 2, kPathScalar = 3, kPathStream = 4;
-constexpr int kPathGemv = 5;           // reported only: RMSNorm fused with the GEMV,
-constexpr int kPathGemvTma = 6;        // A in registers (5) or by bulk copies (6)
+constexpr int kPathGemv = 5;           // RMSNorm fused with the GEMV: A in registers (5,
+constexpr int kPathGemvTma = 6;        // reported only), by bulk copies (6), or the
+constexpr int kPathGemvUmma = 7;       // product on tcgen05 (7); 6 and 7 also force it
 constexpr int kGemvMaxRows = 64;
 constexpr int64_t kGemvMaxSmem = 227 * 1024;
 constexpr int kSplitMaxRows = 64;      // decode-sized batches ([P2 §3.2])
@@ -795,6 +799,27 @@ struct GemvTmaPlan {
 };
 
 constexpr int64_t kGemvMinSliceTwoCtas = 256;
+// The tcgen05 kernel (gemv_umma.cuh) runs a ring of kGemvUmmaStages[1]
+// atoms of A where shared memory allows, else kGemvUmmaStages[0].
+constexpr int kGemvUmmaStages[2] = {3, 6};
+
+// cuTensorMapEncodeTiled, from the driver through the runtime's entry-point
+// query (the library does not link the driver library itself); nullptr if
+// the driver does not offer it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
 
 // cap: most CTAs that may run at once (0: SMs x CTAs per SM), for clusters
 // the resident clusters x CS.
@@ -868,6 +893,65 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
         return st;
     const uint32_t static_w = (flags & RMSNORM_GEMV_STATIC_WEIGHTS) ? 1 : 0;
     const int ov = g_path_override.load(std::memory_order_relaxed);
+
+    // The product on tcgen05 when forced (override 7), where y and a ring of
+    // A fit in shared memory. Not the automatic choice: measured at 16-64
+    // rows it is no faster than the bulk-copy kernel overall (every CTA loads
+    // all of x and r, up to 229 KB at 64 x 896, at some 25-50 GB/s per SM).
+    if (ov == kPathGemvUmma) {
+        const int T = (int)((M + 15) / 16 * 16);
+        int vi = 1;                                // ring of six atoms, else three
+        int64_t smem = gemv_umma_smem_bytes(T, (int)H, kGemvUmmaStages[vi]);
+        if (smem > kGemvMaxSmem) {
+            vi = 0;
+            smem = gemv_umma_smem_bytes(T, (int)H, kGemvUmmaStages[vi]);
+        }
+        PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+        if (H <= kUmmaMaxH && H % 16 == 0 && smem <= kGemvMaxSmem && encode != nullptr) {
+            // A as a 2-D tensor [N rows][H columns], boxes of 128 rows x 64
+            // columns, 128-byte swizzle, out-of-range rows and columns read
+            // as zero
+            CUtensorMap map;
+            const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)N};
+            const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+            const cuuint32_t box[2] = {(cuuint32_t)kUmmaKC, (cuuint32_t)kUmmaM};
+            const cuuint32_t estr[2] = {1, 1};
+            const CUresult cr = encode(
+                &map, dt == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                2, const_cast<void *>(A), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (cr != CUDA_SUCCESS)
+                return cuda_fail(cudaErrorInvalidValue);
+            const void *fn = gemv_umma_kernels.fn[dt][r != nullptr ? 1 : 0][vi];
+            int bps;
+            if ((st = blocks_per_sm(fn, kUmmaThreads, dev, &bps, (int)smem)))
+                return st;
+            unsigned int *tmo = stream_timeout_counter(dev);
+            if (tmo == nullptr)
+                return cuda_fail(cudaErrorInvalidSymbol);
+            GemvUmmaParams p = {x,      r,      w,      out, h,   y,   rstd,
+                                (int)M, (int)H, (int)N, T,   eps, (int)static_w,
+                                g_test_extra_tx.load(std::memory_order_relaxed),
+                                g_test_wait_us.load(std::memory_order_relaxed)};
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)((N + kUmmaM - 1) / kUmmaM));
+            cfg.blockDim = dim3(kUmmaThreads);
+            cfg.dynamicSmemBytes = (size_t)smem;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr.val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            void *args[3] = {&p, &map, &tmo};
+            const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+            if (e != cudaSuccess)
+                return cuda_fail(e);
+            t_last_path = kPathGemvUmma;
+            return RMSNORM_OK;
+        }
+    }
 
     GemvTmaPlan pl;
     bool tma = ov != kPathRows && gemv_tma_plan(M, H, N, r != nullptr, sms, 0, &pl);
@@ -1143,7 +1227,9 @@ int rmsnorm_last_cuda_error(void) { return t_last_cuda_error; }
 
 void rmsnorm_set_path_override(int path)
 {
-    g_path_override.store(path >= kPathAuto && path <= kPathStream ? path : kPathAuto);
+    const bool ok = (path >= kPathAuto && path <= kPathStream) || path == kPathGemvTma ||
+                    path == kPathGemvUmma;
+    g_path_override.store(ok ? path : kPathAuto);
 }
 
 void rmsnorm_set_stream_test_fault(unsigned int extra_tx_bytes, unsigned int wait_limit_us)

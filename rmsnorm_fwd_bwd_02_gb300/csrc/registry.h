@@ -100,6 +100,12 @@ struct GemvKernels {
 };
 extern const GemvKernels gemv_kernels;       // A in registers (gemv.cuh)
 extern const GemvKernels gemv_tma_kernels;   // A by bulk copies (gemv_tma.cuh)
+// The product on tcgen05 (gemv_umma.cuh): fn[bf16 = 0, fp16 = 1][residual]
+//   [ring stages: 0 = three, 1 = six]
+struct GemvUmmaKernels {
+    const void *fn[2][2][2];
+};
+extern const GemvUmmaKernels gemv_umma_kernels;
 // Device address of the counter of streamed-kernel waits that ran out.
 unsigned int *stream_timeout_counter(int dev);
 

@@ -21,7 +21,8 @@ DTYPES = {torch.float32: RMSNORM_F32, torch.bfloat16: RMSNORM_BF16,
 MAX_H = 16384
 PATH_AUTO, PATH_ROWS, PATH_SPLIT, PATH_SCALAR, PATH_STREAM = 0, 1, 2, 3, 4
 PATH_GEMV = 5            # reported by last_path() after rmsnorm_gemv_fwd: the
-PATH_GEMV_TMA = 6        # weight in registers (5) or fed by bulk copies (6)
+PATH_GEMV_TMA = 6        # weight in registers (5), fed by bulk copies (6), or
+PATH_GEMV_UMMA = 7       # the product on tcgen05 (7); 6 and 7 also force it
 
 # Entry points of include/rmsnorm.h with their ctypes signatures.
 _i64, _vp, _sz, _int, _f = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,

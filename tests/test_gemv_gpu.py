@@ -8,9 +8,11 @@ y the norm's output as the separate norm would store it. Compared element
 by element on every output (out, h, y, rstd) over dtypes, row counts that
 fill one to four 16-row MMA tiles (and leave them ragged), feature counts,
 output counts that leave the last 8-row tile of A ragged, with and without
-the residual add, for both kernels: the weight in registers (gemv.cuh,
-forced with the row-wise path override) and the weight fed by bulk copies
-(gemv_tma.cuh, the automatic choice).
+the residual add, for the three kernels: the weight in registers (gemv.cuh,
+forced with the row-wise path override), the weight fed by bulk copies
+(gemv_tma.cuh) and the product on tcgen05 (gemv_umma.cuh), each forced with
+its own override; a kernel whose shared memory does not fit the call falls
+back to the next.
 """
 import pytest
 import torch
@@ -23,7 +25,17 @@ from tests.tolerances import check_bits, check_rows, check_rstd
 pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
-KERNELS = {"regs": rn.PATH_ROWS, "tma": rn.PATH_AUTO}
+KERNELS = {"regs": rn.PATH_ROWS, "tma": rn.PATH_GEMV_TMA, "umma": rn.PATH_GEMV_UMMA}
+
+
+def umma_fits(M, H):
+    """Whether the tcgen05 kernel takes the call: H <= 2048 and y (M rounded
+    up to 16 rows, 64-column swizzle atoms), w and a ring of three 16 KB
+    atoms of A in 227 KB."""
+    T = (M + 15) // 16 * 16
+    y = (H + 63) // 64 * T * 128
+    w = (2 * H + 127) // 128 * 128
+    return H <= 2048 and H % 16 == 0 and 1024 + y + 3 * 16384 + w + 64 <= 227 * 1024
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -65,10 +77,16 @@ def run(inp, residual, eps=1e-6, want_y=True, static=False, kernel="tma"):
         path = rn.last_path()
     finally:
         rn.set_path_override(rn.PATH_AUTO)
-    # the automatic choice takes the bulk-copy kernel where its ring fits in
-    # shared memory beside y, and the register kernel otherwise
-    assert path == rn.PATH_GEMV if kernel == "regs" else path in (rn.PATH_GEMV,
-                                                                   rn.PATH_GEMV_TMA), path
+    # a forced kernel runs where its shared memory fits; the bulk-copy kernel
+    # falls back to the register one, the tcgen05 kernel to the other two
+    if kernel == "regs":
+        assert path == rn.PATH_GEMV, path
+    elif kernel == "tma":
+        assert path in (rn.PATH_GEMV, rn.PATH_GEMV_TMA), path
+    elif umma_fits(M, H):
+        assert path == rn.PATH_GEMV_UMMA, (M, H, path)
+    else:
+        assert path in (rn.PATH_GEMV, rn.PATH_GEMV_TMA), (M, H, path)
     torch.cuda.synchronize()
     return {"out": out, "h": h, "y": y, "rstd": rstd}
 
@@ -142,23 +160,26 @@ def test_decode_workloads_full(orc, name):
                     om, wm.dtype)
 
 
-def test_automatic_choice_is_the_bulk_copy_kernel_for_decode_shapes():
-    for M, H, N in ((1, 896, 2048), (8, 896, 9728), (64, 896, 2048), (16, 4096, 6144),
-                    (1, 6720, 64)):
+def test_automatic_choice_is_the_bulk_copy_kernel():
+    """The bulk-copy kernel wherever its ring fits (the tcgen05 kernel runs
+    only when forced)."""
+    for M, H, N in ((1, 896, 2048), (8, 896, 9728), (9, 896, 2048), (64, 896, 2048),
+                    (64, 896, 9728), (16, 4096, 6144), (1, 6720, 64)):
         inp = synth(M, H, N, torch.bfloat16, seed=2, residual=True)
         g = {k: v.to(DEV) for k, v in inp.items()}
         rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"])
-        assert rn.last_path() == rn.PATH_GEMV_TMA, (M, H, N)
+        assert rn.last_path() == rn.PATH_GEMV_TMA, (M, H, N, rn.last_path())
     torch.cuda.synchronize()
 
 
-def test_y_matches_the_unfused_norm():
-    """The fused kernel's y and h equal the residual forward's to within one
+@pytest.mark.parametrize("kernel", list(KERNELS))
+def test_y_matches_the_unfused_norm(kernel):
+    """The fused kernels' y and h equal the residual forward's to within one
     ulp of y (the fp32 sums of squares run in a different order) and
     bit-exactly for h."""
     for dt in (torch.bfloat16, torch.float16):
         inp = synth(64, 896, 16, dt, seed=3, residual=True)
-        got = run(inp, True)
+        got = run(inp, True, kernel=kernel)
         g = {k: v.to(DEV) for k, v in inp.items()}
         h, y, rstd = rn.rmsnorm_residual_fwd(g["x"], g["r"], g["w"])
         torch.cuda.synchronize()
@@ -176,17 +197,23 @@ def test_deterministic_and_optional_outputs(orc):
     for k in ("out", "h", "y", "rstd"):
         check_bits(f"run-to-run {k}", a[k], b[k])
         check_bits(f"static weights {k}", c[k], a[k])
-    # both kernels: the same h bits; y within one ulp (above 16 rows the
-    # bulk-copy kernel's norm runs its fp32 sums in another order)
-    d = run(inp, True, kernel="regs")
-    check_bits("regs vs tma h", d["h"], a["h"])
-    ya = a["y"].view(torch.int16).to(torch.int32).cpu()
-    yd = d["y"].view(torch.int16).to(torch.int32).cpu()
-    assert int((ya - yd).abs().max()) <= 1, "regs vs tma y: more than 1 ulp apart"
-    # no y, no h, no rstd: out unchanged
+    # the other kernels: the same h bits; y within one ulp (their norms run
+    # the fp32 sums in other orders); each deterministic too
+    for other in ("regs", "umma"):
+        d = run(inp, True, kernel=other)
+        check_bits(f"{other} vs tma h", d["h"], a["h"])
+        ya = a["y"].view(torch.int16).to(torch.int32).cpu()
+        yd = d["y"].view(torch.int16).to(torch.int32).cpu()
+        assert int((ya - yd).abs().max()) <= 1, f"{other} vs tma y: more than 1 ulp apart"
+        e = run(inp, True, kernel=other)
+        for k in ("out", "h", "y", "rstd"):
+            check_bits(f"{other} run-to-run {k}", e[k], d[k])
+    # no y, no h, no rstd: out unchanged (the automatic choice is the
+    # bulk-copy kernel)
     g = {k: v.to(DEV) for k, v in inp.items()}
     out, h, rstd = rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], want_h=False)
     torch.cuda.synchronize()
+    assert rn.last_path() == rn.PATH_GEMV_TMA
     assert h is None and rstd is None
     check_bits("out without optional outputs", out, a["out"])
 
@@ -292,4 +319,23 @@ def test_gemv_wait_runs_out_and_context_survives(orc):
     assert rn.wait_timeouts(reset=True) > 0
     o = oracle_all(orc, inp, True)
     compare("after timeouts", run(inp, True), o, torch.bfloat16)
+    assert rn.wait_timeouts() == 0
+
+
+def test_umma_wait_runs_out_and_context_survives(orc):
+    """Every copy of A into the tcgen05 kernel's ring is made to wait for 16
+    bytes no copy delivers (20 ms limit): the waits run out, are counted, the
+    copies in flight are let land, the tensor memory is freed, and the next
+    call is right."""
+    inp = synth(40, 896, 1000, torch.bfloat16, seed=11, residual=True)
+    rn.wait_timeouts(reset=True)
+    rn.set_stream_test_fault(16, 20000)
+    try:
+        run(inp, True, kernel="umma")             # results incomplete by design
+        torch.cuda.synchronize()
+    finally:
+        rn.set_stream_test_fault(0, 0)
+    assert rn.wait_timeouts(reset=True) > 0
+    o = oracle_all(orc, inp, True)
+    compare("umma after timeouts", run(inp, True, kernel="umma"), o, torch.bfloat16)
     assert rn.wait_timeouts() == 0
