@@ -455,6 +455,8 @@ def gpu_uuid():
 def run_ours(args, wl):
     from rmsnorm_fwd_bwd_02_gb300 import rmsnorm as rn
     rn.lib()
+    if args.path_override:
+        rn.set_path_override(args.path_override)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -600,7 +602,8 @@ def run_ours(args, wl):
     dom_is_bwd = has_bwd_call(wl) and bwd_b >= fwd_b
     dom_bytes, dom_ms = (bwd_b, bwd_avg) if dom_is_bwd else (fwd_b, fwd_avg)
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = load_traffic(wl, "bwd" if dom_is_bwd else "fwd")
+    # recorded for the automatic kernels only
+    traffic = None if args.path_override else load_traffic(wl, "bwd" if dom_is_bwd else "fwd")
 
     def roof(b, ms, kernel):
         a = b / (ms * 1e-3) / 1e9
@@ -617,7 +620,7 @@ def run_ours(args, wl):
     bwd_api = "rmsnorm_bwd_strided" if wl.ld else (
         "rmsnorm_residual_bwd" if wl.residual else "rmsnorm_bwd")
     fwd_kernel = fwd_api + (
-        (" (rms_gemv_tma)" if path_f == 6 else " (rms_gemv)") if wl.N else
+        {6: " (rms_gemv_tma)", 7: " (rms_gemv_umma)"}.get(path_f, " (rms_gemv)") if wl.N else
         f" (rms_bwd2_{fam.get(path_f, 'rows').split(',')[0]} + dw_reduce)"
         if wl.double_backward else
         f" (rms_fwd_{fam.get(path_f, 'rows').split(',')[0]})")
@@ -644,7 +647,8 @@ def run_ours(args, wl):
                    if wl.N else
                    f"{n_sets} rotating buffer sets of {x_bytes / 1e6:.3f} MB per "
                    f"row tensor (L2-resident; launch-bound)"),
-            "parallelism": "replicas" if world > 1 else "single"}),
+            "parallelism": "replicas" if world > 1 else "single"},
+            **({"path_override": args.path_override} if args.path_override else {})),
         "rows_per_s": round(wl.M * world / (ms_step * 1e-3), 1),
         "pct_of_measured_hbm": round(100 * value / world / peak, 2),
         "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
@@ -982,6 +986,11 @@ def main(argv=None):
     ap.add_argument("--rows", type=int, default=0,
                     help="run the workload with this many rows (profiling a "
                          "smaller case); the default is the workload's own M")
+    ap.add_argument("--path-override", type=int, default=0,
+                    help="profiling aid: force a kernel family through the "
+                         "library's path override (rmsnorm_set_path_override; "
+                         "e.g. 1 the register-fed projection, 7 the tcgen05 "
+                         "one); the line then records it under config")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
