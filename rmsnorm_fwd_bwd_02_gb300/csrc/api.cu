@@ -799,9 +799,9 @@ struct GemvTmaPlan {
 };
 
 constexpr int64_t kGemvMinSliceTwoCtas = 256;
-// The tcgen05 kernel (gemv_umma.cuh) runs a ring of kGemvUmmaStages[1]
-// atoms of A where shared memory allows, else kGemvUmmaStages[0].
-constexpr int kGemvUmmaStages[2] = {3, 6};
+// The tcgen05 kernel (gemv_umma.cuh) shares the norm over a cluster from
+// this many tokens on (below, the exchange costs more than it saves).
+constexpr int kGemvUmmaClusterTokens = 32;
 
 // cuTensorMapEncodeTiled, from the driver through the runtime's entry-point
 // query (the library does not link the driver library itself); nullptr if
@@ -900,12 +900,13 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
     // all of x and r, up to 229 KB at 64 x 896, at some 25-50 GB/s per SM).
     if (ov == kPathGemvUmma) {
         const int T = (int)((M + 15) / 16 * 16);
-        int vi = 1;                                // ring of six atoms, else three
-        int64_t smem = gemv_umma_smem_bytes(T, (int)H, kGemvUmmaStages[vi]);
-        if (smem > kGemvMaxSmem) {
-            vi = 0;
-            smem = gemv_umma_smem_bytes(T, (int)H, kGemvUmmaStages[vi]);
-        }
+        // the deepest ring of A that fits beside y (at least two stages)
+        const int nk = (int)((H + kUmmaKC - 1) / kUmmaKC);
+        int NS = kUmmaMaxStages < nk ? kUmmaMaxStages : nk;
+        NS = NS < 2 ? 2 : NS;
+        while (NS > 2 && gemv_umma_smem_bytes(T, (int)H, NS) > kGemvMaxSmem)
+            --NS;
+        const int64_t smem = gemv_umma_smem_bytes(T, (int)H, NS);
         PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
         if (H <= kUmmaMaxH && H % 16 == 0 && smem <= kGemvMaxSmem && encode != nullptr) {
             // A as a 2-D tensor [N rows][H columns], boxes of 128 rows x 64
@@ -923,27 +924,47 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             if (cr != CUDA_SUCCESS)
                 return cuda_fail(cudaErrorInvalidValue);
-            const void *fn = gemv_umma_kernels.fn[dt][r != nullptr ? 1 : 0][vi];
+            // the norm shared by a cluster from kGemvUmmaClusterTokens tokens
+            // on, when the grid, whole clusters, fits at once; else every CTA
+            // normalises every row
+            int64_t ctas = (N + kUmmaM - 1) / kUmmaM;
+            const int64_t ctas_cl = (ctas + kUmmaCluster - 1) / kUmmaCluster * kUmmaCluster;
+            const void *fn_cl = gemv_umma_kernels.fn[dt][r != nullptr ? 1 : 0][1];
+            bool cl = false;
+            if (T >= kGemvUmmaClusterTokens) {
+                int maxc;
+                if ((st = max_active_clusters(fn_cl, kUmmaThreads, (int)smem, kUmmaCluster,
+                                              dev, &maxc)))
+                    return st;
+                cl = ctas_cl <= (int64_t)maxc * kUmmaCluster;
+            }
+            if (cl)
+                ctas = ctas_cl;
+            const void *fn = gemv_umma_kernels.fn[dt][r != nullptr ? 1 : 0][cl ? 1 : 0];
             int bps;
             if ((st = blocks_per_sm(fn, kUmmaThreads, dev, &bps, (int)smem)))
                 return st;
             unsigned int *tmo = stream_timeout_counter(dev);
             if (tmo == nullptr)
                 return cuda_fail(cudaErrorInvalidSymbol);
-            GemvUmmaParams p = {x,      r,      w,      out, h,   y,   rstd,
-                                (int)M, (int)H, (int)N, T,   eps, (int)static_w,
+            GemvUmmaParams p = {x,      r,      w,      out, h,   y,  rstd,
+                                (int)M, (int)H, (int)N, T,   NS, eps, (int)static_w,
                                 g_test_extra_tx.load(std::memory_order_relaxed),
                                 g_test_wait_us.load(std::memory_order_relaxed)};
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)((N + kUmmaM - 1) / kUmmaM));
+            cfg.gridDim = dim3((unsigned)ctas);
             cfg.blockDim = dim3(kUmmaThreads);
             cfg.dynamicSmemBytes = (size_t)smem;
             cfg.stream = stream;
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr.val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
+            cudaLaunchAttribute attrs[2];
+            attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attrs[0].val.programmaticStreamSerializationAllowed = 1;
+            attrs[1].id = cudaLaunchAttributeClusterDimension;
+            attrs[1].val.clusterDim.x = (unsigned)kUmmaCluster;
+            attrs[1].val.clusterDim.y = 1;
+            attrs[1].val.clusterDim.z = 1;
+            cfg.attrs = attrs;
+            cfg.numAttrs = cl ? 2 : 1;
             void *args[3] = {&p, &map, &tmo};
             const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
             if (e != cudaSuccess)

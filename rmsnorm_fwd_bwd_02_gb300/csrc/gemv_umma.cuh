@@ -26,17 +26,23 @@
 //     rows past N filled with zeros; every thread copies its part of w by
 //     cp.async. With static weights this happens before the wait on the
 //     previous kernel.
-//  3. The norm of every token, by all eight warps in rounds of eight 8-row
-//     groups; lane (row % 8, pack % 4) so that the 16-byte stores into the
-//     swizzled layout of y hit 8 different chunk positions per quarter warp,
-//     and a lane loads 16 packs of x (and r) before using any. Pass one adds
-//     r, rounds h, stores it in place of y and sums the squares (the four
-//     lanes of a row combine by shuffles); pass two scales the stored h by
-//     rstd and w and rounds y. The first CTA also writes h, y and rstd.
+//  3. The norm, one 8-row group of tokens at a time by all 256 threads:
+//     lane (row % 8, pack % 4), warp w takes packs 4 w + lane / 8 + 32 u, so
+//     a thread holds at most 8 packs (H <= 2048) and loads them all at once;
+//     the row sums of the eight warps meet in shared memory in warp order.
+//     Without a cluster a CTA normalises every group. With a cluster of 8
+//     (32 tokens or more) rank p normalises groups p, p + 8, ... and sends
+//     each group's 1024-byte block of every atom of y (8 rows of 128 bytes:
+//     one whole swizzle block, valid as it is at the same offset in any
+//     CTA) to the other seven by bulk copies that complete on their "y"
+//     mbarrier; a first cluster barrier phase, arrived at the start, makes
+//     sure every CTA runs before its shared memory is written. The first
+//     CTA (the first cluster) also writes h, y and rstd.
 //  4. Thread 0 alone walks the K atoms: wait for the atom's copy (full
 //     barrier), issue four MMAs (m128 nT k16) and commit them to the stage's
-//     empty barrier, then refill the stage the atom `lag` before used once
-//     its MMAs are done.
+//     empty barrier, then refill the stage of the atom three before once its
+//     MMAs are done (the copies run NS - 3 atoms ahead; NS as deep as shared
+//     memory allows, up to 12).
 //  5. The commit of the last atom completes once every MMA has: warp w reads
 //     lanes 32 (w % 4) .. +31 (its 32 features) of the accumulator, blocks
 //     of 16 tokens alternating between warps w and w + 4, rounds them and
@@ -53,6 +59,7 @@
 #include <cuda.h>
 
 #include "gemv.cuh"
+#include "split.cuh"
 #include "stream.cuh"
 
 namespace rmsk {
@@ -64,10 +71,10 @@ constexpr int kUmmaThreads = 256;  // eight warps; warp w reads tensor-memory la
 constexpr int kUmmaMaxH = 2048;    // the norm holds no row in registers; the
                                    // limit is shared memory (y beside the ring)
 constexpr uint32_t kUmmaStageBytes = kUmmaM * kUmmaKC * 2;   // 16 KB
-// The stage of atom k is refilled (with atom k + NS) once the MMAs of atom
-// k are done, waited for after the MMAs of atom k + lag are issued (lag =
-// kUmmaLag, at most NS - 1): the MMAs' latency overlaps lag atoms, the
-// copies run NS - lag atoms ahead.
+// Most ring stages: a deep ring keeps enough of A in flight per SM (the K
+// loop is otherwise bound by it), as far as shared memory allows beside y;
+// the refill lag of the K loop (see the kernel).
+constexpr int kUmmaMaxStages = 12;
 constexpr int kUmmaLag = 3;
 
 struct GemvUmmaParams {
@@ -80,6 +87,7 @@ struct GemvUmmaParams {
     float *rstd;      // [M] or nullptr
     int M, H, N;
     int T;            // tokens as the MMA's N: M rounded up to 16 (<= 64)
+    int NS;           // ring stages (16 KB atoms of A), 2 .. kUmmaMaxStages
     float eps;
     int static_w;     // w and A may be read before the wait on the previous kernel
     // test hook of the bounded waits: bytes a copy of A is expected to bring
@@ -101,12 +109,18 @@ __host__ __device__ constexpr int64_t gemv_umma_w_bytes(int H)
 }
 
 // Bytes of shared memory: up to 1023 of alignment, y, NS ring stages, w,
-// 2 NS mbarriers, the tensor-memory address.
+// 2 NS mbarriers, three words (tensor-memory address, atoms multiplied, a
+// wait ran out), the mbarrier of y's rows from the cluster and the [8][8]
+// row sums of the shared norm.
 __host__ __device__ constexpr int64_t gemv_umma_smem_bytes(int T, int H, int NS)
 {
     return 1024 + gemv_umma_y_bytes(T, H) + (int64_t)NS * kUmmaStageBytes +
-           gemv_umma_w_bytes(H) + 16 * NS + 16;
+           gemv_umma_w_bytes(H) + 16 * NS + 16 + 16 + 256;
 }
+
+// CTAs of a cluster sharing the norm (each normalises the 8-row groups g
+// with g % kUmmaCluster = its rank and sends them to the others).
+constexpr int kUmmaCluster = 8;
 
 // Tensor-memory columns of a T-token accumulator (fp32, one column per token).
 __host__ __device__ constexpr uint32_t gemv_umma_tmem_cols(int T)
@@ -218,23 +232,53 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
                  : "memory");
 }
 
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Bulk copy of `bytes` (a multiple of 16, 16-byte aligned) from this CTA's
+// shared memory into another CTA's of the cluster, completing on that CTA's
+// mbarrier (both given as cluster addresses).
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                 uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes "
+                 "[%0], [%1], %2, [%3];" ::"r"(dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// This thread's bulk copies issued so far have read their source.
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.commit_group;\ncp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all_groups()
 {
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
-template <typename T, bool RES, int NS>
+template <typename T, bool RES, int CS>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
 rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
               unsigned int *timeouts)
 {
+    static_assert(CS == 1 || CS == kUmmaCluster, "no cluster, or the norm shared by one");
+    const int NS = p.NS;
     using P = Pack<T, 8>;
     using X = Vals<8>;
     using F = float2;
-    static_assert(NS >= 2, "an atom is copied while the one before is multiplied");
-    // the refill lag stays below the ring depth: atom k + NS goes into the
-    // stage of atom k, and must be copied before the loop needs it
-    constexpr int LAG = kUmmaLag < NS ? kUmmaLag : NS - 1;
+    // The stage of atom k is refilled with atom k + NS once the MMAs of atom
+    // k are done, waited for after the MMAs of atom k + LAG are issued (LAG
+    // at most NS - 1): the MMAs' completion overlaps LAG atoms, the copies
+    // run NS - LAG atoms ahead. (A lag of 1 measured slower at 64 x 896 ->
+    // 9728: 16.3 against 13.9 us.)
+    const int LAG = NS > kUmmaLag ? kUmmaLag : NS - 1;
     extern __shared__ __align__(1024) unsigned char umma_smem[];
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -250,36 +294,54 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
     const uint32_t empty0 = full0 + 8 * NS;                           // NS "MMAs done"
     int *slots = reinterpret_cast<int *>(wsm + gemv_umma_w_bytes(H) + 16 * NS);
     // slots[0]: tensor-memory address, [1]: atoms multiplied, [2]: a wait ran out
+    const uint32_t ybar = smem_addr(slots) + 16;              // y's rows from the cluster
+    float *red = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(slots) + 32);
     const uint32_t ncols = gemv_umma_tmem_cols(NT);
     const unsigned long long limit = wait_limit_ns(p.wait_limit_us);
+    const bool has_a = f0 < p.N;                              // the grid may be padded to
+                                                              // whole clusters
+    // The shared norm: 8-row groups g of y, owned by rank g % CS; a CTA
+    // receives every group it does not own, one 1024-byte block per atom.
+    const int ngroups = NT / 8, na = (H + 63) / 64;
+    const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
+    const int owned = ngroups > rank ? (ngroups - 1 - rank) / CS + 1 : 0;
 
     // 1. tensor memory and the stage barriers
     if (warp == 0) {
         tmem_alloc(smem_addr(slots), ncols);
         tmem_relinquish();
     }
-    if (tid == 0)
+    if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
+        if constexpr (CS > 1) {
+            mbar_init(ybar, 1);
+            mbar_expect_tx(ybar, (uint32_t)((ngroups - owned) * na * 1024));
+        }
+    }
     mbar_init_fence();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = static_cast<uint32_t>(slots[0]);
+    // Peers write into this CTA's shared memory only once every CTA of the
+    // cluster runs with its barriers initialised: arrive now, wait before
+    // the first such write.
+    if constexpr (CS > 1)
+        cluster_arrive_release();
 
     // 2. copies of A (thread 0: atom kc into stage kc % NS) and of w
-    auto issue = [&](int kc) {
-        const int s = kc % NS;
+    auto issue = [&](int kc, int s) {                          // atom kc into stage s
         mbar_expect_tx(full0 + 8 * s, kUmmaStageBytes + p.extra_tx);
         tma_load_2d(ring_s + s * kUmmaStageBytes, &tmA, kc * kUmmaKC, f0, full0 + 8 * s);
     };
     const int first = nk < NS ? nk : NS;                      // atoms copied up front
     auto prologue = [&]() {
-        if (tid == 0)
+        if (tid == 0 && has_a)
             for (int kc = 0; kc < first; ++kc)
-                issue(kc);
+                issue(kc, kc);
         for (int j = tid; j < NP; j += kUmmaThreads)
             cp_async16(wsm + j * 16, static_cast<const uint4 *>(p.w) + j);
     };
@@ -289,120 +351,141 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
     if (!p.static_w)
         prologue();
 
-    // 3. the norm, in rounds of four 8-row groups: warp `warp` takes group
-    //    g0 + warp; lane = (row % 8) + 8 (pack % 4). A lane's packs of x (and
-    //    r) are loaded kNormBatch at a time, so that many reads are in
-    //    flight; w comes from shared memory (waited for once, after the first
-    //    pass one).
-    const bool writer = blockIdx.x == 0;
-    const int r8 = lane & 7, jq = lane >> 3;
-    const float fH = (float)H;
-    constexpr int kNormBatch = 16, kScaleBatch = 8;   // packs in flight per lane
-    for (int g0 = 0; g0 < NT / 8; g0 += kUmmaThreads / 32) {
-        const int g = g0 + warp;
-        const bool gv = g < NT / 8;
-        const int t = g * 8 + r8;
-        const bool tok = gv && t < p.M;
-        const int64_t rb = (int64_t)t * NP;
-        F acc = splat<F>(0.f);
-        for (int j0 = jq; gv && j0 < NP; j0 += 4 * kNormBatch) {
-            P xs[kNormBatch], rsv[kNormBatch];
+    // 3. the norm
+    {
+        // The norm of this CTA's 8-row groups g = rank, rank + CS, ... (all of
+        // them without a cluster): all 256 threads on one group: lane (row %
+        // 8, pack % 4), warp w takes packs 4 w + (lane / 8) + 32 u; the row
+        // sums of the eight warps meet in shared memory in warp order.
+        const bool writer = blockIdx.x < CS;                  // the first cluster
+        const int r8 = lane & 7, pj = warp * 4 + (lane >> 3);
+        const float fH = (float)H;
+        constexpr int kU = kUmmaMaxH / 8 / 32;                // packs per thread, at most
+        for (int g = rank; g < ngroups; g += CS) {
+            const int t = g * 8 + r8;
+            const bool tok = t < p.M;
+            const int64_t rb = (int64_t)t * NP;
+            P hs[kU];
+            F acc = splat<F>(0.f);
+            {
+                P xs[kU], rsv[kU];
 #pragma unroll
-            for (int u = 0; u < kNormBatch; ++u) {
-                const int j = j0 + 4 * u;
-                xs[u] = P::zero();
-                rsv[u] = P::zero();
-                if (tok && j < NP) {
-                    xs[u] = P::load(p.x, rb + j);
-                    if constexpr (RES)
-                        rsv[u] = P::load(p.r, rb + j);
+                for (int u = 0; u < kU; ++u) {
+                    const int j = pj + 32 * u;
+                    xs[u] = P::zero();
+                    rsv[u] = P::zero();
+                    if (tok && j < NP) {
+                        xs[u] = P::load(p.x, rb + j);
+                        if constexpr (RES)
+                            rsv[u] = P::load(p.r, rb + j);
+                    }
                 }
-            }
 #pragma unroll
-            for (int u = 0; u < kNormBatch; ++u) {
-                const int j = j0 + 4 * u;
-                if (j >= NP)
-                    break;
-                P hv = xs[u];
-                if (tok) {
-                    X a;
-                    if constexpr (RES) {
-                        X b;
-                        xs[u].widen(a);
-                        rsv[u].widen(b);
+                for (int u = 0; u < kU; ++u) {
+                    const int j = pj + 32 * u;
+                    hs[u] = xs[u];
+                    if (tok && j < NP) {
+                        X a;
+                        if constexpr (RES) {
+                            X b;
+                            xs[u].widen(a);
+                            rsv[u].widen(b);
+#pragma unroll
+                            for (int i = 0; i < X::N; ++i)
+                                a.v[i] = vadd(a.v[i], b.v[i]);
+                            hs[u] = P::narrow(a);             // h as stored
+                            if (writer && p.h != nullptr)
+                                hs[u].store(p.h, rb + j);
+                        }
+                        hs[u].widen(a);
 #pragma unroll
                         for (int i = 0; i < X::N; ++i)
-                            a.v[i] = vadd(a.v[i], b.v[i]);
-                        hv = P::narrow(a);                    // h as stored
-                        if (writer && p.h != nullptr)
-                            hv.store(p.h, rb + j);
+                            acc = vfma(a.v[i], a.v[i], acc);
                     }
-                    hv.widen(a);
-#pragma unroll
-                    for (int i = 0; i < X::N; ++i)
-                        acc = vfma(a.v[i], a.v[i], acc);
                 }
-                *reinterpret_cast<uint4 *>(ysm + sw128_offset(NT, t, j)) = hv.u;
             }
-        }
-        float ss = hsum(acc);
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 8);
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 16);
-        const float rs = rsqrtf(ss / fH + p.eps);
-        if (tok && writer && jq == 0 && p.rstd != nullptr)
-            p.rstd[t] = rs;
-        if (g0 == 0) {             // w is in (every thread's copies of it)
-            cp_async_wait_all_groups();
+            float ss = hsum(acc);
+            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 8);
+            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 16);
+            if (lane < 8)
+                red[warp * 8 + lane] = ss;
+            if (g == rank) {       // w is in (every thread's copies of it)
+                cp_async_wait_all_groups();
+            }
             __syncthreads();
-        }
-        if (tok) {
+            float tot = 0.f;
+#pragma unroll
+            for (int q = 0; q < kUmmaThreads / 32; ++q)
+                tot += red[q * 8 + r8];
+            const float rs = rsqrtf(tot / fH + p.eps);
+            if (tok && writer && pj == 0 && p.rstd != nullptr)
+                p.rstd[t] = rs;
             const F r2 = splat<F>(rs);
-            for (int j0 = jq; j0 < NP; j0 += 4 * kScaleBatch) {
-                P hs[kScaleBatch], ws[kScaleBatch];
 #pragma unroll
-                for (int u = 0; u < kScaleBatch; ++u) {
-                    const int j = j0 + 4 * u;
-                    if (j < NP) {
-                        hs[u].u = *reinterpret_cast<const uint4 *>(ysm + sw128_offset(NT, t, j));
-                        ws[u].u = *reinterpret_cast<const uint4 *>(wsm + j * 16);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kScaleBatch; ++u) {
-                    const int j = j0 + 4 * u;
-                    if (j >= NP)
-                        break;
+            for (int u = 0; u < kU; ++u) {
+                const int j = pj + 32 * u;
+                if (j >= NP)
+                    break;
+                P yv = P::zero();
+                if (tok) {
+                    P wp;
+                    wp.u = *reinterpret_cast<const uint4 *>(wsm + j * 16);
                     X a, wv;
                     hs[u].widen(a);
-                    ws[u].widen(wv);
+                    wp.widen(wv);
 #pragma unroll
                     for (int i = 0; i < X::N; ++i)
                         a.v[i] = vmul(vmul(a.v[i], r2), wv.v[i]);
-                    const P yv = P::narrow(a);
-                    *reinterpret_cast<uint4 *>(ysm + sw128_offset(NT, t, j)) = yv.u;
+                    yv = P::narrow(a);
                     if (writer && p.y != nullptr)
                         yv.store(p.y, rb + j);
                 }
+                *reinterpret_cast<uint4 *>(ysm + sw128_offset(NT, t, j)) = yv.u;
             }
+            __syncthreads();       // the row sums' slots are reused by the next group
+        }
+        if (owned == 0) {          // w unused here, but its copies must land
+            cp_async_wait_all_groups();
         }
     }
-    // every input but A is read: the next kernel may be scheduled; y is
-    // complete (and, fenced, visible to the tensor cores' reads)
+    // every input but A is read: the next kernel may be scheduled; this
+    // CTA's part of y is complete (and, fenced, visible to the async proxy:
+    // the tensor cores and the bulk copies)
     griddep_launch_dependents();
     fence_proxy_async_smem();
     __syncthreads();
+    bool y_failed = false;
+    if constexpr (CS > 1) {
+        // send each owned group's block of every atom to the other CTAs,
+        // then wait for theirs
+        cluster_wait_acquire();
+        const int ncopy = owned * na * (CS - 1);
+        for (int i = tid; i < ncopy; i += kUmmaThreads) {
+            const int d = 1 + i % (CS - 1), rest = i / (CS - 1);
+            const int a = rest % na, g = rank + (rest / na) * CS;
+            const uint32_t off = (uint32_t)(a * NT * 128 + g * 1024);
+            const uint32_t peer = (uint32_t)((rank + d) % CS);
+            bulk_s2s_cluster(cluster_map(y_s + off, peer), y_s + off, 1024,
+                             cluster_map(ybar, peer));
+        }
+        const bool ok = mbar_wait_bounded(ybar, 0, limit);
+        y_failed = __syncthreads_or(!ok);
+    }
 
     // 4. thread 0 walks the K atoms: MMAs as each atom lands, the stage of
     //    the atom before refilled once its MMAs are done
     if (tid == 0) {
         const uint32_t idesc = umma_idesc_f16(UmmaFormat<T>::value, kUmmaM, NT);
-        int loaded = first;                                   // atoms whose copy started
+        int loaded = has_a ? first : 0;                       // atoms whose copy started
         int kc = 0;
-        bool failed = false;
+        bool failed = y_failed;
         tc_fence_after_sync();
-        for (; kc < nk; ++kc) {
-            const int s = kc % NS;
-            if (!mbar_wait_bounded(full0 + 8 * s, (uint32_t)((kc / NS) & 1), limit)) {
+        // stage and phase parity of atom kc, and of atom kc - LAG (the one
+        // refilled), advanced without dividing
+        int s = 0, ps = 0;
+        uint32_t ph = 0, pph = 0;
+        for (; has_a && !failed && kc < nk; ++kc) {
+            if (!mbar_wait_bounded(full0 + 8 * s, ph, limit)) {
                 failed = true;
                 break;
             }
@@ -414,16 +497,24 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
                 umma_f16(tmem, ad, bd, idesc, (kc | k4) != 0 ? 1u : 0u);
             }
             umma_commit(empty0 + 8 * s);
-            if (kc >= LAG && kc - LAG + NS < nk) {
-                const int pc = kc - LAG;
-                if (!mbar_wait_bounded(empty0 + 8 * (pc % NS), (uint32_t)((pc / NS) & 1),
-                                       limit)) {
-                    failed = true;
-                    ++kc;                                     // atom kc's MMAs were issued
-                    break;
+            if (kc >= LAG) {
+                if (kc - LAG + NS < nk) {
+                    if (!mbar_wait_bounded(empty0 + 8 * ps, pph, limit)) {
+                        failed = true;
+                        ++kc;                                 // atom kc's MMAs were issued
+                        break;
+                    }
+                    issue(kc - LAG + NS, ps);                 // the same stage
+                    ++loaded;
                 }
-                issue(pc + NS);
-                ++loaded;
+                if (++ps == NS) {
+                    ps = 0;
+                    pph ^= 1u;
+                }
+            }
+            if (++s == NS) {
+                s = 0;
+                ph ^= 1u;
             }
         }
         slots[1] = kc;                                        // atoms whose MMAs were issued
@@ -469,8 +560,18 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
         }
     }
 
-    // 6. free the tensor memory (every tcgen05 access of the CTA is ordered
-    //    before it by the barrier)
+    // 6. with a cluster: this CTA's copies have read their source, the
+    //    others' copies into it have landed (waited for again, bounded, if
+    //    that wait ran out), and no CTA leaves before all are done
+    if constexpr (CS > 1) {
+        if (y_failed && tid == 0)
+            (void)mbar_wait_bounded(ybar, 0, limit);
+        bulk_wait_read_all();
+        cluster_arrive_release();
+        cluster_wait_acquire();
+    }
+    // free the tensor memory (every tcgen05 access of the CTA is ordered
+    // before it by the barrier)
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {

@@ -101,7 +101,7 @@ struct GemvKernels {
 extern const GemvKernels gemv_kernels;       // A in registers (gemv.cuh)
 extern const GemvKernels gemv_tma_kernels;   // A by bulk copies (gemv_tma.cuh)
 // The product on tcgen05 (gemv_umma.cuh): fn[bf16 = 0, fp16 = 1][residual]
-//   [ring stages: 0 = three, 1 = six]
+//   [0: no cluster, 1: the norm shared by a cluster of kUmmaCluster]
 struct GemvUmmaKernels {
     const void *fn[2][2][2];
 };

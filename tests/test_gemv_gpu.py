@@ -30,12 +30,12 @@ KERNELS = {"regs": rn.PATH_ROWS, "tma": rn.PATH_GEMV_TMA, "umma": rn.PATH_GEMV_U
 
 def umma_fits(M, H):
     """Whether the tcgen05 kernel takes the call: H <= 2048 and y (M rounded
-    up to 16 rows, 64-column swizzle atoms), w and a ring of three 16 KB
+    up to 16 rows, 64-column swizzle atoms), w and a ring of two 16 KB
     atoms of A in 227 KB."""
     T = (M + 15) // 16 * 16
     y = (H + 63) // 64 * T * 128
     w = (2 * H + 127) // 128 * 128
-    return H <= 2048 and H % 16 == 0 and 1024 + y + 3 * 16384 + w + 64 <= 227 * 1024
+    return H <= 2048 and H % 16 == 0 and 1024 + y + 2 * 16384 + w + 2 * 16 + 288 <= 227 * 1024
 
 
 @pytest.fixture(scope="module", autouse=True)
