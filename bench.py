@@ -228,6 +228,19 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle leg
+def host_cpu_model():
+    """The host CPU's model name (lscpu), else the machine architecture."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
 def host_cores():
     """Host threads this process may run on."""
     try:
@@ -302,7 +315,8 @@ def cpu_baseline(wl, inp, budget_s=8.0):
                       f"fp64 oracle on {used} threads (contiguous row chunks), "
                       f"{secs_mt:.2f} s; single thread: {rows} rows, {secs:.2f} s",
             "rows_per_s": round(rows_mt / secs_mt, 2),
-            "single_thread_value": round(single, 4)}
+            "single_thread_value": round(single, 4),
+            "cpu_model": host_cpu_model()}
 
 
 def run_reference(args, wl):
@@ -335,7 +349,7 @@ def run_reference(args, wl):
         "config": base_config(wl),
         "rows_per_s": round(per_step * args.steps / total, 2),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": used,
-                         "kind": "oracle",
+                         "kind": "oracle", "cpu_model": host_cpu_model(),
                          "sample": f"{per_step} rows of {wl.name} per step "
                                    f"({step_name(wl)}), "
                                    f"fp64 oracle on {used} threads"},
