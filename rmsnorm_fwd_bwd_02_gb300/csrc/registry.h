@@ -126,7 +126,7 @@ unsigned int *stream_timeout_counter(int dev);
 #define RMSK_ROWS(NAME, T, E, FL, FV, FG, FS, FMB, FEX, BL, BV, BG, BS, BMB, BEX)          \
     RMSK_ROWS2(NAME, T, E, FL, FV, FG, FS, FMB, FEX, E, BL, BV, BG, BS, BMB, BEX)
 
-#define RMSK_STREAM(NAME, T, H, FGW, FV, FNG, FNS, BGW, BV, BNG, BNS, DGW, DV, DNG, DNS)  \
+#define RMSK_STREAM(NAME, T, H, FGW, FV, FNG, FNS, BGW, BV, BNG, BNS, BH, DGW, DV, DNG, DNS) \
     static_assert(32 * FGW * FV * 8 == H && 32 * BGW * BV * 8 == H &&                    \
                       32 * DGW * DV * 8 == H,                                            \
                   "stream layout");                                                      \
@@ -136,10 +136,10 @@ unsigned int *stream_timeout_counter(int dev);
          (const void *)&rms_fwd_stream<T, FGW, FV, FNG, FNS, true>},                     \
         {StreamSmem<FGW, FV, FNG, FNS, 1, 1>::kBytes,                                    \
          StreamSmem<FGW, FV, FNG, FNS, 2, 1>::kBytes},                                   \
-        {{(const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, false, false>,             \
-          (const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, false, true>},             \
-         {(const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, true, false>,              \
-          (const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, true, true>}},             \
+        {{(const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, false, false, BH>,         \
+          (const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, false, true, BH>},         \
+         {(const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, true, false, BH>,          \
+          (const void *)&rms_bwd_stream<T, BGW, BV, BNG, BNS, true, true, BH>}},         \
         {{StreamSmem<BGW, BV, BNG, BNS, 2, 2>::kBytes,                                   \
           StreamSmem<BGW, BV, BNG, BNS, 2, 1>::kBytes},                                  \
          {StreamSmem<BGW, BV, BNG, BNS, 3, 2>::kBytes,                                   \

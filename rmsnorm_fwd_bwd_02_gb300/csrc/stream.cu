@@ -37,9 +37,9 @@ unsigned int *stream_timeout_counter(int dev)
 // group per CTA and a deep ring (8 stages of 24 KB at H = 4096, 6 of 30 KB at
 // H = 5120: 206 and 204 us at 32768 x 4096 and 26214 x 5120 on GB300, against
 // 234 us for two groups of 4 stages).
-//           name    type   H     |-- forward: GW V NG NS --| |-- backward: GW V NG NS --| |-- double bwd --|
-RMSK_STREAM(s_h4096, bf16, 4096,   4, 4, 4, 4,               8, 2, 2, 6,                  8, 2, 1, 8)
-RMSK_STREAM(s_h5120, bf16, 5120,   4, 5, 3, 3,              10, 2, 2, 3,                 10, 2, 1, 6)
+//           name    type   H     |-- forward: GW V NG NS --| |-- backward: GW V NG NS HOLD --| |-- double bwd --|
+RMSK_STREAM(s_h4096, bf16, 4096,   4, 4, 4, 4,               8, 2, 2, 6, true,            8, 2, 1, 8)
+RMSK_STREAM(s_h5120, bf16, 5120,   4, 5, 3, 3,              10, 2, 2, 3, false,          10, 2, 1, 6)
 
 // 128-wide rows (QK-norm): warps with their own rings of row blocks.
 //          name    type   H    |- forward: RPT NW NS -| |- backward: RPT NW NS -|

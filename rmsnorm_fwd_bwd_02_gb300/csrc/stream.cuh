@@ -298,10 +298,14 @@ rms_fwd_stream(const FwdParams p, unsigned int *timeouts)
 }
 
 // ----------------------------------------------------------------- backward
-template <typename T, int GW, int V, int NG, int NS, bool DH, bool LOADR>
+template <typename T, int GW, int V, int NG, int NS, bool DH, bool LOADR, bool HOLD = false>
 __global__ void __launch_bounds__(NG * GW * 32, 1)
 rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
 {
+    // HOLD: the widened row stays in registers across the group barrier,
+    // which then frees its stage at once (refilled NS rows ahead, not NS - 1)
+    // and spares the second pass its shared-memory reads and conversions.
+    constexpr int LAG = HOLD ? 0 : 1;
     using P = Pack<T, 8>;
     using X = Vals<8>;
     using F = float2;
@@ -379,11 +383,18 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
         const bool ok = mbar_wait_bounded(bar0 + 8 * (int)(k % NSE), (uint32_t)((k / NSE) & 1), limit);
 
         F cs = splat<F>(0.f), ss = splat<F>(0.f);
+        X hx[HOLD ? V : 1], hdy[HOLD ? V : 1], hdh[HOLD && DH ? V : 1];
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             X a, b, wv;
             as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
             as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+            if constexpr (HOLD) {
+                hx[j] = a;
+                hdy[j] = b;
+                if constexpr (DH)
+                    as_pack<T>(lds128(st + 2 * SM::kRowBytes + (t + j * GT) * 16)).widen(hdh[j]);
+            }
             wp[j].widen(wv);
 #pragma unroll
             for (int i = 0; i < X::N; ++i) {
@@ -402,14 +413,15 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
             for (int i = 0; i < NR; ++i)
                 rb[wg * NR + i] = sums[i];
         // Every thread of the group has posted its sums and finished the
-        // previous iteration (whose stage is refilled below).
+        // previous iteration; with HOLD it has also read this row's stage.
+        // The stage used LAG iterations ago is refilled below.
         if (bar_red_or(1 + g, GT, !ok)) {
             failed = true;
             break;
         }
-        if (t == 0 && k >= 1 && k - 1 + NSE < nk) {
+        if (t == 0 && k >= LAG && k - LAG + NSE < nk) {
             fence_proxy_async_smem();
-            issue(k - 1 + NSE);
+            issue(k - LAG + NSE);
         }
 #pragma unroll
         for (int i = 0; i < NR; ++i) {
@@ -430,8 +442,13 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             X a, b, o, wv;
-            as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
-            as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+            if constexpr (HOLD) {
+                a = hx[j];
+                b = hdy[j];
+            } else {
+                as_pack<T>(lds128(st + (t + j * GT) * 16)).widen(a);
+                as_pack<T>(lds128(st + SM::kRowBytes + (t + j * GT) * 16)).widen(b);
+            }
             wp[j].widen(wv);
 #pragma unroll
             for (int i = 0; i < X::N; ++i) {
@@ -440,7 +457,10 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
             }
             if constexpr (DH) {
                 X d;
-                as_pack<T>(lds128(st + 2 * SM::kRowBytes + (t + j * GT) * 16)).widen(d);
+                if constexpr (HOLD)
+                    d = hdh[j];
+                else
+                    as_pack<T>(lds128(st + 2 * SM::kRowBytes + (t + j * GT) * 16)).widen(d);
 #pragma unroll
                 for (int i = 0; i < X::N; ++i)
                     o.v[i] = vadd(o.v[i], d.v[i]);
@@ -450,9 +470,9 @@ rms_bwd_stream(const BwdParams p, unsigned int *timeouts)
     }
     if (failed && t == 0) {
         atomicAdd(timeouts, 1u);
-        // issued and not consumed: rows k .. k+NSE-2, or all NSE of the
+        // issued and not consumed: rows k .. k+NSE-1-LAG, or all NSE of the
         // prologue when the first wait ran out
-        const int64_t last = k == 0 ? NSE - 1 : k + NSE - 2;
+        const int64_t last = k == 0 ? NSE - 1 : k + NSE - 1 - LAG;
         for (int64_t q = k; q <= last && q < nk; ++q)
             (void)mbar_wait_bounded(bar0 + 8 * (int)(q % NSE), (uint32_t)((q / NSE) & 1), limit);
     }
