@@ -238,9 +238,11 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
  *   nothing. Deterministic (fixed-order fp32 sums, no atomics).
  * Performance: built for decode batches. Up to 8 rows the call is faster
  *   than the norm followed by a separate GEMM (measured on GB300 with the
- *   weights streaming from HBM); from 16 rows on it stays correct but its
- *   warp-level MMAs (m16n8k16) bound it, and rmsnorm_fwd /
- *   rmsnorm_residual_fwd followed by a GEMM library call is faster.
+ *   weights streaming from HBM). From 9 rows on it runs the product on the
+ *   tensor cores (tcgen05) with K split over a thread-block cluster; it
+ *   stays correct and deterministic there, but rmsnorm_fwd /
+ *   rmsnorm_residual_fwd followed by a GEMM library call is faster (at 896
+ *   features and 16 to 64 rows by some 1 to 3 us per call).
  * flags: 0, or RMSNORM_GEMV_STATIC_WEIGHTS: the caller guarantees that no
  *   work still in flight on the stream when this call is enqueued writes w
  *   or A (model weights during decoding). The kernel then fetches them while
@@ -309,8 +311,10 @@ int rmsnorm_last_cuda_error(void);
  * (rows staged through shared memory by bulk asynchronous copies; bf16 or
  * fp16 with H = 128 (dense rows only), 4096 or 5120; row-wise elsewhere).
  * For rmsnorm_gemv_fwd: 1 = the weight in registers, 6 = the weight by bulk
- * copies (as automatic), 7 = the product on tcgen05 (H <= 2048 and y beside
- * its ring in shared memory; else as automatic). Other values: automatic.
+ * copies (the automatic choice up to 8 rows), 7 = the product on tcgen05
+ * with K split over a cluster (the automatic choice above 8 rows, where a
+ * cluster of at most 8 CTAs fits its shared memory; else as 6). Other
+ * values: automatic.
  * Forcing a vectorised family on rows that are not 16-byte aligned still
  * takes the scalar one. Not thread-safe against concurrent calls; intended
  * for tests only.
@@ -319,9 +323,9 @@ void rmsnorm_set_path_override(int path);
 
 /* Which kernel family the last call on this thread used: 1 row-wise
  * vectorised, 2 split-row, 3 row-wise scalar, 4 streamed, 5 to 7 the norm
- * fused with the GEMV (rmsnorm_gemv_fwd; 5: the weight in registers, 6: the
- * weight fed by bulk copies, the automatic choice, which override 1 turns
- * off; 7: the product on tcgen05, override 7 only), 0 none. */
+ * fused with the GEMV (rmsnorm_gemv_fwd; 5: the weight in registers, which
+ * override 1 forces; 6: the weight fed by bulk copies, automatic up to 8
+ * rows; 7: the product on tcgen05, automatic above 8 rows), 0 none. */
 int rmsnorm_last_path(void);
 
 /*

@@ -792,6 +792,10 @@ int bwd2_impl(const void *dy, const void *x, const void *w, const float *rstd, c
 // The bulk-copy fed kernel's plan: tiles per warp, K slice, ring stages,
 // shared memory, or false when it does not fit (the register-fed kernel runs
 // then).
+// Rows above which the tcgen05 kernel is the automatic choice (at 1 to 8
+// rows the bulk-copy kernel is faster: its 8-row MMA tile wastes less).
+constexpr int64_t kGemvUmmaMinRows = 8;
+
 struct GemvTmaPlan {
     int TPW, KS, NSW, ctas, CS;
     bool stage_r;
@@ -799,10 +803,6 @@ struct GemvTmaPlan {
 };
 
 constexpr int64_t kGemvMinSliceTwoCtas = 256;
-// The tcgen05 kernel (gemv_umma.cuh) shares the norm over a cluster from
-// this many tokens on (below, the exchange costs more than it saves).
-constexpr int kGemvUmmaClusterTokens = 32;
-
 // cuTensorMapEncodeTiled, from the driver through the runtime's entry-point
 // query (the library does not link the driver library itself); nullptr if
 // the driver does not offer it.
@@ -878,6 +878,46 @@ bool gemv_tma_plan(int64_t M, int64_t H, int64_t N, bool res, int sms, int64_t c
     return false;
 }
 
+// The tcgen05 kernel's plan (gemv_umma.cuh): KS CTAs per tile of 128
+// features split K; among the cluster sizes whose shared memory fits and
+// whose clusters are all resident at once, the fewest atoms per CTA, then
+// the smallest cluster; if none is resident at once, the smallest that fits.
+// KS = 0: none fits.
+struct GemvUmmaPlan {
+    int T, na, KS;
+    int64_t tiles;
+    UmmaLayout L;
+    const void *fn;
+};
+
+int gemv_umma_plan(int64_t M, int64_t H, int64_t N, bool res, int dt, int dev, GemvUmmaPlan *pl)
+{
+    pl->T = (int)((M + 15) / 16 * 16);
+    pl->na = (int)((H + kUmmaKC - 1) / kUmmaKC);
+    pl->tiles = (N + kUmmaM - 1) / kUmmaM;
+    pl->KS = 0;
+    pl->fn = gemv_umma_kernels.fn[dt][res ? 1 : 0];
+    if (pl->T > 64 || H % 16 != 0)
+        return RMSNORM_OK;
+    bool wave = false;
+    for (int ks = 1; ks <= kUmmaMaxCluster && ks <= pl->na; ++ks) {
+        const UmmaLayout L = gemv_umma_layout(pl->T, (int)H, ks, res);
+        if ((int64_t)L.total > kGemvMaxSmem)
+            continue;
+        int maxc;
+        const int st = max_active_clusters(pl->fn, kUmmaThreads, (int)L.total, ks, dev, &maxc);
+        if (st)
+            return st;
+        const bool w1 = pl->tiles <= (int64_t)maxc;
+        if (pl->KS == 0 || (w1 && (!wave || L.apc < pl->L.apc))) {
+            pl->KS = ks;
+            pl->L = L;
+            wave = w1;
+        }
+    }
+    return RMSNORM_OK;
+}
+
 int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *out, void *h,
               void *y, float *rstd, int64_t M, int64_t H, int64_t N, float eps, int dtype,
               int flags, cudaStream_t stream)
@@ -894,79 +934,62 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
     const uint32_t static_w = (flags & RMSNORM_GEMV_STATIC_WEIGHTS) ? 1 : 0;
     const int ov = g_path_override.load(std::memory_order_relaxed);
 
-    // The product on tcgen05 when forced (override 7), where y and a ring of
-    // A fit in shared memory. Not the automatic choice: measured at 16-64
-    // rows it is no faster than the bulk-copy kernel overall (every CTA loads
-    // all of x and r, up to 229 KB at 64 x 896, at some 25-50 GB/s per SM).
-    if (ov == kPathGemvUmma) {
-        const int T = (int)((M + 15) / 16 * 16);
-        // the deepest ring of A that fits beside y (at least two stages)
-        const int nk = (int)((H + kUmmaKC - 1) / kUmmaKC);
-        int NS = kUmmaMaxStages < nk ? kUmmaMaxStages : nk;
-        NS = NS < 2 ? 2 : NS;
-        while (NS > 2 && gemv_umma_smem_bytes(T, (int)H, NS) > kGemvMaxSmem)
-            --NS;
-        const int64_t smem = gemv_umma_smem_bytes(T, (int)H, NS);
+    // The product on tcgen05 with K split over a cluster: automatic above
+    // kGemvUmmaMinRows rows (measured faster there than the warp-level MMA
+    // kernels), or forced (override 7); where no cluster size fits, the
+    // kernels below.
+    if (ov == kPathGemvUmma || (ov == kPathAuto && M > kGemvUmmaMinRows)) {
         PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-        if (H <= kUmmaMaxH && H % 16 == 0 && smem <= kGemvMaxSmem && encode != nullptr) {
-            // A as a 2-D tensor [N rows][H columns], boxes of 128 rows x 64
-            // columns, 128-byte swizzle, out-of-range rows and columns read
-            // as zero
-            CUtensorMap map;
-            const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)N};
-            const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
-            const cuuint32_t box[2] = {(cuuint32_t)kUmmaKC, (cuuint32_t)kUmmaM};
-            const cuuint32_t estr[2] = {1, 1};
-            const CUresult cr = encode(
-                &map, dt == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                2, const_cast<void *>(A), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            if (cr != CUDA_SUCCESS)
-                return cuda_fail(cudaErrorInvalidValue);
-            // the norm shared by a cluster from kGemvUmmaClusterTokens tokens
-            // on, when the grid, whole clusters, fits at once; else every CTA
-            // normalises every row
-            int64_t ctas = (N + kUmmaM - 1) / kUmmaM;
-            const int64_t ctas_cl = (ctas + kUmmaCluster - 1) / kUmmaCluster * kUmmaCluster;
-            const void *fn_cl = gemv_umma_kernels.fn[dt][r != nullptr ? 1 : 0][1];
-            bool cl = false;
-            if (T >= kGemvUmmaClusterTokens) {
-                int maxc;
-                if ((st = max_active_clusters(fn_cl, kUmmaThreads, (int)smem, kUmmaCluster,
-                                              dev, &maxc)))
-                    return st;
-                cl = ctas_cl <= (int64_t)maxc * kUmmaCluster;
-            }
-            if (cl)
-                ctas = ctas_cl;
-            const void *fn = gemv_umma_kernels.fn[dt][r != nullptr ? 1 : 0][cl ? 1 : 0];
-            int bps;
-            if ((st = blocks_per_sm(fn, kUmmaThreads, dev, &bps, (int)smem)))
+        GemvUmmaPlan up;
+        if (encode != nullptr) {
+            if ((st = gemv_umma_plan(M, H, N, r != nullptr, dt, dev, &up)))
                 return st;
+        }
+        if (encode != nullptr && up.KS > 0) {
+            const CUtensorMapDataType et =
+                dt == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+            // 2-D tensors [rows][H columns], 128-byte swizzle, out-of-range
+            // rows and columns read as zero: A in boxes of 128 rows x 64
+            // columns, x and r in boxes of T rows x 64 columns
+            auto make_map = [&](CUtensorMap *map, const void *base, int64_t rows,
+                                uint32_t box_rows) {
+                const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
+                const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+                const cuuint32_t box[2] = {(cuuint32_t)kUmmaKC, (cuuint32_t)box_rows};
+                const cuuint32_t estr[2] = {1, 1};
+                return encode(map, et, 2, const_cast<void *>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            };
+            CUtensorMap mapA, mapX, mapR;
+            if (make_map(&mapA, A, N, kUmmaM) != CUDA_SUCCESS ||
+                make_map(&mapX, x, M, (uint32_t)up.T) != CUDA_SUCCESS ||
+                make_map(&mapR, r != nullptr ? r : x, M, (uint32_t)up.T) != CUDA_SUCCESS)
+                return cuda_fail(cudaErrorInvalidValue);
             unsigned int *tmo = stream_timeout_counter(dev);
             if (tmo == nullptr)
                 return cuda_fail(cudaErrorInvalidSymbol);
-            GemvUmmaParams p = {x,      r,      w,      out, h,   y,  rstd,
-                                (int)M, (int)H, (int)N, T,   NS, eps, (int)static_w,
+            GemvUmmaParams p = {w,       out,           h,   y,   rstd, (int)M, (int)H, (int)N,
+                                up.T,    up.na,         up.L, eps, (int)static_w,
                                 g_test_extra_tx.load(std::memory_order_relaxed),
                                 g_test_wait_us.load(std::memory_order_relaxed)};
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)ctas);
+            cfg.gridDim = dim3((unsigned)(up.tiles * up.KS));
             cfg.blockDim = dim3(kUmmaThreads);
-            cfg.dynamicSmemBytes = (size_t)smem;
+            cfg.dynamicSmemBytes = (size_t)up.L.total;
             cfg.stream = stream;
             cudaLaunchAttribute attrs[2];
             attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
             attrs[0].val.programmaticStreamSerializationAllowed = 1;
             attrs[1].id = cudaLaunchAttributeClusterDimension;
-            attrs[1].val.clusterDim.x = (unsigned)kUmmaCluster;
+            attrs[1].val.clusterDim.x = (unsigned)up.KS;
             attrs[1].val.clusterDim.y = 1;
             attrs[1].val.clusterDim.z = 1;
             cfg.attrs = attrs;
-            cfg.numAttrs = cl ? 2 : 1;
-            void *args[3] = {&p, &map, &tmo};
-            const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+            cfg.numAttrs = 2;
+            void *args[5] = {&p, &mapA, &mapX, &mapR, &tmo};
+            const cudaError_t e = cudaLaunchKernelExC(&cfg, up.fn, args);
             if (e != cudaSuccess)
                 return cuda_fail(e);
             t_last_path = kPathGemvUmma;

@@ -1,59 +1,68 @@
 // gemv_umma.cuh -- RMSNorm fused with the projection, the product on the
-// fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
-// Same result as rms_gemv and rms_gemv_tma: the chain of [P2] (the 0.8B
-// Qwen decode article, trdm.cn news/483216) §2.1, §3.1 with y rounded to the
-// dtype before out = y A^T, fp32 accumulation.
+// fifth-generation tensor cores (tcgen05, accumulators in tensor memory),
+// K split over a thread-block cluster. Same result as rms_gemv and
+// rms_gemv_tma: the chain of [P2] (the 0.8B Qwen decode article,
+// trdm.cn news/483216) §2.1, §3.1 with y rounded to the dtype before
+// out = y A^T, fp32 accumulation.
 //
-// Why a third kernel: the warp-level m16n8k16 MMA of the other two bounds
-// them from 16 rows on (some 40 cycles per MMA per warp on this part). Here
-// one thread per CTA issues tcgen05.mma on operands in shared memory, and
-// the product runs on the tensor cores.
+// Why this shape. In a decode batch of up to 64 tokens every CTA needs y
+// for all of them, and the weight is the only large input. A CTA that
+// normalised whole rows had to load all of x and r (229 KB at 64 x 896,
+// as much as its share of the weight), and a warp-level MMA is bound by its
+// issue rate from 16 rows on. Here a cluster of KS CTAs shares one tile of
+// 128 output features and splits K between them: CTA `rank` owns the
+// 64-column atoms [rank na / KS, (rank + 1) na / KS) of the row. It loads
+// only those columns of x, r, w and of its 128 rows of A, so a grid of
+// (N / 128) x KS CTAs reads every input once per cluster, and KS is chosen
+// so that the grid fills the SMs.
 //
-// The product is laid out for a decode batch: the CTA's 128 output
-// features are the MMA's M (rows of A), the tokens its N (rows of y, M of
-// the call rounded up to 16), K = H. Both operands are K-major in the
-// 128-byte swizzled layout: K is cut into atoms of 64 columns; an atom of R
-// rows holds row i's 128 bytes at i 128, its 16-byte chunk c at position
-// c ^ (i % 8), and starts on a 1024-byte boundary. A descriptor names the
-// atom (start address, advanced 32 bytes per 16-column MMA step), the next
-// 8 rows 1024 bytes on, and the 128-byte swizzle.
+// The product is laid out for a decode batch: the tile's 128 features are
+// the MMA's M (rows of A), the tokens (M of the call rounded up to 16, T)
+// its N, K = the CTA's columns. Operands are K-major in the 128-byte
+// swizzled layout: an atom of R rows x 64 columns holds row i's 128 bytes at
+// i 128, its 16-byte chunk c at position c ^ (i % 8), on a 1024-byte
+// boundary. Tensor copies with the 128-byte swizzle write exactly this
+// layout, for A and for x and r alike, so h and y are computed in place.
 //
-//  1. Warp 0 allocates the tensor-memory columns of the accumulator (a power
-//     of two >= 32 and >= the padded token count); thread 0 initialises a
-//     "full" and an "empty" mbarrier per ring stage.
-//  2. Thread 0 starts tensor copies (the TMA engine, 128-byte swizzle) of the
-//     first NS K atoms of the CTA's 128 rows of A into the ring, 16 KB each,
-//     rows past N filled with zeros; every thread copies its part of w by
-//     cp.async. With static weights this happens before the wait on the
-//     previous kernel.
-//  3. The norm, one 8-row group of tokens at a time by all 256 threads:
-//     lane (row % 8, pack % 4), warp w takes packs 4 w + lane / 8 + 32 u, so
-//     a thread holds at most 8 packs (H <= 2048) and loads them all at once;
-//     the row sums of the eight warps meet in shared memory in warp order.
-//     Without a cluster a CTA normalises every group. With a cluster of 8
-//     (32 tokens or more) rank p normalises groups p, p + 8, ... and sends
-//     each group's 1024-byte block of every atom of y (8 rows of 128 bytes:
-//     one whole swizzle block, valid as it is at the same offset in any
-//     CTA) to the other seven by bulk copies that complete on their "y"
-//     mbarrier; a first cluster barrier phase, arrived at the start, makes
-//     sure every CTA runs before its shared memory is written. The first
-//     CTA (the first cluster) also writes h, y and rstd.
-//  4. Thread 0 alone walks the K atoms: wait for the atom's copy (full
-//     barrier), issue four MMAs (m128 nT k16) and commit them to the stage's
-//     empty barrier, then refill the stage of the atom three before once its
-//     MMAs are done (the copies run NS - 3 atoms ahead; NS as deep as shared
-//     memory allows, up to 12).
-//  5. The commit of the last atom completes once every MMA has: warp w reads
-//     lanes 32 (w % 4) .. +31 (its 32 features) of the accumulator, blocks
-//     of 16 tokens alternating between warps w and w + 4, rounds them and
-//     stores out[token][feature] (32 consecutive features per warp and
-//     token).
-//  6. Warp 0 frees the tensor memory.
+//  1. Warp 0 allocates the accumulator's tensor-memory columns, warp 1
+//     initialises the mbarriers (A's atoms in two groups, one each; x and r;
+//     the MMAs; the partial products received), warp 2 prefetches the three
+//     tensor maps.
+//  2. Tensor copies (the TMA engine, 128-byte swizzle), one per lane: x and
+//     r (T rows x 64 columns per atom, rows past M and columns past H read
+//     as zero) by warp 1 as soon as the previous kernel is complete, A's
+//     atoms (128 rows x 64 columns, 16 KB) by warp 0 behind them. An SM
+//     serves its tensor copies in order and the norm needs x and r first, so
+//     with static weights only the first two atoms of A start before the
+//     wait on the previous kernel. w by cp.async.
+//  3. The norm: h = x + r (rounded, stored in place), the partial sums of
+//     h^2 over the CTA's columns per token, published in shared memory; a
+//     cluster barrier; each token's sum read from every CTA of the cluster
+//     in rank order (distributed shared memory), rstd; y = h rstd w,
+//     rounded, in place. The first cluster also stores h, y and rstd.
+//  4. Thread 0 issues four MMAs (m128 nT k16) per atom, a group of atoms
+//     once its copies have landed, and commits them to one mbarrier. Its
+//     instruction stream is the cost here (some 120 cycles an MMA with the
+//     descriptors built per MMA, about 200 per mbarrier wait even on a
+//     completed phase), so the descriptors advance by additions and A's
+//     atoms have two barriers, not one each.
+//  5. The partial products: each warp reads 32 features x 16 tokens of the
+//     accumulator at a time (tcgen05.ld); each group of 4 tokens belongs to
+//     one CTA of the cluster (group g: rank g % KS). A CTA writes its own
+//     groups into its receive area and the others into a send area, one
+//     contiguous block per owner, which one bulk copy moves into the
+//     owner's receive area, completing on its mbarrier. The owner adds the
+//     KS partials of its groups in rank order (deterministic), rounds and
+//     stores out[token][feature]. The tensor memory is freed as soon as it
+//     is read.
+//  6. A last cluster barrier: no CTA leaves while another may still read its
+//     partial sums or copy products into it.
 //
 // Every mbarrier wait is bounded (about one second, or the test limit); one
 // that runs out counts in the streamed-kernel timeout counter, the CTA skips
-// the rest of its work, waits (bounded again) for its copies and MMAs in
-// flight, and still frees its tensor memory.
+// its remaining work but still takes part in both cluster barriers and in
+// the exchange (sending zeros), waits (bounded again) for its copies in
+// flight, and frees its tensor memory.
 #pragma once
 
 #include <cuda.h>
@@ -64,22 +73,63 @@
 
 namespace rmsk {
 
-constexpr int kUmmaM = 128;        // output features per CTA (the MMA's M)
-constexpr int kUmmaKC = 64;        // K columns per ring stage: one swizzle atom
-constexpr int kUmmaThreads = 256;  // eight warps; warp w reads tensor-memory lanes
+constexpr int kUmmaM = 128;        // output features per tile (the MMA's M)
+constexpr int kUmmaKC = 64;        // K columns per atom: one swizzle span
+constexpr int kUmmaThreads = 512;  // sixteen warps; warp w reads tensor-memory lanes
                                    // 32 (w % 4) .. 32 (w % 4) + 31
-constexpr int kUmmaMaxH = 2048;    // the norm holds no row in registers; the
-                                   // limit is shared memory (y beside the ring)
-constexpr uint32_t kUmmaStageBytes = kUmmaM * kUmmaKC * 2;   // 16 KB
-// Most ring stages: a deep ring keeps enough of A in flight per SM (the K
-// loop is otherwise bound by it), as far as shared memory allows beside y;
-// the refill lag of the K loop (see the kernel).
-constexpr int kUmmaMaxStages = 12;
-constexpr int kUmmaLag = 3;
+constexpr int kUmmaMaxCluster = 8; // CTAs splitting K (portable cluster size)
+constexpr uint32_t kUmmaAtomA = kUmmaM * kUmmaKC * 2;   // 16 KB
+
+// Shared-memory layout of one CTA, byte offsets from a 1024-byte aligned
+// base: y (x copied in, h and y computed in place) at 0, r, the atoms of A,
+// the partial products received (over r when r is large enough: r is
+// consumed before any CTA sends) and those to send (over A when A is large
+// enough: its MMAs are complete before), w, the mbarriers, the
+// tensor-memory address, and the partial row sums and rstd of the T tokens.
+// Both exchange areas are [rank][feature][rs slots of 16 bytes]: the block
+// of one rank is contiguous.
+struct UmmaLayout {
+    int apc;             // most atoms per CTA: ceil(na / KS)
+    int rs;              // 16-byte slots per feature and rank in the exchange
+                         // areas (odd: conflict-free accesses)
+    uint32_t r, a, recv, send, w, bar, total;   // total: with the 1023 bytes of alignment
+};
+
+__host__ __device__ inline UmmaLayout gemv_umma_layout(int T, int H, int KS, bool res)
+{
+    UmmaLayout L;
+    const int na = (H + kUmmaKC - 1) / kUmmaKC;
+    L.apc = (na + KS - 1) / KS;
+    const int g4 = (T / 4 + KS - 1) / KS;                  // 4-token groups per owner, most
+    L.rs = g4 | 1;
+    const uint32_t atom = (uint32_t)T * 128u;               // one atom of x, r or y
+    const uint32_t ybytes = (uint32_t)L.apc * atom;
+    const uint32_t rbytes = res ? ybytes : 0u;
+    const uint32_t recv = (uint32_t)KS * kUmmaM * (uint32_t)L.rs * 16u;
+    const uint32_t abytes = (uint32_t)L.apc * kUmmaAtomA;
+    L.r = ybytes;
+    L.a = ybytes + rbytes;
+    uint32_t end = L.a + abytes;
+    if (rbytes >= recv) {
+        L.recv = L.r;
+    } else {
+        L.recv = end;
+        end += recv;
+    }
+    if (abytes >= recv) {     // A is multiplied before anything is sent
+        L.send = L.a;
+    } else {
+        L.send = end;
+        end += recv;
+    }
+    L.w = end;
+    L.bar = L.w + (uint32_t)L.apc * kUmmaKC * 2;
+    // mbarriers: apc + 3; then 4 words, then T partial sums and T rstd
+    L.total = L.bar + 8u * (uint32_t)(L.apc + 3) + 16u + 8u * (uint32_t)T + 1023u;
+    return L;
+}
 
 struct GemvUmmaParams {
-    const void *x;    // [M,H]
-    const void *r;    // [M,H] residual input, or unused
     const void *w;    // [H]
     void *out;        // [M,N]
     void *h;          // [M,H] residual sum out, or nullptr
@@ -87,7 +137,8 @@ struct GemvUmmaParams {
     float *rstd;      // [M] or nullptr
     int M, H, N;
     int T;            // tokens as the MMA's N: M rounded up to 16 (<= 64)
-    int NS;           // ring stages (16 KB atoms of A), 2 .. kUmmaMaxStages
+    int na;           // atoms of K in a row: ceil(H / 64)
+    UmmaLayout L;     // for T, H, the cluster size and the residual
     float eps;
     int static_w;     // w and A may be read before the wait on the previous kernel
     // test hook of the bounded waits: bytes a copy of A is expected to bring
@@ -96,33 +147,8 @@ struct GemvUmmaParams {
     uint32_t extra_tx, wait_limit_us;
 };
 
-// Bytes of y in shared memory: one swizzle atom of T rows per 64 columns.
-__host__ __device__ constexpr int64_t gemv_umma_y_bytes(int T, int H)
-{
-    return (int64_t)((H + 63) / 64) * T * 128;
-}
-
-// Bytes of w in shared memory (rounded up to 128).
-__host__ __device__ constexpr int64_t gemv_umma_w_bytes(int H)
-{
-    return ((int64_t)H * 2 + 127) / 128 * 128;
-}
-
-// Bytes of shared memory: up to 1023 of alignment, y, NS ring stages, w,
-// 2 NS mbarriers, three words (tensor-memory address, atoms multiplied, a
-// wait ran out), the mbarrier of y's rows from the cluster and the [8][8]
-// row sums of the shared norm.
-__host__ __device__ constexpr int64_t gemv_umma_smem_bytes(int T, int H, int NS)
-{
-    return 1024 + gemv_umma_y_bytes(T, H) + (int64_t)NS * kUmmaStageBytes +
-           gemv_umma_w_bytes(H) + 16 * NS + 16 + 16 + 256;
-}
-
-// CTAs of a cluster sharing the norm (each normalises the 8-row groups g
-// with g % kUmmaCluster = its rank and sends them to the others).
-constexpr int kUmmaCluster = 8;
-
-// Tensor-memory columns of a T-token accumulator (fp32, one column per token).
+// Tensor-memory columns of a T-token accumulator (fp32, one column per
+// token; a power of two, at least 32).
 __host__ __device__ constexpr uint32_t gemv_umma_tmem_cols(int T)
 {
     return T <= 32 ? 32u : (T <= 64 ? 64u : 128u);
@@ -239,6 +265,18 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
+__device__ __forceinline__ void cp_async_wait_all_groups()
+{
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+// Fetch a tensor map (a kernel parameter, by its generic address) into the
+// descriptor cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map))
+                 : "memory");
+}
 
 // Bulk copy of `bytes` (a multiple of 16, 16-byte aligned) from this CTA's
 // shared memory into another CTA's of the cluster, completing on that CTA's
@@ -252,332 +290,429 @@ __device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, uint32_t src, uin
                  : "memory");
 }
 
+// Barrier `id` (not 0: __syncthreads) over `count` threads, whole warps.
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// h = x + r on two packed elements, rounded to nearest even: for bf16 one
+// packed bf16 addition (correctly rounded, so equal to adding in fp32 and
+// rounding: the fp32 sum of two bf16 values is exact unless their exponents
+// differ by more than 15, and then the smaller is far below half an ulp of
+// the larger); fp16 goes through fp32 as the other kernels do.
+template <typename T> __device__ __forceinline__ uint32_t add2_rn(uint32_t a, uint32_t b);
+template <> __device__ __forceinline__ uint32_t add2_rn<bf16>(uint32_t a, uint32_t b)
+{
+    const __nv_bfloat162 s = __hadd2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&b));
+    return *reinterpret_cast<const uint32_t *>(&s);
+}
+template <> __device__ __forceinline__ uint32_t add2_rn<f16>(uint32_t a, uint32_t b)
+{
+    const float2 x = Half16<f16>::wide2(a), y = Half16<f16>::wide2(b);
+    return Half16<f16>::narrow2(x.x + y.x, x.y + y.y);
+}
+
 // This thread's bulk copies issued so far have read their source.
 __device__ __forceinline__ void bulk_wait_read_all()
 {
     asm volatile("cp.async.bulk.commit_group;\ncp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-__device__ __forceinline__ void cp_async_wait_all_groups()
-{
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-}
-
-template <typename T, bool RES, int CS>
+// grid = (N / 128 rounded up) x KS CTAs, cluster = (KS, 1, 1), 256 threads,
+// dynamic shared memory p.L.total.
+template <typename T, bool RES>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
 rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
+              const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR,
               unsigned int *timeouts)
 {
-    static_assert(CS == 1 || CS == kUmmaCluster, "no cluster, or the norm shared by one");
-    const int NS = p.NS;
     using P = Pack<T, 8>;
     using X = Vals<8>;
     using F = float2;
-    // The stage of atom k is refilled with atom k + NS once the MMAs of atom
-    // k are done, waited for after the MMAs of atom k + LAG are issued (LAG
-    // at most NS - 1): the MMAs' completion overlaps LAG atoms, the copies
-    // run NS - LAG atoms ahead. (A lag of 1 measured slower at 64 x 896 ->
-    // 9728: 16.3 against 13.9 us.)
-    const int LAG = NS > kUmmaLag ? kUmmaLag : NS - 1;
+    constexpr int kB = 4;                                     // atoms per batch of loads
+    constexpr int kEarly = 2;                                 // atoms of A before x and r
     extern __shared__ __align__(1024) unsigned char umma_smem[];
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int H = p.H, NP = H / 8, NT = p.T;                 // NT: tokens as the MMA's N
-    const int f0 = blockIdx.x * kUmmaM;
-    const int nk = (H + kUmmaKC - 1) / kUmmaKC;               // K atoms
+    const int H = p.H, NT = p.T, NP = H / 8;                  // NT: tokens as the MMA's N
+    const int KS = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
+    const int f0 = (int)(blockIdx.x / KS) * kUmmaM;           // the tile's first feature
+    const int a0 = rank * p.na / KS;                          // this CTA's atoms of K
+    const int nat = (rank + 1) * p.na / KS - a0;
+    const bool writer = blockIdx.x < (unsigned)KS;            // the first cluster stores
+                                                              // h, y and rstd
+    const UmmaLayout &L = p.L;
     const uint32_t raw_s = smem_addr(umma_smem);
-    unsigned char *ysm = umma_smem + (((raw_s + 1023u) & ~1023u) - raw_s);   // y atoms
-    unsigned char *ring = ysm + gemv_umma_y_bytes(NT, H);     // NS stages of 16 KB
-    unsigned char *wsm = ring + NS * kUmmaStageBytes;         // w [H]
-    const uint32_t y_s = smem_addr(ysm), ring_s = smem_addr(ring);
-    const uint32_t full0 = smem_addr(wsm + gemv_umma_w_bytes(H));   // NS "copy landed"
-    const uint32_t empty0 = full0 + 8 * NS;                           // NS "MMAs done"
-    int *slots = reinterpret_cast<int *>(wsm + gemv_umma_w_bytes(H) + 16 * NS);
-    // slots[0]: tensor-memory address, [1]: atoms multiplied, [2]: a wait ran out
-    const uint32_t ybar = smem_addr(slots) + 16;              // y's rows from the cluster
-    float *red = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(slots) + 32);
+    unsigned char *base = umma_smem + (((raw_s + 1023u) & ~1023u) - raw_s);
+    unsigned char *ysm = base, *rsm = base + L.r, *wsm = base + L.w;
+    const float4 *recv = reinterpret_cast<const float4 *>(base + L.recv);
+    float4 *send = reinterpret_cast<float4 *>(base + L.send);
+    const uint32_t y_s = smem_addr(ysm), r_s = smem_addr(rsm), a_s = smem_addr(base + L.a);
+    const uint32_t recv_s = smem_addr(base + L.recv), send_s = smem_addr(send);
+    // A's atoms land in two groups, each behind one mbarrier (a wait costs
+    // some 200 cycles even when its phase is complete): [0, nh), [nh, nat)
+    const uint32_t abar = smem_addr(base + L.bar);
+    const uint32_t xbar = abar + 8u * (uint32_t)L.apc;        // x and r landed
+    const uint32_t mbar = xbar + 8u, rbar = xbar + 16u;       // MMAs done; products received
+    int *slots = reinterpret_cast<int *>(base + L.bar + 8 * (L.apc + 3));
+    // slots[0]: tensor-memory address, [1]: a wait ran out, [2]: atoms multiplied
+    float *part = reinterpret_cast<float *>(slots + 4);       // [T] sums of h^2, own columns
+    float *rsv = part + NT;                                   // [T] rstd
+    const uint32_t atom = (uint32_t)NT * 128u;                // bytes of an atom of x, r, y
+    const uint32_t block = (uint32_t)kUmmaM * (uint32_t)L.rs * 16u;   // one rank's products
     const uint32_t ncols = gemv_umma_tmem_cols(NT);
     const unsigned long long limit = wait_limit_ns(p.wait_limit_us);
-    const bool has_a = f0 < p.N;                              // the grid may be padded to
-                                                              // whole clusters
-    // The shared norm: 8-row groups g of y, owned by rank g % CS; a CTA
-    // receives every group it does not own, one 1024-byte block per atom.
-    const int ngroups = NT / 8, na = (H + 63) / 64;
-    const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
-    const int owned = ngroups > rank ? (ngroups - 1 - rank) / CS + 1 : 0;
+    const int G4 = NT / 4;                                    // 4-token groups
+    const int own = G4 > rank ? (G4 - 1 - rank) / KS + 1 : 0; // groups this CTA sums
+    const int nh = (nat + 1) / 2;                             // atoms of A's first group
+    constexpr int kWarps = kUmmaThreads / 32;
 
-    // 1. tensor memory and the stage barriers
+    // 1. descriptors, tensor memory and the barriers, by three warps at once
+    if (tid == 64) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmX);
+        if constexpr (RES)
+            prefetch_tmap(&tmR);
+    }
     if (warp == 0) {
         tmem_alloc(smem_addr(slots), ncols);
         tmem_relinquish();
     }
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        if constexpr (CS > 1) {
-            mbar_init(ybar, 1);
-            mbar_expect_tx(ybar, (uint32_t)((ngroups - owned) * na * 1024));
-        }
+    if (tid == 32) {
+        mbar_init(abar, 1);
+        if (nat > nh)
+            mbar_init(abar + 8u, 1);
+        mbar_init(xbar, 1);
+        mbar_init(mbar, 1);
+        mbar_init(rbar, 1);
+        if (own > 0)     // every other CTA of the cluster sends one block
+            mbar_expect_tx(rbar, (uint32_t)(KS - 1) * block);
+        slots[1] = 0;
+        slots[2] = 0;
     }
     mbar_init_fence();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = static_cast<uint32_t>(slots[0]);
-    // Peers write into this CTA's shared memory only once every CTA of the
-    // cluster runs with its barriers initialised: arrive now, wait before
-    // the first such write.
-    if constexpr (CS > 1)
-        cluster_arrive_release();
 
-    // 2. copies of A (thread 0: atom kc into stage kc % NS) and of w
-    auto issue = [&](int kc, int s) {                          // atom kc into stage s
-        mbar_expect_tx(full0 + 8 * s, kUmmaStageBytes + p.extra_tx);
-        tma_load_2d(ring_s + s * kUmmaStageBytes, &tmA, kc * kUmmaKC, f0, full0 + 8 * s);
+    // 2. copies. The tensor copies of one SM are served in order, and x and r
+    //    (the norm's inputs, from L2) are needed first: ahead of them go
+    //    only the atoms of A that static weights allow to start before the
+    //    wait on the previous kernel (at most kEarly), the rest after them.
+    const int c0 = a0 * kUmmaKC;                              // first column of this CTA
+    const int c1 = min(H, (a0 + nat) * kUmmaKC);              // one past its last
+    auto load_a = [&](int i0, int i1) {                       // warp 0, lane i: atom i
+        const int i = i0 + lane;
+        if (i < i1)
+            tma_load_2d(a_s + (uint32_t)i * kUmmaAtomA, &tmA, (a0 + i) * kUmmaKC, f0,
+                        abar + (i < nh ? 0u : 8u));
     };
-    const int first = nk < NS ? nk : NS;                      // atoms copied up front
-    auto prologue = [&]() {
-        if (tid == 0 && has_a)
-            for (int kc = 0; kc < first; ++kc)
-                issue(kc, kc);
-        for (int j = tid; j < NP; j += kUmmaThreads)
-            cp_async16(wsm + j * 16, static_cast<const uint4 *>(p.w) + j);
+    auto load_w = [&]() {
+        for (int j = tid; j < (c1 - c0) / 8; j += kUmmaThreads)
+            cp_async16(wsm + j * 16, static_cast<const uint4 *>(p.w) + c0 / 8 + j);
     };
-    if (p.static_w)
-        prologue();
-    griddep_wait();
-    if (!p.static_w)
-        prologue();
-
-    // 3. the norm
-    {
-        // The norm of this CTA's 8-row groups g = rank, rank + CS, ... (all of
-        // them without a cluster): all 256 threads on one group: lane (row %
-        // 8, pack % 4), warp w takes packs 4 w + (lane / 8) + 32 u; the row
-        // sums of the eight warps meet in shared memory in warp order.
-        const bool writer = blockIdx.x < CS;                  // the first cluster
-        const int r8 = lane & 7, pj = warp * 4 + (lane >> 3);
-        const float fH = (float)H;
-        constexpr int kU = kUmmaMaxH / 8 / 32;                // packs per thread, at most
-        for (int g = rank; g < ngroups; g += CS) {
-            const int t = g * 8 + r8;
-            const bool tok = t < p.M;
-            const int64_t rb = (int64_t)t * NP;
-            P hs[kU];
-            F acc = splat<F>(0.f);
-            {
-                P xs[kU], rsv[kU];
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int j = pj + 32 * u;
-                    xs[u] = P::zero();
-                    rsv[u] = P::zero();
-                    if (tok && j < NP) {
-                        xs[u] = P::load(p.x, rb + j);
-                        if constexpr (RES)
-                            rsv[u] = P::load(p.r, rb + j);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int j = pj + 32 * u;
-                    hs[u] = xs[u];
-                    if (tok && j < NP) {
-                        X a;
-                        if constexpr (RES) {
-                            X b;
-                            xs[u].widen(a);
-                            rsv[u].widen(b);
-#pragma unroll
-                            for (int i = 0; i < X::N; ++i)
-                                a.v[i] = vadd(a.v[i], b.v[i]);
-                            hs[u] = P::narrow(a);             // h as stored
-                            if (writer && p.h != nullptr)
-                                hs[u].store(p.h, rb + j);
-                        }
-                        hs[u].widen(a);
-#pragma unroll
-                        for (int i = 0; i < X::N; ++i)
-                            acc = vfma(a.v[i], a.v[i], acc);
-                    }
-                }
-            }
-            float ss = hsum(acc);
-            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 8);
-            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 16);
-            if (lane < 8)
-                red[warp * 8 + lane] = ss;
-            if (g == rank) {       // w is in (every thread's copies of it)
-                cp_async_wait_all_groups();
-            }
-            __syncthreads();
-            float tot = 0.f;
-#pragma unroll
-            for (int q = 0; q < kUmmaThreads / 32; ++q)
-                tot += red[q * 8 + r8];
-            const float rs = rsqrtf(tot / fH + p.eps);
-            if (tok && writer && pj == 0 && p.rstd != nullptr)
-                p.rstd[t] = rs;
-            const F r2 = splat<F>(rs);
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int j = pj + 32 * u;
-                if (j >= NP)
-                    break;
-                P yv = P::zero();
-                if (tok) {
-                    P wp;
-                    wp.u = *reinterpret_cast<const uint4 *>(wsm + j * 16);
-                    X a, wv;
-                    hs[u].widen(a);
-                    wp.widen(wv);
-#pragma unroll
-                    for (int i = 0; i < X::N; ++i)
-                        a.v[i] = vmul(vmul(a.v[i], r2), wv.v[i]);
-                    yv = P::narrow(a);
-                    if (writer && p.y != nullptr)
-                        yv.store(p.y, rb + j);
-                }
-                *reinterpret_cast<uint4 *>(ysm + sw128_offset(NT, t, j)) = yv.u;
-            }
-            __syncthreads();       // the row sums' slots are reused by the next group
+    const int early = p.static_w ? min(nat, kEarly) : 0;
+    if (warp == 0) {
+        if (lane == 0) {        // each group's bytes, before any of its copies
+            mbar_expect_tx(abar, (uint32_t)nh * (kUmmaAtomA + p.extra_tx));
+            if (nat > nh)
+                mbar_expect_tx(abar + 8u, (uint32_t)(nat - nh) * (kUmmaAtomA + p.extra_tx));
         }
-        if (owned == 0) {          // w unused here, but its copies must land
-            cp_async_wait_all_groups();
+        __syncwarp();
+        load_a(0, early);
+    }
+    if (p.static_w)
+        load_w();
+    griddep_wait();
+    // warp 1 copies x and r (lane i: atom i) and then lets warp 0 copy the
+    // rest of A
+    if (warp == 1) {
+        if (lane == 0)
+            mbar_expect_tx(xbar, atom * (uint32_t)nat * (RES ? 2u : 1u));
+        __syncwarp();
+        if (lane < nat) {
+            tma_load_2d(y_s + (uint32_t)lane * atom, &tmX, (a0 + lane) * kUmmaKC, 0, xbar);
+            if constexpr (RES)
+                tma_load_2d(r_s + (uint32_t)lane * atom, &tmR, (a0 + lane) * kUmmaKC, 0, xbar);
         }
     }
-    // every input but A is read: the next kernel may be scheduled; this
-    // CTA's part of y is complete (and, fenced, visible to the async proxy:
-    // the tensor cores and the bulk copies)
+    if (warp < 2)
+        named_bar_sync(1, 64);
+    if (warp == 0)
+        load_a(early, nat);
+    if (!p.static_w)
+        load_w();
+
+    // 3. the norm. Lane (c8 = lane % 8, rq = lane / 8) of warp w takes the
+    //    16-byte chunk c8 of rows 4 (w + 16 m) + rq of every atom, so a
+    //    quarter-warp reads one row's 128 bytes (all banks once); kB atoms'
+    //    chunks are loaded before any is written back.
+    const int c8 = lane & 7, rq = lane >> 3;
+    const bool xfail = __syncthreads_or(!mbar_wait_bounded(xbar, 0, limit));
+    {
+        F acc[2] = {splat<F>(0.f), splat<F>(0.f)};
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int row = 4 * (warp + kWarps * m) + rq;
+            if (xfail || 4 * (warp + kWarps * m) >= NT)            // warp-uniform
+                break;
+            const uint32_t roff = (uint32_t)row * 128u + ((uint32_t)(c8 ^ (row & 7)) << 4);
+            for (int i0 = 0; i0 < nat; i0 += kB) {
+                uint4 xv[kB], rv[kB];
+#pragma unroll
+                for (int b = 0; b < kB; ++b) {
+                    const int i = i0 + b;
+                    if (i < nat && (a0 + i) * 8 + c8 < NP) {  // zeros past H
+                        xv[b] = *reinterpret_cast<const uint4 *>(ysm + i * atom + roff);
+                        if constexpr (RES)
+                            rv[b] = *reinterpret_cast<const uint4 *>(rsm + i * atom + roff);
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < kB; ++b) {
+                    const int i = i0 + b, col8 = (a0 + i) * 8 + c8;
+                    if (i >= nat || col8 >= NP)
+                        continue;
+                    P hv;
+                    hv.u = xv[b];
+                    X a;
+                    if constexpr (RES) {
+                        hv.u.x = add2_rn<T>(xv[b].x, rv[b].x);   // h as stored
+                        hv.u.y = add2_rn<T>(xv[b].y, rv[b].y);
+                        hv.u.z = add2_rn<T>(xv[b].z, rv[b].z);
+                        hv.u.w = add2_rn<T>(xv[b].w, rv[b].w);
+                        *reinterpret_cast<uint4 *>(ysm + i * atom + roff) = hv.u;
+                        if (writer && p.h != nullptr && row < p.M)
+                            hv.store(p.h, (int64_t)row * NP + col8);
+                    }
+                    hv.widen(a);
+#pragma unroll
+                    for (int e = 0; e < X::N; ++e)
+                        acc[m] = vfma(a.v[e], a.v[e], acc[m]);
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int row = 4 * (warp + kWarps * m) + rq;
+            float s = hsum(acc[m]);
+            s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+            s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+            s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
+            if (c8 == 0 && row < NT)
+                part[row] = s;
+        }
+    }
+    // The partial sums are published, and this CTA is done with r's area
+    // (the peers' copies of partial products may land there after the
+    // barrier): order its accesses before the barrier, for both proxies.
+    fence_proxy_async_smem();
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (tid < NT) {
+        float tot = 0.f;
+        for (int q = 0; q < KS; ++q)                          // rank order
+            tot += ld_cluster_f32(part + tid, (uint32_t)q);
+        const float rs = rsqrtf(tot / (float)H + p.eps);
+        rsv[tid] = rs;
+        if (writer && rank == 0 && p.rstd != nullptr && tid < p.M)
+            p.rstd[tid] = rs;
+    }
+    cp_async_wait_all_groups();                               // this thread's part of w
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const int row = 4 * (warp + kWarps * m) + rq;
+        if (xfail || 4 * (warp + kWarps * m) >= NT)
+            break;
+        const uint32_t roff = (uint32_t)row * 128u + ((uint32_t)(c8 ^ (row & 7)) << 4);
+        const F r2 = splat<F>(rsv[row]);
+        for (int i0 = 0; i0 < nat; i0 += kB) {
+            uint4 hv[kB], wv[kB];
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                const int i = i0 + b;
+                if (i < nat && (a0 + i) * 8 + c8 < NP) {
+                    hv[b] = *reinterpret_cast<const uint4 *>(ysm + i * atom + roff);
+                    wv[b] = *reinterpret_cast<const uint4 *>(wsm + (i * 8 + c8) * 16);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                const int i = i0 + b, col8 = (a0 + i) * 8 + c8;
+                if (i >= nat || col8 >= NP)
+                    continue;
+                P h8, w8;
+                h8.u = hv[b];
+                w8.u = wv[b];
+                X a, e8;
+                h8.widen(a);
+                w8.widen(e8);
+#pragma unroll
+                for (int e = 0; e < X::N; ++e)
+                    a.v[e] = vmul(vmul(a.v[e], r2), e8.v[e]);
+                const P yv = P::narrow(a);
+                *reinterpret_cast<uint4 *>(ysm + i * atom + roff) = yv.u;
+                if (writer && p.y != nullptr && row < p.M)
+                    yv.store(p.y, (int64_t)row * NP + col8);
+            }
+        }
+    }
+    // every input but A is read: the next kernel may be scheduled; y is
+    // complete and, fenced, visible to the tensor cores
     griddep_launch_dependents();
     fence_proxy_async_smem();
     __syncthreads();
-    bool y_failed = false;
-    if constexpr (CS > 1) {
-        // send each owned group's block of every atom to the other CTAs,
-        // then wait for theirs
-        cluster_wait_acquire();
-        const int ncopy = owned * na * (CS - 1);
-        for (int i = tid; i < ncopy; i += kUmmaThreads) {
-            const int d = 1 + i % (CS - 1), rest = i / (CS - 1);
-            const int a = rest % na, g = rank + (rest / na) * CS;
-            const uint32_t off = (uint32_t)(a * NT * 128 + g * 1024);
-            const uint32_t peer = (uint32_t)((rank + d) % CS);
-            bulk_s2s_cluster(cluster_map(y_s + off, peer), y_s + off, 1024,
-                             cluster_map(ybar, peer));
-        }
-        const bool ok = mbar_wait_bounded(ybar, 0, limit);
-        y_failed = __syncthreads_or(!ok);
-    }
 
-    // 4. thread 0 walks the K atoms: MMAs as each atom lands, the stage of
-    //    the atom before refilled once its MMAs are done
+    // 4. thread 0: four MMAs per atom of A, a group of atoms once its copies
+    //    have landed, one commit. The descriptors advance by adding to their
+    //    start-address field (16-byte units): 32 bytes per 16-column step,
+    //    an atom per atom.
     if (tid == 0) {
         const uint32_t idesc = umma_idesc_f16(UmmaFormat<T>::value, kUmmaM, NT);
-        int loaded = has_a ? first : 0;                       // atoms whose copy started
-        int kc = 0;
-        bool failed = y_failed;
-        tc_fence_after_sync();
-        // stage and phase parity of atom kc, and of atom kc - LAG (the one
-        // refilled), advanced without dividing
-        int s = 0, ps = 0;
-        uint32_t ph = 0, pph = 0;
-        for (; has_a && !failed && kc < nk; ++kc) {
-            if (!mbar_wait_bounded(full0 + 8 * s, ph, limit)) {
+        const uint64_t da0 = umma_desc_sw128(a_s), db0 = umma_desc_sw128(y_s);
+        bool failed = xfail;
+        int i = 0, gi = 0;
+        for (; !failed && gi < 2; ++gi) {
+            const int i1 = gi == 0 ? nh : nat;
+            if (i >= i1)
+                break;                                        // no second group
+            if (!mbar_wait_bounded(abar + 8u * (uint32_t)gi, 0, limit)) {
                 failed = true;
                 break;
             }
             tc_fence_after_sync();
-            const int ksteps = min(kUmmaKC, H - kc * kUmmaKC) / 16;
-            for (int k4 = 0; k4 < ksteps; ++k4) {
-                const uint64_t ad = umma_desc_sw128(ring_s + s * kUmmaStageBytes + k4 * 32);
-                const uint64_t bd = umma_desc_sw128(y_s + kc * NT * 128 + k4 * 32);
-                umma_f16(tmem, ad, bd, idesc, (kc | k4) != 0 ? 1u : 0u);
-            }
-            umma_commit(empty0 + 8 * s);
-            if (kc >= LAG) {
-                if (kc - LAG + NS < nk) {
-                    if (!mbar_wait_bounded(empty0 + 8 * ps, pph, limit)) {
-                        failed = true;
-                        ++kc;                                 // atom kc's MMAs were issued
-                        break;
-                    }
-                    issue(kc - LAG + NS, ps);                 // the same stage
-                    ++loaded;
+            for (; i < i1; ++i) {
+                const uint64_t da = da0 + (uint64_t)(i * (int)(kUmmaAtomA >> 4));
+                const uint64_t db = db0 + (uint64_t)(i * (int)(atom >> 4));
+                if (H - (a0 + i) * kUmmaKC >= kUmmaKC) {
+#pragma unroll
+                    for (int k4 = 0; k4 < kUmmaKC / 16; ++k4)
+                        umma_f16(tmem, da + 2 * k4, db + 2 * k4, idesc, (i | k4) != 0 ? 1u : 0u);
+                } else {                                      // the last, partial atom
+                    const int ksteps = (H - (a0 + i) * kUmmaKC) / 16;
+                    for (int k4 = 0; k4 < ksteps; ++k4)
+                        umma_f16(tmem, da + 2 * k4, db + 2 * k4, idesc, (i | k4) != 0 ? 1u : 0u);
                 }
-                if (++ps == NS) {
-                    ps = 0;
-                    pph ^= 1u;
-                }
-            }
-            if (++s == NS) {
-                s = 0;
-                ph ^= 1u;
             }
         }
-        slots[1] = kc;                                        // atoms whose MMAs were issued
-        slots[2] = failed ? 1 : 0;
+        if (i > 0)
+            umma_commit(mbar);
+        slots[1] = failed ? 1 : 0;
+        slots[2] = i;                                         // atoms whose MMAs were issued
         if (failed)            // let the copies started and not waited for land
-            for (int q = kc; q < loaded; ++q)
-                (void)mbar_wait_bounded(full0 + 8 * (q % NS), (uint32_t)((q / NS) & 1), limit);
+            for (int g = gi; g < (nat > nh ? 2 : 1); ++g)
+                (void)mbar_wait_bounded(abar + 8u * (uint32_t)g, 0, limit);
     }
     __syncthreads();
-    const int issued = slots[1];
-    const bool failed = slots[2] != 0;
+    bool failed = slots[1] != 0;
+    if (slots[2] > 0)
+        failed = __syncthreads_or(!mbar_wait_bounded(mbar, 0, limit)) || failed;
 
-    // 5. the accumulator, once the last issued atom's MMAs (and with them
-    //    every earlier one) are complete
-    bool done = true;
-    if (issued > 0) {
-        const int lc = issued - 1;
-        const bool ok = mbar_wait_bounded(empty0 + 8 * (lc % NS), (uint32_t)((lc / NS) & 1), limit);
-        done = !__syncthreads_or(!ok);
-    }
-    if (failed || !done) {
-        if (tid == 0)
-            atomicAdd(timeouts, 1u);
-    } else {
-        tc_fence_after_sync();
+    // 5. the partial products of each 4-token group g go to its owner, rank
+    //    g % KS, slot g / KS: the own ones straight into this CTA's receive
+    //    area, the others into the send area, one block per owner, copied in
+    //    bulk (zeros when this CTA failed, so that no owner waits for them)
+    tc_fence_after_sync();
+    {
+        float4 *recv_own = reinterpret_cast<float4 *>(base + L.recv);
         const int q4 = warp & 3;                              // lane quarter
-        const int f = f0 + q4 * 32 + lane;
+        const int fl = q4 * 32 + lane;                        // feature within the tile
         const uint32_t tw = tmem + ((uint32_t)(q4 * 32) << 16);
-        for (int c0 = 16 * (warp >> 2); c0 < NT; c0 += 32) {  // token blocks by warp pair
+        for (int t0 = 16 * (warp >> 2); t0 < NT; t0 += 16 * (kWarps / 4)) {   // token blocks
             uint32_t v[16];
-            tmem_ld16(tw + (uint32_t)c0, v);
-            if (f < p.N) {
+            if (!failed) {
+                tmem_ld16(tw + (uint32_t)t0, v);
+            } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = c0 + i;
+                for (int e = 0; e < 16; ++e)
+                    v[e] = 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int g = t0 / 4 + j;                     // 4-token group
+                const int owner = g % KS, slot = g / KS;
+                const float4 o = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                             __uint_as_float(v[4 * j + 2]),
+                                             __uint_as_float(v[4 * j + 3]));
+                if (owner == rank)
+                    recv_own[(rank * kUmmaM + fl) * L.rs + slot] = o;
+                else
+                    send[(owner * kUmmaM + fl) * L.rs + slot] = o;
+            }
+        }
+    }
+    // the tensor memory is read (free it now) and the send area written
+    // (visible to the bulk copies)
+    tc_fence_before_sync();
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, ncols);
+    }
+    if (tid == 0)
+        for (int d = 1; d < KS; ++d) {
+            const int o = (rank + d) % KS;
+            if (G4 > o)                                       // o owns a group
+                bulk_s2s_cluster(cluster_map(recv_s + (uint32_t)rank * block, (uint32_t)o),
+                                 send_s + (uint32_t)o * block, block,
+                                 cluster_map(rbar, (uint32_t)o));
+        }
+    bool got = true;
+    if (own > 0)
+        got = !__syncthreads_or(!mbar_wait_bounded(rbar, 0, limit));
+    if (got && !failed) {
+        // sum the KS partials of each owned group in rank order, round, store
+        for (int idx = tid; idx < kUmmaM * own; idx += kUmmaThreads) {
+            const int fl = idx % kUmmaM, slot = idx / kUmmaM;
+            const int g = slot * KS + rank;
+            float4 pv[kUmmaMaxCluster];
+#pragma unroll
+            for (int q = 0; q < kUmmaMaxCluster; ++q)
+                if (q < KS)
+                    pv[q] = recv[(q * kUmmaM + fl) * L.rs + slot];
+            float4 s = pv[0];
+#pragma unroll
+            for (int q = 1; q < kUmmaMaxCluster; ++q)
+                if (q < KS) {
+                    s.x += pv[q].x;
+                    s.y += pv[q].y;
+                    s.z += pv[q].z;
+                    s.w += pv[q].w;
+                }
+            const int f = f0 + fl;
+            if (f < p.N) {
+                const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = 4 * g + e;
                     if (t < p.M) {
                         Vals<1> o;
-                        o.v[0] = __uint_as_float(v[i]);
+                        o.v[0] = sv[e];
                         Pack<T, 1>::narrow(o).store(p.out, (int64_t)t * p.N + f);
                     }
                 }
             }
         }
     }
+    if ((failed || !got) && tid == 0)
+        atomicAdd(timeouts, 1u);
 
-    // 6. with a cluster: this CTA's copies have read their source, the
-    //    others' copies into it have landed (waited for again, bounded, if
-    //    that wait ran out), and no CTA leaves before all are done
-    if constexpr (CS > 1) {
-        if (y_failed && tid == 0)
-            (void)mbar_wait_bounded(ybar, 0, limit);
+    // 6. the products this CTA waited for have landed (waited for again,
+    //    bounded, if that wait ran out) and its own copies have read their
+    //    source; no CTA leaves while a peer may still read its partial sums
+    //    or copy products into it
+    if (tid == 0) {
+        if (!got)
+            (void)mbar_wait_bounded(rbar, 0, limit);
         bulk_wait_read_all();
-        cluster_arrive_release();
-        cluster_wait_acquire();
     }
-    // free the tensor memory (every tcgen05 access of the CTA is ordered
-    // before it by the barrier)
-    tc_fence_before_sync();
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after_sync();
-        tmem_dealloc(tmem, ncols);
-    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
 }
 
 } // namespace rmsk

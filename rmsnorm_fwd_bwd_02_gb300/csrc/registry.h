@@ -100,10 +100,10 @@ struct GemvKernels {
 };
 extern const GemvKernels gemv_kernels;       // A in registers (gemv.cuh)
 extern const GemvKernels gemv_tma_kernels;   // A by bulk copies (gemv_tma.cuh)
-// The product on tcgen05 (gemv_umma.cuh): fn[bf16 = 0, fp16 = 1][residual]
-//   [0: no cluster, 1: the norm shared by a cluster of kUmmaCluster]
+// The product on tcgen05, K split over a cluster (gemv_umma.cuh):
+// fn[bf16 = 0, fp16 = 1][residual]
 struct GemvUmmaKernels {
-    const void *fn[2][2][2];
+    const void *fn[2][2];
 };
 extern const GemvUmmaKernels gemv_umma_kernels;
 // Device address of the counter of streamed-kernel waits that ran out.

@@ -28,14 +28,32 @@ DEV = torch.device("cuda:0")
 KERNELS = {"regs": rn.PATH_ROWS, "tma": rn.PATH_GEMV_TMA, "umma": rn.PATH_GEMV_UMMA}
 
 
-def umma_fits(M, H):
-    """Whether the tcgen05 kernel takes the call: H <= 2048 and y (M rounded
-    up to 16 rows, 64-column swizzle atoms), w and a ring of two 16 KB
-    atoms of A in 227 KB."""
+def umma_layout_bytes(T, H, KS, res):
+    """Shared memory of one CTA of the tcgen05 kernel for T tokens, H
+    features, K split over KS CTAs: its atoms (64 columns) of y, r (with the
+    residual) and A (128 rows), the partial products received (over r when
+    they fit there) and sent (over A when they fit there), w, 3 + atoms
+    mbarriers, 16 bytes of words, the partial sums and rstd of T tokens,
+    1023 bytes of alignment."""
+    na = (H + 63) // 64
+    apc = (na + KS - 1) // KS
+    rs = ((T // 4 + KS - 1) // KS) | 1
+    y = apc * T * 128
+    r = y if res else 0
+    a = apc * 16384
+    xchg = KS * 128 * rs * 16
+    total = y + r + a + (0 if r >= xchg else xchg) + (0 if a >= xchg else xchg)
+    return total + apc * 128 + 8 * (apc + 3) + 16 + 8 * T + 1023
+
+
+def umma_fits(M, H, res=True):
+    """Whether the tcgen05 kernel takes the call: at most 64 tokens, H a
+    multiple of 16, and a cluster of at most 8 CTAs (no more than the atoms
+    of K) whose shared memory fits in 227 KB."""
     T = (M + 15) // 16 * 16
-    y = (H + 63) // 64 * T * 128
-    w = (2 * H + 127) // 128 * 128
-    return H <= 2048 and H % 16 == 0 and 1024 + y + 2 * 16384 + w + 2 * 16 + 288 <= 227 * 1024
+    na = (H + 63) // 64
+    return T <= 64 and H % 16 == 0 and any(
+        umma_layout_bytes(T, H, ks, res) <= 227 * 1024 for ks in range(1, min(8, na) + 1))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -83,7 +101,7 @@ def run(inp, residual, eps=1e-6, want_y=True, static=False, kernel="tma"):
         assert path == rn.PATH_GEMV, path
     elif kernel == "tma":
         assert path in (rn.PATH_GEMV, rn.PATH_GEMV_TMA), path
-    elif umma_fits(M, H):
+    elif umma_fits(M, H, residual):
         assert path == rn.PATH_GEMV_UMMA, (M, H, path)
     else:
         assert path in (rn.PATH_GEMV, rn.PATH_GEMV_TMA), (M, H, path)
@@ -160,15 +178,19 @@ def test_decode_workloads_full(orc, name):
                     om, wm.dtype)
 
 
-def test_automatic_choice_is_the_bulk_copy_kernel():
-    """The bulk-copy kernel wherever its ring fits (the tcgen05 kernel runs
-    only when forced)."""
+def test_automatic_choice():
+    """Up to 8 rows the bulk-copy kernel (wherever its ring fits); above, the
+    tcgen05 kernel wherever a cluster of it fits, else the bulk-copy one."""
     for M, H, N in ((1, 896, 2048), (8, 896, 9728), (9, 896, 2048), (64, 896, 2048),
                     (64, 896, 9728), (16, 4096, 6144), (1, 6720, 64)):
         inp = synth(M, H, N, torch.bfloat16, seed=2, residual=True)
         g = {k: v.to(DEV) for k, v in inp.items()}
         rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"])
-        assert rn.last_path() == rn.PATH_GEMV_TMA, (M, H, N, rn.last_path())
+        want = rn.PATH_GEMV_UMMA if M > 8 and umma_fits(M, H) else rn.PATH_GEMV_TMA
+        got = rn.last_path()
+        if want == rn.PATH_GEMV_TMA and got == rn.PATH_GEMV:
+            want = rn.PATH_GEMV          # no ring of the bulk-copy kernel fits either
+        assert got == want, (M, H, N, got)
     torch.cuda.synchronize()
 
 
@@ -199,8 +221,9 @@ def test_deterministic_and_optional_outputs(orc):
         check_bits(f"static weights {k}", c[k], a[k])
     # the other kernels: the same h bits; y within one ulp (their norms run
     # the fp32 sums in other orders); each deterministic too
+    forced = {}
     for other in ("regs", "umma"):
-        d = run(inp, True, kernel=other)
+        d = forced[other] = run(inp, True, kernel=other)
         check_bits(f"{other} vs tma h", d["h"], a["h"])
         ya = a["y"].view(torch.int16).to(torch.int32).cpu()
         yd = d["y"].view(torch.int16).to(torch.int32).cpu()
@@ -208,14 +231,14 @@ def test_deterministic_and_optional_outputs(orc):
         e = run(inp, True, kernel=other)
         for k in ("out", "h", "y", "rstd"):
             check_bits(f"{other} run-to-run {k}", e[k], d[k])
-    # no y, no h, no rstd: out unchanged (the automatic choice is the
-    # bulk-copy kernel)
+    # no y, no h, no rstd: out unchanged (the automatic choice at 17 rows is
+    # the tcgen05 kernel)
     g = {k: v.to(DEV) for k, v in inp.items()}
     out, h, rstd = rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], want_h=False)
     torch.cuda.synchronize()
-    assert rn.last_path() == rn.PATH_GEMV_TMA
+    assert rn.last_path() == rn.PATH_GEMV_UMMA
     assert h is None and rstd is None
-    check_bits("out without optional outputs", out, a["out"])
+    check_bits("out without optional outputs", out, forced["umma"]["out"])
 
 
 def test_guard_words_untouched(orc):
