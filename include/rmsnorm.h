@@ -63,7 +63,7 @@ typedef enum {
                                      size (16 bytes for the workspace) */
     RMSNORM_ERR_WORKSPACE = -6,   /* workspace NULL or smaller than
                                      rmsnorm_bwd_workspace_bytes() */
-    RMSNORM_ERR_UNSUPPORTED = -7, /* H > RMSNORM_MAX_H */
+    RMSNORM_ERR_UNSUPPORTED = -7, /* H > RMSNORM_MAX_H, or outside an entry point's limits */
     RMSNORM_ERR_CUDA = -8,        /* a CUDA runtime call failed */
     RMSNORM_ERR_ALIAS = -9,       /* buffers overlap in a way not allowed */
     RMSNORM_ERR_SCRATCH_LIMIT = -10, /* rmsnorm_bwd_static_scratch: the problem
@@ -226,10 +226,16 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
  *   y [M,H] out or NULL (the norm's output, when a caller needs it too);
  *   rstd [M] fp32 out or NULL. All dense row-major.
  * Limits (else RMSNORM_ERR_UNSUPPORTED): dtype RMSNORM_BF16 or RMSNORM_F16;
- *   M <= 64 (decode batches); H a multiple of 32 with
- *   ceil(M/16) * (16 * (2H + 64) + 2048) + 2H + 16 <= 227 KB, i.e.
- *   H <= 6720 for M <= 16, 3424 for M <= 32, 2272 for M <= 48, 1664 for
- *   M <= 64;
+ *   M <= 64 (decode batches); H a multiple of 32 that one of the kernels
+ *   holds in shared memory: the warp-level MMA kernels when
+ *   ceil(M/16) * (16 * (2H + 64) + 2048) + 2H + 16 <= 227 KB (H <= 6720
+ *   for M <= 16, 3424 for M <= 32, 2272 for M <= 48, 1664 for M <= 64),
+ *   or above 8 rows the tcgen05 kernel, whose K is split over a cluster of
+ *   up to 8 CTAs (with r: H <= 4608 for M <= 32, 4096 for M <= 48, 3584
+ *   for M <= 64; without r: 5120 for M <= 32). Calls only the tcgen05
+ *   kernel holds also return RMSNORM_ERR_UNSUPPORTED when another kernel
+ *   is forced (rmsnorm_set_path_override) or the driver offers no
+ *   tensor-map encoder;
  *   1 <= N < 2^30 (else RMSNORM_ERR_BAD_SHAPE).
  * Alignment: x, r, w, A, h, y 16-byte aligned (RMSNORM_ERR_MISALIGNED).
  * Aliasing: no output (out, h, y, rstd) may share a byte with an input or

@@ -890,6 +890,19 @@ struct GemvUmmaPlan {
     const void *fn;
 };
 
+// Whether some cluster of the tcgen05 kernel fits (M rows, H features).
+bool gemv_umma_fits(int64_t M, int64_t H, bool res)
+{
+    const int T = (int)((M + 15) / 16 * 16);
+    const int na = (int)((H + kUmmaKC - 1) / kUmmaKC);
+    if (T > 64 || H % 16 != 0)
+        return false;
+    for (int ks = 1; ks <= kUmmaMaxCluster && ks <= na; ++ks)
+        if ((int64_t)gemv_umma_layout(T, (int)H, ks, res).total <= kGemvMaxSmem)
+            return true;
+    return false;
+}
+
 int gemv_umma_plan(int64_t M, int64_t H, int64_t N, bool res, int dt, int dev, GemvUmmaPlan *pl)
 {
     pl->T = (int)((M + 15) / 16 * 16);
@@ -997,6 +1010,11 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
         }
     }
 
+    // The warp-level MMA kernels need y (16-row tiles) and w in shared
+    // memory: a call accepted for the tcgen05 kernel alone stops here when
+    // that kernel was not taken (override 1 or 6, or no tensor-map encoder).
+    if (gemv_smem_bytes(MT, half, (int)M, (int)H, false) > kGemvMaxSmem)
+        return RMSNORM_ERR_UNSUPPORTED;
     GemvTmaPlan pl;
     bool tma = ov != kPathRows && gemv_tma_plan(M, H, N, r != nullptr, sms, 0, &pl);
     auto tma_fn = [&]() {
@@ -1178,8 +1196,11 @@ int rmsnorm_gemv_fwd(const void *x, const void *r, const void *w, const void *A,
         return RMSNORM_ERR_BAD_SHAPE;
     if (dtype == RMSNORM_F32 || M > kGemvMaxRows || H % 32 != 0)
         return RMSNORM_ERR_UNSUPPORTED;
+    // the warp-level MMA kernels fit, or above kGemvUmmaMinRows rows the
+    // tcgen05 kernel does
     const int MT = (int)((M + 15) / 16);
-    if (gemv_smem_bytes(MT > 0 ? MT : 1, false, (int)M, (int)H, false) > kGemvMaxSmem)
+    if (gemv_smem_bytes(MT > 0 ? MT : 1, false, (int)M, (int)H, false) > kGemvMaxSmem &&
+        !(M > kGemvUmmaMinRows && gemv_umma_fits(M, H, r != nullptr)))
         return RMSNORM_ERR_UNSUPPORTED;
     if (h != nullptr && r == nullptr)
         return RMSNORM_ERR_NULLPTR;
@@ -1256,7 +1277,7 @@ const char *rmsnorm_status_string(int status)
     case RMSNORM_ERR_BAD_EPS: return "eps must be finite and >= 0";
     case RMSNORM_ERR_MISALIGNED: return "pointer not aligned to its element size (workspace: 16 bytes)";
     case RMSNORM_ERR_WORKSPACE: return "workspace missing or smaller than rmsnorm_bwd_workspace_bytes()";
-    case RMSNORM_ERR_UNSUPPORTED: return "H exceeds RMSNORM_MAX_H";
+    case RMSNORM_ERR_UNSUPPORTED: return "H exceeds RMSNORM_MAX_H, or the call is outside the limits of its entry point";
     case RMSNORM_ERR_CUDA: return "a CUDA runtime call failed (see rmsnorm_last_cuda_error)";
     case RMSNORM_ERR_ALIAS: return "output buffers overlap inputs or each other in a way not allowed";
     case RMSNORM_ERR_BAD_FLAGS: return "unknown bits in flags";

@@ -181,6 +181,13 @@ def test_gemv_argument_checks(lib):
     assert call(M=65) == UNSUPPORTED
     assert call(H=900) == UNSUPPORTED
     assert call(M=64, H=4096) == UNSUPPORTED
+    # wider rows that only the tcgen05 kernel holds pass the checks (and then
+    # fail on the missing device)
+    assert call(M=64, H=3584) == CUDA
+    assert call(M=64, H=3616) == UNSUPPORTED
+    assert call(M=32, H=4608, r=E) == CUDA
+    assert call(M=32, H=4640, r=E) == UNSUPPORTED
+    assert call(M=8, H=6752) == UNSUPPORTED
     assert call(dtype=F32) == UNSUPPORTED
     assert call(N=0) == BAD_SHAPE
     assert call(h=E) == NULLPTR

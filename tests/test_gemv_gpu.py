@@ -160,6 +160,29 @@ def test_gemv_largest_shared_memory(orc, kernel, H, M):
             torch.bfloat16)
 
 
+@pytest.mark.parametrize("H,M", [(4608, 32), (4096, 48), (3584, 64), (4096, 17)])
+def test_gemv_widest_rows_tcgen05_only(orc, H, M):
+    """Rows that only the tcgen05 kernel holds (K split over a cluster of up
+    to 8 CTAs), with the residual: right through the automatic choice, and
+    refused when a warp-level MMA kernel is forced."""
+    inp = synth(M, H, 300, torch.bfloat16, seed=H + M, residual=True)
+    assert umma_fits(M, H, True)
+    o = oracle_all(orc, inp, True)
+    compare(f"widest tcgen05 H={H} M={M}", run(inp, True, kernel="umma"), o, torch.bfloat16)
+    g = {k: v.to(DEV) for k, v in inp.items()}
+    out, _, _ = rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"])
+    torch.cuda.synchronize()
+    assert rn.last_path() == rn.PATH_GEMV_UMMA
+    check_rows(f"widest tcgen05 automatic H={H} M={M}", out, o["out"], torch.bfloat16, o["tout"])
+    for forced in (rn.PATH_GEMV_TMA, rn.PATH_ROWS):
+        rn.set_path_override(forced)
+        try:
+            with pytest.raises(rn.RmsNormError):
+                rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"])
+        finally:
+            rn.set_path_override(rn.PATH_AUTO)
+
+
 @pytest.mark.parametrize("name", ["decode-qkv-m1", "decode-gateup-m1"])
 def test_decode_workloads_full(orc, name):
     wl = W.WORKLOADS[name]
