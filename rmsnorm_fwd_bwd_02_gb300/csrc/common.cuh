@@ -491,4 +491,11 @@ __device__ __forceinline__ void griddep_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" :::);
 }
 
+// Bring the line holding p into L2 (L2 is the coherence point, so what a
+// later load finds there is never stale). Holds no register.
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 } // namespace rmsk

@@ -97,11 +97,6 @@ template <> struct MmaOp<f16> {
     }
 };
 
-__device__ __forceinline__ void prefetch_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ uint4 lds_v4(const unsigned char *p)
 {
     return *reinterpret_cast<const uint4 *>(p);
