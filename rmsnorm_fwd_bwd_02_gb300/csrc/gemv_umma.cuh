@@ -55,8 +55,10 @@
 //     KS partials of its groups in rank order (deterministic), rounds and
 //     stores out[token][feature]. The tensor memory is freed as soon as it
 //     is read.
-//  6. A last cluster barrier: no CTA leaves while another may still read its
-//     partial sums or copy products into it.
+//  6. A CTA leaves once the copies into it have landed, its own copies have
+//     read their source and every CTA of the cluster has read the partial
+//     sums it needed (a cluster barrier arrived at right after that read and
+//     waited for only here).
 //
 // Every mbarrier wait is bounded (about one second, or the test limit); one
 // that runs out counts in the streamed-kernel timeout counter, the CTA skips
@@ -177,13 +179,6 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr)
 {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(16 >> 4) << 16) |
            ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Byte offset of 16-byte chunk c8 (columns 8 c8 .. 8 c8 + 7) of row i in a
-// swizzled K-major matrix of R rows.
-__device__ __forceinline__ uint32_t sw128_offset(int R, int i, int c8)
-{
-    return (uint32_t)((c8 >> 3) * R * 128 + i * 128 + (((c8 & 7) ^ (i & 7)) << 4));
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
@@ -521,6 +516,9 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
         if (writer && rank == 0 && p.rstd != nullptr && tid < p.M)
             p.rstd[tid] = rs;
     }
+    // done with the peers' shared memory: a CTA waits for this arrival of
+    // every CTA only when it leaves
+    cluster_arrive_release();
     cp_async_wait_all_groups();                               // this thread's part of w
     __syncthreads();
 #pragma unroll
@@ -705,13 +703,12 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
     // 6. the products this CTA waited for have landed (waited for again,
     //    bounded, if that wait ran out) and its own copies have read their
     //    source; no CTA leaves while a peer may still read its partial sums
-    //    or copy products into it
+    //    (the peers arrived after reading them)
     if (tid == 0) {
         if (!got)
             (void)mbar_wait_bounded(rbar, 0, limit);
         bulk_wait_read_all();
     }
-    cluster_arrive_release();
     cluster_wait_acquire();
 }
 
