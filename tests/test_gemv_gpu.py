@@ -10,9 +10,11 @@ fill one to four 16-row MMA tiles (and leave them ragged), feature counts,
 output counts that leave the last 8-row tile of A ragged, with and without
 the residual add, for the three kernels: the weight in registers (gemv.cuh,
 forced with the row-wise path override), the weight fed by bulk copies
-(gemv_tma.cuh) and the product on tcgen05 (gemv_umma.cuh), each forced with
-its own override; a kernel whose shared memory does not fit the call falls
-back to the next.
+(gemv_tma.cuh) and the product on tcgen05 with K split over a cluster
+(gemv_umma.cuh), each forced with its own override; a kernel whose shared
+memory does not fit the call falls back to the next, and rows only the
+tcgen05 kernel holds are refused when a warp-level kernel is forced. The
+automatic choice (bulk copies up to 8 rows, tcgen05 above) is checked too.
 """
 import pytest
 import torch
