@@ -294,13 +294,16 @@ def test_guard_words_untouched(orc):
                         "rstd": rstd}, o, torch.float16)
 
 
-def test_cuda_graph_replay(orc):
+@pytest.mark.parametrize("rows", [1, 24])
+def test_cuda_graph_replay(orc, rows):
     """Captured once and replayed with new activations copied into the
-    static inputs (the decode loop of the article's §4)."""
-    wl = W.WORKLOADS["decode-qkv-m1"]
+    static inputs (the decode loop of the article's §4): one row (the
+    bulk-copy kernel) and 24 rows (the tcgen05 kernel, whose tensor maps
+    are captured with the launch)."""
+    wl = W.WORKLOADS["decode-qkv-m1"].with_rows(rows)
     inp = W.make_inputs(wl)
     g = {k: v.to(DEV) for k, v in inp.items()}
-    out = torch.empty(1, wl.N, device=DEV, dtype=wl.dtype)
+    out = torch.empty(rows, wl.N, device=DEV, dtype=wl.dtype)
     h = torch.empty_like(g["x"])
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -312,8 +315,9 @@ def test_cuda_graph_replay(orc):
     with torch.cuda.graph(graph):
         rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], out=out, h=h,
                             static_weights=True)
+    assert rn.last_path() == (rn.PATH_GEMV_TMA if rows == 1 else rn.PATH_GEMV_UMMA)
     for step in range(3):
-        x2 = (torch.randn(1, wl.H, generator=torch.Generator().manual_seed(step))
+        x2 = (torch.randn(rows, wl.H, generator=torch.Generator().manual_seed(step))
               ).to(wl.dtype)
         g["x"].copy_(x2.to(DEV))
         graph.replay()
