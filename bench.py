@@ -78,7 +78,6 @@ def read_peaks():
 
 
 L2_BYTES = 129 * 2 ** 20
-EVERY = 8        # per-call CUDA events on one step in EVERY (see run_ours)
 
 
 def streams_from_hbm(wl):
@@ -466,6 +465,193 @@ def gpu_uuid():
         return None
 
 
+PER_CALL_N = 200   # calls per direction in the per-call statistics
+
+
+def time_back_to_back(stream, fns, n):
+    """Mean ms per call of n consecutive calls fns[i % len(fns)]() on
+    `stream`, with events at the two ends only, so consecutive launches keep
+    their programmatic-dependent-launch overlap (as a caller runs them)."""
+    for f in fns:                      # warm: every buffer set once
+        f()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for i in range(n):
+        fns[i % len(fns)]()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / n
+
+
+def time_each(stream, fns, n):
+    """Per-call ms of n calls, each between its own pair of events on
+    `stream`. An event between two launches stops the second from starting
+    while the first drains, so these are isolated-call times, a little
+    slower than back-to-back calls."""
+    for f in fns:
+        f()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    ev[0].record(stream)
+    for i in range(n):
+        fns[i % len(fns)]()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+
+
+def build_sets(rn, wl, dev):
+    """Rotating device buffer sets for the workload (see buffer_sets), with
+    their C-ABI calls bound to the current stream."""
+    src = W.make_inputs(wl)
+    w = src["w"].to(dev)
+    ws = torch.empty(max(16, rn.bwd_workspace_bytes(wl.M, wl.H, wl.dtype)),
+                     device=dev, dtype=torch.uint8)
+    sets = [Calls(rn, wl, src, dev, ws, w) for _ in range(buffer_sets(wl))]
+    if wl.N:
+        # decode: the activations (x, r and the outputs) are one small set
+        # that stays in L2, as the previous kernel's output would; only the
+        # projection weights rotate, so each call streams its weight from HBM
+        for c in sets[1:]:
+            c.x, c.r, c.h, c.out = sets[0].x, sets[0].r, sets[0].h, sets[0].out
+            c.bind(torch.cuda.current_stream())
+    return src, sets
+
+
+def uses_graph(wl):
+    """Decode-sized steps are a few microseconds of GPU work, less than the
+    host needs to issue them one by one; they are timed the way a decoder
+    runs them, replayed from a CUDA graph of consecutive calls."""
+    fwd_b, bwd_b = step_bytes(wl)
+    return fwd_b + bwd_b < 64 * 2 ** 20
+
+
+def capture_graphs(sets, counts, fwd=True, bwd=True):
+    """CUDA graphs of consecutive steps over the rotating sets, one per count
+    in `counts`, captured on a side stream (the sets are bound back to the
+    current stream afterwards)."""
+    gstream = torch.cuda.Stream()
+    gstream.wait_stream(torch.cuda.current_stream())
+    for c in sets:
+        c.bind(gstream)
+    with torch.cuda.stream(gstream):
+        for c in sets:                    # warm the library's caches
+            if fwd:
+                c.fwd()
+            if bwd:
+                c.bwd()
+    torch.cuda.synchronize()
+    graphs = []
+    for n in counts:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=gstream):
+            for i in range(n):
+                if fwd:
+                    sets[i % len(sets)].fwd()
+                if bwd:
+                    sets[i % len(sets)].bwd()
+        graphs.append((n, gr))
+    for c in sets:
+        c.bind(torch.cuda.current_stream())
+    return graphs
+
+
+def time_graph(stream, graph, n_per, reps):
+    """ms per step of a graph of n_per consecutive steps, replayed reps times."""
+    graph.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / (reps * n_per)
+
+
+def direction_times(wl, sets, stream):
+    """Per-direction times: the mean of PER_CALL_N back-to-back calls (the
+    roofline's figure) and PER_CALL_N isolated calls (median, P95). Graph
+    workloads: the mean per call of graph-replayed forward-only and
+    backward-only runs of 64 calls."""
+    out = {}
+    dirs = [("fwd", [c.fwd for c in sets])]
+    if has_bwd_call(wl):
+        dirs.append(("bwd", [c.bwd for c in sets]))
+    if uses_graph(wl):
+        for name, _ in dirs:
+            (n, gr), = capture_graphs(sets, [64], fwd=name == "fwd", bwd=name == "bwd")
+            out[name] = {"back_to_back_ms": time_graph(stream, gr, n, max(4, PER_CALL_N // n)),
+                         "n": 64 * max(4, PER_CALL_N // n), "each_ms": None}
+        return out
+    for name, fns in dirs:
+        b2b = time_back_to_back(stream, fns, PER_CALL_N)
+        each = time_each(stream, fns, PER_CALL_N)
+        out[name] = {"back_to_back_ms": b2b, "n": PER_CALL_N, "each_ms": each}
+    return out
+
+
+# The method's workloads, reported together by the default run: the
+# training shapes (fwd + bwd), the decode split-row norms (fwd) and the tiny
+# fp32 reference case.
+SUITE = ("qwen3-8b-train", "qwen3-qknorm", "residual-14b", "decode-m1", "decode-m8",
+         "decode-m64", "tiny-fp32")
+
+
+def measure_suite(rn, dev, args, headline):
+    """Figures for each workload of SUITE in the same run: the headline
+    workload's from the main measurement, the others measured here on their
+    own rotating buffers. Streamed workloads: max(steps, 20) forward +
+    backward steps back to back between two events, and per direction the
+    mean of PER_CALL_N back-to-back calls. Decode-sized workloads: CUDA-graph
+    replay of 64 consecutive steps, microseconds per step (their inputs are
+    L2-resident, so they are latency-bound and a bandwidth fraction says
+    little about them)."""
+    peak, peak_kind = read_peaks()
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name in SUITE:
+        wl = W.WORKLOADS[name]
+        fwd_b, bwd_b = step_bytes(wl)
+        graph = uses_graph(wl)
+        if name == headline["workload"]:
+            step_ms, fwd_ms, bwd_ms = (headline["ms_per_step"], headline["fwd_ms"],
+                                       headline["bwd_ms"])
+        else:
+            src, sets = build_sets(rn, wl, dev)
+            if graph:
+                (n, gr), = capture_graphs(sets, [64])
+                step_ms = time_graph(stream, gr, n, 50)
+            else:
+                step_ms = time_back_to_back(
+                    stream, [lambda c=c: (c.fwd(), c.bwd()) for c in sets],
+                    max(args.steps, 20))
+            dt = direction_times(wl, sets, stream)
+            fwd_ms = dt["fwd"]["back_to_back_ms"]
+            bwd_ms = dt["bwd"]["back_to_back_ms"] if "bwd" in dt else 0.0
+            del sets, src
+            torch.cuda.empty_cache()
+        gbs = (fwd_b + bwd_b) / (step_ms * 1e-3) / 1e9
+        e = {"M": wl.M, "H": wl.H, "dtype": str(wl.dtype).replace("torch.", ""),
+             "step": step_name(wl) + (" (dh_out given)" if wl.residual and wl.backward else ""),
+             "us_per_step": round(1e3 * step_ms, 3), "GB_per_s": round(gbs, 1),
+             "rows_per_s": round(wl.M / (step_ms * 1e-3), 1),
+             "frac_of_measured_hbm": round(gbs / peak, 4),
+             "frac_of_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+             "step_bytes": fwd_b + bwd_b,
+             "timing": ("CUDA-graph replay of 64 consecutive steps, L2-resident "
+                        "inputs (latency-bound)" if graph else
+                        "steps back to back over rotating buffer sets larger than L2")}
+        for d, b, ms in (("fwd", fwd_b, fwd_ms), ("bwd", bwd_b, bwd_ms)):
+            if b and ms:
+                g = b / (ms * 1e-3) / 1e9
+                e[d] = {"us": round(1e3 * ms, 3), "GB_per_s": round(g, 1),
+                        "frac_of_measured_hbm": round(g / peak, 4), "bytes": b}
+        out[name] = e
+    out["peak_gbs"] = peak
+    out["peak_kind"] = peak_kind
+    return out
+
+
 def run_ours(args, wl):
     from rmsnorm_fwd_bwd_02_gb300 import rmsnorm as rn
     rn.lib()
@@ -482,20 +668,10 @@ def run_ours(args, wl):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
 
-    src = W.make_inputs(wl)
-    w = src["w"].to(dev)
-    ws = torch.empty(max(16, rn.bwd_workspace_bytes(wl.M, wl.H, wl.dtype)),
-                     device=dev, dtype=torch.uint8)
+    src, sets = build_sets(rn, wl, dev)
+    ws = sets[0].ws
+    n_sets = len(sets)
     x_bytes = wl.M * wl.H * wl.elem_bytes
-    n_sets = buffer_sets(wl)
-    sets = [Calls(rn, wl, src, dev, ws, w) for _ in range(n_sets)]
-    if wl.N:
-        # decode: the activations (x, r and the outputs) are one small set
-        # that stays in L2, as the previous kernel's output would; only the
-        # projection weights rotate, so each call streams its weight from HBM
-        for c in sets[1:]:
-            c.x, c.r, c.h, c.out = sets[0].x, sets[0].r, sets[0].h, sets[0].out
-            c.bind(torch.cuda.current_stream())
     fwd_b, bwd_b = step_bytes(wl)
 
     def barrier():
@@ -503,31 +679,11 @@ def run_ours(args, wl):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # Decode-sized steps are a few microseconds of GPU work, less than the
-    # host needs to issue them one by one; they are timed the way a decoder
-    # runs them, replayed from a CUDA graph of consecutive calls.
-    use_graph = fwd_b + bwd_b < 64 * 2 ** 20
+    use_graph = uses_graph(wl)
     graphs = []
     if use_graph:
-        gstream = torch.cuda.Stream()
-        gstream.wait_stream(torch.cuda.current_stream())
-        for c in sets:
-            c.bind(gstream)
-        with torch.cuda.stream(gstream):
-            for i in range(n_sets):          # warm the library's caches
-                sets[i].fwd()
-                sets[i].bwd()
-        torch.cuda.synchronize()
         per = min(args.steps, 64)
-        for n in sorted({per, args.steps % per} - {0}, reverse=True):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=gstream):
-                for i in range(n):
-                    sets[i % n_sets].fwd()
-                    sets[i % n_sets].bwd()
-            graphs.append((n, gr))
-        for c in sets:
-            c.bind(torch.cuda.current_stream())
+        graphs = capture_graphs(sets, sorted({per, args.steps % per} - {0}, reverse=True))
 
     # warm-up: W steps
     path_f = path_b = 0
@@ -545,8 +701,6 @@ def run_ours(args, wl):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
-          for _ in range((args.steps + EVERY - 1) // EVERY)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -559,23 +713,12 @@ def run_ours(args, wl):
         for n, gr in graphs[1:]:
             gr.replay()
     else:
-        # Per-call events on every EVERY-th step only: an event between two
-        # launches stops the second from starting while the first drains
-        # (programmatic dependent launch), so instrumented steps run a little
-        # slower; the per-call averages come from them (conservative) and the
-        # other steps run as a caller would run them.
+        # the steps run back to back, as a caller runs them (no event in
+        # between); the per-call figures come from separate loops below
         for i in range(args.steps):
             c = sets[i % n_sets]
-            if i % EVERY == 0:
-                e = ev[i // EVERY]
-                e[0].record(stream)
-                c.fwd()
-                e[1].record(stream)
-                c.bwd()
-                e[2].record(stream)
-            else:
-                c.fwd()
-                c.bwd()
+            c.fwd()
+            c.bwd()
     end.record(stream)
     barrier()
     t_wall1 = time.time()
@@ -586,14 +729,12 @@ def run_ours(args, wl):
         clocks = sampler.summary(t_wall0, t_wall1)
 
     total_ms = reduce_max(start.elapsed_time(end), dist)
-    if use_graph:      # per-call times: the step time split by the byte shares
-        step = total_ms / args.steps
-        fwd_ms = [step * fwd_b / (fwd_b + bwd_b)]
-        bwd_ms = [step * bwd_b / (fwd_b + bwd_b)] if has_bwd_call(wl) else [0.0]
-    else:
-        fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-        bwd_ms = [e[1].elapsed_time(e[2]) for e in ev] if has_bwd_call(wl) else [0.0]
     ms_step = total_ms / args.steps
+
+    # per-direction figures, outside the value's timed region
+    dt = direction_times(wl, sets, stream)
+    fwd_avg = dt["fwd"]["back_to_back_ms"]
+    bwd_avg = dt["bwd"]["back_to_back_ms"] if "bwd" in dt else 0.0
 
     unfused = time_unfused_gemv(rn, wl, sets, args.steps) if wl.N else None
 
@@ -604,6 +745,14 @@ def run_ours(args, wl):
                run_e2e_bwd2(rn, wl, src, sets[0], args, dist) if wl.double_backward else
                run_e2e(rn, wl, src, dev, ws, args, dist))
 
+    suite = None
+    if not args.no_workloads and world == 1 and wl.name == DEFAULT_WORKLOAD \
+            and not args.path_override:
+        del sets
+        torch.cuda.empty_cache()
+        suite = measure_suite(rn, dev, args, {"workload": wl.name, "ms_per_step": ms_step,
+                                              "fwd_ms": fwd_avg, "bwd_ms": bwd_avg})
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -611,14 +760,11 @@ def run_ours(args, wl):
 
     peak, peak_kind = read_peaks()
     value = whole_job_gbs(fwd_b + bwd_b, world, ms_step)
-    fwd_avg = statistics.mean(fwd_ms)
-    bwd_avg = statistics.mean(bwd_ms)
     dom_is_bwd = has_bwd_call(wl) and bwd_b >= fwd_b
     dom_bytes, dom_ms = (bwd_b, bwd_avg) if dom_is_bwd else (fwd_b, fwd_avg)
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     # recorded for the automatic kernels only
     traffic = None if args.path_override else load_traffic(wl, "bwd" if dom_is_bwd else "fwd")
-
     def roof(b, ms, kernel):
         a = b / (ms * 1e-3) / 1e9
         return {"kernel": kernel, "bound": "hbm", "achieved": round(a, 1),
@@ -670,20 +816,27 @@ def run_ours(args, wl):
         "roofline": roofline,
         "roofline_fwd": roof(fwd_b, fwd_avg, fwd_kernel),
         "gpu_launches": args.steps * launches_per_step(wl),
-        "timing": ("CUDA-graph replay of consecutive calls (decode-sized step)"
+        "timing": ("CUDA-graph replay of consecutive calls (decode-sized step); "
+                   "per direction, graph replays of 64 calls of that direction"
                    if use_graph else
-                   f"value from events around all {args.steps} steps; per-call "
-                   f"times from events on every {EVERY}th step, launching stream"),
+                   f"value from events around all {args.steps} steps run back to back "
+                   f"on the launching stream; per direction afterwards, "
+                   f"{PER_CALL_N} back-to-back calls between two events (roofline) "
+                   f"and {PER_CALL_N} calls each between its own events (per_call_us)"),
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": None,
     }
     if has_bwd_call(wl):
         line["roofline_bwd"] = roof(bwd_b, bwd_avg, bwd_kernel)
-    if not use_graph:
-        line["per_call_us"] = {"fwd": call_stats(fwd_ms)}
-        if has_bwd_call(wl):
-            line["per_call_us"]["bwd"] = call_stats(bwd_ms)
+    line["per_call_us"] = {}
+    for name, d in dt.items():
+        st = call_stats(d["each_ms"]) if d["each_ms"] else {"n": d["n"]}
+        st["back_to_back_mean"] = round(1e3 * d["back_to_back_ms"], 3)
+        st["back_to_back_n"] = d["n"]
+        line["per_call_us"][name] = st
+    if suite is not None:
+        line["workloads"] = suite
     if wl.N:
         line["unfused"] = unfused
     if not args.no_cpu_baseline and world == 1:
@@ -696,7 +849,7 @@ def run_ours(args, wl):
 
 def call_stats(ms):
     """Mean, median and 95th percentile (nearest rank) of per-call times in
-    microseconds, over the event-instrumented steps."""
+    microseconds, over calls each timed between its own events."""
     us = sorted(1e3 * m for m in ms)
     p95 = us[min(len(us) - 1, max(0, -(-95 * len(us) // 100) - 1))]
     return {"n": len(us), "mean": round(statistics.mean(us), 3),
@@ -1006,6 +1159,9 @@ def main(argv=None):
                          "e.g. 1 the register-fed projection, 7 the tcgen05 "
                          "one); the line then records it under config")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads' figures (the 'workloads' key "
+                         "of the default run)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
