@@ -378,7 +378,9 @@ void rmsnorm_set_stream_test_fault(unsigned int extra_tx_bytes,
  *    on a 152-SM GB300 the need is at most about 10 MiB).
  *  - Set-up: the first call on each device looks up the array's device
  *    address (cudaGetSymbolAddress) with that device current; make that
- *    first call before any stream capture.
+ *    first call before any stream capture. The address is kept for that
+ *    device's CUDA context: after cudaDeviceReset (a new context) the next
+ *    call looks it up again, so make that call before any capture too.
  *  - Sharing: all calls, on every stream and thread, share the one array.
  *    Calls whose executions overlap on the GPU race on it and give wrong dw;
  *    serialise them (one stream, or events). Nothing in it needs clearing
@@ -389,6 +391,15 @@ int rmsnorm_bwd_static_scratch(const void *dy, const void *x, const void *w,
                                const float *rstd, void *dx, float *dw,
                                int64_t M, int64_t H, float eps, int dtype,
                                void *stream);
+
+/*
+ * Test hook for rmsnorm_bwd_static_scratch, process-wide, not thread-safe
+ * against concurrent calls: later calls treat the built-in array as holding
+ * only min(bytes, RMSNORM_STATIC_SCRATCH_BYTES) bytes (0 restores the full
+ * size). On a 152-SM GB300 no problem within RMSNORM_MAX_H needs the whole
+ * array, so this is how the RMSNORM_ERR_SCRATCH_LIMIT refusal is exercised.
+ */
+void rmsnorm_set_static_scratch_test_limit(size_t bytes);
 
 #ifdef __cplusplus
 }

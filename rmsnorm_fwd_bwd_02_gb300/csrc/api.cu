@@ -16,6 +16,7 @@
 #include <utility>
 
 #include "rmsnorm.h"
+#include "context.h"
 #include "params.h"
 #include "bwd2.cuh"
 #include "gemv.cuh"
@@ -152,14 +153,15 @@ int sm_count(int dev, int *sms)
 // shared memory, cached per (kernel, device, smem). A kernel that needs more
 // than the default 48 KB is opted in to the device's maximum (not to this
 // size: a later call with more shared memory must still launch).
+// Entries hold for the context they were made in (context.h).
 int blocks_per_sm(const void *fn, int threads, int dev, int *out, int smem = 0)
 {
     static std::mutex mu;
-    static std::map<std::tuple<const void *, int, int>, int> cache;
-    const auto key = std::make_tuple(fn, dev, smem);
-    {
+    static std::map<std::tuple<const void *, int, int, unsigned long long>, int> cache;
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0) {
         std::lock_guard<std::mutex> g(mu);
-        auto it = cache.find(key);
+        auto it = cache.find(std::make_tuple(fn, dev, smem, ctx));
         if (it != cache.end()) {
             *out = it->second;
             return RMSNORM_OK;
@@ -181,8 +183,13 @@ int blocks_per_sm(const void *fn, int threads, int dev, int *out, int smem = 0)
         return cuda_fail(e);
     if (n < 1)
         return cuda_fail(cudaErrorInvalidConfiguration);
-    std::lock_guard<std::mutex> g(mu);
-    cache[key] = n;
+    // the context the attribute was set in (the calls above create the
+    // primary context if none was current)
+    const unsigned long long made_in = current_context_id();
+    if (made_in != 0) {
+        std::lock_guard<std::mutex> g(mu);
+        cache[std::make_tuple(fn, dev, smem, made_in)] = n;
+    }
     *out = n;
     return RMSNORM_OK;
 }
@@ -193,11 +200,11 @@ int blocks_per_sm(const void *fn, int threads, int dev, int *out, int smem = 0)
 int max_active_clusters(const void *fn, int threads, int smem, int cs, int dev, int *out)
 {
     static std::mutex mu;
-    static std::map<std::tuple<const void *, int, int, int>, int> cache;
-    const auto key = std::make_tuple(fn, dev, smem, cs);
-    {
+    static std::map<std::tuple<const void *, int, int, int, unsigned long long>, int> cache;
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0) {
         std::lock_guard<std::mutex> g(mu);
-        auto it = cache.find(key);
+        auto it = cache.find(std::make_tuple(fn, dev, smem, cs, ctx));
         if (it != cache.end()) {
             *out = it->second;
             return RMSNORM_OK;
@@ -224,8 +231,11 @@ int max_active_clusters(const void *fn, int threads, int smem, int cs, int dev, 
         return cuda_fail(e);
     if (n < 1)
         return cuda_fail(cudaErrorInvalidConfiguration);
-    std::lock_guard<std::mutex> g(mu);
-    cache[key] = n;
+    const unsigned long long made_in = current_context_id();
+    if (made_in != 0) {
+        std::lock_guard<std::mutex> g(mu);
+        cache[std::make_tuple(fn, dev, smem, cs, made_in)] = n;
+    }
     *out = n;
     return RMSNORM_OK;
 }
@@ -1328,7 +1338,8 @@ int rmsnorm_last_path(void) { return t_last_path; }
 // partial rows live in this file-scope device array instead of a
 // caller-provided workspace. Host code must not use the array's name as a
 // pointer (on the host it is only a stand-in); the device address comes
-// from cudaGetSymbolAddress, looked up once per device on first use.
+// from cudaGetSymbolAddress, looked up once per device (and again only if
+// that device's context has been replaced, as by cudaDeviceReset).
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -1336,6 +1347,9 @@ static __device__ __align__(256) unsigned char g_static_scratch[RMSNORM_STATIC_S
 
 std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices] = {};
+// Test hook: a smaller usable size of the array (0: all of it).
+std::atomic<size_t> g_scratch_test_limit{0};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
 // Device address of g_static_scratch on the current device.
 int static_scratch_address(void **out)
@@ -1346,12 +1360,14 @@ int static_scratch_address(void **out)
     if (dev < 0 || dev >= kMaxDevices)
         return cuda_fail(cudaErrorInvalidDevice);
     std::lock_guard<std::mutex> g(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    const unsigned long long ctx = current_context_id();
+    if (g_scratch_addr[dev] == nullptr || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess)
             return cuda_fail(e);
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = current_context_id();
     }
     *out = g_scratch_addr[dev];
     return RMSNORM_OK;
@@ -1368,7 +1384,11 @@ extern "C" int rmsnorm_bwd_static_scratch(const void *dy, const void *x, const v
         return st;
     // The bound covers every kernel variant this call could take. (Without a
     // device the query gives 0 and the address lookup below reports it.)
-    if (rmsnorm_bwd_workspace_bytes(M, H, dtype) > RMSNORM_STATIC_SCRATCH_BYTES)
+    const size_t test_limit = g_scratch_test_limit.load(std::memory_order_relaxed);
+    const size_t usable = test_limit != 0 && test_limit < RMSNORM_STATIC_SCRATCH_BYTES
+                              ? test_limit
+                              : RMSNORM_STATIC_SCRATCH_BYTES;
+    if (rmsnorm_bwd_workspace_bytes(M, H, dtype) > usable)
         return RMSNORM_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;
     if ((st = static_scratch_address(&scratch)))
@@ -1376,4 +1396,9 @@ extern "C" int rmsnorm_bwd_static_scratch(const void *dy, const void *x, const v
     return bwd_impl(dy, H, nullptr, H, x, H, w, rstd, dx, H, dw, scratch,
                     RMSNORM_STATIC_SCRATCH_BYTES, M, H, eps, dtype,
                     static_cast<cudaStream_t>(stream));
+}
+
+extern "C" void rmsnorm_set_static_scratch_test_limit(size_t bytes)
+{
+    g_scratch_test_limit.store(bytes);
 }

@@ -5,6 +5,7 @@
 
 #include <mutex>
 
+#include "context.h"
 #include "registry.h"
 #include "stream.cuh"
 #include "stream_small.cuh"
@@ -15,18 +16,23 @@ namespace {
 __device__ unsigned int g_stream_timeouts;
 std::mutex g_mu;
 unsigned int *g_addr[64] = {};
+unsigned long long g_ctx[64] = {};    // the context each address belongs to
 } // namespace
 
+// The counter's device address on device `dev` (current), looked up once
+// per context (context.h).
 unsigned int *stream_timeout_counter(int dev)
 {
     if (dev < 0 || dev >= 64)
         return nullptr;
     std::lock_guard<std::mutex> g(g_mu);
-    if (g_addr[dev] == nullptr) {
+    const unsigned long long ctx = current_context_id();
+    if (g_addr[dev] == nullptr || ctx == 0 || g_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_stream_timeouts) != cudaSuccess)
             return nullptr;
         g_addr[dev] = static_cast<unsigned int *>(p);
+        g_ctx[dev] = current_context_id();
     }
     return g_addr[dev];
 }

@@ -42,6 +42,7 @@ SIGNATURES = {
     "rmsnorm_last_path": (_int, []),
     "rmsnorm_bwd_static_scratch": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64,
                                           _i64, _f, _int, _vp]),
+    "rmsnorm_set_static_scratch_test_limit": (None, [_sz]),
     "rmsnorm_wait_timeouts": (_int, [ctypes.POINTER(ctypes.c_uint), _int]),
     "rmsnorm_set_stream_test_fault": (None, [ctypes.c_uint, ctypes.c_uint]),
     "rmsnorm_bwd_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64,
@@ -405,7 +406,8 @@ def rmsnorm_gemv_fwd(x, w, A, r=None, out=None, h=None, want_h=True, y=None,
     return out, h, rstd
 
 
-STATIC_SCRATCH_BYTES = 16 << 20
+STATIC_SCRATCH_BYTES = 16 << 20     # RMSNORM_STATIC_SCRATCH_BYTES
+ERR_SCRATCH_LIMIT = -10             # RMSNORM_ERR_SCRATCH_LIMIT
 
 
 def rmsnorm_bwd_static_scratch(dy, x, w, rstd=None, dx=None, dw=None, eps=1e-6,
@@ -427,3 +429,9 @@ def rmsnorm_bwd_static_scratch(dy, x, w, rstd=None, dx=None, dw=None, eps=1e-6,
         float(eps), _dtype_code(x), _stream(stream)),
         "rmsnorm_bwd_static_scratch")
     return dx, dw
+
+
+def set_static_scratch_test_limit(nbytes):
+    """Test hook: rmsnorm_bwd_static_scratch treats its array as holding only
+    nbytes (0: the full RMSNORM_STATIC_SCRATCH_BYTES)."""
+    lib().rmsnorm_set_static_scratch_test_limit(int(nbytes))

@@ -42,6 +42,9 @@ class Workload:
     def with_rows(self, M: int) -> "Workload":
         return replace(self, M=int(M), name=f"{self.name}[M={M}]")
 
+    def with_features(self, H: int) -> "Workload":
+        return replace(self, H=int(H), name=f"{self.name}[H={H}]")
+
     @property
     def elem_bytes(self) -> int:
         return torch.empty(0, dtype=self.dtype).element_size()

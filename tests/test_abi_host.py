@@ -48,6 +48,18 @@ def test_every_declared_symbol_is_exported(lib):
         assert n in rn.SIGNATURES, f"{n} has no ctypes signature in the binding"
 
 
+def test_static_scratch_limit_matches_header():
+    """The binding's copies of the built-in scratch size and of its refusal
+    code are the header's."""
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+RMSNORM_STATIC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)",
+                  text)
+    assert m is not None
+    assert int(m.group(1)) << int(m.group(2)) == rn.STATIC_SCRATCH_BYTES
+    m = re.search(r"RMSNORM_ERR_SCRATCH_LIMIT\s*=\s*(-\d+)", text)
+    assert m is not None and int(m.group(1)) == rn.ERR_SCRATCH_LIMIT
+
+
 def test_status_strings(lib):
     for code in (OK, NULLPTR, BAD_SHAPE, BAD_DTYPE, BAD_EPS, MISALIGNED,
                  WORKSPACE, UNSUPPORTED, CUDA, ALIAS, BAD_STRIDE):
