@@ -170,12 +170,18 @@ int blocks_per_sm(const void *fn, int threads, int dev, int *out, int smem = 0)
     int n = 0;
     cudaError_t e = cudaSuccess;
     if (smem > 48 * 1024) {
+        // the device's per-CTA maximum less the kernel's static shared memory
         int most = 0;
+        cudaFuncAttributes fa;
         e = cudaDeviceGetAttribute(&most, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess && smem > most)
-            return cuda_fail(cudaErrorInvalidValue);
         if (e == cudaSuccess)
+            e = cudaFuncGetAttributes(&fa, fn);
+        if (e == cudaSuccess) {
+            most -= (int)fa.sharedSizeBytes;
+            if (smem > most)
+                return cuda_fail(cudaErrorInvalidValue);
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+        }
     }
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
