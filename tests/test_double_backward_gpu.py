@@ -14,6 +14,7 @@ import torch
 import oracle
 from rmsnorm_fwd_bwd_02_gb300 import rmsnorm as rn
 from rmsnorm_fwd_bwd_02_gb300 import workloads as W
+from tests.chunked import chunk_rows, for_row_chunks, rows_of
 from tests.tolerances import check_bits, check_dw, check_rows
 
 pytestmark = pytest.mark.gpu
@@ -115,9 +116,10 @@ def test_scalar_path(orc, dtype):
     compare(f"odd H {dtype}", got, o, dtype)
 
 
-def test_full_size_sampled(orc):
-    """The Qwen3-8B training shape: dw2 over all rows, ddy and dx2 on
-    sampled rows, same bits run to run."""
+def test_full_size_all_elements(orc):
+    """The Qwen3-8B training shape: every element of ddy and dx2 against the
+    oracle (row chunks on host threads), dw2 over all rows, same bits run
+    to run."""
     wl = W.WORKLOADS["qwen3-8b-train"]
     inp = W.make_inputs(wl)
     g = torch.Generator().manual_seed(99)
@@ -130,12 +132,16 @@ def test_full_size_sampled(orc):
     _, _, dw2, _, _, tdw2 = orc.bwd_bwd(inp["dy"], inp["x"], inp["w"], inp["gx"],
                                          inp["gw"], wl.eps, want_terms=True)
     check_dw("full size dw2 (all rows)", got[2], dw2, tdw2)
-    rows = W.random_rows(wl.M, 48, seed=5)
-    sub = {k: (v[rows].contiguous() if v.dim() == 2 else v) for k, v in inp.items()}
-    o = orc.bwd_bwd(sub["dy"], sub["x"], sub["w"], sub["gx"], sub["gw"], wl.eps,
-                    want_terms=True)
-    check_rows("full size ddy", got[0][rows], o[0], wl.dtype, o[3])
-    check_rows("full size dx2", got[1][rows], o[1], wl.dtype, o[4])
+    ddy, dx2 = got[0].cpu(), got[1].cpu()
+
+    def work(a, b):
+        sub = rows_of(inp, a, b)
+        o = orc.bwd_bwd(sub["dy"], sub["x"], sub["w"], sub["gx"], sub["gw"], wl.eps,
+                        want_terms=True)
+        check_rows(f"full size ddy rows {a}:{b}", ddy[a:b], o[0], wl.dtype, o[3])
+        check_rows(f"full size dx2 rows {a}:{b}", dx2[a:b], o[1], wl.dtype, o[4])
+
+    for_row_chunks(wl.M, work, chunk_rows(wl.H))
 
 
 def test_error_returns():

@@ -2,9 +2,9 @@
 
 * every workload at a reduced row count that spans several tiles and ends in
   a ragged tail, compared element by element;
-* the three large workloads at full size in the launch configuration the
-  benchmark times, compared on sampled rows (y, rstd, dx, h) and on all of
-  dw and h;
+* the three large workloads (and fp16 storage) at full size in the launch
+  configuration the benchmark times, every element of y, rstd, dx, h and dw
+  (the oracle runs over row chunks on host threads, tests/chunked.py);
 * edge shapes and dtypes, misaligned and odd rows (scalar kernels), in-place
   calls, saved vs recomputed rstd, split-row vs row-wise, determinism,
   guard words around every output, M == 0, error returns, CUDA-graph replay.
@@ -16,6 +16,7 @@ import torch
 import oracle
 from rmsnorm_fwd_bwd_02_gb300 import rmsnorm as rn
 from rmsnorm_fwd_bwd_02_gb300 import workloads as W
+from tests.chunked import chunk_rows, for_row_chunks, rows_of
 from tests.tolerances import check_bits, check_dw, check_rows, check_rstd
 
 pytestmark = pytest.mark.gpu
@@ -124,37 +125,41 @@ def test_workload_reduced_all_elements(orc, name):
         compare_all(name + " dh=None", wl, got2, o2)
 
 
+def check_full_size(orc, wl, inp, got, tag):
+    """Every element of the GPU results `got` (host tensors) against the
+    oracle, over row chunks: y, rstd, dx and (residual) h bit-exact; then dw
+    over all rows (for the residual variant, from the oracle's own h)."""
+    oh_full = torch.empty_like(inp["x"]) if wl.residual else None
+
+    def work(a, b):
+        o = oracle_all(orc, wl.with_rows(b - a), rows_of(inp, a, b))
+        t = f"{tag} rows {a}:{b}"
+        if wl.residual:
+            check_bits(f"{t} h", got["h"][a:b], o["h"])
+            oh_full[a:b] = o["h"]
+        check_rows(f"{t} y", got["y"][a:b], o["y"], wl.dtype)
+        check_rstd(f"{t} rstd", got["rstd"][a:b], o["rstd"])
+        check_rows(f"{t} dx", got["dx"][a:b], o["dx"], wl.dtype, o["tdx"])
+
+    for_row_chunks(wl.M, work, chunk_rows(wl.H))
+    if wl.residual:
+        _, dw, _, tdw = orc.residual_bwd(inp["dy"], inp["dh"], oh_full, inp["w"], wl.eps,
+                                         want_dx=False, want_terms=True)
+    else:
+        _, dw, _, tdw = orc.bwd(inp["dy"], inp["x"], inp["w"], wl.eps, want_dx=False,
+                                want_terms=True)
+    check_dw(f"{tag} dw (all rows)", got["dw"], dw, tdw)
+
+
 @pytest.mark.parametrize("name", ["qwen3-8b-train", "qwen3-qknorm", "residual-14b",
                                   "qwen3-8b-train-fp16"])
-def test_workload_full_size_sampled(orc, name):
+def test_workload_full_size_all_elements(orc, name):
+    """The large workloads at full size, as the benchmark runs them (automatic
+    kernel choice, dh_out given), every output element against the oracle."""
     wl = W.WORKLOADS[name]
     inp = W.make_inputs(wl)
-    got = gpu_fwd_bwd(wl, to_dev(inp))
-    # h and dw over all rows
-    if wl.residual:
-        h_full, _, _ = orc.residual_fwd(inp["x"], inp["r"], inp["w"], wl.eps)
-        check_bits(f"{name} h (all rows)", got["h"], h_full)
-        _, dw, _, tdw = orc.residual_bwd(inp["dy"], inp["dh"], h_full, inp["w"],
-                                         wl.eps, want_dx=False, want_terms=True)
-        del h_full
-    else:
-        _, dw, _, tdw = orc.bwd(inp["dy"], inp["x"], inp["w"], wl.eps,
-                                want_dx=False, want_terms=True)
-    # y, rstd, dx, h on sampled rows
-    rows = W.random_rows(wl.M, 64, seed=wl.seed)
-    sub = {k: (v[rows].contiguous() if v.dim() == 2 else v) for k, v in inp.items()}
-    o = oracle_all(orc, wl.with_rows(len(rows)), sub)
-    for key in ("y", "dx", "h"):
-        if key in got:
-            got[key] = got[key][rows]
-    got["rstd"] = got["rstd"][rows]
-    check_dw(f"{name} dw (all rows)", got.pop("dw"), dw, tdw)
-    o.pop("dw"), o.pop("tdw")
-    if "h" in o:
-        check_bits(f"{name} h", got["h"], o["h"])
-    check_rows(f"{name} y", got["y"], o["y"], wl.dtype)
-    check_rstd(f"{name} rstd", got["rstd"], o["rstd"])
-    check_rows(f"{name} dx", got["dx"], o["dx"], wl.dtype, o["tdx"])
+    got = {k: v.cpu() for k, v in gpu_fwd_bwd(wl, to_dev(inp)).items()}
+    check_full_size(orc, wl, inp, got, name)
 
 
 # ------------------------------------------------------------ edge shapes
@@ -245,31 +250,16 @@ def test_stream_path_ragged(orc, name, M):
 
 
 @pytest.mark.parametrize("name", ["qwen3-8b-train", "residual-14b", "qwen3-qknorm"])
-def test_stream_path_full_size_sampled(orc, name):
+def test_stream_path_full_size_all_elements(orc, name):
+    """The streamed kernels forced for both directions at full size: every
+    element against the oracle, and the same bits run to run."""
     wl = W.WORKLOADS[name]
     inp = W.make_inputs(wl)
     with forced_path(rn.PATH_STREAM):
         got = gpu_fwd_bwd(wl, to_dev(inp))
         assert rn.last_path() == rn.PATH_STREAM
-    if wl.residual:
-        h_full, _, _ = orc.residual_fwd(inp["x"], inp["r"], inp["w"], wl.eps)
-        check_bits(f"stream {name} h (all rows)", got["h"], h_full)
-        _, dw, _, tdw = orc.residual_bwd(inp["dy"], inp["dh"], h_full, inp["w"],
-                                         wl.eps, want_dx=False, want_terms=True)
-        del h_full
-    else:
-        _, dw, _, tdw = orc.bwd(inp["dy"], inp["x"], inp["w"], wl.eps,
-                                want_dx=False, want_terms=True)
-    check_dw(f"stream {name} dw (all rows)", got["dw"], dw, tdw)
-    rows = W.random_rows(wl.M, 64, seed=wl.seed + 1)
-    sub = {k: (v[rows].contiguous() if v.dim() == 2 else v) for k, v in inp.items()}
-    o = oracle_all(orc, wl.with_rows(len(rows)), sub)
-    check_rows(f"stream {name} y", got["y"][rows], o["y"], wl.dtype)
-    check_rstd(f"stream {name} rstd", got["rstd"][rows], o["rstd"])
-    check_rows(f"stream {name} dx", got["dx"][rows], o["dx"], wl.dtype, o["tdx"])
-    if wl.residual:
-        check_bits(f"stream {name} h", got["h"][rows], o["h"])
-    # deterministic run to run
+    host = {k: v.cpu() for k, v in got.items()}
+    check_full_size(orc, wl, inp, host, f"stream {name}")
     with forced_path(rn.PATH_STREAM):
         again = gpu_fwd_bwd(wl, to_dev(inp))
     for k in got:

@@ -16,6 +16,7 @@ import torch
 import oracle
 from rmsnorm_fwd_bwd_02_gb300 import rmsnorm as rn
 from rmsnorm_fwd_bwd_02_gb300 import workloads as W
+from tests.chunked import chunk_rows, for_row_chunks, rows_of
 from tests.tolerances import check_bits, check_dw, check_rows, check_rstd
 
 pytestmark = pytest.mark.gpu
@@ -277,10 +278,10 @@ def test_strided_rejects_bad_strides():
     assert st == -12
 
 
-def test_full_size_strided_workload_sampled(orc):
+def test_full_size_strided_workload_all_elements(orc):
     """The strided benchmark workload at full size, in the layout the
-    benchmark times: sampled rows against the oracle, dw over all rows, and
-    the same bits as the dense call."""
+    benchmark times: every element against the oracle (row chunks on host
+    threads), dw over all rows, and the same bits as the dense call."""
     wl = W.WORKLOADS["qwen3-8b-train-strided"]
     inp = W.make_inputs(wl)
     got, bufs, used = run_strided(inp, wl.ld, wl.ld, False, eps=wl.eps)
@@ -289,12 +290,16 @@ def test_full_size_strided_workload_sampled(orc):
     _, dw, _, tdw = orc.bwd(inp["dy"], inp["x"], inp["w"], wl.eps, want_dx=False,
                             want_terms=True)
     check_dw("full strided dw (all rows)", got["dw"], dw, tdw)
-    rows = W.random_rows(wl.M, 64, seed=wl.seed + 2)
-    sub = {k: (v[rows].contiguous() if v.dim() == 2 else v) for k, v in inp.items()}
-    o = oracle_all(orc, sub, wl.eps, False)
-    check_rows("full strided y", got["y"][rows], o["y"], wl.dtype)
-    check_rstd("full strided rstd", got["rstd"][rows], o["rstd"])
-    check_rows("full strided dx", got["dx"][rows], o["dx"], wl.dtype, o["tdx"])
+    host = {k: got[k].cpu() for k in ("y", "rstd", "dx")}
+
+    def work(a, b):
+        o = oracle_all(orc, rows_of(inp, a, b), wl.eps, False)
+        check_rows(f"full strided y rows {a}:{b}", host["y"][a:b], o["y"], wl.dtype)
+        check_rstd(f"full strided rstd rows {a}:{b}", host["rstd"][a:b], o["rstd"])
+        check_rows(f"full strided dx rows {a}:{b}", host["dx"][a:b], o["dx"], wl.dtype,
+                   o["tdx"])
+
+    for_row_chunks(wl.M, work, chunk_rows(wl.H))
     dense, dense_used = run_dense(inp, False, eps=wl.eps)
     assert used == dense_used, (used, dense_used)
     same_bits_where_same_family("full strided", got, used, dense, dense_used)
