@@ -230,12 +230,13 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
  *   holds in shared memory: the warp-level MMA kernels when
  *   ceil(M/16) * (16 * (2H + 64) + 2048) + 2H + 16 <= 227 KB (H <= 6720
  *   for M <= 16, 3424 for M <= 32, 2272 for M <= 48, 1664 for M <= 64),
- *   or above 8 rows the tcgen05 kernel, whose K is split over a cluster of
- *   up to 8 CTAs (with r: H <= 4608 for M <= 32, 4096 for M <= 48, 3584
- *   for M <= 64; without r: 5120 for M <= 32). Calls only the tcgen05
- *   kernel holds also return RMSNORM_ERR_UNSUPPORTED when another kernel
- *   is forced (rmsnorm_set_path_override) or the driver offers no
- *   tensor-map encoder;
+ *   or above 8 rows a tcgen05 kernel: the one whose K is split over a
+ *   cluster of up to 8 CTAs (with r: H <= 4608 for M <= 32, 4096 for
+ *   M <= 48, 3584 for M <= 64; without r: 5120 for M <= 32) or the
+ *   persistent one that holds y whole per CTA (H <= 5632 for M <= 16).
+ *   Calls only a tcgen05 kernel holds also return RMSNORM_ERR_UNSUPPORTED
+ *   when a warp-level kernel is forced (rmsnorm_set_path_override) or the
+ *   driver offers no tensor-map encoder;
  *   1 <= N < 2^30 (else RMSNORM_ERR_BAD_SHAPE).
  * Alignment: x, r, w, A, h, y 16-byte aligned (RMSNORM_ERR_MISALIGNED).
  * Aliasing: no output (out, h, y, rstd) may share a byte with an input or
@@ -245,12 +246,13 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
  * Performance: built for decode batches. Up to 8 rows the call is faster
  *   than the norm followed by a separate GEMM (measured on GB300 with the
  *   weights streaming from HBM). From 9 rows on it runs the product on the
- *   tensor cores (tcgen05) with K split over a thread-block cluster; it
- *   stays correct and deterministic there, but rmsnorm_fwd /
- *   rmsnorm_residual_fwd followed by a GEMM library call is faster (at 896
- *   features and 16 to 64 rows by some 0.8 to 2.4 us per call; at 4096
- *   features, 16 to 48 rows and 6144 to 24576 outputs the fused call takes
- *   2.2 to 3.4 times as long).
+ *   tensor cores (tcgen05): with K split over a thread-block cluster, or,
+ *   on rows of at least 2048 features with more 128-feature tiles than SMs,
+ *   in the persistent kernel. It stays correct and deterministic there, but
+ *   rmsnorm_fwd / rmsnorm_residual_fwd followed by a GEMM library call is
+ *   faster (at 896 features and 9 to 64 rows by some 0.8 to 2.5 us per
+ *   call; at 4096 features, 9 to 48 rows and 6144 to 24576 outputs the
+ *   fused call takes 1.9 to 3.5 times as long).
  * flags: 0, or RMSNORM_GEMV_STATIC_WEIGHTS: the caller guarantees that no
  *   work still in flight on the stream when this call is enqueued writes w
  *   or A (model weights during decoding). The kernel then fetches them while
@@ -320,9 +322,12 @@ int rmsnorm_last_cuda_error(void);
  * fp16 with H = 128 (dense rows only), 4096 or 5120; row-wise elsewhere).
  * For rmsnorm_gemv_fwd: 1 = the weight in registers, 6 = the weight by bulk
  * copies (the automatic choice up to 8 rows), 7 = the product on tcgen05
- * with K split over a cluster (the automatic choice above 8 rows, where a
- * cluster of at most 8 CTAs fits its shared memory; else as 6). Other
- * values: automatic.
+ * with K split over a cluster (the automatic choice above 8 rows where y is
+ * too large for one CTA and a cluster of at most 8 CTAs fits its shared
+ * memory; else as 6), 8 = the persistent product on tcgen05 with y held
+ * whole by each CTA (the automatic choice above 8 rows where it fits: T x H
+ * x 2 bytes of y, T = rows rounded up to 16, with a ring of the weight in
+ * 227 KB; else as 6). Other values: automatic.
  * Forcing a vectorised family on rows that are not 16-byte aligned still
  * takes the scalar one. Not thread-safe against concurrent calls; intended
  * for tests only.
@@ -330,10 +335,12 @@ int rmsnorm_last_cuda_error(void);
 void rmsnorm_set_path_override(int path);
 
 /* Which kernel family the last call on this thread used: 1 row-wise
- * vectorised, 2 split-row, 3 row-wise scalar, 4 streamed, 5 to 7 the norm
+ * vectorised, 2 split-row, 3 row-wise scalar, 4 streamed, 5 to 8 the norm
  * fused with the GEMV (rmsnorm_gemv_fwd; 5: the weight in registers, which
  * override 1 forces; 6: the weight fed by bulk copies, automatic up to 8
- * rows; 7: the product on tcgen05, automatic above 8 rows), 0 none. */
+ * rows; 7: the product on tcgen05 with K split over a cluster, automatic
+ * above 8 rows where y does not fit one CTA; 8: the persistent product on
+ * tcgen05, automatic above 8 rows where y fits one CTA), 0 none. */
 int rmsnorm_last_path(void);
 
 /*

@@ -21,6 +21,7 @@
 #include "bwd2.cuh"
 #include "gemv.cuh"
 #include "gemv_tma.cuh"
+#include "gemv_tc.cuh"
 #include "gemv_umma.cuh"
 #include "reduce.cuh"
 #include "registry.h"
@@ -33,6 +34,7 @@ constexpr int kPathAuto = 0, kPathRows = 1, kPathSplit = 2, kPathScalar = 3, kPa
 constexpr int kPathGemv = 5;           // RMSNorm fused with the GEMV: A in registers (5,
 constexpr int kPathGemvTma = 6;        // reported only), by bulk copies (6), or the
 constexpr int kPathGemvUmma = 7;       // product on tcgen05 (7); 6 and 7 also force it
+constexpr int kPathGemvTc = 8;         // persistent tcgen05, y held per CTA (8; forces it)
 constexpr int kGemvMaxRows = 64;
 constexpr int64_t kGemvMaxSmem = 227 * 1024;
 constexpr int kSplitMaxRows = 64;      // decode-sized batches ([P2 §3.2])
@@ -811,6 +813,7 @@ int bwd2_impl(const void *dy, const void *x, const void *w, const float *rstd, c
 // Rows above which the tcgen05 kernel is the automatic choice (at 1 to 8
 // rows the bulk-copy kernel is faster: its 8-row MMA tile wastes less).
 constexpr int64_t kGemvUmmaMinRows = 8;
+constexpr int64_t kGemvTcMinH = 2048;     // rows wide enough for the persistent kernel
 
 struct GemvTmaPlan {
     int TPW, KS, NSW, ctas, CS;
@@ -947,6 +950,37 @@ int gemv_umma_plan(int64_t M, int64_t H, int64_t N, bool res, int dt, int dev, G
     return RMSNORM_OK;
 }
 
+// The persistent tcgen05 kernel's plan (gemv_tc.cuh): y for T tokens held
+// whole, the rest of shared memory a ring of A's atoms, two atoms a stage
+// when three such stages fit, else one. false: y does not fit.
+struct GemvTcPlan {
+    int T, na;
+    TcLayout L;
+};
+
+bool gemv_tc_plan(int64_t M, int64_t H, GemvTcPlan *pl)
+{
+    pl->T = (int)((M + 15) / 16 * 16);
+    pl->na = (int)((H + kUmmaKC - 1) / kUmmaKC);
+    if (pl->T > 64 || H % 16 != 0)
+        return false;
+    for (int aps : {2, 1})
+        for (int nst = 16; nst >= (aps == 2 ? 3 : 2); --nst) {
+            const TcLayout L = gemv_tc_layout(pl->T, (int)H, nst, aps);
+            if ((int64_t)L.total <= kGemvMaxSmem) {
+                pl->L = L;
+                return true;
+            }
+        }
+    return false;
+}
+
+bool gemv_tc_fits(int64_t M, int64_t H)
+{
+    GemvTcPlan pl;
+    return gemv_tc_plan(M, H, &pl);
+}
+
 int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *out, void *h,
               void *y, float *rstd, int64_t M, int64_t H, int64_t N, float eps, int dtype,
               int flags, cudaStream_t stream)
@@ -963,10 +997,79 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
     const uint32_t static_w = (flags & RMSNORM_GEMV_STATIC_WEIGHTS) ? 1 : 0;
     const int ov = g_path_override.load(std::memory_order_relaxed);
 
+    // The persistent tcgen05 kernel, y held whole per CTA: forced (override
+    // 8), or automatic above kGemvUmmaMinRows rows where y fits and the
+    // projection has more 128-feature tiles than SMs on rows of at least
+    // kGemvTcMinH features. Measured on GB300 (residual, weights from HBM):
+    // 4096 -> 24576 at 9 and 16 rows 63.7 and 64.7 us against 86.6 and 85.0
+    // for the K-split kernel, whose clusters run there in several waves;
+    // with fewer tiles, or at 896 features, the K-split kernel is faster
+    // (4096 -> 6144 at 16 rows: 27.2 against 38.3 us; 896 -> 9728 at 64
+    // rows: 10.3 against 15.0 us): one CTA per tile, each with a weight ring
+    // of 80-96 KB beside y, keeps too few bytes in flight.
+    GemvTcPlan tp;
+    if ((ov == kPathGemvTc ||
+         (ov == kPathAuto && M > kGemvUmmaMinRows && H >= kGemvTcMinH &&
+          (N + kUmmaM - 1) / kUmmaM > sms)) &&
+        gemv_tc_plan(M, H, &tp)) {
+        PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+        if (encode != nullptr) {
+            const CUtensorMapDataType et =
+                dt == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+            // [rows][H] with the 128-byte swizzle, out-of-range reads zero:
+            // A in boxes of 128 rows x 64 columns, x in boxes of T x 64
+            auto make_map = [&](CUtensorMap *map, const void *base, int64_t rows,
+                                uint32_t box_rows) {
+                const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
+                const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+                const cuuint32_t box[2] = {(cuuint32_t)kUmmaKC, (cuuint32_t)box_rows};
+                const cuuint32_t estr[2] = {1, 1};
+                return encode(map, et, 2, const_cast<void *>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            };
+            CUtensorMap mapA, mapX;
+            if (make_map(&mapA, A, N, kUmmaM) != CUDA_SUCCESS ||
+                make_map(&mapX, x, M, (uint32_t)tp.T) != CUDA_SUCCESS)
+                return cuda_fail(cudaErrorInvalidValue);
+            const void *fn = gemv_tc_kernels.fn[dt][r != nullptr ? 1 : 0];
+            int bps;
+            if ((st = blocks_per_sm(fn, kTcThreads, dev, &bps, (int)tp.L.total)))
+                return st;
+            unsigned int *tmo = stream_timeout_counter(dev);
+            if (tmo == nullptr)
+                return cuda_fail(cudaErrorInvalidSymbol);
+            const int64_t tiles = (N + kUmmaM - 1) / kUmmaM;
+            const int64_t cap = (int64_t)bps * sms;
+            GemvTcParams p = {r,    w,     out,   h,    y,      rstd,
+                              (int)M, (int)H, (int)N, tp.T, tp.na, tp.L,
+                              eps,  (int)static_w,
+                              g_test_extra_tx.load(std::memory_order_relaxed),
+                              g_test_wait_us.load(std::memory_order_relaxed)};
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(tiles < cap ? tiles : cap));
+            cfg.blockDim = dim3(kTcThreads);
+            cfg.dynamicSmemBytes = (size_t)tp.L.total;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr.val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            void *args[4] = {&p, &mapA, &mapX, &tmo};
+            const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+            if (e != cudaSuccess)
+                return cuda_fail(e);
+            t_last_path = kPathGemvTc;
+            return RMSNORM_OK;
+        }
+    }
+
     // The product on tcgen05 with K split over a cluster: automatic above
-    // kGemvUmmaMinRows rows (measured faster there than the warp-level MMA
-    // kernels), or forced (override 7); where no cluster size fits, the
-    // kernels below.
+    // kGemvUmmaMinRows rows where y is too large for one CTA (measured faster
+    // there than the warp-level MMA kernels), or forced (override 7); where
+    // no cluster size fits, the kernels below.
     if (ov == kPathGemvUmma || (ov == kPathAuto && M > kGemvUmmaMinRows)) {
         PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
         GemvUmmaPlan up;
@@ -1216,7 +1319,7 @@ int rmsnorm_gemv_fwd(const void *x, const void *r, const void *w, const void *A,
     // tcgen05 kernel does
     const int MT = (int)((M + 15) / 16);
     if (gemv_smem_bytes(MT > 0 ? MT : 1, false, (int)M, (int)H, false) > kGemvMaxSmem &&
-        !(M > kGemvUmmaMinRows && gemv_umma_fits(M, H, r != nullptr)))
+        !(M > kGemvUmmaMinRows && (gemv_umma_fits(M, H, r != nullptr) || gemv_tc_fits(M, H))))
         return RMSNORM_ERR_UNSUPPORTED;
     if (h != nullptr && r == nullptr)
         return RMSNORM_ERR_NULLPTR;
@@ -1309,7 +1412,7 @@ int rmsnorm_last_cuda_error(void) { return t_last_cuda_error; }
 void rmsnorm_set_path_override(int path)
 {
     const bool ok = (path >= kPathAuto && path <= kPathStream) || path == kPathGemvTma ||
-                    path == kPathGemvUmma;
+                    path == kPathGemvUmma || path == kPathGemvTc;
     g_path_override.store(ok ? path : kPathAuto);
 }
 

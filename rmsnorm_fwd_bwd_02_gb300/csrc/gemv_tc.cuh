@@ -1,0 +1,427 @@
+// gemv_tc.cuh -- RMSNorm fused with the projection, persistent, one CTA per
+// SM, the product on tcgen05 with two accumulators in tensor memory. Same
+// result as the other projection kernels: the chain of [P2] (the 0.8B Qwen
+// decode article, trdm.cn news/483216) §2.1, §3.1 with y rounded to the
+// dtype before out = y A^T, fp32 accumulation.
+//
+// For the shapes where a decode batch's y (T tokens x H features, T = M
+// rounded up to 16) fits in one CTA's shared memory next to a ring of the
+// weight: every H of the 0.8B model up to 64 tokens, 4096 features up to 16.
+// Each CTA then needs no other: it normalises all T tokens once, keeps y in
+// shared memory, and takes the 128-feature tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... of A, streaming them through one ring that
+// runs on across tile boundaries. Nothing is exchanged between CTAs and
+// nothing is repeated per tile but the MMAs and the epilogue.
+//
+// Roles (512 threads, 16 warps):
+//  - warp 0, lane 0: the copies of A. Stage q of the ring (APS atoms of 128
+//    features x 64 columns, 16 KB each, 128-byte swizzle) waits until the
+//    MMAs that read its previous contents are complete (the `empty`
+//    barrier, committed by the MMA thread), then is refilled, completing on
+//    its `full` barrier. With static weights it starts before the wait on
+//    the previous kernel.
+//  - warps 1-15 first normalise, all 480 threads: x arrives by tensor copies
+//    (T x 64 per atom, rows past M and columns past H read as zero) into the
+//    y area in the MMA's K-major layout; h = x + r (r read from global, a
+//    batch of loads in flight per thread) is rounded and stored in place;
+//    the sums of h^2 of each (4 tokens, atom) unit are reduced over the
+//    eight lanes that hold a row's chunks, then over the atoms in atom
+//    order; rstd; y = h rstd w in place. CTA 0 also stores h, y and rstd.
+//  - warp 1, lane 0 then issues the MMAs: per tile, into accumulator
+//    (tile & 1), once the epilogue has released it; per stage, four MMAs
+//    (m128 nT k16) an atom and one commit to the stage's `empty` barrier;
+//    per tile one commit to the accumulator's `full` barrier.
+//  - warps 4-11: the epilogue. Warp w reads lanes 32 (w % 4) .. + 31 of the
+//    accumulator (features) for tokens 16 ((w - 4) / 4) + 32 j (tcgen05.ld),
+//    releases the accumulator, rounds and stores out[token][feature].
+// So the MMAs of tile j + 1 run while the epilogue drains tile j, and the
+// copies run ahead of both.
+//
+// Every wait is bounded (about one second, or the test limit). One that
+// runs out raises a flag in shared memory that every other wait also
+// watches, so all roles stop; the CTA then waits (bounded) for its copies in
+// flight and its MMAs, counts one timeout, frees the tensor memory and ends.
+#pragma once
+
+#include <cuda.h>
+
+#include "gemv_umma.cuh"
+
+namespace rmsk {
+
+constexpr int kTcThreads = 512;
+constexpr int kTcNormWarps = 15;              // warps 1..15
+constexpr int kTcEpiWarp0 = 4, kTcEpiWarps = 8;
+constexpr int kTcBatch = 8;                   // norm units whose r loads are in flight at once
+constexpr uint32_t kTcAtom = kUmmaAtomA;      // 128 x 64 of A: 16 KB
+
+// Shared memory of one CTA, byte offsets from a 1024-byte aligned base: y
+// (na atoms of T x 128 bytes), the ring (NSt stages of APS atoms), w (na x
+// 128 bytes, zero past H), the mbarriers (full[NSt], empty[NSt],
+// acc_full[2], acc_empty[2], x landed, drain, x issued), four words (tensor-memory
+// address, failure flag, copies issued, copies consumed), rstd[T] and the
+// per-atom partial sums of squares [na][T].
+struct TcLayout {
+    int NSt, APS;
+    uint32_t ring, w, bar, slots, total;   // total includes 1023 bytes of alignment
+};
+
+__host__ __device__ inline TcLayout gemv_tc_layout(int T, int H, int NSt, int APS)
+{
+    TcLayout L;
+    const int na = (H + kUmmaKC - 1) / kUmmaKC;
+    L.NSt = NSt;
+    L.APS = APS;
+    L.ring = (uint32_t)na * (uint32_t)T * 128u;
+    L.w = L.ring + (uint32_t)NSt * (uint32_t)APS * kTcAtom;
+    L.bar = L.w + (uint32_t)na * 128u;
+    L.slots = L.bar + 8u * (uint32_t)(2 * NSt + 7);
+    L.total = L.slots + 16u + 4u * (uint32_t)T + 4u * (uint32_t)na * (uint32_t)T + 1023u;
+    return L;
+}
+
+struct GemvTcParams {
+    const void *r;    // [M,H] residual, or nullptr
+    const void *w;    // [H]
+    void *out;        // [M,N]
+    void *h;          // [M,H] residual sum out, or nullptr
+    void *y;          // [M,H] stored norm output, or nullptr
+    float *rstd;      // [M] or nullptr
+    int M, H, N;
+    int T;            // tokens as the MMA's N: M rounded up to 16 (<= 64)
+    int na;           // atoms of K in a row: ceil(H / 64)
+    TcLayout L;
+    float eps;
+    int static_w;     // w and A may be read before the wait on the previous kernel
+    uint32_t extra_tx, wait_limit_us;   // test hook of the bounded waits (A's copies)
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait that also gives up when another role has raised `fail`; a
+// wait that runs out raises it.
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, unsigned long long limit,
+                                        volatile int *fail)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*fail)
+            return false;
+        if (global_ns() - t0 > limit) {
+            *fail = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// grid = min(tiles, SMs), 512 threads, dynamic shared memory p.L.total.
+template <typename T, bool RES>
+__global__ void __launch_bounds__(kTcThreads, 1)
+rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
+            const __grid_constant__ CUtensorMap tmX, unsigned int *timeouts)
+{
+    using P = Pack<T, 8>;
+    using X = Vals<8>;
+    using F = float2;
+    extern __shared__ __align__(1024) unsigned char tc_smem[];
+
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int H = p.H, NT = p.T, NP = H / 8, na = p.na;
+    const TcLayout &L = p.L;
+    const int NSt = L.NSt, APS = L.APS;
+    const uint32_t raw_s = smem_addr(tc_smem);
+    unsigned char *base = tc_smem + (((raw_s + 1023u) & ~1023u) - raw_s);
+    unsigned char *ysm = base, *wsm = base + L.w;
+    const uint32_t y_s = smem_addr(ysm), ring_s = smem_addr(base + L.ring);
+    const uint32_t full0 = smem_addr(base + L.bar), empty0 = full0 + 8u * (uint32_t)NSt;
+    const uint32_t accf0 = empty0 + 8u * (uint32_t)NSt, acce0 = accf0 + 16u;
+    const uint32_t xbar = acce0 + 16u, dbar = xbar + 8u, xiss = dbar + 8u;
+    int *slots = reinterpret_cast<int *>(base + L.slots);
+    volatile int *fail = slots + 1;
+    // slots[0]: tensor-memory address, [1]: a wait ran out, [2]: stages
+    // issued, [3]: stages whose copies were consumed
+    float *rsv = reinterpret_cast<float *>(slots + 4);        // [T] rstd
+    float *part = rsv + NT;                                   // [na][T] sums of h^2
+    const uint32_t atom = (uint32_t)NT * 128u;                // bytes of an atom of y
+    const uint32_t ncols = gemv_umma_tmem_cols(NT);           // one accumulator
+    const uint32_t stage = (uint32_t)APS * kTcAtom;
+    const unsigned long long limit = wait_limit_ns(p.wait_limit_us);
+    const int ntiles = (p.N + kUmmaM - 1) / kUmmaM;
+    const int mt = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int ng = (na + APS - 1) / APS;                      // stages per tile
+    const int nq = mt * ng;                                   // stages of this CTA
+    const bool writer = blockIdx.x == 0;
+
+    // set-up: tensor memory (both accumulators), the barriers, the maps
+    if (warp == 0) {
+        tmem_alloc(smem_addr(slots), 2u * ncols);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        for (int s = 0; s < NSt; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8u * b, 1);
+            mbar_init(acce0 + 8u * b, kTcEpiWarps);
+        }
+        mbar_init(xbar, 1);
+        mbar_init(dbar, 1);
+        mbar_init(xiss, 1);
+        slots[1] = 0;
+        slots[2] = 0;
+        slots[3] = 0;
+    }
+    if (tid == 64) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmX);
+    }
+    mbar_init_fence();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = static_cast<uint32_t>(slots[0]);
+
+    if (warp == 0) {
+        // ---------------------------------------------------- copies of A
+        if (lane == 0) {
+            if (!p.static_w)
+                griddep_wait();
+            // An SM serves its tensor copies in order and the norm needs x
+            // first: one stage of A goes ahead of x (static weights only),
+            // the rest once x's copies are issued.
+            int q = 0;
+            for (; q < nq; ++q) {
+                const int s = q % NSt, u = q / NSt;
+                if (q == (p.static_w ? 1 : 0) && !tc_wait(xiss, 0, limit, fail))
+                    break;
+                if (u > 0 && !tc_wait(empty0 + 8u * s, (uint32_t)((u - 1) & 1), limit, fail))
+                    break;
+                if (*fail)
+                    break;
+                const int jt = q / ng, g = q % ng;
+                const int f0 = ((int)blockIdx.x + jt * (int)gridDim.x) * kUmmaM;
+                const int alo = g * APS, ahi = min(na, alo + APS);
+                const uint32_t bar = full0 + 8u * s;
+                mbar_expect_tx(bar, (uint32_t)(ahi - alo) * (kTcAtom + p.extra_tx));
+                for (int a = alo; a < ahi; ++a)
+                    tma_load_2d(ring_s + (uint32_t)s * stage + (uint32_t)(a - alo) * kTcAtom, &tmA,
+                                a * kUmmaKC, f0, bar);
+                slots[2] = q + 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- the norm
+        griddep_wait();
+        const int nw = warp - 1;                              // 0..14
+        if (warp == 1) {            // x: lane i copies atoms i, i + 32, ...
+            if (lane == 0)
+                mbar_expect_tx(xbar, atom * (uint32_t)na);
+            __syncwarp();
+            for (int a = lane; a < na; a += 32)
+                tma_load_2d(y_s + (uint32_t)a * atom, &tmX, a * kUmmaKC, 0, xbar);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(xiss);                            // the weight's copies may follow
+        }
+        // w, zero past H (so the padded columns of y are exact zeros)
+        for (int j = tid - 32; j < na * 8; j += kTcNormWarps * 32) {
+            if (j < NP)
+                cp_async16(wsm + j * 16, static_cast<const uint4 *>(p.w) + j);
+            else
+                *reinterpret_cast<uint4 *>(wsm + j * 16) = make_uint4(0, 0, 0, 0);
+        }
+        // Units of work: (row quad, atom), U = (T / 4) na of them; norm warp
+        // nw takes units nw, nw + 15, ...; in a unit, lane (c8 = lane % 8,
+        // rq = lane / 8) takes the 16-byte chunk c8 of row 4 quad + rq
+        // (a quarter-warp reads one row's 128 bytes: all banks once). r is
+        // loaded kTcBatch units at a time, all loads first.
+        const int c8 = lane & 7, rq = lane >> 3;
+        const int RQ = NT / 4, U = RQ * na;
+        const bool ok = tc_wait(xbar, 0, limit, fail);
+        for (int u0 = nw; ok && u0 < U; u0 += kTcNormWarps * kTcBatch) {
+            uint4 rv[kTcBatch];
+            if constexpr (RES) {
+#pragma unroll
+                for (int k = 0; k < kTcBatch; ++k) {
+                    const int u = u0 + k * kTcNormWarps;
+                    const int row = 4 * (u % RQ) + rq, col8 = (u / RQ) * 8 + c8;
+                    rv[k] = (u < U && row < p.M && col8 < NP)
+                                ? ld_row_v4(static_cast<const uint4 *>(p.r) + (int64_t)row * NP + col8)
+                                : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kTcBatch; ++k) {
+                const int u = u0 + k * kTcNormWarps;
+                if (u >= U)                                   // warp-uniform
+                    break;
+                const int a = u / RQ, row = 4 * (u % RQ) + rq, col8 = a * 8 + c8;
+                const uint32_t off = (uint32_t)a * atom + (uint32_t)row * 128u +
+                                     ((uint32_t)(c8 ^ (row & 7)) << 4);
+                F acc = splat<F>(0.f);
+                if (row < p.M && col8 < NP) {
+                    P hv;
+                    hv.u = *reinterpret_cast<const uint4 *>(ysm + off);
+                    if constexpr (RES) {
+                        hv.u.x = add2_rn<T>(hv.u.x, rv[k].x);   // h as stored
+                        hv.u.y = add2_rn<T>(hv.u.y, rv[k].y);
+                        hv.u.z = add2_rn<T>(hv.u.z, rv[k].z);
+                        hv.u.w = add2_rn<T>(hv.u.w, rv[k].w);
+                        *reinterpret_cast<uint4 *>(ysm + off) = hv.u;
+                        if (writer && p.h != nullptr)
+                            hv.store(p.h, (int64_t)row * NP + col8);
+                    }
+                    X v;
+                    hv.widen(v);
+#pragma unroll
+                    for (int e = 0; e < X::N; ++e)
+                        acc = vfma(v.v[e], v.v[e], acc);
+                }
+                float sq = hsum(acc);
+                sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 1);
+                sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 2);
+                sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 4);
+                if (c8 == 0)
+                    part[a * NT + row] = sq;                  // atom a's share of row's sum
+            }
+        }
+        cp_async_wait_all_groups();                           // this thread's part of w
+        named_bar_sync(1, kTcNormWarps * 32);
+        // each token's sum over the atoms in atom order; rstd
+        if (ok && tid - 32 < NT) {
+            const int row = tid - 32;
+            float sq = 0.f;
+            for (int a = 0; a < na; ++a)
+                sq += part[a * NT + row];
+            const float r = rsqrtf(sq / (float)H + p.eps);
+            rsv[row] = r;
+            if (writer && p.rstd != nullptr && row < p.M)
+                p.rstd[row] = r;
+        }
+        named_bar_sync(1, kTcNormWarps * 32);
+        for (int u = nw; ok && u < U; u += kTcNormWarps) {
+            const int a = u / RQ, row = 4 * (u % RQ) + rq, col8 = a * 8 + c8;
+            if (row >= p.M || col8 >= NP)
+                continue;
+            const uint32_t off = (uint32_t)a * atom + (uint32_t)row * 128u +
+                                 ((uint32_t)(c8 ^ (row & 7)) << 4);
+            const F r2 = splat<F>(rsv[row]);
+            P h8, w8;
+            h8.u = *reinterpret_cast<const uint4 *>(ysm + off);
+            w8.u = *reinterpret_cast<const uint4 *>(wsm + col8 * 16);
+            X v, e8;
+            h8.widen(v);
+            w8.widen(e8);
+#pragma unroll
+            for (int e = 0; e < X::N; ++e)
+                v.v[e] = vmul(vmul(v.v[e], r2), e8.v[e]);
+            const P yv = P::narrow(v);
+            *reinterpret_cast<uint4 *>(ysm + off) = yv.u;
+            if (writer && p.y != nullptr)
+                yv.store(p.y, (int64_t)row * NP + col8);
+        }
+        // every input but A is read; y is complete and, fenced, visible to
+        // the tensor cores
+        griddep_launch_dependents();
+        fence_proxy_async_smem();
+        named_bar_sync(1, kTcNormWarps * 32);
+
+        if (tid == 32 && !*fail) {
+            // ------------------------------------------------------ MMAs
+            const uint32_t idesc = umma_idesc_f16(UmmaFormat<T>::value, kUmmaM, NT);
+            const uint64_t dr0 = umma_desc_sw128(ring_s), dy0 = umma_desc_sw128(y_s);
+            int q = 0;
+            bool stop = false;
+            for (int jt = 0; jt < mt && !stop; ++jt) {
+                const int b = jt & 1;
+                if (jt >= 2 &&
+                    !tc_wait(acce0 + 8u * b, (uint32_t)(((jt >> 1) - 1) & 1), limit, fail))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)b * ncols;
+                for (int g = 0; g < ng; ++g, ++q) {
+                    const int s = q % NSt;
+                    if (!tc_wait(full0 + 8u * s, (uint32_t)((q / NSt) & 1), limit, fail)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const int alo = g * APS, ahi = min(na, alo + APS);
+                    const uint64_t ds = dr0 + (uint64_t)(s * (int)(stage >> 4));
+                    for (int a = alo; a < ahi; ++a) {
+                        const uint64_t da = ds + (uint64_t)((a - alo) * (int)(kTcAtom >> 4));
+                        const uint64_t dy = dy0 + (uint64_t)(a * (int)(atom >> 4));
+#pragma unroll
+                        for (int k4 = 0; k4 < kUmmaKC / 16; ++k4)
+                            umma_f16(d, da + 2 * k4, dy + 2 * k4, idesc, (a | k4) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty0 + 8u * s);     // the stage is free once these are done
+                    slots[3] = q + 1;
+                }
+                if (!stop)
+                    umma_commit(accf0 + 8u * b);      // tile jt's accumulator is complete
+            }
+        } else if (warp >= kTcEpiWarp0 && warp < kTcEpiWarp0 + kTcEpiWarps) {
+            // -------------------------------------------------- epilogue
+            const int q4 = warp & 3, hh = (warp - kTcEpiWarp0) >> 2;
+            const uint32_t lanes = (uint32_t)(q4 * 32) << 16;
+            for (int jt = 0; jt < mt; ++jt) {
+                const int b = jt & 1;
+                if (!tc_wait(accf0 + 8u * b, (uint32_t)((jt >> 1) & 1), limit, fail))
+                    break;
+                tc_fence_after_sync();
+                const int f = ((int)blockIdx.x + jt * (int)gridDim.x) * kUmmaM + q4 * 32 + lane;
+                for (int t0 = 16 * hh; t0 < NT; t0 += 32) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem + (uint32_t)b * ncols + lanes + (uint32_t)t0, v);
+                    if (f < p.N) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const int t = t0 + k;
+                            if (t < p.M) {
+                                Vals<1> o;
+                                o.v[0] = __uint_as_float(v[k]);
+                                Pack<T, 1>::narrow(o).store(p.out, (int64_t)t * p.N + f);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(acce0 + 8u * b);      // the accumulator may be reused
+            }
+        }
+    }
+
+    // every role has finished or given up
+    __syncthreads();
+    if (*fail) {
+        if (tid == 0) {         // copies issued and not consumed: let them land
+            for (int q = slots[3]; q < slots[2]; ++q)
+                (void)mbar_wait_bounded(full0 + 8u * (q % NSt), (uint32_t)((q / NSt) & 1), limit);
+            atomicAdd(timeouts, 1u);
+        }
+        if (tid == 32) {        // the MMAs issued are complete before the memory is freed
+            umma_commit(dbar);
+            (void)mbar_wait_bounded(dbar, 0, limit);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 2u * ncols);
+    }
+}
+
+} // namespace rmsk

@@ -106,6 +106,8 @@ struct GemvUmmaKernels {
     const void *fn[2][2];
 };
 extern const GemvUmmaKernels gemv_umma_kernels;
+// Persistent, y held whole per CTA, no K split (gemv_tc.cuh); same indexing.
+extern const GemvUmmaKernels gemv_tc_kernels;
 // Device address of the counter of streamed-kernel waits that ran out.
 unsigned int *stream_timeout_counter(int dev);
 

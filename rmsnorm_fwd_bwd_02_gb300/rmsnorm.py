@@ -23,6 +23,7 @@ PATH_AUTO, PATH_ROWS, PATH_SPLIT, PATH_SCALAR, PATH_STREAM = 0, 1, 2, 3, 4
 PATH_GEMV = 5            # reported by last_path() after rmsnorm_gemv_fwd: the
 PATH_GEMV_TMA = 6        # weight in registers (5), fed by bulk copies (6), or
 PATH_GEMV_UMMA = 7       # the product on tcgen05 (7); 6 and 7 also force it
+PATH_GEMV_TC = 8         # persistent tcgen05 kernel, y held per CTA (8; forces it)
 
 # Entry points of include/rmsnorm.h with their ctypes signatures.
 _i64, _vp, _sz, _int, _f = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,

@@ -8,13 +8,17 @@ y the norm's output as the separate norm would store it. Compared element
 by element on every output (out, h, y, rstd) over dtypes, row counts that
 fill one to four 16-row MMA tiles (and leave them ragged), feature counts,
 output counts that leave the last 8-row tile of A ragged, with and without
-the residual add, for the three kernels: the weight in registers (gemv.cuh,
+the residual add, for the four kernels: the weight in registers (gemv.cuh,
 forced with the row-wise path override), the weight fed by bulk copies
-(gemv_tma.cuh) and the product on tcgen05 with K split over a cluster
-(gemv_umma.cuh), each forced with its own override; a kernel whose shared
-memory does not fit the call falls back to the next, and rows only the
-tcgen05 kernel holds are refused when a warp-level kernel is forced. The
-automatic choice (bulk copies up to 8 rows, tcgen05 above) is checked too.
+(gemv_tma.cuh), the product on tcgen05 with K split over a cluster
+(gemv_umma.cuh) and the persistent product on tcgen05 with y held whole
+per CTA (gemv_tc.cuh), each forced with its own override; a kernel whose
+shared memory does not fit the call falls back to the next, and rows only
+the K-split tcgen05 kernel holds are refused when a warp-level kernel is
+forced. The automatic choice (bulk copies up to 8 rows; above them the
+persistent tcgen05 kernel on wide rows with more tiles than SMs where y fits
+one CTA, else the K-split one) is checked too, and so are projections with more 128-feature tiles than SMs
+(each CTA of the persistent kernel takes several).
 """
 import pytest
 import torch
@@ -27,7 +31,8 @@ from tests.tolerances import check_bits, check_rows, check_rstd
 pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
-KERNELS = {"regs": rn.PATH_ROWS, "tma": rn.PATH_GEMV_TMA, "umma": rn.PATH_GEMV_UMMA}
+KERNELS = {"regs": rn.PATH_ROWS, "tma": rn.PATH_GEMV_TMA, "umma": rn.PATH_GEMV_UMMA,
+           "tc": rn.PATH_GEMV_TC}
 
 
 def umma_layout_bytes(T, H, KS, res):
@@ -56,6 +61,25 @@ def umma_fits(M, H, res=True):
     na = (H + 63) // 64
     return T <= 64 and H % 16 == 0 and any(
         umma_layout_bytes(T, H, ks, res) <= 227 * 1024 for ks in range(1, min(8, na) + 1))
+
+
+def tc_layout_bytes(T, H, nst, aps):
+    """Shared memory of one CTA of the persistent tcgen05 kernel: y (atoms
+    of T x 64 columns), the ring of A (nst stages of aps 16 KB atoms), w,
+    2 nst + 7 mbarriers, 16 bytes of words, rstd and the per-atom partial
+    sums of T tokens, 1023 bytes of alignment."""
+    na = (H + 63) // 64
+    return (na * T * 128 + nst * aps * 16384 + na * 128 + 8 * (2 * nst + 7) + 16 + 4 * T
+            + 4 * na * T + 1023)
+
+
+def tc_fits(M, H):
+    """Whether the persistent tcgen05 kernel takes the call: at most 64
+    tokens, H a multiple of 16, and y with a ring of at least three 32 KB or
+    two 16 KB stages in 227 KB."""
+    T = (M + 15) // 16 * 16
+    return T <= 64 and H % 16 == 0 and (tc_layout_bytes(T, H, 3, 2) <= 227 * 1024 or
+                                        tc_layout_bytes(T, H, 2, 1) <= 227 * 1024)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -103,6 +127,11 @@ def run(inp, residual, eps=1e-6, want_y=True, static=False, kernel="tma"):
         assert path == rn.PATH_GEMV, path
     elif kernel == "tma":
         assert path in (rn.PATH_GEMV, rn.PATH_GEMV_TMA), path
+    elif kernel == "tc":
+        if tc_fits(M, H):
+            assert path == rn.PATH_GEMV_TC, (M, H, path)
+        else:
+            assert path in (rn.PATH_GEMV, rn.PATH_GEMV_TMA), (M, H, path)
     elif umma_fits(M, H, residual):
         assert path == rn.PATH_GEMV_UMMA, (M, H, path)
     else:
@@ -205,13 +234,19 @@ def test_decode_workloads_full(orc, name):
 
 def test_automatic_choice():
     """Up to 8 rows the bulk-copy kernel (wherever its ring fits); above, the
+    persistent tcgen05 kernel on rows of at least 2048 features with more
+    128-feature tiles than SMs, where y fits one CTA; else the K-split
     tcgen05 kernel wherever a cluster of it fits, else the bulk-copy one."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
     for M, H, N in ((1, 896, 2048), (8, 896, 9728), (9, 896, 2048), (64, 896, 2048),
-                    (64, 896, 9728), (16, 4096, 6144), (1, 6720, 64)):
+                    (64, 896, 9728), (16, 4096, 6144), (16, 4096, 24576), (9, 4096, 24576),
+                    (17, 4096, 24576), (48, 4096, 512), (1, 6720, 64)):
         inp = synth(M, H, N, torch.bfloat16, seed=2, residual=True)
         g = {k: v.to(DEV) for k, v in inp.items()}
         rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"])
-        want = rn.PATH_GEMV_UMMA if M > 8 and umma_fits(M, H) else rn.PATH_GEMV_TMA
+        tiles = (N + 127) // 128
+        want = (rn.PATH_GEMV_TC if M > 8 and H >= 2048 and tiles > sms and tc_fits(M, H) else
+                rn.PATH_GEMV_UMMA if M > 8 and umma_fits(M, H) else rn.PATH_GEMV_TMA)
         got = rn.last_path()
         if want == rn.PATH_GEMV_TMA and got == rn.PATH_GEMV:
             want = rn.PATH_GEMV          # no ring of the bulk-copy kernel fits either
@@ -247,7 +282,7 @@ def test_deterministic_and_optional_outputs(orc):
     # the other kernels: the same h bits; y within one ulp (their norms run
     # the fp32 sums in other orders); each deterministic too
     forced = {}
-    for other in ("regs", "umma"):
+    for other in ("regs", "umma", "tc"):
         d = forced[other] = run(inp, True, kernel=other)
         check_bits(f"{other} vs tma h", d["h"], a["h"])
         ya = a["y"].view(torch.int16).to(torch.int32).cpu()
@@ -256,8 +291,8 @@ def test_deterministic_and_optional_outputs(orc):
         e = run(inp, True, kernel=other)
         for k in ("out", "h", "y", "rstd"):
             check_bits(f"{other} run-to-run {k}", e[k], d[k])
-    # no y, no h, no rstd: out unchanged (the automatic choice at 17 rows is
-    # the tcgen05 kernel)
+    # no y, no h, no rstd: out unchanged (the automatic choice at 17 rows of
+    # 896 is the K-split tcgen05 kernel)
     g = {k: v.to(DEV) for k, v in inp.items()}
     out, h, rstd = rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], want_h=False)
     torch.cuda.synchronize()
@@ -391,3 +426,76 @@ def test_umma_wait_runs_out_and_context_survives(orc):
     o = oracle_all(orc, inp, True)
     compare("umma after timeouts", run(inp, True, kernel="umma"), o, torch.bfloat16)
     assert rn.wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("M,H,N", [(16, 4096, 24576), (64, 896, 40000), (33, 896, 20001),
+                                   (9, 128, 50000), (1, 896, 38913)])
+def test_tc_many_tiles_per_cta(orc, M, H, N):
+    """More 128-feature tiles than SMs: each CTA of the persistent kernel
+    takes several, its weight ring running on across tiles and its two
+    accumulators alternating; ragged last tiles; against the oracle, and
+    the same bits run to run."""
+    assert tc_fits(M, H)
+    for residual in (True, False):
+        inp = synth(M, H, N, torch.bfloat16, seed=M + H + N, residual=residual)
+        o = oracle_all(orc, inp, residual)
+        a = run(inp, residual, static=True, kernel="tc")
+        compare(f"tc many tiles M={M} H={H} N={N} res={residual}", a, o, torch.bfloat16)
+        b = run(inp, residual, kernel="tc")
+        for k in ("out", "h", "y", "rstd"):
+            if a[k] is not None:
+                check_bits(f"tc run-to-run {k}", b[k], a[k])
+
+
+def test_tc_wait_runs_out_and_context_survives(orc):
+    """Every copy of A into the persistent kernel's ring is made to wait for
+    16 bytes no copy delivers (20 ms limit): a wait runs out, every role
+    stops, the copies in flight land and the MMAs finish before the tensor
+    memory is freed, one timeout per CTA is counted, and the next call is
+    right."""
+    inp = synth(40, 896, 40000, torch.bfloat16, seed=12, residual=True)
+    rn.wait_timeouts(reset=True)
+    rn.set_stream_test_fault(16, 20000)
+    try:
+        run(inp, True, kernel="tc")               # results incomplete by design
+        torch.cuda.synchronize()
+    finally:
+        rn.set_stream_test_fault(0, 0)
+    assert rn.wait_timeouts(reset=True) > 0
+    o = oracle_all(orc, inp, True)
+    compare("tc after timeouts", run(inp, True, kernel="tc"), o, torch.bfloat16)
+    assert rn.wait_timeouts() == 0
+
+
+def test_tc_graph_replay(orc):
+    """The persistent kernel (forced) captured in a CUDA graph with its tensor
+    maps and replayed with new activations copied into the static inputs."""
+    wl = W.WORKLOADS["decode-gateup-m1"].with_rows(24)
+    inp = W.make_inputs(wl)
+    g = {k: v.to(DEV) for k, v in inp.items()}
+    out = torch.empty(24, wl.N, device=DEV, dtype=wl.dtype)
+    h = torch.empty_like(g["x"])
+    rn.set_path_override(rn.PATH_GEMV_TC)
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], out=out, h=h, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"], out=out, h=h,
+                                static_weights=True)
+        assert rn.last_path() == rn.PATH_GEMV_TC
+    finally:
+        rn.set_path_override(rn.PATH_AUTO)
+    for step in range(3):
+        x2 = (torch.randn(24, wl.H, generator=torch.Generator().manual_seed(step + 9))
+              ).to(wl.dtype)
+        g["x"].copy_(x2.to(DEV))
+        graph.replay()
+        torch.cuda.synchronize()
+        o = orc.rmsnorm_gemv(x2, inp["w"], inp["A"], wl.eps, r=inp["r"])
+        check_rows(f"tc graph step {step} out", out, o["out"], wl.dtype, o["tout"])
+        check_bits(f"tc graph step {step} h", h, o["h"])
