@@ -99,6 +99,17 @@ WORKLOADS = {
                  backward=False, N=9728,
                  note="one decode token: residual add + RMSNorm + the stacked "
                       "gate|up projection (2 x 4864 rows of 896)"),
+        Workload("decode-8b-qkv-m16", 16, 4096, torch.bfloat16, seed=7,
+                 outlier_frac=1e-3, outlier_scale=50.0, residual=True,
+                 backward=False, N=6144,
+                 note="16 decode tokens at Qwen3-8B width: residual add + RMSNorm "
+                      "+ the stacked q|k|v projection (4096 + 1024 + 1024 rows "
+                      "of 4096)"),
+        Workload("decode-8b-gateup-m16", 16, 4096, torch.bfloat16, seed=8,
+                 outlier_frac=1e-3, outlier_scale=50.0, residual=True,
+                 backward=False, N=24576,
+                 note="16 decode tokens at Qwen3-8B width: residual add + RMSNorm "
+                      "+ the stacked gate|up projection (2 x 12288 rows of 4096)"),
     ]
 }
 
