@@ -233,7 +233,8 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
  *   or above 8 rows a tcgen05 kernel: the one whose K is split over a
  *   cluster of up to 8 CTAs (with r: H <= 4608 for M <= 32, 4096 for
  *   M <= 48, 3584 for M <= 64; without r: 5120 for M <= 32) or the
- *   persistent one that holds y whole per CTA (H <= 5632 for M <= 16).
+ *   persistent one, whose K is split over a cluster of 1 to 8 CTAs
+ *   (H <= 16384 for M <= 32, 11264 for M <= 48, 7168 for M <= 64).
  *   Calls only a tcgen05 kernel holds also return RMSNORM_ERR_UNSUPPORTED
  *   when a warp-level kernel is forced (rmsnorm_set_path_override) or the
  *   driver offers no tensor-map encoder;
@@ -246,13 +247,13 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
  * Performance: built for decode batches. Up to 8 rows the call is faster
  *   than the norm followed by a separate GEMM (measured on GB300 with the
  *   weights streaming from HBM). From 9 rows on it runs the product on the
- *   tensor cores (tcgen05): with K split over a thread-block cluster, or,
- *   on rows of at least 2048 features with more 128-feature tiles than SMs,
- *   in the persistent kernel. It stays correct and deterministic there, but
+ *   tensor cores (tcgen05): at 896 features with K split over a
+ *   thread-block cluster, on rows of 2048 features or more in the
+ *   persistent kernel. It stays correct and deterministic there, but
  *   rmsnorm_fwd / rmsnorm_residual_fwd followed by a GEMM library call is
  *   faster (at 896 features and 9 to 64 rows by some 0.8 to 2.5 us per
  *   call; at 4096 features, 9 to 48 rows and 6144 to 24576 outputs the
- *   fused call takes 1.9 to 3.5 times as long).
+ *   fused call takes 1.3 to 1.9 times as long).
  * flags: 0, or RMSNORM_GEMV_STATIC_WEIGHTS: the caller guarantees that no
  *   work still in flight on the stream when this call is enqueued writes w
  *   or A (model weights during decoding). The kernel then fetches them while

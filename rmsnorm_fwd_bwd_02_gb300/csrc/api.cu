@@ -950,35 +950,91 @@ int gemv_umma_plan(int64_t M, int64_t H, int64_t N, bool res, int dt, int dev, G
     return RMSNORM_OK;
 }
 
-// The persistent tcgen05 kernel's plan (gemv_tc.cuh): y for T tokens held
-// whole, the rest of shared memory a ring of A's atoms, two atoms a stage
-// when three such stages fit, else one. false: y does not fit.
+// The persistent tcgen05 kernel's plan (gemv_tc.cuh): the cluster size KS
+// is the first of a fixed order that fits (at most the atoms of K, a ring
+// of two stages beside the CTA's slice of y, w and the exchange blocks),
+// with the deepest ring that fits. The order is measured on GB300 (residual,
+// weights from HBM, per call): on rows of more than 1024 features clusters
+// of 4 (4096 -> 6144 at 16 / 48 rows: 18.6 / 28.2 us; against 39.2 us alone
+// at 16 rows, 21.0 in pairs, 32.6 / 39.1 in clusters of 8), then pairs,
+// clusters of 8 and single CTAs; on narrower rows single CTAs first (896 ->
+// 9728 at 16 / 64 rows: 9.4 / 15.6 us alone, 12.9 / 16.0 in pairs, 16.5 /
+// 24.1 in clusters of 4, 33.2 / 45.1 in clusters of 8), then pairs, 4 and
+// 8. Clusters of 8 are last: fewer fit at once (a cluster must sit in one
+// GPC) and each tile's exchange waits on eight CTAs.
 struct GemvTcPlan {
-    int T, na;
+    int T, na, KS;
+    int64_t clusters;
     TcLayout L;
 };
 
-bool gemv_tc_plan(int64_t M, int64_t H, GemvTcPlan *pl)
+// The deepest ring for one cluster size; false if no ring of two stages fits.
+bool gemv_tc_layout_for(int T, int64_t H, int KS, TcLayout *out)
 {
-    pl->T = (int)((M + 15) / 16 * 16);
-    pl->na = (int)((H + kUmmaKC - 1) / kUmmaKC);
-    if (pl->T > 64 || H % 16 != 0)
-        return false;
+    bool found = false;
     for (int aps : {2, 1})
-        for (int nst = 16; nst >= (aps == 2 ? 3 : 2); --nst) {
-            const TcLayout L = gemv_tc_layout(pl->T, (int)H, nst, aps);
-            if ((int64_t)L.total <= kGemvMaxSmem) {
-                pl->L = L;
-                return true;
+        for (int nst = 16; nst >= 2; --nst) {
+            const TcLayout L = gemv_tc_layout(T, (int)H, KS, nst, aps);
+            if ((int64_t)L.total > kGemvMaxSmem)
+                continue;
+            if (!found || L.NSt * L.APS > out->NSt * out->APS) {
+                *out = L;
+                found = true;
             }
+            break;
         }
-    return false;
+    return found;
 }
 
 bool gemv_tc_fits(int64_t M, int64_t H)
 {
-    GemvTcPlan pl;
-    return gemv_tc_plan(M, H, &pl);
+    const int T = (int)((M + 15) / 16 * 16);
+    const int na = (int)((H + kUmmaKC - 1) / kUmmaKC);
+    if (T > 64 || H % 16 != 0)
+        return false;
+    TcLayout L;
+    for (int ks : {1, 2, 4, 8})
+        if (ks <= na && gemv_tc_layout_for(T, H, ks, &L))
+            return true;
+    return false;
+}
+
+// st != 0: a CUDA query failed; pl->KS == 0: nothing fits.
+int gemv_tc_plan(int64_t M, int64_t H, int64_t N, const void *fn, int dev, int sms,
+                 GemvTcPlan *pl)
+{
+    pl->T = (int)((M + 15) / 16 * 16);
+    pl->na = (int)((H + kUmmaKC - 1) / kUmmaKC);
+    pl->KS = 0;
+    if (pl->T > 64 || H % 16 != 0)
+        return RMSNORM_OK;
+    static const int wide[4] = {4, 2, 8, 1}, narrow[4] = {1, 2, 4, 8};
+    const int *order = pl->na > 16 ? wide : narrow;
+    for (int i = 0; i < 4 && pl->KS == 0; ++i) {
+        const int ks = order[i];
+        TcLayout L;
+        if (ks > pl->na || !gemv_tc_layout_for(pl->T, H, ks, &L))
+            continue;
+        int64_t resident;
+        if (ks == 1) {
+            int bps;
+            const int st = blocks_per_sm(fn, kTcThreads, dev, &bps, (int)L.total);
+            if (st)
+                return st;
+            resident = (int64_t)bps * sms;
+        } else {
+            int maxc;
+            const int st = max_active_clusters(fn, kTcThreads, (int)L.total, ks, dev, &maxc);
+            if (st)
+                return st;
+            resident = maxc;
+        }
+        const int64_t tiles = (N + kUmmaM - 1) / kUmmaM;
+        pl->KS = ks;
+        pl->clusters = tiles < resident ? tiles : resident;
+        pl->L = L;
+    }
+    return RMSNORM_OK;
 }
 
 int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *out, void *h,
@@ -997,23 +1053,22 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
     const uint32_t static_w = (flags & RMSNORM_GEMV_STATIC_WEIGHTS) ? 1 : 0;
     const int ov = g_path_override.load(std::memory_order_relaxed);
 
-    // The persistent tcgen05 kernel, y held whole per CTA: forced (override
-    // 8), or automatic above kGemvUmmaMinRows rows where y fits and the
-    // projection has more 128-feature tiles than SMs on rows of at least
-    // kGemvTcMinH features. Measured on GB300 (residual, weights from HBM):
-    // 4096 -> 24576 at 9 and 16 rows 63.7 and 64.7 us against 86.6 and 85.0
-    // for the K-split kernel, whose clusters run there in several waves;
-    // with fewer tiles, or at 896 features, the K-split kernel is faster
-    // (4096 -> 6144 at 16 rows: 27.2 against 38.3 us; 896 -> 9728 at 64
-    // rows: 10.3 against 15.0 us): one CTA per tile, each with a weight ring
-    // of 80-96 KB beside y, keeps too few bytes in flight.
-    GemvTcPlan tp;
-    if ((ov == kPathGemvTc ||
-         (ov == kPathAuto && M > kGemvUmmaMinRows && H >= kGemvTcMinH &&
-          (N + kUmmaM - 1) / kUmmaM > sms)) &&
-        gemv_tc_plan(M, H, &tp)) {
+    // The persistent tcgen05 kernel (gemv_tc.cuh): forced (override 8); or
+    // automatic above kGemvUmmaMinRows rows on rows of at least kGemvTcMinH
+    // features (measured faster there than the K-split kernel at every size
+    // tried: 4096 -> 6144 at 16 / 48 rows 18.6 / 28.2 against 27.2 / 37.1
+    // us, 4096 -> 24576 46 / 59 against 85 / 122 us); or automatic above
+    // kGemvUmmaMinRows rows wherever the K-split kernel does not fit. At 896
+    // features the K-split kernel is faster (896 -> 9728 at 16 rows: 8.0
+    // against 9.4 us). launch_tc returns 1 when it did not take the call.
+    auto launch_tc = [&]() -> int {
         PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-        if (encode != nullptr) {
+        const void *fn = gemv_tc_kernels.fn[dt][r != nullptr ? 1 : 0];
+        GemvTcPlan tp;
+        tp.KS = 0;
+        if (encode != nullptr && (st = gemv_tc_plan(M, H, N, fn, dev, sms, &tp)))
+            return st;
+        if (encode != nullptr && tp.KS > 0) {
             const CUtensorMapDataType et =
                 dt == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
             // [rows][H] with the 128-byte swizzle, out-of-range reads zero:
@@ -1033,37 +1088,40 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
             if (make_map(&mapA, A, N, kUmmaM) != CUDA_SUCCESS ||
                 make_map(&mapX, x, M, (uint32_t)tp.T) != CUDA_SUCCESS)
                 return cuda_fail(cudaErrorInvalidValue);
-            const void *fn = gemv_tc_kernels.fn[dt][r != nullptr ? 1 : 0];
-            int bps;
-            if ((st = blocks_per_sm(fn, kTcThreads, dev, &bps, (int)tp.L.total)))
-                return st;
             unsigned int *tmo = stream_timeout_counter(dev);
             if (tmo == nullptr)
                 return cuda_fail(cudaErrorInvalidSymbol);
-            const int64_t tiles = (N + kUmmaM - 1) / kUmmaM;
-            const int64_t cap = (int64_t)bps * sms;
             GemvTcParams p = {r,    w,     out,   h,    y,      rstd,
                               (int)M, (int)H, (int)N, tp.T, tp.na, tp.L,
                               eps,  (int)static_w,
                               g_test_extra_tx.load(std::memory_order_relaxed),
                               g_test_wait_us.load(std::memory_order_relaxed)};
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)(tiles < cap ? tiles : cap));
+            cfg.gridDim = dim3((unsigned)(tp.clusters * tp.KS));
             cfg.blockDim = dim3(kTcThreads);
             cfg.dynamicSmemBytes = (size_t)tp.L.total;
             cfg.stream = stream;
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr.val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
+            cudaLaunchAttribute attrs[2];
+            attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attrs[0].val.programmaticStreamSerializationAllowed = 1;
+            attrs[1].id = cudaLaunchAttributeClusterDimension;
+            attrs[1].val.clusterDim.x = (unsigned)tp.KS;
+            attrs[1].val.clusterDim.y = 1;
+            attrs[1].val.clusterDim.z = 1;
+            cfg.attrs = attrs;
+            cfg.numAttrs = tp.KS > 1 ? 2 : 1;
             void *args[4] = {&p, &mapA, &mapX, &tmo};
             const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
             if (e != cudaSuccess)
                 return cuda_fail(e);
             t_last_path = kPathGemvTc;
-            return RMSNORM_OK;
+            return (int)RMSNORM_OK;
         }
+        return 1;
+    };
+    if (ov == kPathGemvTc || (ov == kPathAuto && M > kGemvUmmaMinRows && H >= kGemvTcMinH)) {
+        if ((st = launch_tc()) <= 0)
+            return st;
     }
 
     // The product on tcgen05 with K split over a cluster: automatic above
@@ -1129,9 +1187,17 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
         }
     }
 
+    // Above kGemvUmmaMinRows rows where no K-split cluster fits: the
+    // persistent kernel, whose slices of y are smaller.
+    if (ov == kPathAuto && M > kGemvUmmaMinRows &&
+        gemv_smem_bytes(MT, half, (int)M, (int)H, false) > kGemvMaxSmem) {
+        if ((st = launch_tc()) <= 0)
+            return st;
+    }
+
     // The warp-level MMA kernels need y (16-row tiles) and w in shared
-    // memory: a call accepted for the tcgen05 kernel alone stops here when
-    // that kernel was not taken (override 1 or 6, or no tensor-map encoder).
+    // memory: a call accepted for a tcgen05 kernel alone stops here when
+    // none was taken (override 1 or 6, or no tensor-map encoder).
     if (gemv_smem_bytes(MT, half, (int)M, (int)H, false) > kGemvMaxSmem)
         return RMSNORM_ERR_UNSUPPORTED;
     GemvTmaPlan pl;

@@ -192,13 +192,17 @@ def test_gemv_argument_checks(lib):
     assert call(flags=4) == -11
     assert call(M=65) == UNSUPPORTED
     assert call(H=900) == UNSUPPORTED
-    assert call(M=64, H=4096) == UNSUPPORTED
-    # wider rows that only the tcgen05 kernel holds pass the checks (and then
-    # fail on the missing device)
+    assert call(M=64, H=16384) == UNSUPPORTED
+    # wider rows that only a tcgen05 kernel holds pass the checks (and then
+    # fail on the missing device): the K-split kernel up to 3584 at 64 rows,
+    # the persistent one with K split over up to 8 CTAs up to 7168 at 64
+    # rows, 11264 at 48, all of RMSNORM_MAX_H at 32; none above 8 rows
     assert call(M=64, H=3584) == CUDA
-    assert call(M=64, H=3616) == UNSUPPORTED
-    assert call(M=32, H=4608, r=E) == CUDA
-    assert call(M=32, H=4640, r=E) == UNSUPPORTED
+    assert call(M=64, H=7168) == CUDA
+    assert call(M=64, H=7200) == UNSUPPORTED
+    assert call(M=48, H=11264, r=E) == CUDA
+    assert call(M=48, H=11296, r=E) == UNSUPPORTED
+    assert call(M=32, H=16384, r=E) == CUDA
     assert call(M=8, H=6752) == UNSUPPORTED
     assert call(dtype=F32) == UNSUPPORTED
     assert call(N=0) == BAD_SHAPE

@@ -63,23 +63,28 @@ def umma_fits(M, H, res=True):
         umma_layout_bytes(T, H, ks, res) <= 227 * 1024 for ks in range(1, min(8, na) + 1))
 
 
-def tc_layout_bytes(T, H, nst, aps):
-    """Shared memory of one CTA of the persistent tcgen05 kernel: y (atoms
-    of T x 64 columns), the ring of A (nst stages of aps 16 KB atoms), w,
-    2 nst + 7 mbarriers, 16 bytes of words, rstd and the per-atom partial
-    sums of T tokens, 1023 bytes of alignment."""
+def tc_layout_bytes(T, H, KS, nst, aps):
+    """Shared memory of one CTA of the persistent tcgen05 kernel with K split
+    over KS CTAs: its slice of y (atoms of T x 64 columns), the ring of A
+    (nst stages of aps 16 KB atoms), its slice of w, with KS > 1 the
+    exchange blocks (2 KS blocks of 128 / KS features x (T + 4) floats),
+    2 nst + 10 mbarriers, 32 bytes of words, rstd, the CTA's sums and the
+    per-atom partial sums of T tokens, 1023 bytes of alignment."""
     na = (H + 63) // 64
-    return (na * T * 128 + nst * aps * 16384 + na * 128 + 8 * (2 * nst + 7) + 16 + 4 * T
-            + 4 * na * T + 1023)
+    apc = (na + KS - 1) // KS
+    xbytes = 2 * KS * (128 // KS) * (T + 4) * 4 if KS > 1 else 0
+    return (apc * T * 128 + nst * aps * 16384 + apc * 128 + xbytes + 8 * (2 * nst + 10) + 32
+            + 8 * T + 4 * apc * T + 1023)
 
 
 def tc_fits(M, H):
     """Whether the persistent tcgen05 kernel takes the call: at most 64
-    tokens, H a multiple of 16, and y with a ring of at least three 32 KB or
-    two 16 KB stages in 227 KB."""
+    tokens, H a multiple of 16, and for some cluster size (1, 2, 4, 8, at
+    most the atoms of K) a ring of two 16 KB stages in 227 KB."""
     T = (M + 15) // 16 * 16
-    return T <= 64 and H % 16 == 0 and (tc_layout_bytes(T, H, 3, 2) <= 227 * 1024 or
-                                        tc_layout_bytes(T, H, 2, 1) <= 227 * 1024)
+    na = (H + 63) // 64
+    return T <= 64 and H % 16 == 0 and any(
+        ks <= na and tc_layout_bytes(T, H, ks, 2, 1) <= 227 * 1024 for ks in (1, 2, 4, 8))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -193,17 +198,18 @@ def test_gemv_largest_shared_memory(orc, kernel, H, M):
 
 @pytest.mark.parametrize("H,M", [(4608, 32), (4096, 48), (3584, 64), (4096, 17)])
 def test_gemv_widest_rows_tcgen05_only(orc, H, M):
-    """Rows that only the tcgen05 kernel holds (K split over a cluster of up
-    to 8 CTAs), with the residual: right through the automatic choice, and
-    refused when a warp-level MMA kernel is forced."""
+    """Rows that only the tcgen05 kernels hold, with the residual: right
+    through the K-split kernel and the automatic choice (the persistent
+    kernel at these widths), and refused when a warp-level MMA kernel is
+    forced."""
     inp = synth(M, H, 300, torch.bfloat16, seed=H + M, residual=True)
-    assert umma_fits(M, H, True)
+    assert umma_fits(M, H, True) and tc_fits(M, H)
     o = oracle_all(orc, inp, True)
     compare(f"widest tcgen05 H={H} M={M}", run(inp, True, kernel="umma"), o, torch.bfloat16)
     g = {k: v.to(DEV) for k, v in inp.items()}
     out, _, _ = rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"])
     torch.cuda.synchronize()
-    assert rn.last_path() == rn.PATH_GEMV_UMMA
+    assert rn.last_path() == rn.PATH_GEMV_TC       # the automatic choice at these widths
     check_rows(f"widest tcgen05 automatic H={H} M={M}", out, o["out"], torch.bfloat16, o["tout"])
     for forced in (rn.PATH_GEMV_TMA, rn.PATH_ROWS):
         rn.set_path_override(forced)
@@ -234,19 +240,18 @@ def test_decode_workloads_full(orc, name):
 
 def test_automatic_choice():
     """Up to 8 rows the bulk-copy kernel (wherever its ring fits); above, the
-    persistent tcgen05 kernel on rows of at least 2048 features with more
-    128-feature tiles than SMs, where y fits one CTA; else the K-split
-    tcgen05 kernel wherever a cluster of it fits, else the bulk-copy one."""
-    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    persistent tcgen05 kernel on rows of at least 2048 features; on narrower
+    rows the K-split tcgen05 kernel wherever a cluster of it fits, else the
+    persistent one, else the bulk-copy one."""
     for M, H, N in ((1, 896, 2048), (8, 896, 9728), (9, 896, 2048), (64, 896, 2048),
                     (64, 896, 9728), (16, 4096, 6144), (16, 4096, 24576), (9, 4096, 24576),
-                    (17, 4096, 24576), (48, 4096, 512), (1, 6720, 64)):
+                    (17, 4096, 24576), (48, 4096, 512), (64, 4096, 512), (1, 6720, 64)):
         inp = synth(M, H, N, torch.bfloat16, seed=2, residual=True)
         g = {k: v.to(DEV) for k, v in inp.items()}
         rn.rmsnorm_gemv_fwd(g["x"], g["w"], g["A"], r=g["r"])
-        tiles = (N + 127) // 128
-        want = (rn.PATH_GEMV_TC if M > 8 and H >= 2048 and tiles > sms and tc_fits(M, H) else
-                rn.PATH_GEMV_UMMA if M > 8 and umma_fits(M, H) else rn.PATH_GEMV_TMA)
+        want = (rn.PATH_GEMV_TC if M > 8 and H >= 2048 and tc_fits(M, H) else
+                rn.PATH_GEMV_UMMA if M > 8 and umma_fits(M, H) else
+                rn.PATH_GEMV_TC if M > 8 and tc_fits(M, H) else rn.PATH_GEMV_TMA)
         got = rn.last_path()
         if want == rn.PATH_GEMV_TMA and got == rn.PATH_GEMV:
             want = rn.PATH_GEMV          # no ring of the bulk-copy kernel fits either
@@ -380,7 +385,7 @@ def test_error_returns():
     assert call(flags=2) == -11
     assert call(M=65) == -7                  # beyond 64 rows
     assert call(H=900) == -7                 # H not a multiple of 32
-    assert call(M=64, H=4096) == -7          # y tile beyond shared memory
+    assert call(M=64, H=16384) == -7         # y tile beyond shared memory
     assert call(dtype=rn.RMSNORM_F32) == -7
     assert call(N=0) == -2
     assert call(h=x) == -1                   # h without r
@@ -429,12 +434,17 @@ def test_umma_wait_runs_out_and_context_survives(orc):
 
 
 @pytest.mark.parametrize("M,H,N", [(16, 4096, 24576), (64, 896, 40000), (33, 896, 20001),
-                                   (9, 128, 50000), (1, 896, 38913)])
+                                   (9, 128, 50000), (1, 896, 38913), (32, 4096, 24576),
+                                   (64, 4096, 600), (48, 6720, 300), (16, 16384, 1000),
+                                   (24, 2048, 30000), (40, 1024, 3000)])
 def test_tc_many_tiles_per_cta(orc, M, H, N):
-    """More 128-feature tiles than SMs: each CTA of the persistent kernel
-    takes several, its weight ring running on across tiles and its two
-    accumulators alternating; ragged last tiles; against the oracle, and
-    the same bits run to run."""
+    """The persistent kernel over shapes that make its planner take each
+    cluster size (1 to 8 CTAs splitting K, which exchange partial products
+    per tile) and, with more tiles than clusters, several tiles per
+    cluster: its weight ring running on across tiles, its two accumulators
+    alternating, the exchange's flow control wrapping round; ragged last
+    tiles; rows only it holds (64 x 4096, 48 x 6720, 16 x 16384); against
+    the oracle, and the same bits run to run."""
     assert tc_fits(M, H)
     for residual in (True, False):
         inp = synth(M, H, N, torch.bfloat16, seed=M + H + N, residual=residual)
