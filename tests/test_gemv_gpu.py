@@ -477,6 +477,26 @@ def test_tc_wait_runs_out_and_context_survives(orc):
     assert rn.wait_timeouts() == 0
 
 
+def test_tc_cluster_wait_runs_out_and_context_survives(orc):
+    """The same with K split over a cluster (rows of 4096 features run in
+    clusters of 4): the waits on A's copies run out, the CTAs stop their
+    exchanges, wait (bounded) for anything still landing in them, meet at
+    the final cluster barrier and free their tensor memory; the timeouts are
+    counted and the next call is right."""
+    inp = synth(16, 4096, 6144, torch.bfloat16, seed=13, residual=True)
+    rn.wait_timeouts(reset=True)
+    rn.set_stream_test_fault(16, 20000)
+    try:
+        run(inp, True, kernel="tc")               # results incomplete by design
+        torch.cuda.synchronize()
+    finally:
+        rn.set_stream_test_fault(0, 0)
+    assert rn.wait_timeouts(reset=True) > 0
+    o = oracle_all(orc, inp, True)
+    compare("tc cluster after timeouts", run(inp, True, kernel="tc"), o, torch.bfloat16)
+    assert rn.wait_timeouts() == 0
+
+
 def test_tc_graph_replay(orc):
     """The persistent kernel (forced) captured in a CUDA graph with its tensor
     maps and replayed with new activations copied into the static inputs."""
