@@ -780,7 +780,8 @@ def run_ours(args, wl):
     bwd_api = "rmsnorm_bwd_strided" if wl.ld else (
         "rmsnorm_residual_bwd" if wl.residual else "rmsnorm_bwd")
     fwd_kernel = fwd_api + (
-        {6: " (rms_gemv_tma)", 7: " (rms_gemv_umma)"}.get(path_f, " (rms_gemv)") if wl.N else
+        {6: " (rms_gemv_tma)", 7: " (rms_gemv_umma)", 8: " (rms_gemv_tc)"}.get(
+            path_f, " (rms_gemv)") if wl.N else
         f" (rms_bwd2_{fam.get(path_f, 'rows').split(',')[0]} + dw_reduce)"
         if wl.double_backward else
         f" (rms_fwd_{fam.get(path_f, 'rows').split(',')[0]})")

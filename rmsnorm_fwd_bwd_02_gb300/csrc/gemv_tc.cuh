@@ -29,11 +29,11 @@
 //    batch of loads in flight per thread) is rounded and stored in place;
 //    sums of h^2 per (4 tokens, atom) unit, reduced over the eight lanes
 //    holding a row's chunks, then over the CTA's atoms in atom order; with
-//    a cluster, each CTA publishes its sums, signals every peer (a remote
-//    mbarrier arrival with release semantics) and, once all peers have
-//    signalled, adds the cluster's sums in rank order (distributed shared
-//    memory); rstd; y = h rstd w in place. The first cluster stores h and
-//    y (each CTA its columns), its rank 0 rstd.
+//    a cluster, each CTA stores its sums into every peer (asynchronous
+//    stores counted on the peer's `sums` barrier, so no fence is waited
+//    for) and, once all peers' sums have landed, adds the cluster's sums in
+//    rank order; rstd; y = h rstd w in place. The first cluster stores h
+//    and y (each CTA its columns), its rank 0 rstd.
 //  - warp 1, lane 0 then issues the MMAs: per tile, into accumulator
 //    (tile & 1), once the epilogue has released it; per stage, four MMAs
 //    (m128 nT k16) an atom and one commit to the stage's `empty` barrier;
@@ -131,11 +131,28 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (cluster address),
-// releasing this thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
+// Arrive on a peer's mbarrier with the default (CTA-scope) release: for
+// handing back receive slots, where no data has to become visible to the
+// peer. The slots' readers are done (their values were consumed before the
+// named barrier that precedes this arrival) and the peer writes the slots
+// again only by bulk copies it starts after observing the arrival. A
+// release at cluster scope would also wait for this thread's outstanding
+// memory traffic, which under the stream of A held an epilogue warp for
+// microseconds per tile.
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_bar)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Store one 32-bit word into a peer's shared memory (cluster address) and
+// count its 4 bytes on the peer's mbarrier (cluster address): the word is
+// visible to the peer's threads once they see that barrier's phase complete.
+__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v,
+                                             uint32_t cluster_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     cluster_addr),
+                 "r"(v), "r"(cluster_bar)
                  : "memory");
 }
 
@@ -214,6 +231,7 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
     float *rsv = reinterpret_cast<float *>(slots + 8);        // [T] rstd
     float *csum = rsv + NT;                                   // [T] this CTA's sums of h^2
     float *part = csum + NT;                                  // [apc][T] per atom
+    const float *psum = reinterpret_cast<const float *>(send); // [KS][T] the cluster's sums
     const uint32_t atom = (uint32_t)NT * 128u;                // bytes of an atom of y
     const uint32_t ncols = gemv_umma_tmem_cols(NT);           // one accumulator
     const uint32_t stage = (uint32_t)APS * kTcAtom;
@@ -245,7 +263,10 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
         mbar_init(xiss, 1);
         slots[4] = 0;
         if (KS > 1) {
-            mbar_init(pready, (uint32_t)(KS - 1));
+            // the peers' sums of squares: (KS - 1) T words stored into this
+            // CTA by the peers
+            mbar_init(pready, 1);
+            mbar_expect_tx(pready, (uint32_t)(KS - 1) * (uint32_t)NT * 4u);
             mbar_init(rxfull, 1);
             mbar_init(rxfree, (uint32_t)(KS - 1));
             if (mt > 0) {                       // the first tile's partial products
@@ -385,12 +406,19 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
             csum[tid - 32] = sq;
         }
         named_bar_sync(1, kTcNormWarps * 32);
-        // with a cluster: publish the sums to every peer, wait for theirs
+        // with a cluster: store the sums into every peer (psum[rank][row] of
+        // its send area, unused until its epilogue), wait for theirs
         bool ok2 = ok;
         if (KS > 1) {
-            if (tid == 32 && ok)
-                for (int q = 1; q < KS; ++q)
-                    mbar_arrive_remote(cluster_map(pready, (uint32_t)((rank + q) % KS)));
+            if (ok && tid - 32 < NT) {
+                const int row = tid - 32;
+                const uint32_t at = smem_addr(psum + rank * NT + row);
+                for (int q = 1; q < KS; ++q) {
+                    const uint32_t peer = (uint32_t)((rank + q) % KS);
+                    st_async_b32(cluster_map(at, peer), __float_as_uint(csum[row]),
+                                 cluster_map(pready, peer));
+                }
+            }
             ok2 = ok && tc_wait<true>(pready, 0, limit, fail);
         }
         if (ok2 && tid - 32 < NT) {
@@ -399,7 +427,7 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
             if (KS > 1) {
                 sq = 0.f;
                 for (int q = 0; q < KS; ++q)                  // rank order
-                    sq += q == rank ? csum[row] : ld_cluster_f32(csum + row, (uint32_t)q);
+                    sq += q == rank ? csum[row] : psum[q * NT + row];
             } else {
                 sq = csum[row];
             }
@@ -596,7 +624,7 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
                         slots[4] = slots[4] + 1;
                     }
                     for (int d1 = 1; d1 < KS; ++d1)           // the slots are free again
-                        mbar_arrive_remote(cluster_map(rxfree, (uint32_t)((rank + d1) % KS)));
+                        mbar_arrive_remote_cta(cluster_map(rxfree, (uint32_t)((rank + d1) % KS)));
                 }
             }
         }
@@ -617,6 +645,8 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
         if (KS > 1 && tid == kTcEpiWarp0 * 32 && slots[4] > rx_done)
             // partial products a peer may still be copying into this CTA
             (void)mbar_wait_bounded(rxfull, (uint32_t)(rx_done & 1), limit);
+        if (KS > 1 && tid == 64)   // sums of squares a peer may still be storing
+            (void)mbar_wait_bounded(pready, 0, limit);
     }
     tc_fence_before_sync();
     __syncthreads();
