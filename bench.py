@@ -652,6 +652,44 @@ def measure_suite(rn, dev, args, headline):
     return out
 
 
+# The fused projection (rmsnorm_gemv_fwd) against the same work unfused, per
+# call: the two decode projections of a 896-feature model at 1 to 64 rows
+# and of a 4096-feature model at 16 to 64 rows.
+PROJECTIONS = (("decode-qkv-m1", (1, 16, 32, 48, 64)), ("decode-gateup-m1", (1, 16, 32, 48, 64)),
+               ("decode-8b-qkv-m16", (16, 32, 48, 64)),
+               ("decode-8b-gateup-m16", (16, 32, 48, 64)))
+GEMV_KERNELS = {5: "rms_gemv", 6: "rms_gemv_tma", 7: "rms_gemv_umma", 8: "rms_gemv_tc"}
+
+
+def measure_projections(rn, dev, args):
+    """Microseconds per call of rmsnorm_gemv_fwd and of the unfused pair
+    (this library's norm, then torch.matmul on cuBLAS) for each shape of
+    PROJECTIONS: both replayed from CUDA graphs of consecutive calls, the
+    weights rotating through more than twice L2, the activations L2-resident."""
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name, rows in PROJECTIONS:
+        for M in rows:
+            wl = W.WORKLOADS[name].with_rows(M)
+            src, sets = build_sets(rn, wl, dev)
+            (n, gr), = capture_graphs(sets, [64])
+            sets[0].fwd()
+            path = rn.last_path()
+            fused = 1e3 * time_graph(stream, gr, n, 20)
+            unf = time_unfused_gemv(rn, wl, sets, 64 * 20)["us_per_step"]
+            out[f"{M}x{wl.H}->{wl.N}"] = {
+                "M": M, "H": wl.H, "N": wl.N, "residual": bool(wl.residual),
+                "fused_us": round(fused, 3), "unfused_us": round(unf, 3),
+                "fused_over_unfused": round(fused / unf, 3),
+                "kernel": GEMV_KERNELS.get(path, str(path))}
+            del gr, sets, src
+            torch.cuda.empty_cache()
+    out["timing"] = ("CUDA-graph replay of 64 consecutive calls, weights rotating "
+                     "through more than twice L2; unfused = rmsnorm_residual_fwd + "
+                     "torch.matmul (cuBLAS)")
+    return out
+
+
 def run_ours(args, wl):
     from rmsnorm_fwd_bwd_02_gb300 import rmsnorm as rn
     rn.lib()
@@ -752,6 +790,7 @@ def run_ours(args, wl):
         torch.cuda.empty_cache()
         suite = measure_suite(rn, dev, args, {"workload": wl.name, "ms_per_step": ms_step,
                                               "fwd_ms": fwd_avg, "bwd_ms": bwd_avg})
+        suite["projections"] = measure_projections(rn, dev, args)
 
     if rank != 0:
         if dist is not None:

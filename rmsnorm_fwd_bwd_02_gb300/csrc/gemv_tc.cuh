@@ -1,5 +1,5 @@
 // gemv_tc.cuh -- RMSNorm fused with the projection, persistent, the product
-// on tcgen05 with two accumulators in tensor memory, K optionally split over
+// on tcgen05 with four accumulators in tensor memory, K optionally split over
 // a thread-block cluster. Same result as the other projection kernels: the
 // chain of [P2] (the 0.8B Qwen decode article, trdm.cn news/483216) §2.1,
 // §3.1 with y rounded to the dtype before out = y A^T, fp32 accumulation.
@@ -35,7 +35,7 @@
 //    rank order; rstd; y = h rstd w in place. The first cluster stores h
 //    and y (each CTA its columns), its rank 0 rstd.
 //  - warp 1, lane 0 then issues the MMAs: per tile, into accumulator
-//    (tile & 1), once the epilogue has released it; per stage, four MMAs
+//    (tile % 4), once the epilogue has released it; per stage, four MMAs
 //    (m128 nT k16) an atom and one commit to the stage's `empty` barrier;
 //    per tile one commit to the accumulator's `full` barrier.
 //  - warps 4-11: the epilogue. Warp w reads lanes 32 (w % 4) .. + 31 of the
@@ -51,8 +51,8 @@
 //    owner re-arms its `rx full` barrier for the next tile and then
 //    releases its receive slots by a remote arrival on each peer's `rx
 //    free` barrier, which a sender waits for before its next copies.
-// So the MMAs of tile j + 1 run while the epilogue drains and exchanges
-// tile j, and the copies of A run ahead of both.
+// So the MMAs of tiles j + 1 .. j + 3 run while the epilogue drains and
+// exchanges tile j, and the copies of A run ahead of both.
 //
 // Every wait is bounded (about one second, or the test limit). One that
 // runs out raises a flag in shared memory that every other wait also
@@ -74,13 +74,14 @@ constexpr int kTcEpiWarp0 = 4, kTcEpiWarps = 8;
 constexpr int kTcBatch = 8;                   // norm units whose r loads are in flight at once
 constexpr int kTcMaxCluster = 8;
 constexpr uint32_t kTcAtom = kUmmaAtomA;      // 128 x 64 of A: 16 KB
+constexpr int kTcAcc = 4;                     // accumulators in tensor memory, used in turn
 
 // Shared memory of one CTA, byte offsets from a 1024-byte aligned base: its
 // slice of y (apc atoms of T x 128 bytes), the ring (NSt stages of APS
 // atoms), its slice of w (apc x 128 bytes, zero past H), with a cluster the
 // exchange blocks (receive: one slot per rank; send: one block per rank;
 // the own ones unused; a block = 128 / KS features x xrow floats), the
-// mbarriers (full[NSt], empty[NSt], acc_full[2], acc_empty[2], x landed,
+// mbarriers (full[NSt], empty[NSt], acc_full[4], acc_empty[4], x landed,
 // drain, x issued, sums published, rx full, rx free), eight words
 // (tensor-memory address, failure flag, copies issued, copies consumed,
 // partial products still expected), rstd[T], the CTA's sums of squares [T]
@@ -105,7 +106,7 @@ __host__ __device__ inline TcLayout gemv_tc_layout(int T, int H, int KS, int NSt
     L.xblock = (uint32_t)(kUmmaM / KS) * (uint32_t)L.xrow * 4u;
     const uint32_t xbytes = KS > 1 ? 2u * (uint32_t)KS * L.xblock : 0u;
     L.bar = L.xch + xbytes;
-    L.slots = L.bar + 8u * (uint32_t)(2 * NSt + 10);
+    L.slots = L.bar + 8u * (uint32_t)(2 * NSt + 2 * kTcAcc + 6);
     L.total = L.slots + 32u + 8u * (uint32_t)T + 4u * (uint32_t)L.apc * (uint32_t)T + 1023u;
     return L;
 }
@@ -220,8 +221,8 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
     unsigned char *send = base + L.xch + (uint32_t)KS * L.xblock;
     const uint32_t recv_s = smem_addr(recv), send_s = smem_addr(send);
     const uint32_t full0 = smem_addr(base + L.bar), empty0 = full0 + 8u * (uint32_t)NSt;
-    const uint32_t accf0 = empty0 + 8u * (uint32_t)NSt, acce0 = accf0 + 16u;
-    const uint32_t xbar = acce0 + 16u, dbar = xbar + 8u, xiss = dbar + 8u;
+    const uint32_t accf0 = empty0 + 8u * (uint32_t)NSt, acce0 = accf0 + 8u * kTcAcc;
+    const uint32_t xbar = acce0 + 8u * kTcAcc, dbar = xbar + 8u, xiss = dbar + 8u;
     const uint32_t pready = xiss + 8u, rxfull = pready + 8u, rxfree = rxfull + 8u;
     int *slots = reinterpret_cast<int *>(base + L.slots);
     volatile int *fail = slots + 1;
@@ -244,9 +245,9 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
     const int fpo = kUmmaM / KS;                              // features per owner
     const uint32_t rx_bytes = (uint32_t)(KS - 1) * L.xblock;  // expected per tile
 
-    // set-up: tensor memory (both accumulators), the barriers, the maps
+    // set-up: tensor memory (all accumulators), the barriers, the maps
     if (warp == 0) {
-        tmem_alloc(smem_addr(slots), 2u * ncols);
+        tmem_alloc(smem_addr(slots), (uint32_t)kTcAcc * ncols);
         tmem_relinquish();
     }
     if (tid == 32) {
@@ -254,7 +255,7 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
             mbar_init(full0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kTcAcc; ++b) {
             mbar_init(accf0 + 8u * b, 1);
             mbar_init(acce0 + 8u * b, kTcEpiWarps);
         }
@@ -471,9 +472,9 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
             int q = 0;
             bool stop = false;
             for (int jt = 0; jt < mt && !stop; ++jt) {
-                const int b = jt & 1;
-                if (jt >= 2 &&
-                    !tc_wait(acce0 + 8u * b, (uint32_t)(((jt >> 1) - 1) & 1), limit, fail))
+                const int b = jt % kTcAcc;
+                if (jt >= kTcAcc &&
+                    !tc_wait(acce0 + 8u * b, (uint32_t)((jt / kTcAcc - 1) & 1), limit, fail))
                     break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem + (uint32_t)b * ncols;
@@ -512,8 +513,8 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
             // named barriers, which must not be left by some and waited at
             // by others).
             for (int jt = 0; jt < mt; ++jt) {
-                const int b = jt & 1;
-                const bool okf = tc_wait(accf0 + 8u * b, (uint32_t)((jt >> 1) & 1), limit, fail);
+                const int b = jt % kTcAcc;
+                const bool okf = tc_wait(accf0 + 8u * b, (uint32_t)((jt / kTcAcc) & 1), limit, fail);
                 if (KS > 1 ? bar_red_or(2, kTcEpiWarps * 32, !okf)
                            : !__all_sync(0xFFFFFFFFu, okf))
                     break;
@@ -656,7 +657,7 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
     }
     if (warp == 0) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, 2u * ncols);
+        tmem_dealloc(tmem, (uint32_t)kTcAcc * ncols);
     }
 }
 

@@ -68,12 +68,12 @@ def tc_layout_bytes(T, H, KS, nst, aps):
     over KS CTAs: its slice of y (atoms of T x 64 columns), the ring of A
     (nst stages of aps 16 KB atoms), its slice of w, with KS > 1 the
     exchange blocks (2 KS blocks of 128 / KS features x (T + 4) floats),
-    2 nst + 10 mbarriers, 32 bytes of words, rstd, the CTA's sums and the
+    2 nst + 14 mbarriers, 32 bytes of words, rstd, the CTA's sums and the
     per-atom partial sums of T tokens, 1023 bytes of alignment."""
     na = (H + 63) // 64
     apc = (na + KS - 1) // KS
     xbytes = 2 * KS * (128 // KS) * (T + 4) * 4 if KS > 1 else 0
-    return (apc * T * 128 + nst * aps * 16384 + apc * 128 + xbytes + 8 * (2 * nst + 10) + 32
+    return (apc * T * 128 + nst * aps * 16384 + apc * 128 + xbytes + 8 * (2 * nst + 14) + 32
             + 8 * T + 4 * apc * T + 1023)
 
 
