@@ -955,11 +955,11 @@ int gemv_umma_plan(int64_t M, int64_t H, int64_t N, bool res, int dt, int dev, G
 // of two stages beside the CTA's slice of y, w and the exchange blocks),
 // with the deepest ring that fits. The order is measured on GB300 (residual,
 // weights from HBM, per call): on rows of more than 1024 features clusters
-// of 4 (4096 -> 6144 at 16 / 48 rows: 18.6 / 28.2 us; against 39.2 us alone
-// at 16 rows, 21.0 in pairs, 32.6 / 39.1 in clusters of 8), then pairs,
+// of 4 (4096 -> 6144 at 16 / 48 rows: 17.6 / 26.7 us; against 39.1 us alone
+// at 16 rows, 20.2 in pairs, 21.9 / 29.8 in clusters of 8), then pairs,
 // clusters of 8 and single CTAs; on narrower rows single CTAs first (896 ->
-// 9728 at 16 / 64 rows: 9.4 / 15.6 us alone, 12.9 / 16.0 in pairs, 16.5 /
-// 24.1 in clusters of 4, 33.2 / 45.1 in clusters of 8), then pairs, 4 and
+// 9728 at 16 / 64 rows: 9.4 / 15.5 us alone, 12.0 / 15.5 in pairs, 13.0 /
+// 21.0 in clusters of 4, 23.0 / 35.5 in clusters of 8), then pairs, 4 and
 // 8. Clusters of 8 are last: fewer fit at once (a cluster must sit in one
 // GPC) and each tile's exchange waits on eight CTAs.
 struct GemvTcPlan {
