@@ -508,17 +508,15 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
     cluster_arrive_release();
     cluster_wait_acquire();
     if (tid < NT) {
-        float tot = 0.f;
-        for (int q = 0; q < KS; ++q)                          // rank order
-            tot += ld_cluster_f32(part + tid, (uint32_t)q);
+        const float tot = sum_cluster_f32(part + tid, (uint32_t)KS);   // rank order
         const float rs = rsqrtf(tot / (float)H + p.eps);
         rsv[tid] = rs;
         if (writer && rank == 0 && p.rstd != nullptr && tid < p.M)
             p.rstd[tid] = rs;
     }
-    // done with the peers' shared memory: a CTA waits for this arrival of
-    // every CTA only when it leaves
-    cluster_arrive_release();
+    // done with the peers' shared memory (the loads' values are used above):
+    // a CTA waits for this arrival of every CTA only when it leaves
+    cluster_arrive_relaxed();
     cp_async_wait_all_groups();                               // this thread's part of w
     __syncthreads();
 #pragma unroll

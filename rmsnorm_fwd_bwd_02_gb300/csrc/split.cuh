@@ -42,6 +42,16 @@ __device__ __forceinline__ void cluster_wait_acquire()
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Arrive on the cluster barrier without ordering memory accesses: for a
+// phase that only says "this CTA got here" (for instance, done reading the
+// peers' shared memory: loads whose values this thread has already used are
+// complete). A release here would first wait for the thread's memory
+// traffic still in flight.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 // Read a float that CTA `rank` of this cluster holds at the same shared
 // memory offset as `local` does in this CTA.
 __device__ __forceinline__ float ld_cluster_f32(const float *local, uint32_t rank)
@@ -52,6 +62,24 @@ __device__ __forceinline__ float ld_cluster_f32(const float *local, uint32_t ran
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
     return v;
+}
+
+// The sum over the n <= 8 CTAs of the cluster of the float each holds at
+// `local`'s offset, added in rank order. All loads are issued before the
+// first add, so the n remote round trips overlap.
+__device__ __forceinline__ float sum_cluster_f32(const float *local, uint32_t n)
+{
+    float v[8];
+#pragma unroll
+    for (uint32_t q = 0; q < 8; ++q)
+        if (q < n)
+            v[q] = ld_cluster_f32(local, q);
+    float s = 0.f;
+#pragma unroll
+    for (uint32_t q = 0; q < 8; ++q)
+        if (q < n)
+            s += v[q];
+    return s;
 }
 
 // grid = (K, M), cluster = (K, 1, 1), blockDim.x a multiple of 32 (<= 256).
@@ -125,10 +153,8 @@ rms_fwd_split(const SplitParams p)
 
     cluster_arrive_release();   // publish cta_sum to the cluster
     cluster_wait_acquire();
-    float total = 0.f;
-    for (uint32_t q = 0; q < K; ++q)
-        total += ld_cluster_f32(&cta_sum, q);
-    cluster_arrive_release();   // this CTA is done reading the others
+    const float total = sum_cluster_f32(&cta_sum, K);   // rank order
+    cluster_arrive_relaxed();   // this CTA is done reading the others
     griddep_launch_dependents();
 
     const float rs = rsqrtf(total / (float)p.H + p.eps);
