@@ -341,17 +341,20 @@ void rmsnorm_set_path_override(int path);
  * fused with the GEMV (rmsnorm_gemv_fwd; 5: the weight in registers, which
  * override 1 forces; 6: the weight fed by bulk copies, automatic up to 8
  * rows; 7: the product on tcgen05 with K split over a cluster, automatic
- * above 8 rows where y does not fit one CTA; 8: the persistent product on
- * tcgen05, automatic above 8 rows where y fits one CTA), 0 none. */
+ * above 8 rows on rows narrower than 2048 features; 8: the persistent
+ * product on tcgen05, automatic above 8 rows on rows of 2048 features or
+ * more; each also takes the rows only it holds), 0 none. */
 int rmsnorm_last_path(void);
 
 /*
- * Diagnostic (synchronous, not for the hot path): the number of waits in the
- * streamed kernels on the current device that ran out of time (a bulk copy
- * that never completed; the affected rows are then left unwritten and the
- * results must not be used). *count receives the value; reset != 0 also sets
- * it back to zero. Every wait is bounded at about one second, so a failed
- * copy ends the kernel instead of hanging the GPU.
+ * Diagnostic (synchronous, not for the hot path): the number of bounded
+ * waits on the current device that ran out of time (in the streamed kernels
+ * a bulk copy that never completed, in the split-row forward a peer's sum
+ * that never arrived, in the projection kernels a copy of the weight or a
+ * peer's partial products; the affected rows are then left unwritten or
+ * wrong and the results must not be used). *count receives the value;
+ * reset != 0 also sets it back to zero. Every wait is bounded at about one
+ * second, so a failed copy ends the kernel instead of hanging the GPU.
  */
 int rmsnorm_wait_timeouts(unsigned int *count, int reset);
 
@@ -360,10 +363,12 @@ int rmsnorm_wait_timeouts(unsigned int *count, int reset);
  * thread-safe against concurrent calls: later streamed launches make every
  * stage wait for extra_tx_bytes more than its copies deliver (so each wait
  * runs out) and give up after wait_limit_us microseconds (0 = the default of
- * about one second). (0, 0) restores normal operation. With a non-zero
- * extra_tx_bytes the results of those calls are left incomplete and
- * rmsnorm_wait_timeouts counts the waits that ran out; the kernels still end
- * and the CUDA context stays usable.
+ * about one second). The split-row forward's wait for its peers' sums, the
+ * projection kernels' waits for the weight's copies and the double
+ * backward's stage waits take the same hook. (0, 0) restores normal
+ * operation. With a non-zero extra_tx_bytes the results of those calls are
+ * left incomplete and rmsnorm_wait_timeouts counts the waits that ran out;
+ * the kernels still end and the CUDA context stays usable.
  */
 void rmsnorm_set_stream_test_fault(unsigned int extra_tx_bytes,
                                    unsigned int wait_limit_us);

@@ -436,7 +436,16 @@ int fwd_impl(const void *x, int64_t ldx, const void *r, int64_t ldr, const void 
         NT = NT > 256 ? 256 : NT;
         const int V = (SV + NT - 1) / NT;   // <= 8 for H <= RMSNORM_MAX_H
         const void *fn = V == 1 ? (res ? k.v1_res : k.v1) : (res ? k.v8_res : k.v8);
-        SplitParams p = {x, r, w, y, h, rstd, (int)H, NV, SV, eps, ldx, ldr, ldy, ldh};
+        int dev;
+        cudaError_t de = cudaGetDevice(&dev);
+        if (de != cudaSuccess)
+            return cuda_fail(de);
+        unsigned int *tmo = stream_timeout_counter(dev);
+        if (tmo == nullptr)
+            return cuda_fail(cudaErrorInvalidSymbol);
+        SplitParams p = {x, r, w, y, h, rstd, (int)H, NV, SV, eps, ldx, ldr, ldy, ldh, tmo,
+                         g_test_extra_tx.load(std::memory_order_relaxed),
+                         g_test_wait_us.load(std::memory_order_relaxed)};
         cudaError_t e = launch(fn, dim3(K, (unsigned)M), dim3(NT), stream, &p, true, K);
         if (e != cudaSuccess)
             return cuda_fail(e);

@@ -145,30 +145,6 @@ __device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_bar)
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
-// Store one 32-bit word into a peer's shared memory (cluster address) and
-// count its 4 bytes on the peer's mbarrier (cluster address): the word is
-// visible to the peer's threads once they see that barrier's phase complete.
-__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v,
-                                             uint32_t cluster_bar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
-                     cluster_addr),
-                 "r"(v), "r"(cluster_bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(bar), "r"(parity)
-                 : "memory");
-    return ok != 0;
-}
-
 // Bounded wait that also gives up when another role has raised `fail`; a
 // wait that runs out raises it. CLUSTER: acquire at cluster scope (for
 // barriers that peers arrive on).

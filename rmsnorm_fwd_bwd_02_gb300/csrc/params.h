@@ -75,6 +75,11 @@ struct SplitParams {
     int SV;          // packs per CTA (the last ranks may hold fewer or none)
     float eps;
     int64_t ldx, ldr, ldy, ldh;   // row strides of x, r, y, h
+    unsigned int *timeouts;       // counts waits for the peers' sums that ran out
+    // test hook of the bounded wait: bytes the peers' sums are expected to
+    // bring beyond what they do (0), and the wait limit in microseconds (0:
+    // about one second)
+    uint32_t extra_tx, wait_limit_us;
 };
 
 } // namespace rmsk

@@ -6,15 +6,21 @@
 // §3.3 keeps partials and merge in fp32 and avoids atomics. Here the same
 // split runs as ONE kernel: a thread-block cluster of K CTAs per row. Each
 // CTA loads its slice of the row into registers, reduces its partial sum of
-// squares, publishes it in its own shared memory, and after a cluster
-// barrier every CTA reads all K partials through distributed shared memory
-// and adds them in rank order 0..K-1, so all CTAs of the row compute the
-// same rstd bits. Then each CTA scales and stores its slice. No TMA and no
-// multicast are involved; the waits are the hardware cluster barrier.
+// squares and stores it into every CTA of the cluster (asynchronous stores
+// into distributed shared memory that complete on the receiver's mbarrier,
+// so no cluster-wide barrier sits between the sums and the scaling); once
+// the K - 1 words from its peers have landed, every CTA adds the K partials
+// in rank order 0..K-1, so all CTAs of the row compute the same rstd bits.
+// Then each CTA scales and stores its slice. One phase of the cluster
+// barrier, arrived at after the set-up and waited for just before the
+// stores, makes sure every CTA's mbarrier exists by then. The wait for the
+// peers' words is bounded (about one second; one that runs out counts in
+// the timeout counter). No TMA and no multicast are involved.
 #pragma once
 
 #include "common.cuh"
 #include "params.h"
+#include "stream.cuh"
 
 namespace rmsk {
 
@@ -82,6 +88,52 @@ __device__ __forceinline__ float sum_cluster_f32(const float *local, uint32_t n)
     return s;
 }
 
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Store one 32-bit word into a peer's shared memory (cluster address) and
+// count its 4 bytes on the peer's mbarrier (cluster address): the word is
+// visible to the peer's threads once they see that barrier's phase complete.
+__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v,
+                                             uint32_t cluster_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     cluster_addr),
+                 "r"(v), "r"(cluster_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with acquire at cluster scope (for barriers that peers of the
+// cluster complete); false if the phase has not completed within limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                          unsigned long long limit_ns)
+{
+    if (mbar_try_wait_cluster(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait_cluster(bar, parity))
+        if (global_ns() - t0 > limit_ns)
+            return false;
+    return true;
+}
+
 // grid = (K, M), cluster = (K, 1, 1), blockDim.x a multiple of 32 (<= 256).
 template <typename T, int E, int V, bool RES>
 __global__ void __launch_bounds__(256)
@@ -89,7 +141,8 @@ rms_fwd_split(const SplitParams p)
 {
     using P = Pack<T, E>;
     __shared__ float warp_sum[8];
-    __shared__ float cta_sum;
+    __shared__ float sums[8];                          // each CTA's sum of squares, by rank
+    __shared__ __align__(8) unsigned long long sbar;   // the peers' sums have landed
 
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -101,6 +154,17 @@ rms_fwd_split(const SplitParams p)
     // first pack of this row in each tensor
     const int64_t bx = row * (p.ldx / E), br = row * (p.ldr / E);
     const int64_t by = row * (p.ldy / E), bh = row * (p.ldh / E);
+    const uint32_t sbar_s = (uint32_t)__cvta_generic_to_shared(&sbar);
+    if (tid == 0) {
+        mbar_init(sbar_s, 1);
+        if (K > 1)                 // every other CTA of the cluster stores one word
+            mbar_expect_tx(sbar_s, (K - 1) * 4u + p.extra_tx);
+    }
+    mbar_init_fence();
+    __syncthreads();
+    // this CTA's barrier exists; the peers store into it only after the
+    // matching wait below, so this arrival is not waited for
+    cluster_arrive_relaxed();
 
     griddep_wait();
     P xv[V];
@@ -144,18 +208,27 @@ rms_fwd_split(const SplitParams p)
     if ((tid & 31) == 0)
         warp_sum[tid / 32] = ss;
     __syncthreads();
+    cluster_wait_acquire();        // every peer's barrier exists
     if (tid == 0) {
         float s = 0.f;
         for (int q = 0; q < nt / 32; ++q)
             s += warp_sum[q];
-        cta_sum = s;
+        // this CTA's sum, here and in every peer (asynchronous stores that
+        // complete on the peer's barrier)
+        sums[rank] = s;
+        const uint32_t at = (uint32_t)__cvta_generic_to_shared(&sums[rank]);
+        for (uint32_t d = 1; d < K; ++d) {
+            const uint32_t peer = (rank + d) % K;
+            st_async_b32(cluster_map(at, peer), __float_as_uint(s), cluster_map(sbar_s, peer));
+        }
+        if (K > 1 && !mbar_wait_bounded_cluster(sbar_s, 0, wait_limit_ns(p.wait_limit_us)))
+            atomicAdd(p.timeouts, 1u);
     }
-
-    cluster_arrive_release();   // publish cta_sum to the cluster
-    cluster_wait_acquire();
-    const float total = sum_cluster_f32(&cta_sum, K);   // rank order
-    cluster_arrive_relaxed();   // this CTA is done reading the others
+    __syncthreads();
     griddep_launch_dependents();
+    float total = 0.f;
+    for (uint32_t q = 0; q < K; ++q)   // rank order
+        total += sums[q];
 
     const float rs = rsqrtf(total / (float)p.H + p.eps);
     if (rank == 0 && tid == 0 && p.rstd != nullptr)
@@ -173,8 +246,6 @@ rms_fwd_split(const SplitParams p)
             f[e] = f[e] * rs * fw[e];
         P::from_float(f).store(p.y, by + vi);
     }
-    // Keep this CTA's shared memory alive until every CTA has read cta_sum.
-    cluster_wait_acquire();
 }
 
 } // namespace rmsk

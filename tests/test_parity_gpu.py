@@ -668,6 +668,31 @@ def test_stream_wait_runs_out_and_context_survives(orc, name, M):
     assert rn.wait_timeouts() == 0
 
 
+@pytest.mark.parametrize("name", ["decode-m1", "decode-m64"])
+def test_split_wait_runs_out_and_context_survives(orc, name):
+    """Make the split-row forward's wait for its peers' sums run out (each
+    CTA expects 16 bytes more than its peers store, 20 ms limit): every CTA
+    counts it and ends, and the next normal calls are right."""
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl)
+    g = to_dev(inp)
+    assert rn.wait_timeouts(reset=True) == 0
+    rn.set_stream_test_fault(16, 20000)
+    try:
+        with forced_path(rn.PATH_SPLIT):
+            rn.rmsnorm_fwd(g["x"], g["w"], eps=wl.eps)     # results wrong by design
+            assert rn.last_path() == rn.PATH_SPLIT
+        torch.cuda.synchronize()
+    finally:
+        rn.set_stream_test_fault(0, 0)
+    # every CTA of every row's cluster (at least two per row) gave up once
+    assert rn.wait_timeouts(reset=True) >= 2 * wl.M
+    with forced_path(rn.PATH_SPLIT):
+        got = gpu_fwd_bwd(wl, g)
+    compare_all(f"after timeouts {name}", wl, got, oracle_all(orc, wl, inp))
+    assert rn.wait_timeouts() == 0
+
+
 def test_no_stream_wait_ran_out():
     """Every bounded wait in the streamed kernels completed during this module."""
     assert rn.wait_timeouts() == 0
