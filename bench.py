@@ -1152,18 +1152,43 @@ def run_e2e(rn, wl, src, dev, ws, args, dist):
             "pipeline": f"{chunks} row chunks on 3 streams (copy in / compute / copy out)"}
 
 
-def kernel_src_hash(which=None):
-    """Hash of every source under csrc/ (kernels, their headers and the
-    dispatch that picks them): the DRAM traffic recorded in
-    profiles/traffic.json holds only while it is unchanged."""
+# The sources a workload's kernels are built from, their dispatch in api.cu
+# included: the streamed and row-wise norm kernels and dw_reduce for the
+# training shapes; plus the split-row forward for decode-sized batches (at
+# most 64 rows), the double backward, or the projection kernels.
+_NORM_SOURCES = ("api.cu", "common.cuh", "context.h", "params.h", "registry.h", "reduce.cuh",
+                 "rows.cuh", "rows_bf16_generic.cu", "rows_bf16_shaped.cu",
+                 "rows_f16_generic.cu", "rows_f16_shaped.cu", "rows_f32.cu", "stream.cuh",
+                 "stream_small.cuh", "stream.cu", "stream_f16.cu")
+KERNEL_SOURCES = {
+    "norm": _NORM_SOURCES,
+    "decode": _NORM_SOURCES + ("split.cuh", "split.cu"),
+    "bwd2": _NORM_SOURCES + ("bwd2.cuh", "bwd2.cu"),
+    "gemv": _NORM_SOURCES + ("split.cuh", "gemv.cuh", "gemv.cu", "gemv_tma.cuh",
+                             "gemv_umma.cuh", "gemv_umma.cu", "gemv_tc.cuh", "gemv_tc.cu"),
+}
+
+
+def source_set(wl):
+    if wl.N:
+        return "gemv"
+    if wl.double_backward:
+        return "bwd2"
+    return "decode" if wl.M <= 64 else "norm"
+
+
+def kernel_src_hash(wl):
+    """Hash of the sources the workload's kernels are built from (the
+    kernels, their headers and the dispatch that picks them): the DRAM
+    traffic recorded for it in profiles/traffic.json holds only while they
+    are unchanged."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "rmsnorm_fwd_bwd_02_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    for f in sorted(KERNEL_SOURCES[source_set(wl)]):
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -1176,7 +1201,7 @@ def load_traffic(wl, which):
         with open(p) as f:
             d = json.load(f)
         e = d.get(wl.name, {}).get(which)
-        if not e or e.get("src") != kernel_src_hash(which):
+        if not e or e.get("src") != kernel_src_hash(wl):
             return None
         return int(e["bytes"])
     except (OSError, ValueError, KeyError):
