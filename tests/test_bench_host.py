@@ -132,3 +132,17 @@ def test_launch_counts_and_step_calls():
     gemv = W.WORKLOADS["decode-qkv-m1"]
     assert bench.launches_per_step(gemv) == 1 and not bench.has_bwd_call(gemv)
     assert bench.step_name(bwd2) == "double backward"
+
+
+def test_every_kernel_source_is_in_a_traffic_source_set():
+    """Each source under csrc/ belongs to the source set of some workload,
+    so a change to it invalidates the DRAM traffic recorded for the
+    workloads whose kernels it builds; the norm kernels' set is in every
+    other set."""
+    d = os.path.join(ROOT, "rmsnorm_fwd_bwd_02_gb300", "csrc")
+    files = {f for f in os.listdir(d) if f.endswith((".cu", ".cuh", ".h"))}
+    named = set().union(*bench.KERNEL_SOURCES.values())
+    assert files == named
+    norm = set(bench.KERNEL_SOURCES["norm"])
+    assert all(norm <= set(v) for v in bench.KERNEL_SOURCES.values())
+    assert {bench.source_set(wl) for wl in W.WORKLOADS.values()} == set(bench.KERNEL_SOURCES)
