@@ -58,8 +58,8 @@
 // runs out raises a flag in shared memory that every other wait also
 // watches, so all roles stop; peers whose waits then run out stop too. The
 // CTA waits (bounded) for its copies in flight, the MMAs and any partial
-// products still landing in it, counts one timeout, meets its peers at the
-// final cluster barrier, frees the tensor memory and ends.
+// products or sums still landing in it, counts one timeout, meets its peers
+// at the final cluster barrier, frees the tensor memory and ends.
 #pragma once
 
 #include <cuda.h>
