@@ -374,6 +374,17 @@ void rmsnorm_set_stream_test_fault(unsigned int extra_tx_bytes,
                                    unsigned int wait_limit_us);
 
 /*
+ * Test hook, process-wide, not thread-safe against concurrent calls: later
+ * rmsnorm_gemv_fwd calls that run the persistent tcgen05 kernel (path 8)
+ * split K over clusters of exactly cluster_size CTAs (1 to 8) instead of
+ * the size the plan picks; where that size does not fit the call, the call
+ * takes another kernel as it would if the persistent one did not fit. 0 (or
+ * any value outside 1..8) restores the plan's choice. Results are the same
+ * up to the order of the fp32 sums.
+ */
+void rmsnorm_set_gemv_cluster_test(int cluster_size);
+
+/*
  * Backward that allocates nothing and needs no workspace from the caller.
  * The pages have no counterpart to this entry point; it exists for callers
  * that cannot call cudaMalloc at all: plug-ins hosted by a runtime that owns

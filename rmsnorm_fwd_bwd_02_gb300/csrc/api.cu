@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <map>
@@ -45,6 +46,7 @@ thread_local int t_last_path = 0;
 std::atomic<int> g_path_override{kPathAuto};
 // Test hook for the streamed kernels' bounded waits (see rmsnorm.h).
 std::atomic<unsigned> g_test_extra_tx{0}, g_test_wait_us{0};
+std::atomic<int> g_test_tc_cluster{0};   // forced cluster size of the persistent projection
 
 int cuda_fail(cudaError_t e)
 {
@@ -959,18 +961,22 @@ int gemv_umma_plan(int64_t M, int64_t H, int64_t N, bool res, int dt, int dev, G
     return RMSNORM_OK;
 }
 
-// The persistent tcgen05 kernel's plan (gemv_tc.cuh): the cluster size KS
-// is the first of a fixed order that fits (at most the atoms of K, a ring
-// of two stages beside the CTA's slice of y, w and the exchange blocks),
-// with the deepest ring that fits. The order is measured on GB300 (residual,
-// weights from HBM, per call): on rows of more than 1024 features clusters
-// of 4 (4096 -> 6144 at 16 / 48 rows: 17.6 / 26.7 us; against 39.1 us alone
-// at 16 rows, 20.2 in pairs, 21.9 / 29.8 in clusters of 8), then pairs,
-// clusters of 8 and single CTAs; on narrower rows single CTAs first (896 ->
-// 9728 at 16 / 64 rows: 9.4 / 15.5 us alone, 12.0 / 15.5 in pairs, 13.0 /
-// 21.0 in clusters of 4, 23.0 / 35.5 in clusters of 8), then pairs, 4 and
-// 8. Clusters of 8 are last: fewer fit at once (a cluster must sit in one
-// GPC) and each tile's exchange waits on eight CTAs.
+// The persistent tcgen05 kernel's plan (gemv_tc.cuh): a cluster size KS
+// from 1 to 8 that fits (at most the atoms of K, a ring of two stages beside
+// the CTA's slice of y, w and the exchange blocks), with the deepest ring
+// that fits. At 16 tokens the first of a fixed order, measured on GB300
+// (residual, weights from HBM, per call): on rows of more than 1024 features
+// clusters of 4 (4096 -> 6144: 17.7 us; against 39.1 alone, 20.3 in pairs,
+// 27.4 in threes, 20.7 in fives, 21.6 in sixes, 24.6 in sevens, 21.8 in
+// eights; 4096 -> 24576: 39.9 us in fours against 43.4 to 62.2 for the
+// other sizes), then pairs, clusters of 8 and single CTAs; on narrower rows
+// single CTAs first (896 -> 9728: 9.4 us alone, 12.0 in pairs, 13.0 in
+// fours, 23.0 in eights), then 2, 4 and 8. Above 16 tokens the MMA thread's
+// pace per atom grows with the tokens and the y slice shrinks the ring, so
+// fewer atoms per CTA pay: there the plan takes the size with the least
+// estimated time (gemv_tc_estimate_us): 4, 5 or 6 at 4096 features (4096
+// -> 24576 at 32 tokens: 43.2 us in fives against 51.5 in fours; at 64
+// tokens 65.7 in sixes against 79.5 in eights).
 struct GemvTcPlan {
     int T, na, KS;
     int64_t clusters;
@@ -1002,10 +1008,33 @@ bool gemv_tc_fits(int64_t M, int64_t H)
     if (T > 64 || H % 16 != 0)
         return false;
     TcLayout L;
-    for (int ks : {1, 2, 4, 8})
+    for (int ks = 1; ks <= kTcMaxCluster; ++ks)
         if (ks <= na && gemv_tc_layout_for(T, H, ks, &L))
             return true;
     return false;
+}
+
+// Estimated microseconds of the persistent kernel's call with clusters of
+// KS (above 16 tokens): the weight's atoms a CTA streams (ceil(tiles /
+// clusters) tiles of its apc atoms) at the slowest of three rates (the MMA
+// thread's pace, 0.1 + 0.1 T / 16 us an atom, 0.05 us more where each atom
+// has its own stage and commit; the ring's bytes in flight over a 1.5 us
+// round trip; the CTA's share of 7 TB/s of HBM), plus the norm of its slice
+// (0.1 us an atom per 16 tokens) and each tile's exchange (0.2 us per peer).
+// Fitted on GB300 to per-call times of every cluster size that fits, at 32,
+// 48 and 64 tokens and 2048-5120 features (15 shapes): the pick is within
+// 5 % of the best measured size in every case, within 1 % in 12.
+static double gemv_tc_estimate_us(int T, int apc, const TcLayout &L, int64_t tiles,
+                                  int64_t clusters, int KS)
+{
+    const double atom = (double)kTcAtom;
+    const double t_atom = 0.1 + 0.1 * (double)T / 16.0 + (L.APS == 1 ? 0.05 : 0.0);
+    const double ring = (double)L.NSt * (double)L.APS * atom;
+    const double rate = std::min({atom / t_atom, ring / 1.5,
+                                  7.0e6 / (double)(clusters * KS)});      // bytes per us
+    const double rounds = (double)((tiles + clusters - 1) / clusters);
+    return rounds * (double)apc * atom / rate + 0.1 * (double)apc * (double)T / 16.0 +
+           0.2 * rounds * (double)(KS - 1);
 }
 
 // st != 0: a CUDA query failed; pl->KS == 0: nothing fits.
@@ -1017,31 +1046,76 @@ int gemv_tc_plan(int64_t M, int64_t H, int64_t N, const void *fn, int dev, int s
     pl->KS = 0;
     if (pl->T > 64 || H % 16 != 0)
         return RMSNORM_OK;
-    static const int wide[4] = {4, 2, 8, 1}, narrow[4] = {1, 2, 4, 8};
-    const int *order = pl->na > 16 ? wide : narrow;
-    for (int i = 0; i < 4 && pl->KS == 0; ++i) {
-        const int ks = order[i];
-        TcLayout L;
-        if (ks > pl->na || !gemv_tc_layout_for(pl->T, H, ks, &L))
-            continue;
-        int64_t resident;
+    const int64_t tiles = (N + kUmmaM - 1) / kUmmaM;
+    // Clusters of KS resident at once, with the layout for KS; false if KS
+    // does not fit.
+    auto resident_for = [&](int ks, TcLayout *L, int64_t *resident) -> int {
+        *resident = 0;
+        if (ks > pl->na || !gemv_tc_layout_for(pl->T, H, ks, L))
+            return RMSNORM_OK;
         if (ks == 1) {
             int bps;
-            const int st = blocks_per_sm(fn, kTcThreads, dev, &bps, (int)L.total);
+            const int st = blocks_per_sm(fn, kTcThreads, dev, &bps, (int)L->total);
             if (st)
                 return st;
-            resident = (int64_t)bps * sms;
+            *resident = (int64_t)bps * sms;
         } else {
             int maxc;
-            const int st = max_active_clusters(fn, kTcThreads, (int)L.total, ks, dev, &maxc);
+            const int st = max_active_clusters(fn, kTcThreads, (int)L->total, ks, dev, &maxc);
             if (st)
                 return st;
-            resident = maxc;
+            *resident = maxc;
         }
-        const int64_t tiles = (N + kUmmaM - 1) / kUmmaM;
-        pl->KS = ks;
-        pl->clusters = tiles < resident ? tiles : resident;
-        pl->L = L;
+        return RMSNORM_OK;
+    };
+    if (const int forced = g_test_tc_cluster.load(std::memory_order_relaxed)) {
+        TcLayout L;
+        int64_t resident;
+        if (const int st = resident_for(forced, &L, &resident))
+            return st;
+        if (resident >= 1) {
+            pl->KS = forced;
+            pl->clusters = tiles < resident ? tiles : resident;
+            pl->L = L;
+        }
+        return RMSNORM_OK;
+    }
+    if (pl->T == 16) {
+        // 16 tokens: a fixed order, measured (the weight's copies, not the
+        // MMAs, pace the call there)
+        static const int wide[4] = {4, 2, 8, 1}, narrow[4] = {1, 2, 4, 8};
+        const int *order = pl->na > 16 ? wide : narrow;
+        for (int i = 0; i < 4 && pl->KS == 0; ++i) {
+            TcLayout L;
+            int64_t resident;
+            if (const int st = resident_for(order[i], &L, &resident))
+                return st;
+            if (resident < 1)
+                continue;
+            pl->KS = order[i];
+            pl->clusters = tiles < resident ? tiles : resident;
+            pl->L = L;
+        }
+        return RMSNORM_OK;
+    }
+    // more tokens: the cluster size with the least estimated time (the
+    // smaller one on a tie)
+    double best = 0.0;
+    for (int ks = 1; ks <= kTcMaxCluster; ++ks) {
+        TcLayout L;
+        int64_t resident;
+        if (const int st = resident_for(ks, &L, &resident))
+            return st;
+        if (resident < 1)
+            continue;
+        const int64_t clusters = tiles < resident ? tiles : resident;
+        const double est = gemv_tc_estimate_us(pl->T, L.apc, L, tiles, clusters, ks);
+        if (pl->KS == 0 || est < best) {
+            best = est;
+            pl->KS = ks;
+            pl->clusters = clusters;
+            pl->L = L;
+        }
     }
     return RMSNORM_OK;
 }
@@ -1489,6 +1563,11 @@ void rmsnorm_set_path_override(int path)
     const bool ok = (path >= kPathAuto && path <= kPathStream) || path == kPathGemvTma ||
                     path == kPathGemvUmma || path == kPathGemvTc;
     g_path_override.store(ok ? path : kPathAuto);
+}
+
+void rmsnorm_set_gemv_cluster_test(int cluster_size)
+{
+    g_test_tc_cluster.store(cluster_size >= 1 && cluster_size <= kTcMaxCluster ? cluster_size : 0);
 }
 
 void rmsnorm_set_stream_test_fault(unsigned int extra_tx_bytes, unsigned int wait_limit_us)

@@ -42,7 +42,7 @@
 //    accumulator (features) for tokens 16 ((w - 4) / 4) + 32 j
 //    (tcgen05.ld) and releases it. Without a cluster it rounds and stores
 //    out[token][feature]. With one, feature f of the tile belongs to rank
-//    f / (128 / KS): a lane keeps its own features' partial sums in
+//    f / ceil(128 / KS): a lane keeps its own features' partial sums in
 //    registers and writes the others into a send block per owner; one
 //    thread copies each block (one bulk copy, shared::cta to
 //    shared::cluster) into the owner's receive slot for this CTA,
@@ -80,7 +80,7 @@ constexpr int kTcAcc = 4;                     // accumulators in tensor memory, 
 // slice of y (apc atoms of T x 128 bytes), the ring (NSt stages of APS
 // atoms), its slice of w (apc x 128 bytes, zero past H), with a cluster the
 // exchange blocks (receive: one slot per rank; send: one block per rank;
-// the own ones unused; a block = 128 / KS features x xrow floats), the
+// the own ones unused; a block = ceil(128 / KS) features x xrow floats), the
 // mbarriers (full[NSt], empty[NSt], acc_full[4], acc_empty[4], x landed,
 // drain, x issued, sums published, rx full, rx free), eight words
 // (tensor-memory address, failure flag, copies issued, copies consumed,
@@ -103,7 +103,7 @@ __host__ __device__ inline TcLayout gemv_tc_layout(int T, int H, int KS, int NSt
     L.ring = (uint32_t)L.apc * (uint32_t)T * 128u;
     L.w = L.ring + (uint32_t)NSt * (uint32_t)APS * kTcAtom;
     L.xch = L.w + (uint32_t)L.apc * 128u;
-    L.xblock = (uint32_t)(kUmmaM / KS) * (uint32_t)L.xrow * 4u;
+    L.xblock = (uint32_t)((kUmmaM + KS - 1) / KS) * (uint32_t)L.xrow * 4u;
     const uint32_t xbytes = KS > 1 ? 2u * (uint32_t)KS * L.xblock : 0u;
     L.bar = L.xch + xbytes;
     L.slots = L.bar + 8u * (uint32_t)(2 * NSt + 2 * kTcAcc + 6);
@@ -218,7 +218,8 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
     const int ng = (nat + APS - 1) / APS;                     // stages per tile
     const int nq = mt * ng;                                   // stages of this CTA
     const bool writer = cid == 0;                             // stores h, y (and rstd)
-    const int fpo = kUmmaM / KS;                              // features per owner
+    const int fpo = (kUmmaM + KS - 1) / KS;                   // features per owner (the last
+                                                              // owner may hold fewer)
     const uint32_t rx_bytes = (uint32_t)(KS - 1) * L.xblock;  // expected per tile
 
     // set-up: tensor memory (all accumulators), the barriers, the maps

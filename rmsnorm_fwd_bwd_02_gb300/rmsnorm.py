@@ -46,6 +46,7 @@ SIGNATURES = {
     "rmsnorm_set_static_scratch_test_limit": (None, [_sz]),
     "rmsnorm_wait_timeouts": (_int, [ctypes.POINTER(ctypes.c_uint), _int]),
     "rmsnorm_set_stream_test_fault": (None, [ctypes.c_uint, ctypes.c_uint]),
+    "rmsnorm_set_gemv_cluster_test": (None, [_int]),
     "rmsnorm_bwd_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64,
                               _i64, _f, _int, _int, _vp]),
     "rmsnorm_fwd_strided": (_int, [_vp, _i64, _vp, _i64, _vp, _vp, _i64, _vp,
@@ -171,6 +172,12 @@ def wait_timeouts(reset: bool = False) -> int:
 def set_stream_test_fault(extra_tx_bytes: int, wait_limit_us: int):
     """Test hook: make the streamed kernels' waits run out (see rmsnorm.h)."""
     lib().rmsnorm_set_stream_test_fault(int(extra_tx_bytes), int(wait_limit_us))
+
+
+def set_gemv_cluster_test(cluster_size: int):
+    """Test hook: force the persistent projection kernel's cluster size (0:
+    the plan's choice; see rmsnorm.h)."""
+    lib().rmsnorm_set_gemv_cluster_test(int(cluster_size))
 
 
 def bwd_workspace_bytes(M: int, H: int, dtype: torch.dtype) -> int:

@@ -67,24 +67,24 @@ def tc_layout_bytes(T, H, KS, nst, aps):
     """Shared memory of one CTA of the persistent tcgen05 kernel with K split
     over KS CTAs: its slice of y (atoms of T x 64 columns), the ring of A
     (nst stages of aps 16 KB atoms), its slice of w, with KS > 1 the
-    exchange blocks (2 KS blocks of 128 / KS features x (T + 4) floats),
+    exchange blocks (2 KS blocks of ceil(128 / KS) features x (T + 4) floats),
     2 nst + 14 mbarriers, 32 bytes of words, rstd, the CTA's sums and the
     per-atom partial sums of T tokens, 1023 bytes of alignment."""
     na = (H + 63) // 64
     apc = (na + KS - 1) // KS
-    xbytes = 2 * KS * (128 // KS) * (T + 4) * 4 if KS > 1 else 0
+    xbytes = 2 * KS * ((128 + KS - 1) // KS) * (T + 4) * 4 if KS > 1 else 0
     return (apc * T * 128 + nst * aps * 16384 + apc * 128 + xbytes + 8 * (2 * nst + 14) + 32
             + 8 * T + 4 * apc * T + 1023)
 
 
 def tc_fits(M, H):
     """Whether the persistent tcgen05 kernel takes the call: at most 64
-    tokens, H a multiple of 16, and for some cluster size (1, 2, 4, 8, at
-    most the atoms of K) a ring of two 16 KB stages in 227 KB."""
+    tokens, H a multiple of 16, and for some cluster size (1 to 8, at most
+    the atoms of K) a ring of two 16 KB stages in 227 KB."""
     T = (M + 15) // 16 * 16
     na = (H + 63) // 64
     return T <= 64 and H % 16 == 0 and any(
-        ks <= na and tc_layout_bytes(T, H, ks, 2, 1) <= 227 * 1024 for ks in (1, 2, 4, 8))
+        ks <= na and tc_layout_bytes(T, H, ks, 2, 1) <= 227 * 1024 for ks in range(1, 9))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -529,3 +529,25 @@ def test_tc_graph_replay(orc):
         o = orc.rmsnorm_gemv(x2, inp["w"], inp["A"], wl.eps, r=inp["r"])
         check_rows(f"tc graph step {step} out", out, o["out"], wl.dtype, o["tout"])
         check_bits(f"tc graph step {step} h", h, o["h"])
+
+
+@pytest.mark.parametrize("ks", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_tc_every_cluster_size(orc, ks):
+    """The persistent kernel with K split over clusters of every size 1-8
+    (forced with the test hook): sizes that do not divide the 128 features
+    of a tile leave the last owner fewer; several tiles per cluster, ragged
+    N, 16 to 48 tokens, with and without the residual."""
+    rn.set_gemv_cluster_test(ks)
+    try:
+        for M, H, N, residual in ((16, 2048, 3000, True), (33, 4096, 2050, False),
+                                  (48, 1024, 5000, True)):
+            T = (M + 15) // 16 * 16
+            if (H + 63) // 64 < ks or tc_layout_bytes(T, H, ks, 2, 1) > 227 * 1024:
+                continue                 # this size does not fit the call
+            assert tc_fits(M, H)
+            inp = synth(M, H, N, torch.bfloat16, seed=ks * 100 + M, residual=residual)
+            got = run(inp, residual, kernel="tc")
+            compare(f"tc clusters of {ks} M={M} H={H} N={N}", got, oracle_all(orc, inp, residual),
+                    torch.bfloat16)
+    finally:
+        rn.set_gemv_cluster_test(0)
