@@ -4,7 +4,7 @@
 // chain of [P2] (the 0.8B Qwen decode article, trdm.cn news/483216) §2.1,
 // §3.1 with y rounded to the dtype before out = y A^T, fp32 accumulation.
 //
-// A cluster of KS CTAs (KS = 1, 2, 4 or 8; one CTA per SM) normalises a
+// A cluster of KS CTAs (KS = 1 to 8; one CTA per SM) normalises a
 // decode batch once: CTA `rank` owns the 64-column atoms
 // [rank na / KS, (rank + 1) na / KS) of the rows and keeps its slice of y
 // (T tokens, T = M rounded up to 16) in shared memory. The cluster then
