@@ -441,8 +441,8 @@ def test_tc_many_tiles_per_cta(orc, M, H, N):
     """The persistent kernel over shapes that make its planner take each
     cluster size (1 to 8 CTAs splitting K, which exchange partial products
     per tile) and, with more tiles than clusters, several tiles per
-    cluster: its weight ring running on across tiles, its two accumulators
-    alternating, the exchange's flow control wrapping round; ragged last
+    cluster: its weight ring running on across tiles, its four accumulators
+    in turn, the exchange's flow control wrapping round; ragged last
     tiles; rows only it holds (64 x 4096, 48 x 6720, 16 x 16384); against
     the oracle, and the same bits run to run."""
     assert tc_fits(M, H)
