@@ -325,26 +325,41 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
         // loaded kTcBatch units at a time, all loads first.
         const int c8 = lane & 7, rq = lane >> 3;
         const int RQ = NT / 4, U = RQ * nat;
+        // unit u is (atom u / RQ, row quad u % RQ); a warp's units advance by
+        // kTcNormWarps, so both are stepped by addition, not divided out
+        const int dq = kTcNormWarps / RQ, dr = kTcNormWarps % RQ;
+        auto step = [&](int &a, int &q) {
+            q += dr;
+            a += dq;
+            if (q >= RQ) {
+                q -= RQ;
+                ++a;
+            }
+        };
         // warp-uniform (the units' shuffles need every lane of the warp)
         const bool ok = __all_sync(0xFFFFFFFFu, tc_wait(xbar, 0, limit, fail));
+        int ab = nw / RQ, qb = nw % RQ;                       // unit u0's atom and quad
         for (int u0 = nw; ok && u0 < U; u0 += kTcNormWarps * kTcBatch) {
             uint4 rv[kTcBatch];
             if constexpr (RES) {
+                int a = ab, q = qb;
 #pragma unroll
                 for (int k = 0; k < kTcBatch; ++k) {
                     const int u = u0 + k * kTcNormWarps;
-                    const int row = 4 * (u % RQ) + rq, col8 = (a0 + u / RQ) * 8 + c8;
+                    const int row = 4 * q + rq, col8 = (a0 + a) * 8 + c8;
                     rv[k] = (u < U && row < p.M && col8 < NP)
                                 ? ld_row_v4(static_cast<const uint4 *>(p.r) + (int64_t)row * NP + col8)
                                 : make_uint4(0, 0, 0, 0);
+                    step(a, q);
                 }
             }
+            int a = ab, q = qb;
 #pragma unroll
-            for (int k = 0; k < kTcBatch; ++k) {
+            for (int k = 0; k < kTcBatch; ++k, step(a, q)) {
                 const int u = u0 + k * kTcNormWarps;
                 if (u >= U)                                   // warp-uniform
                     break;
-                const int a = u / RQ, row = 4 * (u % RQ) + rq, col8 = (a0 + a) * 8 + c8;
+                const int row = 4 * q + rq, col8 = (a0 + a) * 8 + c8;
                 const uint32_t off = (uint32_t)a * atom + (uint32_t)row * 128u +
                                      ((uint32_t)(c8 ^ (row & 7)) << 4);
                 F acc = splat<F>(0.f);
@@ -373,6 +388,9 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
                 if (c8 == 0)
                     part[a * NT + row] = sq;                  // atom a's share of row's sum
             }
+#pragma unroll
+            for (int k = 0; k < kTcBatch; ++k)
+                step(ab, qb);
         }
         cp_async_wait_all_groups();                           // this thread's part of w
         named_bar_sync(1, kTcNormWarps * 32);
@@ -415,8 +433,9 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
                 p.rstd[row] = r;
         }
         named_bar_sync(1, kTcNormWarps * 32);
-        for (int u = nw; ok2 && u < U; u += kTcNormWarps) {
-            const int a = u / RQ, row = 4 * (u % RQ) + rq, col8 = (a0 + a) * 8 + c8;
+        int a2 = nw / RQ, q2 = nw % RQ;
+        for (int u = nw; ok2 && u < U; u += kTcNormWarps, step(a2, q2)) {
+            const int a = a2, row = 4 * q2 + rq, col8 = (a0 + a) * 8 + c8;
             if (row >= p.M || col8 >= NP)
                 continue;
             const uint32_t off = (uint32_t)a * atom + (uint32_t)row * 128u +
