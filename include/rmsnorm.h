@@ -253,7 +253,7 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
  *   rmsnorm_fwd / rmsnorm_residual_fwd followed by a GEMM library call is
  *   faster (at 896 features and 16 to 64 rows by some 0.3 to 2.7 us per
  *   call; at 4096 features and 6144 to 24576 outputs the fused call takes
- *   1.2 to 1.7 times as long at 16 and 32 rows, 1.5 to 2.3 times at 48
+ *   1.15 to 1.6 times as long at 16 and 32 rows, 1.5 to 2.25 times at 48
  *   and 64).
  * flags: 0, or RMSNORM_GEMV_STATIC_WEIGHTS: the caller guarantees that no
  *   work still in flight on the stream when this call is enqueued writes w
