@@ -336,9 +336,8 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
     unsigned char *base = umma_smem + (((raw_s + 1023u) & ~1023u) - raw_s);
     unsigned char *ysm = base, *rsm = base + L.r, *wsm = base + L.w;
     const float4 *recv = reinterpret_cast<const float4 *>(base + L.recv);
-    float4 *send = reinterpret_cast<float4 *>(base + L.send);
     const uint32_t y_s = smem_addr(ysm), r_s = smem_addr(rsm), a_s = smem_addr(base + L.a);
-    const uint32_t recv_s = smem_addr(base + L.recv), send_s = smem_addr(send);
+    const uint32_t recv_s = smem_addr(base + L.recv);
     // A's atoms land in two groups, each behind one mbarrier (a wait costs
     // some 200 cycles even when its phase is complete): [0, nh), [nh, nat)
     const uint32_t abar = smem_addr(base + L.bar);
@@ -349,7 +348,6 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
     float *part = reinterpret_cast<float *>(slots + 4);       // [T] sums of h^2, own columns
     float *rsv = part + NT;                                   // [T] rstd
     const uint32_t atom = (uint32_t)NT * 128u;                // bytes of an atom of x, r, y
-    const uint32_t block = (uint32_t)kUmmaM * (uint32_t)L.rs * 16u;   // one rank's products
     const uint32_t ncols = gemv_umma_tmem_cols(NT);
     const unsigned long long limit = wait_limit_ns(p.wait_limit_us);
     const int G4 = NT / 4;                                    // 4-token groups
@@ -375,8 +373,8 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
         mbar_init(xbar, 1);
         mbar_init(mbar, 1);
         mbar_init(rbar, 1);
-        if (own > 0)     // every other CTA of the cluster sends one block
-            mbar_expect_tx(rbar, (uint32_t)(KS - 1) * block);
+        if (own > 0)     // every other CTA stores its partials of the owned groups
+            mbar_expect_tx(rbar, (uint32_t)(KS - 1) * (uint32_t)kUmmaM * 16u * (uint32_t)own);
         slots[1] = 0;
         slots[2] = 0;
     }
@@ -603,8 +601,9 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
 
     // 5. the partial products of each 4-token group g go to its owner, rank
     //    g % KS, slot g / KS: the own ones straight into this CTA's receive
-    //    area, the others into the send area, one block per owner, copied in
-    //    bulk (zeros when this CTA failed, so that no owner waits for them)
+    //    area, the others by asynchronous 16-byte stores into the owner's
+    //    receive area, counted on its mbarrier (zeros when this CTA failed,
+    //    so that no owner waits for them)
     tc_fence_after_sync();
     {
         float4 *recv_own = reinterpret_cast<float4 *>(base + L.recv);
@@ -627,30 +626,22 @@ rms_gemv_umma(const GemvUmmaParams p, const __grid_constant__ CUtensorMap tmA,
                 const float4 o = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                              __uint_as_float(v[4 * j + 2]),
                                              __uint_as_float(v[4 * j + 3]));
+                const uint32_t at = (uint32_t)(((rank * kUmmaM + fl) * L.rs + slot) * 16);
                 if (owner == rank)
                     recv_own[(rank * kUmmaM + fl) * L.rs + slot] = o;
                 else
-                    send[(owner * kUmmaM + fl) * L.rs + slot] = o;
+                    st_async_v4(cluster_map(recv_s + at, (uint32_t)owner), o,
+                                cluster_map(rbar, (uint32_t)owner));
             }
         }
     }
-    // the tensor memory is read (free it now) and the send area written
-    // (visible to the bulk copies)
+    // the tensor memory is read: free it now
     tc_fence_before_sync();
-    fence_proxy_async_smem();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, ncols);
     }
-    if (tid == 0)
-        for (int d = 1; d < KS; ++d) {
-            const int o = (rank + d) % KS;
-            if (G4 > o)                                       // o owns a group
-                bulk_s2s_cluster(cluster_map(recv_s + (uint32_t)rank * block, (uint32_t)o),
-                                 send_s + (uint32_t)o * block, block,
-                                 cluster_map(rbar, (uint32_t)o));
-        }
     bool got = true;
     if (own > 0)
         got = !__syncthreads_or(!mbar_wait_bounded(rbar, 0, limit));

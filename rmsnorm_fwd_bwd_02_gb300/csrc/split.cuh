@@ -108,6 +108,16 @@ __device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v,
                  : "memory");
 }
 
+// Store 16 bytes (four floats) into a peer's shared memory (cluster
+// address, 16-byte aligned) and count them on the peer's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float4 v, uint32_t cluster_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, "
+                 "%4}, [%5];" ::"r"(cluster_addr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cluster_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
