@@ -49,16 +49,16 @@
 //  5. The partial products: each warp reads 32 features x 16 tokens of the
 //     accumulator at a time (tcgen05.ld); each group of 4 tokens belongs to
 //     one CTA of the cluster (group g: rank g % KS). A CTA writes its own
-//     groups into its receive area and the others into a send area, one
-//     contiguous block per owner, which one bulk copy moves into the
-//     owner's receive area, completing on its mbarrier. The owner adds the
-//     KS partials of its groups in rank order (deterministic), rounds and
-//     stores out[token][feature]. The tensor memory is freed as soon as it
-//     is read.
-//  6. A CTA leaves once the copies into it have landed, its own copies have
-//     read their source and every CTA of the cluster has read the partial
-//     sums it needed (a cluster barrier arrived at right after that read and
-//     waited for only here).
+//     groups into its receive area and stores the others straight into
+//     their owner's receive area (asynchronous 16-byte stores into
+//     distributed shared memory, counted on the owner's mbarrier: no
+//     staging, no copy to issue). The owner adds the KS partials of its
+//     groups in rank order (deterministic), rounds and stores
+//     out[token][feature]. The tensor memory is freed as soon as it is
+//     read.
+//  6. A CTA leaves once the stores into it have landed and every CTA of
+//     the cluster has read the partial sums it needed (a cluster barrier
+//     arrived at right after that read and waited for only here).
 //
 // Every mbarrier wait is bounded (about one second, or the test limit); one
 // that runs out counts in the streamed-kernel timeout counter, the CTA skips
@@ -85,16 +85,14 @@ constexpr uint32_t kUmmaAtomA = kUmmaM * kUmmaKC * 2;   // 16 KB
 // Shared-memory layout of one CTA, byte offsets from a 1024-byte aligned
 // base: y (x copied in, h and y computed in place) at 0, r, the atoms of A,
 // the partial products received (over r when r is large enough: r is
-// consumed before any CTA sends) and those to send (over A when A is large
-// enough: its MMAs are complete before), w, the mbarriers, the
-// tensor-memory address, and the partial row sums and rstd of the T tokens.
-// Both exchange areas are [rank][feature][rs slots of 16 bytes]: the block
-// of one rank is contiguous.
+// consumed before any CTA sends), w, the mbarriers, the tensor-memory
+// address, and the partial row sums and rstd of the T tokens. The receive
+// area is [rank][feature][rs slots of 16 bytes].
 struct UmmaLayout {
     int apc;             // most atoms per CTA: ceil(na / KS)
-    int rs;              // 16-byte slots per feature and rank in the exchange
-                         // areas (odd: conflict-free accesses)
-    uint32_t r, a, recv, send, w, bar, total;   // total: with the 1023 bytes of alignment
+    int rs;              // 16-byte slots per feature and rank in the receive
+                         // area (odd: conflict-free accesses)
+    uint32_t r, a, recv, w, bar, total;   // total: with the 1023 bytes of alignment
 };
 
 __host__ __device__ inline UmmaLayout gemv_umma_layout(int T, int H, int KS, bool res)
@@ -116,12 +114,6 @@ __host__ __device__ inline UmmaLayout gemv_umma_layout(int T, int H, int KS, boo
         L.recv = L.r;
     } else {
         L.recv = end;
-        end += recv;
-    }
-    if (abytes >= recv) {     // A is multiplied before anything is sent
-        L.send = L.a;
-    } else {
-        L.send = end;
         end += recv;
     }
     L.w = end;

@@ -39,9 +39,8 @@ def umma_layout_bytes(T, H, KS, res):
     """Shared memory of one CTA of the tcgen05 kernel for T tokens, H
     features, K split over KS CTAs: its atoms (64 columns) of y, r (with the
     residual) and A (128 rows), the partial products received (over r when
-    they fit there) and sent (over A when they fit there), w, 3 + atoms
-    mbarriers, 16 bytes of words, the partial sums and rstd of T tokens,
-    1023 bytes of alignment."""
+    they fit there), w, 3 + atoms mbarriers, 16 bytes of words, the partial
+    sums and rstd of T tokens, 1023 bytes of alignment."""
     na = (H + 63) // 64
     apc = (na + KS - 1) // KS
     rs = ((T // 4 + KS - 1) // KS) | 1
@@ -49,7 +48,7 @@ def umma_layout_bytes(T, H, KS, res):
     r = y if res else 0
     a = apc * 16384
     xchg = KS * 128 * rs * 16
-    total = y + r + a + (0 if r >= xchg else xchg) + (0 if a >= xchg else xchg)
+    total = y + r + a + (0 if r >= xchg else xchg)
     return total + apc * 128 + 8 * (apc + 3) + 16 + 8 * T + 1023
 
 

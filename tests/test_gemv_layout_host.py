@@ -8,12 +8,12 @@ size that fits, the areas are laid out as the kernel lays them out. The
 accesses the kernel makes to them are then walked:
 - the y, r and A atoms of each rank's K slice;
 - the 16-byte chunks the norm reads and writes;
-- the exchange slots of each 4-token group;
+- the receive slots of each 4-token group;
 - w's chunks, the mbarriers, the words, the partial sums and rstd.
 
 Each access must stay inside its own area, and the areas may not overlap,
-except the two overlays the kernel relies on: receive over r (read before
-any peer sends) and send over A (multiplied before anything is sent).
+except the overlay the kernel relies on: receive over r (read before any
+peer stores into it).
 """
 import pytest
 
@@ -42,11 +42,6 @@ def layout(T, H, KS, res):
         L["recv"] = (L["r"][0], L["r"][0] + xchg)
     else:
         L["recv"] = (end, end + xchg)
-        end += xchg
-    if abytes >= xchg:
-        L["send"] = (L["a"][0], L["a"][0] + xchg)
-    else:
-        L["send"] = (end, end + xchg)
         end += xchg
     L["w"] = (end, end + apc * 128)
     bar = L["w"][1]
@@ -94,15 +89,11 @@ def test_every_access_stays_in_its_area():
         names = ["y", "r", "a", "w", "bar", "slots", "part", "rsv"]
         if L["recv"][0] != L["r"][0]:
             names.append("recv")
-        if L["send"][0] != L["a"][0]:
-            names.append("send")
         spans = sorted(L[k] for k in names if L[k][1] > L[k][0])
         for (lo1, hi1), (lo2, hi2) in zip(spans, spans[1:]):
             assert hi1 <= lo2, (T, H, KS, res)
         if L["recv"][0] == L["r"][0]:
             assert L["recv"][1] <= L["r"][1]
-        if L["send"][0] == L["a"][0]:
-            assert L["send"][1] <= L["a"][1]
         assert L["total"] <= SMEM
         G4 = T // 4
         for rank in range(KS):
@@ -134,11 +125,9 @@ def test_every_access_stays_in_its_area():
                 for fl in (0, 127):
                     off = ((rank * 128 + fl) * rs + slot) * 16
                     assert inside((0, L["recv"][1] - L["recv"][0]), off, 16)
-                    off = ((owner * 128 + fl) * rs + slot) * 16
-                    assert inside((0, L["send"][1] - L["send"][0]), off, 16)
             for slot in range(own):
                 assert slot * KS + rank < G4
-            # a rank's block, moved by one bulk copy
+            # a rank's block of the receive area, 16-byte stores
             block = 128 * rs * 16
             assert (rank + 1) * block <= L["recv"][1] - L["recv"][0]
             assert block % 16 == 0
