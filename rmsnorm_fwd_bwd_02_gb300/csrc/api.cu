@@ -1146,7 +1146,8 @@ int gemv_impl(const void *x, const void *r, const void *w, const void *A, void *
     // against 9.4 us). launch_tc returns 1 when it did not take the call.
     auto launch_tc = [&]() -> int {
         PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-        const void *fn = gemv_tc_kernels.fn[dt][r != nullptr ? 1 : 0];
+        const void *fn =
+            gemv_tc_kernels.fn[dt][r != nullptr ? 1 : 0][(M + 15) / 16 * 16 <= 48 ? 1 : 0];
         GemvTcPlan tp;
         tp.KS = 0;
         if (encode != nullptr && (st = gemv_tc_plan(M, H, N, fn, dev, sms, &tp)))

@@ -6,8 +6,10 @@
 
 namespace rmsk {
 
-const GemvUmmaKernels gemv_tc_kernels = {
-    {{(const void *)&rms_gemv_tc<bf16, false>, (const void *)&rms_gemv_tc<bf16, true>},
-     {(const void *)&rms_gemv_tc<f16, false>, (const void *)&rms_gemv_tc<f16, true>}}};
+const GemvTcKernels gemv_tc_kernels = {
+    {{{(const void *)&rms_gemv_tc<bf16, false, false>, (const void *)&rms_gemv_tc<bf16, false, true>},
+      {(const void *)&rms_gemv_tc<bf16, true, false>, (const void *)&rms_gemv_tc<bf16, true, true>}},
+     {{(const void *)&rms_gemv_tc<f16, false, false>, (const void *)&rms_gemv_tc<f16, false, true>},
+      {(const void *)&rms_gemv_tc<f16, true, false>, (const void *)&rms_gemv_tc<f16, true, true>}}}};
 
 } // namespace rmsk

@@ -43,14 +43,15 @@
 //    (tcgen05.ld) and releases it. Without a cluster it rounds and stores
 //    out[token][feature]. With one, feature f of the tile belongs to rank
 //    f / ceil(128 / KS): a lane keeps its own features' partial sums in
-//    registers and writes the others into a send block per owner; one
-//    thread copies each block (one bulk copy, shared::cta to
-//    shared::cluster) into the owner's receive slot for this CTA,
-//    completing on the owner's `rx full` barrier; the owner adds the KS
-//    partials in rank order, rounds and stores. Flow control per tile: an
-//    owner re-arms its `rx full` barrier for the next tile and then
-//    releases its receive slots by a remote arrival on each peer's `rx
-//    free` barrier, which a sender waits for before its next copies.
+//    registers and stores the others straight into the owner's receive
+//    slot for this CTA (asynchronous 16-byte stores into distributed
+//    shared memory, counted on the owner's `rx full` barrier; at 64
+//    tokens it writes them into a send block per owner instead, which one
+//    thread moves with one bulk copy); the owner adds the KS partials in
+//    rank order, rounds and stores. Flow control per tile: an owner re-arms
+//    its `rx full` barrier for the next tile and then releases its receive
+//    slots by a remote arrival on each peer's `rx free` barrier, which a
+//    sender waits for before its next stores or copies.
 // So the MMAs of tiles j + 1 .. j + 3 run while the epilogue drains and
 // exchanges tile j, and the copies of A run ahead of both.
 //
@@ -79,8 +80,10 @@ constexpr int kTcAcc = 4;                     // accumulators in tensor memory, 
 // Shared memory of one CTA, byte offsets from a 1024-byte aligned base: its
 // slice of y (apc atoms of T x 128 bytes), the ring (NSt stages of APS
 // atoms), its slice of w (apc x 128 bytes, zero past H), with a cluster the
-// exchange blocks (receive: one slot per rank; send: one block per rank;
-// the own ones unused; a block = ceil(128 / KS) features x xrow floats), the
+// exchange blocks (receive: one slot per rank; send: one block per rank,
+// used at 64 tokens and, at its start, for the cluster's sums of squares
+// [KS][T]; the own ones unused; a block = ceil(128 / KS) features x xrow
+// floats), the
 // mbarriers (full[NSt], empty[NSt], acc_full[4], acc_empty[4], x landed,
 // drain, x issued, sums published, rx full, rx free), eight words
 // (tensor-memory address, failure flag, copies issued, copies consumed,
@@ -171,7 +174,10 @@ __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, unsigned 
 
 // grid = (clusters launched) x KS CTAs, cluster (KS, 1, 1) when KS > 1, 512
 // threads, dynamic shared memory p.L.total.
-template <typename T, bool RES>
+// DIRECT: the partial products go to their owners by asynchronous stores
+// (the host picks it up to 48 tokens), else by a send block and one bulk
+// copy per owner.
+template <typename T, bool RES, bool DIRECT>
 __global__ void __launch_bounds__(kTcThreads, 1)
 rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
             const __grid_constant__ CUtensorMap tmX, unsigned int *timeouts)
@@ -195,7 +201,7 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
     const uint32_t y_s = smem_addr(ysm), ring_s = smem_addr(base + L.ring);
     unsigned char *recv = base + L.xch;                       // [KS] slots
     unsigned char *send = base + L.xch + (uint32_t)KS * L.xblock;
-    const uint32_t recv_s = smem_addr(recv), send_s = smem_addr(send);
+    const uint32_t recv_s = smem_addr(recv);
     const uint32_t full0 = smem_addr(base + L.bar), empty0 = full0 + 8u * (uint32_t)NSt;
     const uint32_t accf0 = empty0 + 8u * (uint32_t)NSt, acce0 = accf0 + 8u * kTcAcc;
     const uint32_t xbar = acce0 + 8u * kTcAcc, dbar = xbar + 8u, xiss = dbar + 8u;
@@ -220,7 +226,16 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
     const bool writer = cid == 0;                             // stores h, y (and rstd)
     const int fpo = (kUmmaM + KS - 1) / KS;                   // features per owner (the last
                                                               // owner may hold fewer)
-    const uint32_t rx_bytes = (uint32_t)(KS - 1) * L.xblock;  // expected per tile
+    // The partial products reach their owners by asynchronous 16-byte stores
+    // straight from registers (DIRECT, up to 48 tokens); at 64 the stores'
+    // count (four times that at 16 tokens) costs more than staging each
+    // owner's block in shared memory and moving it with one bulk copy.
+    constexpr bool direct = DIRECT;
+    // expected per tile: every peer's partials of this CTA's features (T
+    // tokens each when stored directly, whole slots when copied)
+    const int nown = max(0, min(fpo, kUmmaM - rank * fpo));
+    const uint32_t rx_bytes = direct ? (uint32_t)(KS - 1) * (uint32_t)nown * (uint32_t)NT * 4u
+                                     : (uint32_t)(KS - 1) * L.xblock;
 
     // set-up: tensor memory (all accumulators), the barriers, the maps
     if (warp == 0) {
@@ -536,7 +551,7 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
                                 }
                             }
                         }
-                    } else if (mine) {
+                    } else if (mine || direct) {
 #pragma unroll
                         for (int k = 0; k < 16; ++k)
                             keep[j][k] = __uint_as_float(v[k]);
@@ -557,21 +572,49 @@ rms_gemv_tc(const GemvTcParams p, const __grid_constant__ CUtensorMap tmA,
                     mbar_arrive(acce0 + 8u * b);      // the accumulator may be reused
                 if (KS == 1)
                     continue;
-                // send this tile's partial products to their owners
-                fence_proxy_async_smem();
-                named_bar_sync(2, kTcEpiWarps * 32);
-                if (etid == 0 && !*fail &&
-                    (jt == 0 || tc_wait<true>(rxfree, (uint32_t)((jt - 1) & 1), limit, fail))) {
-                    for (int d1 = 1; d1 < KS; ++d1) {
-                        const int o = (rank + d1) % KS;
-                        bulk_s2s_cluster(cluster_map(recv_s + (uint32_t)rank * L.xblock, (uint32_t)o),
-                                         send_s + (uint32_t)o * L.xblock, L.xblock,
-                                         cluster_map(rxfull, (uint32_t)o));
+                // send this tile's partial products to their owners once each
+                // owner has freed its slots after the previous tile: straight
+                // from registers into the owner's receive slot for this CTA
+                // (asynchronous stores counted on its `rx full` barrier), or
+                // (64 tokens) one bulk copy of each owner's block
+                if (!direct) {
+                    fence_proxy_async_smem();
+                    named_bar_sync(2, kTcEpiWarps * 32);
+                    if (etid == 0 && !*fail &&
+                        (jt == 0 || tc_wait<true>(rxfree, (uint32_t)((jt - 1) & 1), limit, fail))) {
+                        for (int d1 = 1; d1 < KS; ++d1) {
+                            const int o = (rank + d1) % KS;
+                            bulk_s2s_cluster(
+                                cluster_map(recv_s + (uint32_t)rank * L.xblock, (uint32_t)o),
+                                smem_addr(send) + (uint32_t)o * L.xblock, L.xblock,
+                                cluster_map(rxfull, (uint32_t)o));
+                        }
+                        bulk_wait_read_all();         // the send blocks are free again
                     }
-                    bulk_wait_read_all();             // the send blocks are free again
+                    if (bar_red_or(2, kTcEpiWarps * 32, *fail != 0))
+                        break;
+                } else {
+                    const bool fr =
+                        jt == 0 || tc_wait<true>(rxfree, (uint32_t)((jt - 1) & 1), limit, fail);
+                    if (bar_red_or(2, kTcEpiWarps * 32, !fr || *fail != 0))
+                        break;
                 }
-                if (bar_red_or(2, kTcEpiWarps * 32, *fail != 0))
-                    break;
+                if (direct && !mine) {
+                    const uint32_t slot = cluster_map(recv_s + (uint32_t)rank * L.xblock, (uint32_t)owner);
+                    const uint32_t rbar = cluster_map(rxfull, (uint32_t)owner);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        if (16 * hh + 32 * j >= NT)
+                            break;
+                        const int t0 = 16 * hh + 32 * j;
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            st_async_v4(slot + ((uint32_t)fl * L.xrow + t0 + 4 * k4) * 4u,
+                                        make_float4(keep[j][4 * k4], keep[j][4 * k4 + 1],
+                                                    keep[j][4 * k4 + 2], keep[j][4 * k4 + 3]),
+                                        rbar);
+                    }
+                }
                 // the peers' partial products for this CTA's features
                 const bool got = tc_wait<true>(rxfull, (uint32_t)(jt & 1), limit, fail);
                 if (bar_red_or(2, kTcEpiWarps * 32, !got))

@@ -106,8 +106,12 @@ struct GemvUmmaKernels {
     const void *fn[2][2];
 };
 extern const GemvUmmaKernels gemv_umma_kernels;
-// Persistent, y held whole per CTA, no K split (gemv_tc.cuh); same indexing.
-extern const GemvUmmaKernels gemv_tc_kernels;
+// Persistent, K optionally split over a cluster (gemv_tc.cuh):
+// fn[bf16 = 0, fp16 = 1][residual][partials stored directly (<= 48 tokens)]
+struct GemvTcKernels {
+    const void *fn[2][2][2];
+};
+extern const GemvTcKernels gemv_tc_kernels;
 // Device address of the counter of streamed-kernel waits that ran out.
 unsigned int *stream_timeout_counter(int dev);
 
