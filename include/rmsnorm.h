@@ -249,12 +249,13 @@ int rmsnorm_bwd_strided(const void *dy, int64_t lddy, const void *dh_out,
  *   weights streaming from HBM). From 9 rows on it runs the product on the
  *   tensor cores (tcgen05): at 896 features with K split over a
  *   thread-block cluster, on rows of 2048 features or more in the
- *   persistent kernel. It stays correct and deterministic there, but
- *   rmsnorm_fwd / rmsnorm_residual_fwd followed by a GEMM library call is
- *   faster (at 896 features and 16 to 64 rows by some 0.3 to 2.7 us per
- *   call; at 4096 features and 6144 to 24576 outputs the fused call takes
- *   1.15 to 1.6 times as long at 16 and 32 rows, 1.5 to 2.25 times at 48
- *   and 64).
+ *   persistent kernel. It stays correct and deterministic there; at 896
+ *   features and 16 rows with 2048 outputs it is faster than the norm
+ *   followed by a GEMM library call, elsewhere rmsnorm_fwd /
+ *   rmsnorm_residual_fwd followed by a GEMM library call is faster (at 896
+ *   features by some 0.4 to 2.5 us per call; at 4096 features and 6144 to
+ *   24576 outputs the fused call takes 1.1 to 1.6 times as long at 16 and
+ *   32 rows, 1.5 to 2.25 times at 48 and 64).
  * flags: 0, or RMSNORM_GEMV_STATIC_WEIGHTS: the caller guarantees that no
  *   work still in flight on the stream when this call is enqueued writes w
  *   or A (model weights during decoding). The kernel then fetches them while
